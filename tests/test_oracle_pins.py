@@ -1,0 +1,360 @@
+"""Pins for the CPU oracle: closed forms, brute force, invariants and independent
+library routines (torch CPU in float64), so that a dropped term, a wrong sign, a
+wrong index or a transposed operand in the oracle fails here."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dflash_oracle as O
+from synth import CONFIGS, make_weights, make_workload, workload_taps
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(1234)
+
+
+class DictWeights:
+    """Weights source with per-name overrides (float32 values) over a seeded set."""
+
+    def __init__(self, base, over):
+        self.base, self.over = base, over
+
+    def get(self, name, keep=True):
+        return self.over[name] if name in self.over else self.base.get(name, keep)
+
+
+# ----------------------------------------------------------------------------- RMSNorm
+
+
+def test_rms_norm_hand_example():
+    # x = [3, 4]: mean square 12.5, rms = 3.5355339; w = [1, 2]
+    y = O.rms_norm(np.array([3.0, 4.0]), np.array([1.0, 2.0]), 0.0)
+    np.testing.assert_allclose(y, [3 / math.sqrt(12.5), 8 / math.sqrt(12.5)], rtol=1e-15)
+
+
+def test_rms_norm_matches_torch_and_invariants():
+    x = RNG.standard_normal((7, 96))
+    w = 1 + 0.05 * RNG.standard_normal(96)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (96,), torch.from_numpy(w), eps=1e-6)
+    np.testing.assert_allclose(O.rms_norm(x, w, 1e-6), ref.numpy(), rtol=1e-13, atol=1e-14)
+    y1 = O.rms_norm(x, np.ones(96), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y1 ** 2, axis=-1)), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(O.rms_norm(37.5 * x, w, 0.0), O.rms_norm(x, w, 0.0), rtol=1e-12)
+
+
+def test_silu_matches_torch():
+    z = np.linspace(-30, 30, 1001)
+    np.testing.assert_allclose(O.silu(z), torch.nn.functional.silu(torch.from_numpy(z)).numpy(),
+                               rtol=1e-14, atol=1e-300)
+    assert O.silu(np.array([0.0]))[0] == 0.0
+
+
+# ----------------------------------------------------------------------------- RoPE
+
+
+def test_inv_freq_plain_closed_form():
+    inv, ms = O.rope_inv_freq(128, 1e6)
+    assert ms == 1.0 and inv[0] == 1.0
+    # ratio between consecutive pairs is theta^(2/d); last pair is theta^(-(d-2)/d)
+    np.testing.assert_allclose(inv[:-1] / inv[1:], 10 ** (6 * 2 / 128), rtol=1e-12)
+    np.testing.assert_allclose(inv[-1], 10 ** (-6 * 126 / 128), rtol=1e-12)
+
+
+def test_rope_pairing_is_rotate_half():
+    # a unit vector on dim j must rotate into dim j + d/2 (NeoX), not j + 1 (interleaved)
+    d, p = 64, 7
+    inv, _ = O.rope_inv_freq(d, 1e6)
+    for j in (0, 5, 31):
+        x = np.zeros((1, d))
+        x[0, j] = 1.0
+        y = O.rope(x, np.array([p]), inv)
+        expect = np.zeros(d)
+        expect[j] = math.cos(p * inv[j])
+        expect[j + d // 2] = math.sin(p * inv[j])
+        np.testing.assert_allclose(y[0], expect, atol=1e-15)
+
+
+def test_rope_matches_complex_rotation():
+    d = 128
+    inv, _ = O.rope_inv_freq(d, 1e6)
+    x = RNG.standard_normal((5, 3, d))
+    pos = np.array([0, 1, 17, 4095, 32767])
+    y = O.rope(x, pos, inv)
+    z = (x[..., : d // 2] + 1j * x[..., d // 2:]) * np.exp(1j * pos[:, None, None] * inv)
+    np.testing.assert_allclose(y[..., : d // 2], z.real, atol=1e-12)
+    np.testing.assert_allclose(y[..., d // 2:], z.imag, atol=1e-12)
+
+
+def test_rope_identity_norm_and_relative():
+    d = 128
+    inv, _ = O.rope_inv_freq(d, 1e6)
+    q = RNG.standard_normal((1, d))
+    k = RNG.standard_normal((1, d))
+    np.testing.assert_array_equal(O.rope(q, np.array([0]), inv), q)
+    y = O.rope(q, np.array([1234]), inv)
+    pair = lambda v: v[0, : d // 2] ** 2 + v[0, d // 2:] ** 2  # noqa: E731
+    np.testing.assert_allclose(pair(y), pair(q), rtol=1e-12)
+    dots = [float((O.rope(q, np.array([p + 5]), inv) @ O.rope(k, np.array([p]), inv).T)[0, 0])
+            for p in (0, 100, 3000)]
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-10)
+    ms = 1.3
+    np.testing.assert_allclose(O.rope(q, np.array([9]), inv, ms), ms * O.rope(q, np.array([9]), inv))
+
+
+def test_yarn_wide_drafter_divisors():
+    # head_dim 128, theta 1e6, factor 32, original 8192, beta_fast 32, beta_slow 1:
+    # corr(32) = 17.17 -> low 17, corr(1) = 33.23 -> high 34 (ramp spans 17 dims).
+    # Rearranged closed form: ff_j = factor / (1 + (factor - 1) * ex_j), ex_j = 1 - ramp_j.
+    ff = O.yarn_divisors(128, 1e6, (32.0, 8192.0, 32.0, 1.0))
+    j = np.arange(64)
+    ramp = np.clip((j - 17) / 17.0, 0, 1)
+    expect = 32.0 / (1.0 + 31.0 * (1.0 - ramp))
+    np.testing.assert_allclose(ff, expect, rtol=1e-12)
+    assert np.all(ff[:18] == 1.0) and np.all(np.abs(ff[34:] - 32.0) < 1e-12)
+    assert abs(ff[26] - 2.0528) < 1e-4 and abs(ff[33] - 11.3333) < 1e-4
+    _, ms = O.rope_inv_freq(128, 1e6, (32.0, 8192.0, 32.0, 1.0))
+    assert abs(ms - (1 + 0.1 * math.log(32))) < 1e-15 and abs(ms - 1.346574) < 1e-6
+
+
+def test_yarn_factor_one_is_plain():
+    a, _ = O.rope_inv_freq(128, 1e6)
+    b, ms = O.rope_inv_freq(128, 1e6, (1.0, 8192.0, 32.0, 1.0))
+    np.testing.assert_allclose(a, b, rtol=1e-15)
+    assert ms == 1.0
+
+
+# ----------------------------------------------------------------------------- attention
+
+
+def brute_attention(q, k, v, qp, kp, window):
+    """Per (row, head) loop with an online (running max) softmax."""
+    nq, nh, d = q.shape
+    nkv = k.shape[1]
+    out = np.zeros_like(q)
+    for r in range(nq):
+        for h in range(nh):
+            g = h * nkv // nh
+            m, l, acc = -np.inf, 0.0, np.zeros(d)
+            for j in range(k.shape[0]):
+                if window and qp[r] - kp[j] >= window:
+                    continue
+                s = float(q[r, h] @ k[j, g]) / math.sqrt(d)
+                mn = max(m, s)
+                acc = acc * math.exp(m - mn) + math.exp(s - mn) * v[j, g]
+                l = l * math.exp(m - mn) + math.exp(s - mn)
+                m = mn
+            out[r, h] = acc / l
+    return out
+
+
+@pytest.mark.parametrize("window", [0, 5, 12])
+def test_attention_brute_force(window):
+    q = RNG.standard_normal((4, 6, 8))
+    k = RNG.standard_normal((21, 2, 8))
+    v = RNG.standard_normal((21, 2, 8))
+    kp = np.concatenate([np.arange(17), 17 + np.arange(4)])
+    qp = 17 + np.arange(4)
+    np.testing.assert_allclose(O.block_attention(q, k, v, qp, kp, window),
+                               brute_attention(q, k, v, qp, kp, window), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_gqa_equals_mha_replicated():
+    q = RNG.standard_normal((16, 8, 16))
+    k = RNG.standard_normal((40, 2, 16))
+    v = RNG.standard_normal((40, 2, 16))
+    p = np.arange(40)
+    a = O.block_attention(q, k, v, p[-16:], p)
+    b = O.block_attention(q, np.repeat(k, 4, axis=1), np.repeat(v, 4, axis=1), p[-16:], p)
+    np.testing.assert_allclose(a, b, rtol=1e-13)
+
+
+def test_attention_matches_torch_sdpa():
+    q = RNG.standard_normal((16, 8, 32))
+    k = RNG.standard_normal((50, 2, 32))
+    v = RNG.standard_normal((50, 2, 32))
+    p = np.arange(50)
+    a = O.block_attention(q, k, v, p[-16:], p)
+    tq = torch.from_numpy(q).permute(1, 0, 2)
+    tk = torch.from_numpy(np.repeat(k, 4, axis=1)).permute(1, 0, 2)
+    tv = torch.from_numpy(np.repeat(v, 4, axis=1)).permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=False)
+    np.testing.assert_allclose(a, ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_window_special_cases():
+    q = RNG.standard_normal((16, 4, 16))
+    k = RNG.standard_normal((100, 1, 16))
+    v = RNG.standard_normal((100, 1, 16))
+    kp, qp = np.arange(100), 84 + np.arange(16)
+    full = O.block_attention(q, k, v, qp, kp, 0)
+    np.testing.assert_allclose(O.block_attention(q, k, v, qp, kp, 100), full, rtol=1e-14)
+    # window 1: each query sees only keys at or after its own position
+    w1 = O.block_attention(q, k, v, qp, kp, 1)
+    for r in range(16):
+        sel = kp >= qp[r]
+        np.testing.assert_allclose(
+            w1[r:r + 1], O.block_attention(q[r:r + 1], k[sel], v[sel], qp[r:r + 1], kp[sel]),
+            rtol=1e-13)
+    # constant value rows give exactly that row
+    vc = np.broadcast_to(RNG.standard_normal((1, 1, 16)), (100, 1, 16))
+    np.testing.assert_allclose(O.block_attention(q, k, vc, qp, kp, 7), np.broadcast_to(vc[:1], (16, 4, 16)),
+                               rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------- paging
+
+
+def test_page_slots_and_paged_equals_contiguous():
+    rng = np.random.default_rng(7)
+    n, ps, npages = 77, 16, 13
+    pt = rng.permutation(npages)[:(n + ps - 1) // ps]
+    sl = O.page_slots(pt, 0, n, ps)
+    assert [int(s) for s in sl] == [int(pt[i // 16]) * 16 + i % 16 for i in range(n)]
+    assert len(set(sl.tolist())) == n
+    pool = O.PagedPool(2, npages, 2, 8, ps)
+    k = rng.standard_normal((n, 2, 8))
+    v = rng.standard_normal((n, 2, 8))
+    pool.store(1, pt, 0, k[:30], v[:30])
+    pool.store(1, pt, 30, k[30:], v[30:])
+    kk, vv = pool.gather(1, pt, n)
+    np.testing.assert_array_equal(kk, k)
+    np.testing.assert_array_equal(vv, v)
+    assert np.isnan(pool.k[0]).all()
+
+
+# ----------------------------------------------------------------------------- FP8 e4m3
+
+
+def test_e4m3_decode_all_codes_vs_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_decode(codes)
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and np.array_equal(nan, np.isnan(got))
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_roundtrip_and_spec_points():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    np.testing.assert_array_equal(O.e4m3_encode(O.e4m3_decode(codes)), codes)
+    # OCP OFP8 E4M3: max normal 448 = 0.1111.110, min normal 2^-6 = 0.0001.000,
+    # min subnormal 2^-9 = 0.0000.001; NaN = S.1111.111.
+    with open(os.path.join(GOLDEN, "e4m3_points.txt")) as fh:
+        rows = [ln.split() for ln in fh if ln.strip() and not ln.startswith("#")]
+    xs = np.array([float(r[0]) for r in rows])
+    want = np.array([int(r[1], 16) for r in rows], dtype=np.uint8)
+    np.testing.assert_array_equal(O.e4m3_encode(xs), want)
+
+
+def test_e4m3_encode_matches_torch_cast():
+    x = np.concatenate([RNG.standard_normal(200_000) * s for s in (0.003, 0.1, 1, 30, 200)])
+    x = np.clip(x, -448, 448).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(O.e4m3_encode(x), ref)
+
+
+def test_fp8_quantize_rows():
+    w = (RNG.standard_normal((64, 300)) * 0.02).astype(np.float32)
+    w[5] = 0.0
+    codes, scale = O.fp8_quantize_rows(w)
+    assert scale.dtype == np.float32 and scale[5] == 1.0 and not codes[5].any()
+    np.testing.assert_array_equal(scale[:5], (np.abs(w[:5]).max(1) / np.float32(448)).astype(np.float32))
+    dec = O.e4m3_decode(codes) * scale[:, None]
+    # the largest element of each row lands on +-448 (or just below through fp32 division)
+    amax = np.argmax(np.abs(w), axis=1)
+    assert np.all(np.abs(O.e4m3_decode(codes[np.arange(64), amax])[np.arange(64) != 5]) == 448.0)
+    # normal-range error bound: half a mantissa step (1/16 relative to the binade)
+    rel = np.abs(dec - w) / np.maximum(np.abs(w), 2.0 ** -6 * scale[:, None])
+    assert rel.max() <= 1.0 / 16 + 1e-7
+
+
+# ----------------------------------------------------------------------------- forward
+
+
+def tiny():
+    cfg = CONFIGS["tiny_fp32"]
+    wl = make_workload(cfg, 1, [64])
+    return cfg, wl, make_weights(cfg, 1)
+
+
+def test_argmax_ties_lowest_index():
+    z = np.array([[0.0, 2.0, 2.0, 1.0], [5.0, 5.0, 5.0, 5.0]])
+    idx, margin = O.Oracle.argmax_rows(z)
+    assert idx.tolist() == [1, 0] and margin.tolist() == [0.0, 0.0]
+
+
+def test_forward_cached_equals_uncached():
+    cfg, wl, W = tiny()
+    o = O.Oracle(cfg, W, cache=True)
+    taps = workload_taps(wl, 0, 0, 64)
+    pos = wl.ctx_positions(0, 0, 64)
+    f = o.ctx_features(taps)
+    ks, vs = o.ctx_kv(f, pos)
+    a = o.forward_block(ks, vs, pos, 77, 64)
+    b = o.forward_uncached(f, pos, 77)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_shift_invariance():
+    # shifting every position (context and block) by the same offset leaves the
+    # forward unchanged: RoPE only sees relative offsets and nothing else reads positions
+    cfg, wl, W = tiny()
+    o = O.Oracle(cfg, W, cache=True)
+    f = o.ctx_features(workload_taps(wl, 0, 0, 64))
+    pos = np.arange(64)
+    ks, vs = o.ctx_kv(f, pos)
+    k2, v2 = o.ctx_kv(f, pos + 1000)
+    a = o.forward_block(ks, vs, pos, 5, 64)
+    b = o.forward_block(k2, v2, pos + 1000, 5, 64, block_pos0=1064)
+    np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-9)
+    c = o.forward_block(k2, v2, pos + 1000, 5, 64, block_pos0=1070)
+    assert np.abs(a - c).max() > 1e-3
+
+
+def test_forward_context_permutation_invariance():
+    cfg, wl, W = tiny()
+    o = O.Oracle(cfg, W, cache=True)
+    f = o.ctx_features(workload_taps(wl, 0, 0, 64))
+    pos = np.arange(64)
+    ks, vs = o.ctx_kv(f, pos)
+    perm = np.random.default_rng(3).permutation(64)
+    a = o.forward_block(ks, vs, pos, 5, 64)
+    b = o.forward_block([k[perm] for k in ks], [v[perm] for v in vs], pos[perm], 5, 64)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_identity_layer():
+    # with o_proj and down_proj zero, each layer passes the residual through, so the
+    # output is norm(embed[token]) row by row
+    cfg, wl, W = tiny()
+    over = {"L0.wo": np.zeros((cfg.hidden, cfg.q_dim), np.float32),
+            "L0.w_down": np.zeros((cfg.hidden, cfg.n_ff), np.float32)}
+    o = O.Oracle(cfg, DictWeights(W, over))
+    f = o.ctx_features(workload_taps(wl, 0, 0, 64))
+    ks, vs = o.ctx_kv(f, np.arange(64))
+    h = o.forward_block(ks, vs, np.arange(64), 9, 64)
+    e = W.get("embed")[[9] + [cfg.mask_token_id] * 15].astype(np.float64)
+    np.testing.assert_allclose(h, O.rms_norm(e, W.get("norm"), cfg.rms_eps), rtol=1e-12)
+
+
+def test_forward_single_block_key_context_free():
+    # a context of 0 rows: attention sees only the gamma block keys
+    cfg, wl, W = tiny()
+    o = O.Oracle(cfg, W, cache=True)
+    empty = [np.zeros((0, 1, 64))]
+    h0 = o.forward_block(empty, empty, np.zeros(0), 3, 0)
+    hu = o.forward_uncached(np.zeros((0, cfg.hidden)), np.zeros(0), 3)
+    np.testing.assert_allclose(h0, hu, rtol=1e-12, atol=1e-12)
+    assert np.isfinite(h0).all()
+
+
+def test_drafts_drop_anchor_row():
+    cfg, wl, W = tiny()
+    o = O.Oracle(cfg, W, cache=True)
+    h = RNG.standard_normal((16, cfg.hidden))
+    z, tok, _ = o.drafts(h)
+    lm = W.get("lm_head").astype(np.float64)
+    np.testing.assert_allclose(z, h @ lm.T, rtol=1e-12)
+    assert tok.tolist() == np.argmax(h[1:] @ lm.T, axis=1).tolist() and tok.shape == (15,)
