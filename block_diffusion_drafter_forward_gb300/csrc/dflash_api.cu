@@ -1,0 +1,441 @@
+// C ABI of the drafter library: handle creation (weight packing, pool, RoPE table, FP8
+// lm_head), the context-K/V writer and the gamma-block propose.  Host-side checks run
+// before any launch; every launch is stream-ordered on the caller's stream.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+
+#include "dflash_internal.cuh"
+
+using namespace dflash;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+int fail(dflash_handle* h, int code, const std::string& msg) {
+  if (h) h->err = msg; else g_create_error = msg;
+  return code;
+}
+
+int cuda_fail(dflash_handle* h, cudaError_t e, const char* where) {
+  return fail(h, DFLASH_ECUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+#define CK(call, where)                                  \
+  do {                                                   \
+    cudaError_t e_ = (call);                             \
+    if (e_ != cudaSuccess) return cuda_fail(h, e_, where); \
+  } while (0)
+
+cudaEvent_t ev_get(dflash_handle* h) {
+  if (!h->prof.spare.empty()) {
+    cudaEvent_t e = h->prof.spare.back();
+    h->prof.spare.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Launch `call` as kernel kind `kind`: counted always, bracketed by events when profiling.
+#define KL(kind, call, where)                                                   \
+  do {                                                                          \
+    cudaEvent_t e0_ = nullptr;                                                  \
+    if (h->prof.on) {                                                           \
+      e0_ = ev_get(h);                                                          \
+      cudaEventRecord(e0_, st);                                                 \
+    }                                                                           \
+    CK((call), where);                                                          \
+    h->prof.launches[kind]++;                                                   \
+    if (h->prof.on) {                                                           \
+      cudaEvent_t e1_ = ev_get(h);                                              \
+      cudaEventRecord(e1_, st);                                                 \
+      h->prof.pending.push_back({(int)(kind), {e0_, e1_}});                     \
+    }                                                                           \
+  } while (0)
+
+void prof_drain(dflash_handle* h) {
+  for (auto& p : h->prof.pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(p.second.second) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, p.second.first, p.second.second) == cudaSuccess)
+      h->prof.ms[p.first] += ms;
+    h->prof.spare.push_back(p.second.first);
+    h->prof.spare.push_back(p.second.second);
+  }
+  h->prof.pending.clear();
+}
+
+void* dev_alloc(dflash_handle* h, size_t bytes) {
+  void* p = nullptr;
+  if (bytes == 0) bytes = 16;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  h->allocs.push_back(p);
+  return p;
+}
+
+void free_all(dflash_handle* h) {
+  for (void* p : h->allocs) cudaFree(p);
+  h->allocs.clear();
+  prof_drain(h);
+  for (cudaEvent_t e : h->prof.spare) cudaEventDestroy(e);
+  h->prof.spare.clear();
+}
+
+// Host float64 RoPE table: inv_freq_j (plain theta^(-2j/d), or the YaRN remap of
+// from_weights.rs / dflash.rs load) divided by pi, and the post-rotation scale.
+void rope_table(const dflash_cfg& c, std::vector<double>& inv_pi, float& mscale) {
+  const int half = c.head_dim / 2;
+  const double d = c.head_dim, theta = c.rope_theta;
+  inv_pi.resize(half);
+  mscale = 1.f;
+  double low = 0, high = 0, denom = 1, factor = 1;
+  if (c.rope_yarn) {
+    factor = c.yarn_factor;
+    auto corr = [&](double r) { return d * log(c.yarn_orig_max_pos / (r * 2.0 * M_PI)) / (2.0 * log(theta)); };
+    low = fmax(floor(corr(c.yarn_beta_fast)), 0.0);
+    high = fmin(ceil(corr(c.yarn_beta_slow)), d - 1.0);
+    denom = fabs(high - low) < 1e-6 ? high - low + 0.001 : high - low;
+    mscale = (float)(0.1 * log(factor) + 1.0);
+  }
+  for (int j = 0; j < half; ++j) {
+    const double base = pow(theta, -2.0 * j / d);
+    double inv = base;
+    if (c.rope_yarn) {
+      double ramp = (j - low) / denom;
+      ramp = ramp < 0 ? 0 : (ramp > 1 ? 1 : ramp);
+      const double ex = 1.0 - ramp;
+      inv = (base / factor) * (1.0 - ex) + base * ex;
+    }
+    inv_pi[j] = inv / M_PI;
+  }
+}
+
+int check_cfg(const dflash_cfg& c) {
+  auto bad = [](const char* m) { return fail(nullptr, DFLASH_EINVAL, m); };
+  if (c.hidden <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.head_dim <= 0 || c.n_ff <= 0 ||
+      c.vocab <= 0 || c.n_taps <= 0 || c.target_hidden <= 0)
+    return bad("non-positive dimension in cfg");
+  if (c.n_layers < 1 || c.n_layers > 64) return bad("n_layers must be in [1, 64]");
+  if (c.n_q_heads % c.n_kv_heads) return bad("n_q_heads must be a multiple of n_kv_heads");
+  if (c.gamma != kGamma) return fail(nullptr, DFLASH_EUNSUPPORTED, "gamma must be 16");
+  if (c.page_size != kPage) return fail(nullptr, DFLASH_EUNSUPPORTED, "page_size must be 16");
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(nullptr, DFLASH_EUNSUPPORTED, "head_dim must be 64 or 128");
+  if (c.dtype != DFLASH_F32 && c.dtype != DFLASH_BF16) return bad("dtype must be DFLASH_F32 or DFLASH_BF16");
+  if (c.lm_head_dtype != c.dtype && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE)
+    return bad("lm_head_dtype must equal dtype or be DFLASH_FP8E4M3_ROWSCALE");
+  if (c.mask_token_id < 0 || c.mask_token_id >= c.vocab) return bad("mask_token_id outside the vocabulary");
+  if (c.num_pages < 1 || c.max_batch < 1 || c.max_pages_per_seq < 1) return bad("pool/batch sizes must be >= 1");
+  if (c.max_write_rows < 16) return bad("max_write_rows must be >= 16");
+  if (!(c.rms_eps > 0.f) || !(c.rope_theta > 1.f)) return bad("rms_eps must be > 0 and rope_theta > 1");
+  if (c.rope_yarn && (!(c.yarn_factor >= 1.f) || !(c.yarn_orig_max_pos > 0.f) || !(c.yarn_beta_fast > 0.f) ||
+                      !(c.yarn_beta_slow > 0.f)))
+    return bad("bad YaRN parameters");
+  for (int l = 0; l < c.n_layers; ++l)
+    if (c.layer_sliding[l] && c.sliding_window <= 0) return bad("sliding layer with sliding_window <= 0");
+  if ((int64_t)c.max_pages_per_seq * kPage > (1ll << 30)) return bad("max_pages_per_seq too large");
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_last_error(const dflash_handle* h) { return h ? h->err.c_str() : g_create_error.c_str(); }
+
+int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream stream, dflash_handle** out) {
+  g_create_error.clear();
+  if (!cfg || !w || !out) return fail(nullptr, DFLASH_EINVAL, "null argument");
+  *out = nullptr;
+  int rc = check_cfg(*cfg);
+  if (rc) return rc;
+  const dflash_cfg& c = *cfg;
+  if (!w->fc || !w->hidden_norm || !w->norm || !w->embed || !w->lm_head || !w->layers)
+    return fail(nullptr, DFLASH_EINVAL, "null weight pointer");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& lw = w->layers[l];
+    if (!lw.ln_in || !lw.wq || !lw.wk || !lw.wv || !lw.q_norm || !lw.k_norm || !lw.wo || !lw.ln_post ||
+        !lw.w_gate || !lw.w_up || !lw.w_down)
+      return fail(nullptr, DFLASH_EINVAL, "null layer weight pointer");
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  dflash_handle* h = new dflash_handle();
+  h->cfg = c;
+  h->esz = c.dtype == DFLASH_F32 ? 4 : 2;
+  auto bail = [&](int code) {
+    g_create_error = h->err;
+    cudaStreamSynchronize(st);
+    free_all(h);
+    delete h;
+    return code;
+  };
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    fail(h, DFLASH_ECUDA, "no CUDA device");
+    return bail(DFLASH_ECUDA);
+  }
+  const size_t es = h->esz;
+  const int64_t H = c.hidden, hd = c.head_dim, nh = c.n_q_heads, nkv = c.n_kv_heads, F = c.n_ff, V = c.vocab;
+  const int64_t qd = nh * hd, kvd = nkv * hd, qkvd = qd + 2 * kvd, L = c.n_layers;
+  const int64_t tapd = (int64_t)c.n_taps * c.target_hidden;
+
+#define ALLOC(dst, bytes)                                                   \
+  do {                                                                      \
+    (dst) = (decltype(dst))dev_alloc(h, (bytes));                           \
+    if (!(dst)) {                                                           \
+      fail(h, DFLASH_ENOMEM, "cudaMalloc failed: " #dst);                   \
+      return bail(DFLASH_ENOMEM);                                           \
+    }                                                                       \
+  } while (0)
+#define D2D(dst, src, bytes)                                                                 \
+  do {                                                                                       \
+    cudaError_t e_ = cudaMemcpyAsync((dst), (src), (bytes), cudaMemcpyDeviceToDevice, st);   \
+    if (e_ != cudaSuccess) {                                                                 \
+      cuda_fail(h, e_, "weight copy");                                                       \
+      return bail(DFLASH_ECUDA);                                                             \
+    }                                                                                        \
+  } while (0)
+
+  // ---- weights: copy + repack (layer tensors), borrow embed / lm_head
+  ALLOC(h->fc, H * tapd * es);
+  D2D(h->fc, w->fc, H * tapd * es);
+  ALLOC(h->hidden_norm, H * es);
+  D2D(h->hidden_norm, w->hidden_norm, H * es);
+  ALLOC(h->norm, H * es);
+  D2D(h->norm, w->norm, H * es);
+  h->embed = w->embed;
+  h->lm_head = w->lm_head;
+  ALLOC(h->w_ctxkv, L * 2 * kvd * H * es);
+  ALLOC(h->kn_all, L * hd * es);
+  for (int l = 0; l < L; ++l) {
+    const dflash_layer_weights& lw = w->layers[l];
+    LayerW& d = h->layer[l];
+    ALLOC(d.ln_in, H * es);
+    D2D(d.ln_in, lw.ln_in, H * es);
+    ALLOC(d.ln_post, H * es);
+    D2D(d.ln_post, lw.ln_post, H * es);
+    ALLOC(d.q_norm, hd * es);
+    D2D(d.q_norm, lw.q_norm, hd * es);
+    ALLOC(d.k_norm, hd * es);
+    D2D(d.k_norm, lw.k_norm, hd * es);
+    ALLOC(d.w_qkv, qkvd * H * es);
+    D2D(d.w_qkv, lw.wq, qd * H * es);
+    D2D((char*)d.w_qkv + qd * H * es, lw.wk, kvd * H * es);
+    D2D((char*)d.w_qkv + (qd + kvd) * H * es, lw.wv, kvd * H * es);
+    ALLOC(d.w_o, H * qd * es);
+    D2D(d.w_o, lw.wo, H * qd * es);
+    ALLOC(d.w_gu, 2 * F * H * es);
+    D2D(d.w_gu, lw.w_gate, F * H * es);
+    D2D((char*)d.w_gu + F * H * es, lw.w_up, F * H * es);
+    ALLOC(d.w_down, H * F * es);
+    D2D(d.w_down, lw.w_down, H * F * es);
+    // fused context K/V weight [K_0; V_0; K_1; V_1; ...] (from_weights.rs fused K/V block)
+    D2D((char*)h->w_ctxkv + (2 * l) * kvd * H * es, lw.wk, kvd * H * es);
+    D2D((char*)h->w_ctxkv + (2 * l + 1) * kvd * H * es, lw.wv, kvd * H * es);
+    D2D((char*)h->kn_all + l * hd * es, lw.k_norm, hd * es);
+  }
+
+  // ---- RoPE table
+  std::vector<double> inv_pi;
+  rope_table(c, inv_pi, h->rope_mscale);
+  ALLOC(h->rope_inv_pi, inv_pi.size() * sizeof(double));
+  {
+    cudaError_t e = cudaMemcpyAsync(h->rope_inv_pi, inv_pi.data(), inv_pi.size() * sizeof(double),
+                                    cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) { cuda_fail(h, e, "rope table"); return bail(DFLASH_ECUDA); }
+  }
+
+  // ---- paged pool
+  PoolGeom& g = h->geom;
+  g.tile = kPage * hd;
+  g.head_stride = g.tile;
+  g.kv_stride = nkv * g.tile;
+  g.page_stride = 2 * nkv * g.tile;
+  g.layer_stride = (int64_t)c.num_pages * g.page_stride;
+  g.num_pages = c.num_pages;
+  g.nkv = (int)nkv;
+  g.hd = (int)hd;
+  h->pool_bytes = (size_t)(L * g.layer_stride) * es;
+  ALLOC(h->pool, h->pool_bytes);
+  if (cudaMemsetAsync(h->pool, 0, h->pool_bytes, st) != cudaSuccess) {
+    fail(h, DFLASH_ECUDA, "pool memset");
+    return bail(DFLASH_ECUDA);
+  }
+
+  // ---- scratch
+  h->rows_max = c.max_batch * kGamma;
+  const int64_t R = h->rows_max, Rw = c.max_write_rows;
+  const int64_t ymax = std::max(std::max(qkvd, 2 * F), H);
+  ALLOC(h->x, R * H * 4);
+  ALLOC(h->xn, R * H * es);
+  ALLOC(h->y, R * ymax * 4);
+  ALLOC(h->q, R * qd * es);
+  ALLOC(h->attn, R * qd * es);
+  ALLOC(h->act, R * F * es);
+  ALLOC(h->logits32, R * V * 4);
+  ALLOC(h->wy, Rw * std::max(H, L * 2 * kvd) * 4);
+  ALLOC(h->wf, Rw * H * es);
+  ALLOC(h->d_status, sizeof(unsigned));
+  if (cudaMemsetAsync(h->d_status, 0, sizeof(unsigned), st) != cudaSuccess) {
+    fail(h, DFLASH_ECUDA, "status memset");
+    return bail(DFLASH_ECUDA);
+  }
+
+  // ---- FP8 lm_head (from_weights.rs FP8 block; quantised once here)
+  if (c.lm_head_dtype == DFLASH_FP8E4M3_ROWSCALE) {
+    ALLOC(h->lm_fp8, V * H);
+    ALLOC(h->lm_scale, V * 4);
+    cudaError_t e = launch_quantize_fp8(w->lm_head, (int)V, (int)H, c.dtype, h->lm_fp8, h->lm_scale, st);
+    if (e != cudaSuccess) { cuda_fail(h, e, "fp8 quantise"); return bail(DFLASH_ECUDA); }
+  }
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) { cuda_fail(h, e, "create"); return bail(DFLASH_ECUDA); }
+  *out = h;
+  return DFLASH_OK;
+#undef ALLOC
+#undef D2D
+}
+
+int dflash_destroy(dflash_handle* h) {
+  if (!h) return DFLASH_OK;
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+  return DFLASH_OK;
+}
+
+int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* positions, const int32_t* page_table,
+                        int32_t first, int32_t n, dflash_stream stream) {
+  if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
+  h->err.clear();
+  const dflash_cfg& c = h->cfg;
+  if (n < 0 || first < 0) return fail(h, DFLASH_EINVAL, "first and n must be >= 0");
+  if ((int64_t)first + n > (int64_t)kPage * c.max_pages_per_seq)
+    return fail(h, DFLASH_ECAPACITY, "first + n beyond the page-table capacity (16 * max_pages_per_seq)");
+  if (n == 0) return DFLASH_OK;
+  if (!taps || !positions || !page_table) return fail(h, DFLASH_EINVAL, "null pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t H = c.hidden, tapd = (int64_t)c.n_taps * c.target_hidden;
+  const int kvall = c.n_layers * 2 * c.n_kv_heads * c.head_dim;
+  for (int32_t done = 0; done < n; done += c.max_write_rows) {
+    const int m = std::min<int32_t>(c.max_write_rows, n - done);
+    const void* tp = static_cast<const char*>(taps) + (int64_t)done * tapd * h->esz;
+    // f = hidden_norm(fc . taps)  (dflash.rs ctx_features)
+    KL(K_W_FC, launch_gemm(h, tp, (int)tapd, h->fc, m, (int)H, (int)tapd, h->wy, (int)H, false, st), "writer fc");
+    KL(K_W_NORM, launch_rmsnorm_f32in(h, h->wy, h->hidden_norm, h->wf, m, (int)H, st), "writer hidden_norm");
+    // every layer's K and V in one GEMM over the fused weight, then k_norm / RoPE / scatter
+    KL(K_W_KV, launch_gemm(h, h->wf, (int)H, h->w_ctxkv, m, kvall, (int)H, h->wy, kvall, false, st), "writer kv");
+    KL(K_W_POST, launch_ctxkv_post(h, h->wy, m, positions + done, page_table, first + done, st), "writer post");
+  }
+  return DFLASH_OK;
+}
+
+int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens,
+                   const int32_t* page_tables, int32_t nb, int32_t max_ctx_len, int32_t* draft_tokens,
+                   void* logits, void* final_hidden, dflash_stream stream) {
+  if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
+  h->err.clear();
+  const dflash_cfg& c = h->cfg;
+  if (nb < 1) return fail(h, DFLASH_EINVAL, "nb must be >= 1");
+  if (nb > c.max_batch) return fail(h, DFLASH_ECAPACITY, "nb > max_batch");
+  if (max_ctx_len < 0) return fail(h, DFLASH_EINVAL, "max_ctx_len must be >= 0");
+  if ((int64_t)max_ctx_len + kGamma > (int64_t)kPage * c.max_pages_per_seq)
+    return fail(h, DFLASH_ECAPACITY, "max_ctx_len + gamma beyond the page-table capacity");
+  if (!bonus_tokens || !ctx_lens || !page_tables || !draft_tokens) return fail(h, DFLASH_EINVAL, "null pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int M = nb * kGamma;
+  const int H = c.hidden, F = c.n_ff, qd = c.n_q_heads * c.head_dim;
+  const int qkvd = qd + 2 * c.n_kv_heads * c.head_dim;
+
+  KL(K_EMBED, launch_embed(h, bonus_tokens, nb, h->x, st), "embed");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& w = h->layer[l];
+    KL(K_NORM, launch_rmsnorm_f32in(h, h->x, w.ln_in, h->xn, M, H, st), "ln_in");
+    KL(K_QKV, launch_gemm(h, h->xn, H, w.w_qkv, M, qkvd, H, h->y, qkvd, false, st), "qkv");
+    KL(K_QKV_POST, launch_qkv_post(h, l, h->y, ctx_lens, page_tables, nb, h->q, st), "qkv post");
+    KL(K_ATTN, launch_attention(h, l, h->q, ctx_lens, page_tables, nb, max_ctx_len, h->attn, st), "attention");
+    KL(K_OPROJ, launch_gemm(h, h->attn, qd, w.w_o, M, H, qd, h->x, H, true, st), "o_proj");
+    KL(K_NORM, launch_rmsnorm_f32in(h, h->x, w.ln_post, h->xn, M, H, st), "ln_post");
+    KL(K_GATEUP, launch_gemm(h, h->xn, H, w.w_gu, M, 2 * F, H, h->y, 2 * F, false, st), "gate/up");
+    KL(K_SILU, launch_silu_mul(h, h->y, M, h->act, st), "silu_mul");
+    KL(K_DOWN, launch_gemm(h, h->act, F, w.w_down, M, H, F, h->x, H, true, st), "down");
+  }
+  KL(K_NORM, launch_rmsnorm_f32in(h, h->x, h->norm, h->xn, M, H, st), "final norm");
+  if (final_hidden) KL(K_COPY, launch_copy_hidden(h, h->xn, M, final_hidden, st), "final hidden");
+  if (c.lm_head_dtype == DFLASH_FP8E4M3_ROWSCALE)
+    KL(K_LMHEAD, launch_gemm_fp8w(h, h->xn, H, h->lm_fp8, h->lm_scale, M, c.vocab, H, h->logits32, c.vocab, st), "lm_head");
+  else
+    KL(K_LMHEAD, launch_gemm(h, h->xn, H, h->lm_head, M, c.vocab, H, h->logits32, c.vocab, false, st), "lm_head");
+  KL(K_ARGMAX, launch_argmax(h, h->logits32, nb, draft_tokens, logits, st), "argmax");
+  return DFLASH_OK;
+}
+
+int dflash_kv_layout(const dflash_handle* h, void** pool, size_t* bytes, int64_t strides[6]) {
+  if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
+  if (pool) *pool = h->pool;
+  if (bytes) *bytes = h->pool_bytes;
+  if (strides) {
+    strides[0] = h->geom.layer_stride;
+    strides[1] = h->geom.page_stride;
+    strides[2] = h->geom.kv_stride;
+    strides[3] = h->geom.head_stride;
+    strides[4] = h->geom.tile;
+    strides[5] = (int64_t)h->esz;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_profile(dflash_handle* h, int enable) {
+  if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
+  prof_drain(h);
+  for (int k = 0; k < K_COUNT; ++k) {
+    h->prof.launches[k] = 0;
+    h->prof.ms[k] = 0.0;
+  }
+  h->prof.on = enable != 0;
+  return DFLASH_OK;
+}
+
+int dflash_profile_kinds(void) { return K_COUNT; }
+
+int dflash_profile_read(dflash_handle* h, int kind, const char** name, double* total_ms, int64_t* launches) {
+  if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
+  if (kind < 0 || kind >= K_COUNT) return fail(h, DFLASH_EINVAL, "kernel kind out of range");
+  prof_drain(h);
+  if (name) *name = kKindNames[kind];
+  if (total_ms) *total_ms = h->prof.ms[kind];
+  if (launches) *launches = h->prof.launches[kind];
+  return DFLASH_OK;
+}
+
+int dflash_fp8_lm_head(const dflash_handle* h, const uint8_t** codes, const float** scales) {
+  if (!h || !codes || !scales) return fail(nullptr, DFLASH_EINVAL, "null argument");
+  if (!h->lm_fp8) return DFLASH_EINVAL;
+  *codes = h->lm_fp8;
+  *scales = h->lm_scale;
+  return DFLASH_OK;
+}
+
+int dflash_device_status(dflash_handle* h, dflash_stream stream, uint32_t* flags) {
+  if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  CK(cudaMemcpyAsync(&v, h->d_status, sizeof(unsigned), cudaMemcpyDeviceToHost, st), "status read");
+  CK(cudaMemsetAsync(h->d_status, 0, sizeof(unsigned), st), "status clear");
+  CK(cudaStreamSynchronize(st), "status sync");
+  if (flags) *flags = v;
+  if (v) return fail(h, DFLASH_EDEVICE, "device-side check fired (see flags)");
+  return DFLASH_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,159 @@
+// Internal declarations shared by the library's translation units: the handle, the
+// paged-pool addressing, small device helpers and the kernel launchers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "dflash.h"
+
+namespace dflash {
+
+constexpr int kPage = 16;     // rows per K/V page (from_weights.rs paged pool: block size 16)
+constexpr int kGamma = 16;    // block rows (drafts = gamma - 1)
+
+// ---------------------------------------------------------------- paged pool addressing
+// Pool = [layer][page][kv][kv_head] tiles of 16 x hd elements.  Inside a tile the rows
+// (page offset j) and head dims d are stored in 8x8 blocks, the operand layout of the
+// tensor-core attention kernel (K: keys x dims, dims fastest; V: dims x keys, keys fastest).
+__host__ __device__ inline int64_t k_in_tile(int j, int d, int hd) {
+  return (int64_t)(((j >> 3) * (hd >> 3) + (d >> 3)) * 64 + (j & 7) * 8 + (d & 7));
+}
+__host__ __device__ inline int64_t v_in_tile(int j, int d, int /*hd*/) {
+  return (int64_t)(((d >> 3) * 2 + (j >> 3)) * 64 + (d & 7) * 8 + (j & 7));
+}
+
+struct PoolGeom {
+  int64_t tile;        // elements per tile: 16 * hd
+  int64_t head_stride; // = tile
+  int64_t kv_stride;   // = nkv * tile
+  int64_t page_stride; // = 2 * nkv * tile
+  int64_t layer_stride;// = num_pages * page_stride
+  int num_pages;
+  int nkv, hd;
+};
+
+__host__ __device__ inline int64_t tile_base(const PoolGeom& g, int layer, int page, int kv, int head) {
+  return layer * g.layer_stride + (int64_t)page * g.page_stride + kv * g.kv_stride + head * g.head_stride;
+}
+
+// ---------------------------------------------------------------- element conversions
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  __device__ static float load(const float* p) { return *p; }
+  __device__ static float to_f(float v) { return v; }
+  __device__ static float from_f(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  __device__ static float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  __device__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// ---------------------------------------------------------------- profiling
+enum Kind {
+  K_EMBED, K_NORM, K_QKV, K_QKV_POST, K_ATTN, K_OPROJ, K_GATEUP, K_SILU, K_DOWN, K_LMHEAD, K_ARGMAX,
+  K_COPY, K_W_FC, K_W_NORM, K_W_KV, K_W_POST, K_COUNT
+};
+static const char* const kKindNames[K_COUNT] = {
+    "embed", "rmsnorm", "qkv_gemm", "qkv_post", "attention", "o_proj_gemm", "gate_up_gemm", "silu_mul",
+    "down_gemm", "lm_head", "argmax", "copy", "writer_fc_gemm", "writer_norm", "writer_kv_gemm", "writer_post"};
+
+struct Prof {
+  bool on = false;
+  int64_t launches[K_COUNT] = {};
+  double ms[K_COUNT] = {};
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> pending;
+  std::vector<cudaEvent_t> spare;
+};
+
+// ---------------------------------------------------------------- the handle
+struct LayerW {
+  void* ln_in = nullptr;
+  void* ln_post = nullptr;
+  void* q_norm = nullptr;
+  void* k_norm = nullptr;
+  void* w_qkv = nullptr;   // [(nh + 2 nkv) hd, H]: q rows, then k rows, then v rows
+  void* w_o = nullptr;     // [H, nh hd]
+  void* w_gu = nullptr;    // [2F, H]: gate rows then up rows
+  void* w_down = nullptr;  // [H, F]
+};
+
+}  // namespace dflash
+
+struct dflash_handle {
+  dflash_cfg cfg{};
+  int device = 0;
+  int num_sms = 0;
+  size_t esz = 2;                      // bytes per element of cfg.dtype
+  std::vector<void*> allocs;           // every library-owned device buffer
+
+  // weights
+  void* fc = nullptr;                  // [H, n_taps * Ht]
+  void* hidden_norm = nullptr;         // [H]
+  void* norm = nullptr;                // [H]
+  const void* embed = nullptr;         // [V, H] borrowed
+  const void* lm_head = nullptr;       // [V, H] borrowed (cfg.dtype)
+  uint8_t* lm_fp8 = nullptr;           // [V, H] e4m3 codes (owned) when FP8
+  float* lm_scale = nullptr;           // [V]
+  void* w_ctxkv = nullptr;             // [L * 2 * kv, H]: K_0, V_0, K_1, V_1, ...
+  void* kn_all = nullptr;              // [L, hd] every layer's k_norm (writer epilogue)
+  dflash::LayerW layer[64];
+  double* rope_inv_pi = nullptr;       // [hd/2] inv_freq_j / pi (float64)
+  float rope_mscale = 1.f;
+
+  // paged K/V pool
+  void* pool = nullptr;
+  size_t pool_bytes = 0;
+  dflash::PoolGeom geom{};
+
+  // propose scratch (rows = max_batch * gamma)
+  int rows_max = 0;
+  float* x = nullptr;                  // [rows, H] residual stream, fp32
+  void* xn = nullptr;                  // [rows, H] normed activations (cfg.dtype)
+  float* y = nullptr;                  // [rows, ymax] fp32 projection outputs
+  void* q = nullptr;                   // [rows, nh hd]
+  void* attn = nullptr;                // [rows, nh hd]
+  void* act = nullptr;                 // [rows, F]
+  float* logits32 = nullptr;           // [rows, V] fp32 logits
+  // writer scratch (rows = max_write_rows)
+  float* wy = nullptr;                 // [Rw, max(H, L*2*kv)] fp32
+  void* wf = nullptr;                  // [Rw, H] ctx features (cfg.dtype)
+
+  unsigned* d_status = nullptr;        // device status word
+  dflash::Prof prof;
+  std::string err;
+};
+
+namespace dflash {
+
+// ---------------------------------------------------------------- launchers (kernels_simple.cu)
+// All launchers are stream-ordered and return cudaGetLastError() of the launch.
+cudaError_t launch_embed(const dflash_handle* h, const int32_t* bonus, int nb, float* x, cudaStream_t st);
+cudaError_t launch_rmsnorm_f32in(const dflash_handle* h, const float* x, const void* w, void* out,
+                                 int rows, int n, cudaStream_t st);
+// Y[m, n] (+)= sum_k X[m, k] W[n, k]; X, W in cfg.dtype; Y fp32 with row stride ldy.
+cudaError_t launch_gemm(const dflash_handle* h, const void* X, int ldx, const void* W, int M, int N,
+                        int K, float* Y, int ldy, bool accumulate, cudaStream_t st);
+cudaError_t launch_gemm_fp8w(const dflash_handle* h, const void* X, int ldx, const uint8_t* Wq,
+                             const float* scale, int M, int N, int K, float* Y, int ldy,
+                             cudaStream_t st);
+cudaError_t launch_qkv_post(const dflash_handle* h, int layer, const float* y, const int32_t* ctx_lens,
+                            const int32_t* page_tables, int nb, void* q, cudaStream_t st);
+cudaError_t launch_attention(const dflash_handle* h, int layer, const void* q, const int32_t* ctx_lens,
+                             const int32_t* page_tables, int nb, int max_ctx_len, void* out,
+                             cudaStream_t st);
+cudaError_t launch_silu_mul(const dflash_handle* h, const float* y, int rows, void* act, cudaStream_t st);
+cudaError_t launch_argmax(const dflash_handle* h, const float* logits32, int nb, int32_t* drafts,
+                          void* logits_out, cudaStream_t st);
+cudaError_t launch_copy_hidden(const dflash_handle* h, const void* src, int rows, void* dst, cudaStream_t st);
+cudaError_t launch_ctxkv_post(const dflash_handle* h, const float* ykv, int n, const int32_t* positions,
+                              const int32_t* page_table, int first, cudaStream_t st);
+cudaError_t launch_quantize_fp8(const void* w, int rows, int cols, int dtype, uint8_t* codes,
+                                float* scale, cudaStream_t st);
+
+}  // namespace dflash

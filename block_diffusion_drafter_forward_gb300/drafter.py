@@ -1,0 +1,99 @@
+"""Python handle over the C ABI: keeps the device weights alive (the embedding and the
+lm_head are borrowed by the library) and passes torch device buffers as raw pointers.
+PyTorch only provides device memory and streams here."""
+from __future__ import annotations
+
+from typing import Dict, Optional, Tuple
+
+import torch
+
+from . import _lib as L
+
+_DT = {"f32": L.DFLASH_F32, "bf16": L.DFLASH_BF16, "fp8": L.DFLASH_FP8E4M3_ROWSCALE}
+TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+LAYER_TENSORS = ("ln_in", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "ln_post", "w_gate", "w_up", "w_down")
+
+
+def make_cfg(cfg, num_pages: int, max_batch: int, max_pages_per_seq: int, max_write_rows: int = 4096) -> L.dflash_cfg:
+    """dflash_cfg from a config object carrying the drafter's shape attributes."""
+    c = L.dflash_cfg()
+    for f in ("hidden", "n_q_heads", "n_kv_heads", "head_dim", "n_ff", "n_layers", "vocab", "gamma",
+              "mask_token_id", "n_taps", "target_hidden"):
+        setattr(c, f, int(getattr(cfg, f)))
+    c.rms_eps = float(cfg.rms_eps)
+    c.rope_theta = float(cfg.rope_theta)
+    if cfg.yarn is not None:
+        c.rope_yarn = 1
+        c.yarn_factor, c.yarn_orig_max_pos, c.yarn_beta_fast, c.yarn_beta_slow = (float(v) for v in cfg.yarn)
+    c.sliding_window = int(cfg.sliding_window)
+    for i, s in enumerate(cfg.layer_sliding or ()):
+        c.layer_sliding[i] = 1 if s else 0
+    c.dtype = _DT[cfg.dtype]
+    c.lm_head_dtype = _DT[cfg.lm_head_dtype]
+    c.page_size = int(cfg.page_size)
+    c.num_pages = int(num_pages)
+    c.max_batch = int(max_batch)
+    c.max_pages_per_seq = int(max_pages_per_seq)
+    c.max_write_rows = int(max_write_rows)
+    return c
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    return (stream or torch.cuda.current_stream()).cuda_stream
+
+
+class Drafter:
+    """One drafter handle.  `tensors` maps fc, hidden_norm, norm, embed, lm_head and
+    L{l}.{ln_in, wq, ...} to contiguous device tensors of the config's dtype."""
+
+    def __init__(self, cfg, tensors: Dict[str, torch.Tensor], num_pages: int, max_batch: int,
+                 max_pages_per_seq: int, max_write_rows: int = 4096, stream=None):
+        self.cfg = cfg
+        self.tensors = tensors
+        self.ccfg = make_cfg(cfg, num_pages, max_batch, max_pages_per_seq, max_write_rows)
+        layers = (L.dflash_layer_weights * cfg.n_layers)()
+        for l in range(cfg.n_layers):
+            for t in LAYER_TENSORS:
+                setattr(layers[l], t, tensors[f"L{l}.{t}"].data_ptr())
+        self._layers = layers
+        w = L.dflash_weights()
+        for t in ("fc", "hidden_norm", "norm", "embed", "lm_head"):
+            setattr(w, t, tensors[t].data_ptr())
+        w.layers = layers
+        self._w = w
+        self.handle = L.dflash_create(self.ccfg, w, _stream(stream))
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            L.dflash_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def write_ctx_kv(self, taps: torch.Tensor, positions: torch.Tensor, page_table: torch.Tensor, first: int,
+                     stream=None) -> None:
+        n = int(taps.shape[0])
+        L.dflash_write_ctx_kv(self.handle, taps.data_ptr(), positions.data_ptr(), page_table.data_ptr(), first, n,
+                              _stream(stream))
+
+    def propose(self, bonus: torch.Tensor, ctx_lens: torch.Tensor, page_tables: torch.Tensor, max_ctx_len: int,
+                drafts: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+                hidden: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        nb = int(bonus.shape[0])
+        dev = bonus.device
+        if drafts is None:
+            drafts = torch.empty((nb, self.cfg.gamma - 1), dtype=torch.int32, device=dev)
+        L.dflash_propose(self.handle, bonus.data_ptr(), ctx_lens.data_ptr(), page_tables.data_ptr(), nb,
+                         int(max_ctx_len), drafts.data_ptr(), logits.data_ptr() if logits is not None else 0,
+                         hidden.data_ptr() if hidden is not None else 0, _stream(stream))
+        return drafts
+
+    def kv_layout(self) -> Tuple[int, int, Tuple[int, ...]]:
+        return L.dflash_kv_layout(self.handle)
+
+    def device_status(self, stream=None) -> int:
+        return L.dflash_device_status(self.handle, _stream(stream))
