@@ -25,6 +25,7 @@ DFLASH_FP8E4M3_ROWSCALE = 2
 DFLASH_DEV_BAD_PAGE = 0x1
 DFLASH_DEV_BAD_CTX = 0x2
 DFLASH_DEV_BAD_TOKEN = 0x4
+DFLASH_DEV_TIMEOUT = 0x8
 
 STATUS_NAMES = {0: "OK", -1: "EINVAL", -2: "ENOMEM", -3: "ECUDA", -4: "ECAPACITY", -5: "EUNSUPPORTED",
                 -6: "EDEVICE"}
@@ -65,7 +66,7 @@ class dflash_weights(ctypes.Structure):
 
 EXPORTS = ("dflash_create", "dflash_destroy", "dflash_write_ctx_kv", "dflash_propose", "dflash_kv_layout",
            "dflash_device_status", "dflash_last_error", "dflash_fp8_lm_head", "dflash_profile",
-           "dflash_profile_kinds", "dflash_profile_read")
+           "dflash_profile_kinds", "dflash_profile_read", "dflash_gemm_bf16")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -100,6 +101,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_profile_read.argtypes = [vp, c.c_int, c.POINTER(c.c_char_p), c.POINTER(c.c_double),
                                         c.POINTER(c.c_int64)]
     lib.dflash_profile_read.restype = c.c_int
+    lib.dflash_gemm_bf16.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp]
+    lib.dflash_gemm_bf16.restype = c.c_int
     lib.dflash_last_error.argtypes = [vp]
     lib.dflash_last_error.restype = c.c_char_p
     _lib = lib
@@ -184,3 +187,9 @@ def dflash_profile_read(handle: int) -> dict:
                                        ctypes.byref(n)), ctypes.c_void_p(handle))
         out[name.value.decode()] = (ms.value, n.value)
     return out
+
+
+def dflash_gemm_bf16(W: int, N: int, K: int, X: int, M: int, out: int, stream: int = 0) -> None:
+    """out[M, N] fp32 = X[M, K] . W[N, K]^T on the tensor-core GEMM (device pointers)."""
+    _check(load().dflash_gemm_bf16(ctypes.c_void_p(W), N, K, ctypes.c_void_p(X), M, ctypes.c_void_p(out), 1,
+                                   ctypes.c_void_p(stream)), None)

@@ -9,6 +9,7 @@
 #include <string>
 
 #include "dflash_internal.cuh"
+#include "gemm_tc.cuh"
 
 using namespace dflash;
 
@@ -119,6 +120,8 @@ void rope_table(const dflash_cfg& c, std::vector<double>& inv_pi, float& mscale)
   }
 }
 
+constexpr int64_t kCounters = 16384;  // split-K tile counters; the last 64 count argmax tiles
+
 int check_cfg(const dflash_cfg& c) {
   auto bad = [](const char* m) { return fail(nullptr, DFLASH_EINVAL, m); };
   if (c.hidden <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.head_dim <= 0 || c.n_ff <= 0 ||
@@ -142,6 +145,97 @@ int check_cfg(const dflash_cfg& c) {
   for (int l = 0; l < c.n_layers; ++l)
     if (c.layer_sliding[l] && c.sliding_window <= 0) return bad("sliding layer with sliding_window <= 0");
   if ((int64_t)c.max_pages_per_seq * kPage > (1ll << 30)) return bad("max_pages_per_seq too large");
+  return DFLASH_OK;
+}
+
+// The bf16 gamma-block forward on the tensor-core kernels (dflash.rs forward_round +
+// final norm + lm_head + argmax).  Every projection is one tcgen05 GEMM launch with its
+// epilogue fused; launches after the first may start early (programmatic dependent launch)
+// and prefetch their weights while the previous kernel drains.
+int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens, const int32_t* page_tables,
+               int nb, int max_ctx_len, int32_t* draft_tokens, void* logits, void* final_hidden, cudaStream_t st) {
+  const dflash_cfg& c = h->cfg;
+  const int M = nb * kGamma;
+  const int H = c.hidden, F = c.n_ff, qd = c.n_q_heads * c.head_dim;
+  const int qkvd = qd + 2 * c.n_kv_heads * c.head_dim;
+  const int Mp = h->rows_max;
+  const int tn = pick_tn(M);
+  auto splits = [&](int N, int K) {
+    const int tiles = ((N + 127) / 128) * ((M + tn - 1) / tn);
+    return pick_splits(tiles, K / 64, h->num_sms);
+  };
+  GemmParams base;
+  base.ws = h->ws;
+  base.counters = h->counters;
+  base.status = h->d_status;
+  base.Mp = Mp;
+  base.eps = c.rms_eps;
+  base.ss_n = H;
+
+  KL(K_EMBED, launch_embed_tc(h, bonus_tokens, nb, st), "embed");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& w = h->layer[l];
+    {
+      GemmParams p = base;
+      p.ss_in = h->ss_b;
+      p.ss_parts = H / 128;
+      p.q = static_cast<__nv_bfloat16*>(h->q);
+      p.q_norm = static_cast<const __nv_bfloat16*>(w.q_norm);
+      p.k_norm = static_cast<const __nv_bfloat16*>(w.k_norm);
+      p.inv_pi = h->rope_inv_pi;
+      p.mscale = h->rope_mscale;
+      p.nh = c.n_q_heads;
+      p.nkv = c.n_kv_heads;
+      p.ctx_lens = ctx_lens;
+      p.page_tables = page_tables;
+      p.mpps = c.max_pages_per_seq;
+      p.g = h->geom;
+      p.layer = l;
+      p.pool = static_cast<__nv_bfloat16*>(h->pool);
+      KL(K_QKV, launch_gemm_tc(EPI_QKV, w.w_qkv, qkvd, H, h->xb, H, M, p, splits(qkvd, H), st, l > 0), "qkv");
+    }
+    KL(K_ATTN, launch_attention(h, l, h->q, ctx_lens, page_tables, nb, max_ctx_len, h->attn, st), "attention");
+    {
+      GemmParams p = base;
+      p.x = h->x;
+      p.xb = static_cast<__nv_bfloat16*>(h->xb);
+      p.ss_out = h->ss_a;
+      p.H = H;
+      KL(K_OPROJ, launch_gemm_tc(EPI_RESID, w.w_o, H, qd, h->attn, qd, M, p, splits(H, qd), st, false), "o_proj");
+    }
+    {
+      GemmParams p = base;
+      p.ss_in = h->ss_a;
+      p.ss_parts = H / 128;
+      p.act = static_cast<__nv_bfloat16*>(h->act);
+      p.F = F;
+      KL(K_GATEUP, launch_gemm_tc(EPI_GATEUP, w.w_gu, 2 * F, H, h->xb, H, M, p, splits(2 * F, H), st, true),
+         "gate/up");
+    }
+    {
+      GemmParams p = base;
+      p.x = h->x;
+      p.xb = static_cast<__nv_bfloat16*>(h->xb);
+      p.ss_out = h->ss_b;
+      p.H = H;
+      KL(K_DOWN, launch_gemm_tc(EPI_RESID, w.w_down, H, F, h->act, F, M, p, splits(H, F), st, true), "down");
+    }
+  }
+  KL(K_NORM, launch_rmsnorm_f32in(h, h->x, h->norm, h->xn, M, H, st), "final norm");
+  if (final_hidden) KL(K_COPY, launch_copy_hidden(h, h->xn, M, final_hidden, st), "final hidden");
+  if (c.lm_head_dtype == DFLASH_FP8E4M3_ROWSCALE) {
+    KL(K_LMHEAD, launch_gemm_fp8w(h, h->xn, H, h->lm_fp8, h->lm_scale, M, c.vocab, H, h->logits32, c.vocab, st),
+       "lm_head");
+    KL(K_ARGMAX, launch_argmax(h, h->logits32, nb, draft_tokens, logits, st), "argmax");
+  } else {
+    GemmParams p = base;
+    p.logits = static_cast<__nv_bfloat16*>(logits);
+    p.amax_val = h->amax_val;
+    p.amax_idx = h->amax_idx;
+    p.amax_counter = h->counters + kCounters - 64;
+    p.drafts = draft_tokens;
+    KL(K_LMHEAD, launch_gemm_tc(EPI_LMHEAD, h->lm_head, c.vocab, H, h->xn, H, M, p, 1, st, false), "lm_head");
+  }
   return DFLASH_OK;
 }
 
@@ -182,6 +276,11 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
     fail(h, DFLASH_ECUDA, "no CUDA device");
     return bail(DFLASH_ECUDA);
+  }
+  h->tc = c.dtype == DFLASH_BF16;
+  if (h->tc && (c.head_dim != 128 || c.hidden % 128 || c.n_ff % 64 || c.target_hidden % 8)) {
+    fail(h, DFLASH_EUNSUPPORTED, "bf16 path needs head_dim 128, hidden % 128 == 0 and n_ff % 64 == 0");
+    return bail(DFLASH_EUNSUPPORTED);
   }
   const size_t es = h->esz;
   const int64_t H = c.hidden, hd = c.head_dim, nh = c.n_q_heads, nkv = c.n_kv_heads, F = c.n_ff, V = c.vocab;
@@ -234,8 +333,19 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     ALLOC(d.w_o, H * qd * es);
     D2D(d.w_o, lw.wo, H * qd * es);
     ALLOC(d.w_gu, 2 * F * H * es);
-    D2D(d.w_gu, lw.w_gate, F * H * es);
-    D2D((char*)d.w_gu + F * H * es, lw.w_up, F * H * es);
+    if (h->tc) {
+      // tensor-core path: input RMSNorm weights folded into the projections that read the
+      // normed activations (W' = W diag(ln)); gate/up interleaved in 64-row blocks
+      cudaError_t e1 = launch_fold_norm(d.w_qkv, nullptr, 0, (int)qkvd, (int)H, lw.ln_in, d.w_qkv, st);
+      cudaError_t e2 = launch_fold_norm(lw.w_gate, lw.w_up, 1, (int)(2 * F), (int)H, lw.ln_post, d.w_gu, st);
+      if (e1 != cudaSuccess || e2 != cudaSuccess) {
+        cuda_fail(h, e1 != cudaSuccess ? e1 : e2, "fold norms");
+        return bail(DFLASH_ECUDA);
+      }
+    } else {
+      D2D(d.w_gu, lw.w_gate, F * H * es);
+      D2D((char*)d.w_gu + F * H * es, lw.w_up, F * H * es);
+    }
     ALLOC(d.w_down, H * F * es);
     D2D(d.w_down, lw.w_down, H * F * es);
     // fused context K/V weight [K_0; V_0; K_1; V_1; ...] (from_weights.rs fused K/V block)
@@ -284,6 +394,35 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
   ALLOC(h->logits32, R * V * 4);
   ALLOC(h->wy, Rw * std::max(H, L * 2 * kvd) * 4);
   ALLOC(h->wf, Rw * H * es);
+  if (h->tc) {
+    ALLOC(h->xb, R * H * es);
+    ALLOC(h->ss_a, (H / 128) * R * 4);
+    ALLOC(h->ss_b, (H / 128) * R * 4);
+    ALLOC(h->amax_val, ((V + 127) / 128) * R * 4);
+    ALLOC(h->amax_idx, ((V + 127) / 128) * R * 4);
+    ALLOC(h->counters, kCounters * sizeof(unsigned));
+    if (cudaMemsetAsync(h->counters, 0, kCounters * sizeof(unsigned), st) != cudaSuccess) {
+      fail(h, DFLASH_ECUDA, "counter memset");
+      return bail(DFLASH_ECUDA);
+    }
+    // split-K workspace: the largest need over every projection and batch size
+    size_t need = 16;
+    const int64_t shapes[4][2] = {{qkvd, H}, {H, qd}, {2 * F, H}, {H, F}};
+    for (int64_t m = kGamma; m <= R; m += kGamma) {
+      const int tn = pick_tn((int)m);
+      for (auto& sh : shapes) {
+        const int64_t tiles = ((sh[0] + 127) / 128) * ((m + tn - 1) / tn);
+        const int ns = pick_splits((int)tiles, (int)(sh[1] / 64), h->num_sms);
+        if (tiles > kCounters - 64) {
+          fail(h, DFLASH_EUNSUPPORTED, "too many GEMM tiles");
+          return bail(DFLASH_EUNSUPPORTED);
+        }
+        if (ns > 1) need = std::max(need, (size_t)(tiles * ns * 128 * tn));
+      }
+    }
+    h->ws_floats = need;
+    ALLOC(h->ws, need * 4);
+  }
   ALLOC(h->d_status, sizeof(unsigned));
   if (cudaMemsetAsync(h->d_status, 0, sizeof(unsigned), st) != cudaSuccess) {
     fail(h, DFLASH_ECUDA, "status memset");
@@ -353,6 +492,8 @@ int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t*
     return fail(h, DFLASH_ECAPACITY, "max_ctx_len + gamma beyond the page-table capacity");
   if (!bonus_tokens || !ctx_lens || !page_tables || !draft_tokens) return fail(h, DFLASH_EINVAL, "null pointer");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (h->tc) return propose_tc(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits,
+                               final_hidden, st);
   const int M = nb * kGamma;
   const int H = c.hidden, F = c.n_ff, qd = c.n_q_heads * c.head_dim;
   const int qkvd = qd + 2 * c.n_kv_heads * c.head_dim;
@@ -415,6 +556,19 @@ int dflash_profile_read(dflash_handle* h, int kind, const char** name, double* t
   if (name) *name = kKindNames[kind];
   if (total_ms) *total_ms = h->prof.ms[kind];
   if (launches) *launches = h->prof.launches[kind];
+  return DFLASH_OK;
+}
+
+int dflash_gemm_bf16(const void* W, int32_t N, int32_t K, const void* X, int32_t M, float* out, int32_t nsplit,
+                     dflash_stream stream) {
+  if (!W || !X || !out) return fail(nullptr, DFLASH_EINVAL, "null pointer");
+  if (N < 1 || M < 1 || K < 64 || K % 64) return fail(nullptr, DFLASH_EINVAL, "need N, M >= 1 and K % 64 == 0");
+  if (nsplit != 1) return fail(nullptr, DFLASH_EINVAL, "nsplit must be 1 (no workspace)");
+  GemmParams p;
+  p.out = out;
+  p.ldo = N;
+  cudaError_t e = launch_gemm_tc(EPI_STORE, W, N, K, X, K, M, p, 1, reinterpret_cast<cudaStream_t>(stream), false);
+  if (e != cudaSuccess) return fail(nullptr, DFLASH_ECUDA, std::string("gemm: ") + cudaGetErrorString(e));
   return DFLASH_OK;
 }
 

@@ -124,6 +124,17 @@ struct dflash_handle {
   float* wy = nullptr;                 // [Rw, max(H, L*2*kv)] fp32
   void* wf = nullptr;                  // [Rw, H] ctx features (cfg.dtype)
 
+  // tensor-core (bf16) path scratch
+  void* xb = nullptr;                  // [rows, H] bf16 copy of the residual stream
+  float* ss_a = nullptr;               // [H/128, rows] partial sums of x^2 after o_proj
+  float* ss_b = nullptr;               // [H/128, rows] partial sums of x^2 after down_proj / embed
+  float* ws = nullptr;                 // split-K partials
+  size_t ws_floats = 0;
+  unsigned* counters = nullptr;        // split-K / argmax counters (zero between launches)
+  float* amax_val = nullptr;           // [V/128 tiles, rows] per-tile argmax partials
+  int* amax_idx = nullptr;
+  bool tc = false;                     // bf16 tensor-core path in use
+
   unsigned* d_status = nullptr;        // device status word
   dflash::Prof prof;
   std::string err;
@@ -153,6 +164,9 @@ cudaError_t launch_argmax(const dflash_handle* h, const float* logits32, int nb,
 cudaError_t launch_copy_hidden(const dflash_handle* h, const void* src, int rows, void* dst, cudaStream_t st);
 cudaError_t launch_ctxkv_post(const dflash_handle* h, const float* ykv, int n, const int32_t* positions,
                               const int32_t* page_table, int first, cudaStream_t st);
+cudaError_t launch_embed_tc(const dflash_handle* h, const int32_t* bonus, int nb, cudaStream_t st);
+cudaError_t launch_fold_norm(const void* A, const void* B, int mode, int rows, int cols, const void* ln, void* out,
+                             cudaStream_t st);
 cudaError_t launch_quantize_fp8(const void* w, int rows, int cols, int dtype, uint8_t* codes,
                                 float* scale, cudaStream_t st);
 

@@ -1,0 +1,528 @@
+// Weight-streaming projection GEMM on the 5th-generation tensor cores (tcgen05 + TMEM),
+// with the drafter's per-projection epilogues fused in.
+//
+// Orientation ("swap AB"): the weight W [N, K] is the A operand, so 128 weight rows fill
+// the UMMA M = 128 dimension, and the TN (16..256) token rows of the activation X [M, K]
+// are the N dimension.  The accumulator tile D[n, m] sits in TMEM, one weight row per
+// TMEM lane.  Tiles are staged by TMA (128-byte swizzle) through an mbarrier ring;
+// weights are requested before the programmatic-dependent-launch wait, so a kernel
+// streams its weights while its predecessor in the stream is still finishing.
+// Split-K: each split writes fp32 partials, the last split of a tile (atomic counter)
+// sums them in split order (deterministic) and runs the epilogue.
+//
+// Epilogues (memra-engine `dflash.rs` forward_round; spark_model `dflash_head` pages):
+//   EPI_STORE : out[m, n] = r_m * D                       (plain projection, fp32 out)
+//   EPI_QKV   : one tile = one head of the fused q|k|v projection.  r_m * D (the
+//               input RMSNorm weight is folded into W at create, r_m = 1/RMS(x_m));
+//               q/k: per-head RMSNorm (q_norm/k_norm), RoPE at ctx_len + r, * mscale;
+//               q -> q buffer, k/v -> paged pool rows ctx_len..ctx_len+15 (block K/V).
+//   EPI_RESID : x[m, n] += D (o_proj / down_proj residual), bf16 copy of x for the next
+//               projection, per-tile partial sums of x^2 for the next RMSNorm.
+//   EPI_GATEUP: tile = 64 gate rows + 64 up rows; act = silu(r_m g) * (r_m u).
+//   EPI_LMHEAD: logits (optional, bf16), per-row fp32 scale for the FP8 head, per-tile
+//               argmax partials and, in the last tile, the per-row argmax -> drafts.
+#include <cudaTypedefs.h>
+#include <float.h>
+
+#include <mutex>
+
+#include "dflash_internal.cuh"
+#include "gemm_tc.cuh"
+#include "tc_common.cuh"
+
+namespace dflash {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 128;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void rope_cs(const double* inv_pi, int j, int pos, float* c, float* s) {
+  double t = (double)pos * inv_pi[j];
+  t -= 2.0 * rint(0.5 * t);
+  sincospif((float)t, s, c);
+}
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// Shared-memory carve-up of the epilogue (aliases the drained pipeline stages).
+struct EpiSmem {
+  float xch[kThreads][17];   // one 16-token chunk of the tile, transposed exchange
+  float red[4][16];          // per-warp partial reductions for 16 tokens
+  float rsc[256];            // per-token input row scale
+  float bv[4][16];
+  int bi[4][16];
+};
+
+template <int EPI>
+__device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, float (&v)[16], int t, int n, int m0, int c0,
+                               int tile_n) {
+  const int warp = t >> 5, lane = t & 31;
+  if constexpr (EPI == EPI_STORE) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int m = m0 + c0 + c;
+      if (m < p.M && n < p.N) p.out[(int64_t)m * p.ldo + n] = v[c] * (p.ss_in ? es.rsc[c0 + c] : 1.f);
+    }
+  } else if constexpr (EPI == EPI_RESID) {
+    float sq[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int m = m0 + c0 + c;
+      float xv = 0.f;
+      if (m < p.M) {
+        const int64_t o = (int64_t)m * p.H + n;
+        xv = p.x[o] + v[c];
+        p.x[o] = xv;
+        p.xb[o] = __float2bfloat16_rn(xv);
+      }
+      sq[c] = warp_sum(xv * xv);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) es.red[warp][c] = sq[c];
+    }
+    __syncthreads();
+    if (t < 16) {
+      const int m = m0 + c0 + t;
+      if (m < p.M) p.ss_out[(int64_t)tile_n * p.Mp + m] = es.red[0][t] + es.red[1][t] + es.red[2][t] + es.red[3][t];
+    }
+    __syncthreads();
+  } else if constexpr (EPI == EPI_GATEUP) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * es.rsc[c0 + c];
+    __syncthreads();
+    const int f = tile_n * 64 + (t & 63);
+    const int cb = (t >> 6) * 8;
+#pragma unroll
+    for (int c = cb; c < cb + 8; ++c) {
+      const int m = m0 + c0 + c;
+      if (m < p.M) {
+        const float g = es.xch[t & 63][c], u = es.xch[(t & 63) + 64][c];
+        p.act[(int64_t)m * p.F + f] = __float2bfloat16_rn(g / (1.f + __expf(-g)) * u);
+      }
+    }
+    __syncthreads();
+  } else if constexpr (EPI == EPI_QKV) {
+    const int hh = tile_n;
+    const bool is_q = hh < p.nh, is_k = !is_q && hh < p.nh + p.nkv;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) v[c] *= es.rsc[c0 + c];
+    if (is_q || is_k) {
+      // per-head RMSNorm over the 128 rows of the tile
+      float sq[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sq[c] = warp_sum(v[c] * v[c]);
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) es.red[warp][c] = sq[c];
+      }
+      __syncthreads();
+      const float w = __bfloat162float((is_q ? p.q_norm : p.k_norm)[t]);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float ss = es.red[0][c] + es.red[1][c] + es.red[2][c] + es.red[3][c];
+        es.xch[t][c] = v[c] * (1.f / sqrtf(ss * (1.f / 128.f) + p.eps)) * w;
+      }
+      __syncthreads();
+      // RoPE: pair (j, j + 64), NeoX rotate-half
+      const int j = t & 63;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c0 + c;
+        const int s = m / kGamma, r = m % kGamma;
+        const int ctx = m < p.M ? p.ctx_lens[s] : 0;
+        float cs, sn;
+        rope_cs(p.inv_pi, j, ctx + r, &cs, &sn);
+        const float a = es.xch[j][c], b = es.xch[j + 64][c];
+        v[c] = (t < 64 ? a * cs - b * sn : b * cs + a * sn) * p.mscale;
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int m = m0 + c0 + c;
+      if (m >= p.M) continue;
+      if (is_q) {
+        p.q[(int64_t)m * p.nh * 128 + hh * 128 + t] = __float2bfloat16_rn(v[c]);
+        continue;
+      }
+      const int s = m / kGamma, r = m % kGamma;
+      const int ctx = p.ctx_lens[s];
+      if (ctx < 0 || ctx + kGamma > p.mpps * kPage) {
+        if (t == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
+        continue;
+      }
+      const int li = ctx + r;
+      const int page = p.page_tables[(int64_t)s * p.mpps + li / kPage];
+      if (page < 0 || page >= p.g.num_pages) {
+        if (t == 0) atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
+        continue;
+      }
+      const int head = is_k ? hh - p.nh : hh - p.nh - p.nkv;
+      const int64_t base = tile_base(p.g, p.layer, page, is_k ? 0 : 1, head);
+      p.pool[base + (is_k ? k_in_tile(li % kPage, t, 128) : v_in_tile(li % kPage, t, 128))] =
+          __float2bfloat16_rn(v[c]);
+    }
+  } else if constexpr (EPI == EPI_LMHEAD) {
+    const bool valid_row = n < p.N;
+    const float sc = (p.row_scale && valid_row) ? p.row_scale[n] : 1.f;
+    float bv[16];
+    int bi[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int m = m0 + c0 + c;
+      const float z = v[c] * sc;
+      if (p.logits && valid_row && m < p.M) p.logits[(int64_t)m * p.N + n] = __float2bfloat16_rn(z);
+      bv[c] = valid_row ? z : -FLT_MAX;
+      bi[c] = valid_row ? n : 0x7fffffff;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv[c], o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi[c], o);
+        if (better(ov, oi, bv[c], bi[c])) { bv[c] = ov; bi[c] = oi; }
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) { es.bv[warp][c] = bv[c]; es.bi[warp][c] = bi[c]; }
+    }
+    __syncthreads();
+    if (t < 16) {
+      float b = es.bv[0][t];
+      int i = es.bi[0][t];
+      for (int w2 = 1; w2 < 4; ++w2)
+        if (better(es.bv[w2][t], es.bi[w2][t], b, i)) { b = es.bv[w2][t]; i = es.bi[w2][t]; }
+      const int m = m0 + c0 + t;
+      if (m < p.M) {
+        p.amax_val[(int64_t)tile_n * p.Mp + m] = b;
+        p.amax_idx[(int64_t)tile_n * p.Mp + m] = i;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <int EPI, int TN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const GemmParams p) {
+  constexpr int A_BYTES = 128 * 64 * 2;
+  constexpr int B_BYTES = TN * 64 * 2;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = TN < 32 ? 32 : TN;
+  static_assert(sizeof(EpiSmem) <= STAGES * STAGE_BYTES, "epilogue scratch must fit in the stages");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accf = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] timed out, [1] last split
+
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
+  const int kb0 = (int)((int64_t)split * p.nkb / p.nsplit);
+  const int kb1 = (int)((int64_t)(split + 1) * p.nkb / p.nsplit);
+  const int nloc = kb1 - kb0;
+
+  if (t == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accf, 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmW);
+    prefetch_tensormap(&tmX);
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      const int pre = nloc < STAGES ? nloc : STAGES;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], STAGE_BYTES);
+        tma_load_2d(smem + i * STAGE_BYTES, &tmW, &full[i], (kb0 + i) * 64, tile_n * 128, pol_w);
+      }
+      pdl_wait();  // everything the previous kernel wrote is visible from here on
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(smem + i * STAGE_BYTES + A_BYTES, &tmX, &full[i], (kb0 + i) * 64, tile_m * TN, pol_x);
+      for (int i = pre; i < nloc; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait(&empty[s], ((i / STAGES) - 1) & 1)) {
+          flags[0] = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+        tma_load_2d(smem + s * STAGE_BYTES, &tmW, &full[s], (kb0 + i) * 64, tile_n * 128, pol_w);
+        tma_load_2d(smem + s * STAGE_BYTES + A_BYTES, &tmX, &full[s], (kb0 + i) * 64, tile_m * TN, pol_x);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer (single thread)
+      constexpr uint32_t idesc = idesc_bf16(128, TN);
+      for (int i = 0; i < nloc; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait(&full[s], (i / STAGES) & 1)) {
+          flags[0] = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = desc_sw128(smem + s * STAGE_BYTES);
+        const uint64_t bd = desc_sw128(smem + s * STAGE_BYTES + A_BYTES);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(accf);
+    }
+    __syncwarp();
+  }
+
+  // ---------------- epilogue: all four warps
+  pdl_wait();
+  const bool ok = mbar_wait(accf, 0);
+  tc_fence_after();
+  __syncthreads();
+  if (!ok || flags[0]) {
+    // a wait gave up: record it, give copies still in flight time to land, unwind
+    if (t == 0) atomicOr(p.status, DFLASH_DEV_TIMEOUT);
+    for (int i = 0; i < 2000; ++i) __nanosleep(1000);
+  } else {
+    EpiSmem& es = *reinterpret_cast<EpiSmem*>(smem);
+    const int m0 = tile_m * TN;
+    const int n = tile_n * 128 + t;
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const int64_t tile_lin = (int64_t)tile_n * gridDim.y + tile_m;
+    if (p.ss_in) {
+      for (int c = t; c < TN; c += kThreads) {
+        const int m = m0 + c;
+        float r = 1.f;
+        if (m < p.M) {
+          float ssum = 0.f;
+          for (int q = 0; q < p.ss_parts; ++q) ssum += p.ss_in[(int64_t)q * p.Mp + m];
+          r = 1.f / sqrtf(ssum / (float)p.ss_n + p.eps);
+        }
+        es.rsc[c] = r;
+      }
+    }
+    __syncthreads();
+    bool last = true;
+    if (p.nsplit > 1) {
+      float* mine = p.ws + ((tile_lin * p.nsplit + split) * kThreads + t) * TN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < TN; c0 += 16) {
+        float v[16];
+        tmem_ld16(lane_addr + c0, v);
+#pragma unroll
+        for (int c = 0; c < 16; c += 4)
+          __stcg(reinterpret_cast<float4*>(mine + c0 + c), make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]));
+      }
+      __threadfence();
+      __syncthreads();
+      if (t == 0) flags[1] = atomicAdd(&p.counters[tile_lin], 1u) == (unsigned)(p.nsplit - 1);
+      __syncthreads();
+      last = flags[1] != 0;
+      if (last) __threadfence();
+    }
+    if (last) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < TN; c0 += 16) {
+        float v[16];
+        if (p.nsplit > 1) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] = 0.f;
+          for (int s = 0; s < p.nsplit; ++s) {
+            const float* src = p.ws + ((tile_lin * p.nsplit + s) * kThreads + t) * TN + c0;
+#pragma unroll
+            for (int c = 0; c < 16; c += 4) {
+              const float4 q4 = __ldcg(reinterpret_cast<const float4*>(src + c));
+              v[c] += q4.x;
+              v[c + 1] += q4.y;
+              v[c + 2] += q4.z;
+              v[c + 3] += q4.w;
+            }
+          }
+        } else {
+          tmem_ld16(lane_addr + c0, v);
+        }
+        epilogue_chunk<EPI>(p, es, v, t, n, m0, c0, tile_n);
+      }
+      if (p.nsplit > 1 && t == 0) p.counters[tile_lin] = 0;
+      if constexpr (EPI == EPI_LMHEAD) {
+        // the last vocabulary tile of this token tile reduces the per-tile argmaxes
+        __threadfence();
+        __syncthreads();
+        if (t == 0) flags[1] = atomicAdd(&p.amax_counter[tile_m], 1u) == (unsigned)(gridDim.x - 1);
+        __syncthreads();
+        if (flags[1]) {
+          __threadfence();
+          // 8 threads per token, 16 tokens per pass
+          for (int cb = 0; cb < TN; cb += 16) {
+            const int c = cb + (t >> 3), sub = t & 7;
+            const int m = m0 + c;
+            float b = -FLT_MAX;
+            int bi = 0x7fffffff;
+            if (m < p.M) {
+              for (int q = sub; q < (int)gridDim.x; q += 8) {
+                const float vv = __ldcg(p.amax_val + (int64_t)q * p.Mp + m);
+                const int ii = __ldcg(p.amax_idx + (int64_t)q * p.Mp + m);
+                if (better(vv, ii, b, bi)) { b = vv; bi = ii; }
+              }
+            }
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) {
+              const float ov = __shfl_xor_sync(0xffffffffu, b, o);
+              const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+              if (better(ov, oi, b, bi)) { b = ov; bi = oi; }
+            }
+            if (sub == 0 && m < p.M) {
+              const int r = m % kGamma;
+              if (r > 0) p.drafts[(m / kGamma) * (kGamma - 1) + r - 1] = bi;
+            }
+          }
+          if (t == 0) p.amax_counter[tile_m] = 0;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+template <int EPI, int TN, int STAGES>
+cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
+                     cudaStream_t st, bool pdl) {
+  constexpr int smem = STAGES * (128 * 64 * 2 + TN * 64 * 2) + 1024 + 256;
+  auto kern = gemm_tc_kernel<EPI, TN, STAGES>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, p);
+}
+
+template <int EPI, int TN>
+cudaError_t launch_tn(const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
+                      cudaStream_t st, bool pdl) {
+  // stages: keep two CTAs per SM possible for the skinny shapes
+  constexpr int STAGES = TN <= 32 ? 6 : (TN <= 64 ? 5 : (TN <= 128 ? 4 : 3));
+  return launch_t<EPI, TN, STAGES>(tw, tx, p, grid, st, pdl);
+}
+
+template <int EPI>
+cudaError_t launch_epi(int TN, const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
+                       cudaStream_t st, bool pdl) {
+  switch (TN) {
+    case 16: return launch_tn<EPI, 16>(tw, tx, p, grid, st, pdl);
+    case 32: return launch_tn<EPI, 32>(tw, tx, p, grid, st, pdl);
+    case 64: return launch_tn<EPI, 64>(tw, tx, p, grid, st, pdl);
+    case 128: return launch_tn<EPI, 128>(tw, tx, p, grid, st, pdl);
+    case 256: return launch_tn<EPI, 256>(tw, tx, p, grid, st, pdl);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld_elems,
+                    int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld_elems * 2)};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int pick_tn(int M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+int pick_splits(int tiles, int nkb, int num_sms) {
+  int s = (num_sms + tiles - 1) / tiles;  // about one CTA per SM
+  if (s > nkb) s = nkb;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return s < 1 ? 1 : s;
+}
+
+cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, int ldx, int M, GemmParams p,
+                           int nsplit, cudaStream_t st, bool pdl) {
+  const int TN = pick_tn(M);
+  CUtensorMap tw, tx;
+  if (!make_tmap_bf16(&tw, W, N, K, K, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tx, X, M, K, ldx, TN)) return cudaErrorInvalidValue;
+  p.N = N;
+  p.K = K;
+  p.M = M;
+  p.nkb = K / 64;
+  p.nsplit = nsplit;
+  dim3 grid((N + 127) / 128, (M + TN - 1) / TN, nsplit);
+  switch (epi) {
+    case EPI_STORE: return launch_epi<EPI_STORE>(TN, tw, tx, p, grid, st, pdl);
+    case EPI_QKV: return launch_epi<EPI_QKV>(TN, tw, tx, p, grid, st, pdl);
+    case EPI_RESID: return launch_epi<EPI_RESID>(TN, tw, tx, p, grid, st, pdl);
+    case EPI_GATEUP: return launch_epi<EPI_GATEUP>(TN, tw, tx, p, grid, st, pdl);
+    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(TN, tw, tx, p, grid, st, pdl);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dflash

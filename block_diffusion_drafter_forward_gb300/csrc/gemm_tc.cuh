@@ -1,0 +1,64 @@
+// Host interface of the tensor-core projection GEMM (gemm_tc.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dflash_internal.cuh"
+
+namespace dflash {
+
+enum GemmEpi { EPI_STORE = 0, EPI_QKV = 1, EPI_RESID = 2, EPI_GATEUP = 3, EPI_LMHEAD = 4 };
+constexpr int kMaxSplits = 16;
+
+// Everything an epilogue may need; fields an epilogue does not use stay zero.
+struct GemmParams {
+  int N = 0, K = 0, M = 0, nkb = 0, nsplit = 1;
+  float* ws = nullptr;              // split-K partials
+  unsigned* counters = nullptr;     // split-K tile counters (zero between launches)
+  unsigned* status = nullptr;       // device status word
+  // input row scale r_m = 1/sqrt(sum_q ss_in[q*Mp + m] / ss_n + eps) (nullptr: none)
+  const float* ss_in = nullptr;
+  int ss_parts = 0, ss_n = 1, Mp = 0;
+  float eps = 1e-6f;
+  // EPI_STORE
+  float* out = nullptr;
+  int ldo = 0;
+  // EPI_QKV
+  __nv_bfloat16* q = nullptr;
+  const __nv_bfloat16* q_norm = nullptr;
+  const __nv_bfloat16* k_norm = nullptr;
+  const double* inv_pi = nullptr;
+  float mscale = 1.f;
+  int nh = 0, nkv = 0, mpps = 0, layer = 0;
+  const int32_t* ctx_lens = nullptr;
+  const int32_t* page_tables = nullptr;
+  PoolGeom g{};
+  __nv_bfloat16* pool = nullptr;
+  // EPI_RESID
+  float* x = nullptr;
+  __nv_bfloat16* xb = nullptr;
+  float* ss_out = nullptr;
+  int H = 0;
+  // EPI_GATEUP
+  __nv_bfloat16* act = nullptr;
+  int F = 0;
+  // EPI_LMHEAD
+  __nv_bfloat16* logits = nullptr;
+  const float* row_scale = nullptr;
+  float* amax_val = nullptr;
+  int* amax_idx = nullptr;
+  unsigned* amax_counter = nullptr;
+  int32_t* drafts = nullptr;
+};
+
+int pick_tn(int M);
+int pick_splits(int tiles, int nkb, int num_sms);
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld_elems, int box_rows);
+// D = W [N, K] x X [M, K]^T with the epilogue `epi`; nsplit K-splits (1 for EPI_LMHEAD).
+cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, int ldx, int M, GemmParams p,
+                           int nsplit, cudaStream_t st, bool pdl);
+
+}  // namespace dflash

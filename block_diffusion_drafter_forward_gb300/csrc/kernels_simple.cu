@@ -351,7 +351,68 @@ __global__ void quantize_fp8_kernel(const T* __restrict__ w, int cols, uint8_t* 
         (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(Elem<T>::to_f(wr[k]), s), __NV_SATFINITE, __NV_E4M3);
 }
 
+// ------------------------------------------------------------------------ tensor-core path helpers
+// Embedding rows for the tensor-core path: fp32 residual x, its bf16 copy xb (operand of
+// the first projection) and per-128-column partial sums of x^2 (ss[g * Mp + row]), from
+// which the next projection's epilogue forms 1/RMS(x).
+__global__ void embed_tc_kernel(const __nv_bfloat16* __restrict__ E, const int32_t* __restrict__ bonus, int mask,
+                                int V, int H, int Mp, float* __restrict__ x, __nv_bfloat16* __restrict__ xb,
+                                float* __restrict__ ss, unsigned* status) {
+  __shared__ float part[4];
+  const int row = blockIdx.x, t = threadIdx.x;
+  const int r = row % kGamma, s = row / kGamma;
+  const int tok = r == 0 ? bonus[s] : mask;
+  const bool ok = tok >= 0 && tok < V;
+  if (!ok && t == 0) flag(status, DFLASH_DEV_BAD_TOKEN);
+  for (int g = 0; g < H / 128; ++g) {
+    const int i = g * 128 + t;
+    const __nv_bfloat16 e = ok ? E[(int64_t)tok * H + i] : __float2bfloat16_rn(0.f);
+    const float v = __bfloat162float(e);
+    x[(int64_t)row * H + i] = v;
+    xb[(int64_t)row * H + i] = e;
+    const float w = warp_sum(v * v);
+    if ((t & 31) == 0) part[t >> 5] = w;
+    __syncthreads();
+    if (t == 0) ss[(int64_t)g * Mp + row] = part[0] + part[1] + part[2] + part[3];
+    __syncthreads();
+  }
+}
+
+// out[p, k] = W_src(p)[k] * ln[k] in bf16, with W_src(p) the packed row p:
+//  mode 0: rows of A (fused q|k|v, already packed), in place;
+//  mode 1: gate/up interleaved in blocks of 64 rows (block b = gate rows 64b..64b+63, then
+//          up rows 64b..64b+63), so one 128-row GEMM tile holds matching gate and up rows.
+__global__ void fold_norm_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B, int mode,
+                                 int cols, const __nv_bfloat16* __restrict__ ln, __nv_bfloat16* __restrict__ out) {
+  const int p = blockIdx.x;
+  const __nv_bfloat16* src;
+  if (mode == 0) {
+    src = A + (int64_t)p * cols;
+  } else {
+    const int b = p / 128, w = p % 128;
+    src = w < 64 ? A + (int64_t)(b * 64 + w) * cols : B + (int64_t)(b * 64 + w - 64) * cols;
+  }
+  for (int k = threadIdx.x; k < cols; k += blockDim.x)
+    out[(int64_t)p * cols + k] = __float2bfloat16_rn(__bfloat162float(src[k]) * __bfloat162float(ln[k]));
+}
+
 }  // namespace
+
+cudaError_t launch_embed_tc(const dflash_handle* h, const int32_t* bonus, int nb, cudaStream_t st) {
+  const dflash_cfg& c = h->cfg;
+  embed_tc_kernel<<<nb * kGamma, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(h->embed), bonus, c.mask_token_id,
+                                               c.vocab, c.hidden, h->rows_max, h->x,
+                                               static_cast<__nv_bfloat16*>(h->xb), h->ss_b, h->d_status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fold_norm(const void* A, const void* B, int mode, int rows, int cols, const void* ln, void* out,
+                             cudaStream_t st) {
+  fold_norm_kernel<<<rows, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B),
+                                         mode, cols, static_cast<const __nv_bfloat16*>(ln),
+                                         static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
 
 // ------------------------------------------------------------------------ launchers
 

@@ -60,6 +60,7 @@ typedef enum {
 #define DFLASH_DEV_BAD_PAGE 0x1u    /* a page id outside [0, num_pages) was met */
 #define DFLASH_DEV_BAD_CTX 0x2u     /* ctx_len < 0 or > max_ctx_len, or ctx_len+gamma > capacity */
 #define DFLASH_DEV_BAD_TOKEN 0x4u   /* a bonus token outside [0, vocab) (row embedded as zeros) */
+#define DFLASH_DEV_TIMEOUT 0x8u     /* a kernel's bounded wait gave up (its outputs are invalid) */
 
 /* Drafter configuration.  Names follow the drafter config.json of the pages
  * (hidden_size, num_attention_heads, num_key_value_heads, head_dim, intermediate_size,
@@ -195,6 +196,12 @@ int dflash_profile(dflash_handle* h, int enable);
 int dflash_profile_kinds(void);
 int dflash_profile_read(dflash_handle* h, int kind, const char** name, double* total_ms,
                         int64_t* launches);
+
+/* The tensor-core projection GEMM on its own (for tests): out[m, n] = sum_k W[n, k] X[m, k]
+ * with W [N, K] and X [M, K] bf16 row-major device arrays, out [M, N] fp32.  K % 64 == 0,
+ * nsplit must be 1.  Same kernel as every bf16 projection of dflash_propose. */
+int dflash_gemm_bf16(const void* W, int32_t N, int32_t K, const void* X, int32_t M, float* out,
+                     int32_t nsplit, dflash_stream stream);
 
 /* Synchronise `stream`, read the device status word into *flags (may be NULL) and clear
  * it.  Returns DFLASH_EDEVICE when any bit was set, else DFLASH_OK. */

@@ -2,6 +2,9 @@
 context K/V through the library, run the oracle on sampled bands, compare."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -116,6 +119,10 @@ def check_band(rig, s, ref, drafts, z, h, tol):
     sure = ref["margin"] > tol["margin"]
     out["n_sure"] = int(sure.sum())
     out["mismatch"] = int((dt[sure] != ref["tokens"][sure]).sum())
+    log = os.environ.get("DFLASH_PARITY_LOG")
+    if log:
+        with open(log, "a") as fh:
+            fh.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", ""), "band": s, **out}) + "\n")
     assert out["hidden"] <= tol["hidden"], (s, out)
     if zs is not None:
         assert out["logits"] <= tol["logits"], (s, out)
