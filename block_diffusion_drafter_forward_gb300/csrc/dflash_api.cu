@@ -200,6 +200,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.x = h->x;
       p.xb = static_cast<__nv_bfloat16*>(h->xb);
       p.ss_out = h->ss_a;
+      p.ln_next = static_cast<const __nv_bfloat16*>(w.ln_post);
       p.H = H;
       KL(K_OPROJ, launch_gemm_tc(EPI_RESID, w.w_o, H, qd, h->attn, qd, M, p, splits(H, qd), st, false), "o_proj");
     }
@@ -217,6 +218,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.x = h->x;
       p.xb = static_cast<__nv_bfloat16*>(h->xb);
       p.ss_out = h->ss_b;
+      p.ln_next = l + 1 < c.n_layers ? static_cast<const __nv_bfloat16*>(h->layer[l + 1].ln_in) : nullptr;
       p.H = H;
       KL(K_DOWN, launch_gemm_tc(EPI_RESID, w.w_down, H, F, h->act, F, M, p, splits(H, F), st, true), "down");
     }
@@ -334,12 +336,11 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     D2D(d.w_o, lw.wo, H * qd * es);
     ALLOC(d.w_gu, 2 * F * H * es);
     if (h->tc) {
-      // tensor-core path: input RMSNorm weights folded into the projections that read the
-      // normed activations (W' = W diag(ln)); gate/up interleaved in 64-row blocks
-      cudaError_t e1 = launch_fold_norm(d.w_qkv, nullptr, 0, (int)qkvd, (int)H, lw.ln_in, d.w_qkv, st);
-      cudaError_t e2 = launch_fold_norm(lw.w_gate, lw.w_up, 1, (int)(2 * F), (int)H, lw.ln_post, d.w_gu, st);
-      if (e1 != cudaSuccess || e2 != cudaSuccess) {
-        cuda_fail(h, e1 != cudaSuccess ? e1 : e2, "fold norms");
+      // tensor-core path: gate/up interleaved in 64-row blocks so one 128-row GEMM tile
+      // holds matching gate and up rows
+      cudaError_t e2 = launch_fold_norm(lw.w_gate, lw.w_up, 1, (int)(2 * F), (int)H, nullptr, d.w_gu, st);
+      if (e2 != cudaSuccess) {
+        cuda_fail(h, e2, "pack gate/up");
         return bail(DFLASH_ECUDA);
       }
     } else {
@@ -393,7 +394,7 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
   ALLOC(h->act, R * F * es);
   ALLOC(h->logits32, R * V * 4);
   ALLOC(h->wy, Rw * std::max(H, L * 2 * kvd) * 4);
-  ALLOC(h->wf, Rw * H * es);
+  ALLOC(h->wf, Rw * H * 4);
   if (h->tc) {
     ALLOC(h->xb, R * H * es);
     ALLOC(h->ss_a, (H / 128) * R * 4);
@@ -471,9 +472,10 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
     const void* tp = static_cast<const char*>(taps) + (int64_t)done * tapd * h->esz;
     // f = hidden_norm(fc . taps)  (dflash.rs ctx_features)
     KL(K_W_FC, launch_gemm(h, tp, (int)tapd, h->fc, m, (int)H, (int)tapd, h->wy, (int)H, false, st), "writer fc");
-    KL(K_W_NORM, launch_rmsnorm_f32in(h, h->wy, h->hidden_norm, h->wf, m, (int)H, st), "writer hidden_norm");
-    // every layer's K and V in one GEMM over the fused weight, then k_norm / RoPE / scatter
-    KL(K_W_KV, launch_gemm(h, h->wf, (int)H, h->w_ctxkv, m, kvall, (int)H, h->wy, kvall, false, st), "writer kv");
+    KL(K_W_NORM, launch_rmsnorm_f32out(h, h->wy, h->hidden_norm, h->wf, m, (int)H, st), "writer hidden_norm");
+    // every layer's K and V in one GEMM over the fused weight (fp32 features), then
+    // k_norm / RoPE / scatter
+    KL(K_W_KV, launch_gemm_xf32(h, h->wf, (int)H, h->w_ctxkv, m, kvall, (int)H, h->wy, kvall, st), "writer kv");
     KL(K_W_POST, launch_ctxkv_post(h, h->wy, m, positions + done, page_table, first + done, st), "writer post");
   }
   return DFLASH_OK;

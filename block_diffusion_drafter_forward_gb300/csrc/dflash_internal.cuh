@@ -122,7 +122,7 @@ struct dflash_handle {
   float* logits32 = nullptr;           // [rows, V] fp32 logits
   // writer scratch (rows = max_write_rows)
   float* wy = nullptr;                 // [Rw, max(H, L*2*kv)] fp32
-  void* wf = nullptr;                  // [Rw, H] ctx features (cfg.dtype)
+  float* wf = nullptr;                 // [Rw, H] ctx features (fp32)
 
   // tensor-core (bf16) path scratch
   void* xb = nullptr;                  // [rows, H] bf16 copy of the residual stream
@@ -150,6 +150,10 @@ cudaError_t launch_rmsnorm_f32in(const dflash_handle* h, const float* x, const v
 // Y[m, n] (+)= sum_k X[m, k] W[n, k]; X, W in cfg.dtype; Y fp32 with row stride ldy.
 cudaError_t launch_gemm(const dflash_handle* h, const void* X, int ldx, const void* W, int M, int N,
                         int K, float* Y, int ldy, bool accumulate, cudaStream_t st);
+cudaError_t launch_gemm_xf32(const dflash_handle* h, const float* X, int ldx, const void* W, int M, int N, int K,
+                             float* Y, int ldy, cudaStream_t st);
+cudaError_t launch_rmsnorm_f32out(const dflash_handle* h, const float* x, const void* w, float* out, int rows, int n,
+                                  cudaStream_t st);
 cudaError_t launch_gemm_fp8w(const dflash_handle* h, const void* X, int ldx, const uint8_t* Wq,
                              const float* scale, int M, int N, int K, float* Y, int ldy,
                              cudaStream_t st);

@@ -13,11 +13,11 @@
 // Epilogues (memra-engine `dflash.rs` forward_round; spark_model `dflash_head` pages):
 //   EPI_STORE : out[m, n] = r_m * D                       (plain projection, fp32 out)
 //   EPI_QKV   : one tile = one head of the fused q|k|v projection.  r_m * D (the
-//               input RMSNorm weight is folded into W at create, r_m = 1/RMS(x_m));
+//               operand is x * ln_in in bf16, r_m = 1/RMS(x_m), so r_m D = W RMSNorm(x));
 //               q/k: per-head RMSNorm (q_norm/k_norm), RoPE at ctx_len + r, * mscale;
 //               q -> q buffer, k/v -> paged pool rows ctx_len..ctx_len+15 (block K/V).
-//   EPI_RESID : x[m, n] += D (o_proj / down_proj residual), bf16 copy of x for the next
-//               projection, per-tile partial sums of x^2 for the next RMSNorm.
+//   EPI_RESID : x[m, n] += D (o_proj / down_proj residual), bf16(x * ln_next) as the next
+//               projection's operand, per-tile partial sums of x^2 for the next RMSNorm.
 //   EPI_GATEUP: tile = 64 gate rows + 64 up rows; act = silu(r_m g) * (r_m u).
 //   EPI_LMHEAD: logits (optional, bf16), per-row fp32 scale for the FP8 head, per-tile
 //               argmax partials and, in the last tile, the per-row argmax -> drafts.
@@ -82,7 +82,7 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, float (&v)[16],
         const int64_t o = (int64_t)m * p.H + n;
         xv = p.x[o] + v[c];
         p.x[o] = xv;
-        p.xb[o] = __float2bfloat16_rn(xv);
+        p.xb[o] = __float2bfloat16_rn(p.ln_next ? xv * __bfloat162float(p.ln_next[n]) : xv);
       }
       sq[c] = warp_sum(xv * xv);
     }

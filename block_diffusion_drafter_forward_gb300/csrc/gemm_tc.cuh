@@ -41,6 +41,7 @@ struct GemmParams {
   float* x = nullptr;
   __nv_bfloat16* xb = nullptr;
   float* ss_out = nullptr;
+  const __nv_bfloat16* ln_next = nullptr;  // next RMSNorm weight: xb = bf16(x * ln_next)
   int H = 0;
   // EPI_GATEUP
   __nv_bfloat16* act = nullptr;

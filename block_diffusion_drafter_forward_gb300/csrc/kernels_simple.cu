@@ -66,8 +66,8 @@ __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict_
 
 // ------------------------------------------------------------------------ RMSNorm
 // out = x * w / sqrt(mean(x^2) + eps)   (vanilla form, from_weights.rs kernel table)
-template <typename T>
-__global__ void rmsnorm_kernel(const float* __restrict__ x, const T* __restrict__ w, T* __restrict__ out,
+template <typename T, typename TO = T>
+__global__ void rmsnorm_kernel(const float* __restrict__ x, const T* __restrict__ w, TO* __restrict__ out,
                                int n, float eps) {
   const float* xr = x + (int64_t)blockIdx.x * n;
   float ss = 0.f;
@@ -75,14 +75,14 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const T* __restrict_
   ss = block_sum(ss);
   const float inv = 1.f / sqrtf(ss / (float)n + eps);
   for (int i = threadIdx.x; i < n; i += blockDim.x)
-    out[(int64_t)blockIdx.x * n + i] = Elem<T>::from_f(xr[i] * inv * Elem<T>::to_f(w[i]));
+    out[(int64_t)blockIdx.x * n + i] = Elem<TO>::from_f(xr[i] * inv * Elem<T>::to_f(w[i]));
 }
 
 // ------------------------------------------------------------------------ GEMM (CUDA cores)
 // Y[m, n] (+)= sum_k X[m, k] W[n, k].  64x64 tile per block, 16-deep k slices, 4x4 per
 // thread, fp32 accumulation.
-template <typename T, bool FP8W>
-__global__ void __launch_bounds__(256) gemm_kernel(const T* __restrict__ X, int ldx, const void* __restrict__ Wv,
+template <typename TX, typename T, bool FP8W>
+__global__ void __launch_bounds__(256) gemm_kernel(const TX* __restrict__ X, int ldx, const void* __restrict__ Wv,
                                                    const float* __restrict__ wscale, int M, int N, int K,
                                                    float* __restrict__ Y, int ldy, int accumulate) {
   __shared__ float Xs[16][68];
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const T* __restrict__ X, int 
       const int rr = i >> 4, kk = i & 15;
       const int k = k0 + kk;
       const int m = m0 + rr, n = n0 + rr;
-      Xs[kk][rr] = (m < M && k < K) ? Elem<T>::to_f(X[(int64_t)m * ldx + k]) : 0.f;
+      Xs[kk][rr] = (m < M && k < K) ? Elem<TX>::to_f(X[(int64_t)m * ldx + k]) : 0.f;
       float wv = 0.f;
       if (n < N && k < K) {
         if constexpr (FP8W) {
@@ -352,12 +352,13 @@ __global__ void quantize_fp8_kernel(const T* __restrict__ w, int cols, uint8_t* 
 }
 
 // ------------------------------------------------------------------------ tensor-core path helpers
-// Embedding rows for the tensor-core path: fp32 residual x, its bf16 copy xb (operand of
-// the first projection) and per-128-column partial sums of x^2 (ss[g * Mp + row]), from
-// which the next projection's epilogue forms 1/RMS(x).
+// Embedding rows for the tensor-core path: fp32 residual x, xb = bf16(x * ln) with ln the
+// first layer's input RMSNorm weight (operand of the first projection), and per-128-column
+// partial sums of x^2 (ss[g * Mp + row]), from which that projection's epilogue forms
+// 1/RMS(x): W (x * ln) / RMS(x) = W RMSNorm(x).
 __global__ void embed_tc_kernel(const __nv_bfloat16* __restrict__ E, const int32_t* __restrict__ bonus, int mask,
-                                int V, int H, int Mp, float* __restrict__ x, __nv_bfloat16* __restrict__ xb,
-                                float* __restrict__ ss, unsigned* status) {
+                                int V, int H, int Mp, const __nv_bfloat16* __restrict__ ln, float* __restrict__ x,
+                                __nv_bfloat16* __restrict__ xb, float* __restrict__ ss, unsigned* status) {
   __shared__ float part[4];
   const int row = blockIdx.x, t = threadIdx.x;
   const int r = row % kGamma, s = row / kGamma;
@@ -369,7 +370,7 @@ __global__ void embed_tc_kernel(const __nv_bfloat16* __restrict__ E, const int32
     const __nv_bfloat16 e = ok ? E[(int64_t)tok * H + i] : __float2bfloat16_rn(0.f);
     const float v = __bfloat162float(e);
     x[(int64_t)row * H + i] = v;
-    xb[(int64_t)row * H + i] = e;
+    xb[(int64_t)row * H + i] = __float2bfloat16_rn(v * __bfloat162float(ln[i]));
     const float w = warp_sum(v * v);
     if ((t & 31) == 0) part[t >> 5] = w;
     __syncthreads();
@@ -378,7 +379,7 @@ __global__ void embed_tc_kernel(const __nv_bfloat16* __restrict__ E, const int32
   }
 }
 
-// out[p, k] = W_src(p)[k] * ln[k] in bf16, with W_src(p) the packed row p:
+// out[p, k] = W_src(p)[k] (* ln[k] when ln is given) in bf16, with W_src(p) the packed row p:
 //  mode 0: rows of A (fused q|k|v, already packed), in place;
 //  mode 1: gate/up interleaved in blocks of 64 rows (block b = gate rows 64b..64b+63, then
 //          up rows 64b..64b+63), so one 128-row GEMM tile holds matching gate and up rows.
@@ -393,7 +394,7 @@ __global__ void fold_norm_kernel(const __nv_bfloat16* __restrict__ A, const __nv
     src = w < 64 ? A + (int64_t)(b * 64 + w) * cols : B + (int64_t)(b * 64 + w - 64) * cols;
   }
   for (int k = threadIdx.x; k < cols; k += blockDim.x)
-    out[(int64_t)p * cols + k] = __float2bfloat16_rn(__bfloat162float(src[k]) * __bfloat162float(ln[k]));
+    out[(int64_t)p * cols + k] = ln ? __float2bfloat16_rn(__bfloat162float(src[k]) * __bfloat162float(ln[k])) : src[k];
 }
 
 }  // namespace
@@ -401,7 +402,8 @@ __global__ void fold_norm_kernel(const __nv_bfloat16* __restrict__ A, const __nv
 cudaError_t launch_embed_tc(const dflash_handle* h, const int32_t* bonus, int nb, cudaStream_t st) {
   const dflash_cfg& c = h->cfg;
   embed_tc_kernel<<<nb * kGamma, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(h->embed), bonus, c.mask_token_id,
-                                               c.vocab, c.hidden, h->rows_max, h->x,
+                                               c.vocab, c.hidden, h->rows_max,
+                                               static_cast<const __nv_bfloat16*>(h->layer[0].ln_in), h->x,
                                                static_cast<__nv_bfloat16*>(h->xb), h->ss_b, h->d_status);
   return cudaGetLastError();
 }
@@ -447,8 +449,24 @@ cudaError_t launch_gemm(const dflash_handle* h, const void* X, int ldx, const vo
                         float* Y, int ldy, bool accumulate, cudaStream_t st) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   dim3 grid((N + 63) / 64, (M + 63) / 64);
-  DISPATCH_T(h->cfg.dtype, (gemm_kernel<T, false><<<grid, 256, 0, st>>>(static_cast<const T*>(X), ldx, W, nullptr,
-                                                                        M, N, K, Y, ldy, accumulate ? 1 : 0)));
+  DISPATCH_T(h->cfg.dtype, (gemm_kernel<T, T, false><<<grid, 256, 0, st>>>(static_cast<const T*>(X), ldx, W, nullptr,
+                                                                           M, N, K, Y, ldy, accumulate ? 1 : 0)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_xf32(const dflash_handle* h, const float* X, int ldx, const void* W, int M, int N, int K,
+                             float* Y, int ldy, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  dim3 grid((N + 63) / 64, (M + 63) / 64);
+  DISPATCH_T(h->cfg.dtype, (gemm_kernel<float, T, false><<<grid, 256, 0, st>>>(X, ldx, W, nullptr, M, N, K, Y, ldy, 0)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_f32out(const dflash_handle* h, const float* x, const void* w, float* out, int rows, int n,
+                                  cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  DISPATCH_T(h->cfg.dtype, (rmsnorm_kernel<T, float><<<rows, 256, 0, st>>>(x, static_cast<const T*>(w), out, n,
+                                                                          h->cfg.rms_eps)));
   return cudaGetLastError();
 }
 
@@ -456,8 +474,8 @@ cudaError_t launch_gemm_fp8w(const dflash_handle* h, const void* X, int ldx, con
                              int M, int N, int K, float* Y, int ldy, cudaStream_t st) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   dim3 grid((N + 63) / 64, (M + 63) / 64);
-  DISPATCH_T(h->cfg.dtype, (gemm_kernel<T, true><<<grid, 256, 0, st>>>(static_cast<const T*>(X), ldx, Wq, scale,
-                                                                       M, N, K, Y, ldy, 0)));
+  DISPATCH_T(h->cfg.dtype, (gemm_kernel<T, T, true><<<grid, 256, 0, st>>>(static_cast<const T*>(X), ldx, Wq, scale,
+                                                                          M, N, K, Y, ldy, 0)));
   return cudaGetLastError();
 }
 

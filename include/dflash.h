@@ -121,8 +121,8 @@ typedef struct {
 } dflash_weights;
 
 /* Create a drafter: validates cfg, copies and repacks the layer weights into
- * library-owned device buffers (fused QKV, fused gate/up, fused context-K/V, RMSNorm
- * weights folded where the kernels need it), allocates the paged K/V pool of
+ * library-owned device buffers (fused QKV, fused gate/up, fused context-K/V), allocates
+ * the paged K/V pool of
  * cfg.num_pages pages and the scratch for cfg.max_batch sequences, builds the RoPE
  * table (from_weights.rs inv_freq / YaRN block, in float64 on the host), and quantises
  * the lm_head to e4m3 when asked (from_weights.rs FP8 block).  Synchronises `stream`.

@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+from block_diffusion_drafter_forward_gb300 import dflash_gemm_bf16
 from synth.inputs import draw
 from synth.torch_io import to_torch
 
@@ -23,7 +24,6 @@ def bf16_to_f64(bits):
 @pytest.mark.parametrize("N,K,M", [(128, 64, 16), (256, 512, 16), (5120, 2048, 16), (384, 128, 48),
                                    (1000, 256, 100), (2048, 6144, 512), (640, 4096, 272)])
 def test_gemm_bf16_matches_exact_product(N, K, M):
-    from block_diffusion_drafter_forward_gb300 import dflash_gemm_bf16
     w = draw(7, f"w{N}_{K}", (N, K), 0.0, 0.02, "bf16")
     x = draw(8, f"x{M}_{K}", (M, K), 0.0, 1.0, "bf16")
     W, X = to_torch(w, "bf16"), to_torch(x, "bf16")

@@ -8,11 +8,13 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.dflash_oracle import Oracle, page_slots
+from block_diffusion_drafter_forward_gb300 import dflash_fp8_lm_head
+from block_diffusion_drafter_forward_gb300._lib import DFLASH_DEV_BAD_PAGE
+from oracle.dflash_oracle import Oracle, fp8_quantize_rows, page_slots, to_f64
 from synth import CONFIGS, WORKLOADS, make_workload
 from synth.torch_io import to_torch
 
-from helpers import TOL, Rig, as_f64, check_band, pool_rows, pool_view, rel_err
+from helpers import TOL, DevView, Rig, as_f64, check_band, pool_rows, pool_view, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -131,7 +133,6 @@ def test_bad_page_id_sets_flag_without_fault():
     bad = rig.page_tables.clone()
     bad[0, 1] = wl.num_pages + 7          # the page holding rows 16..31 (ctx and block rows)
     rig.drafter.propose(rig.bonus, rig.ctx_lens, bad, wl.max_ctx_len)
-    from block_diffusion_drafter_forward_gb300._lib import DFLASH_DEV_BAD_PAGE
     assert rig.drafter.device_status() & DFLASH_DEV_BAD_PAGE
     assert rig.drafter.device_status() == 0   # cleared by the read
     rig.propose()                              # the handle stays usable
@@ -181,12 +182,9 @@ def test_fp8_head_small():
 
 def test_fp8_head_codes_and_scales_bit_exact():
     """The create-time e4m3 quantisation of the lm_head, byte for byte."""
-    from oracle.dflash_oracle import fp8_quantize_rows, to_f64
-    from block_diffusion_drafter_forward_gb300 import dflash_fp8_lm_head
     wl = make_workload(CONFIGS["qwen3_8l_fp8head"], 52, [16])
     rig = Rig(wl, write=False)
     codes_ptr, scale_ptr = dflash_fp8_lm_head(rig.drafter.handle)
-    from helpers import DevView
     V, H = wl.cfg.vocab, wl.cfg.hidden
     codes = torch.as_tensor(DevView(codes_ptr, V * H, "|u1"), device="cuda").view(V, H)
     scale = torch.as_tensor(DevView(scale_ptr, V, "<f4"), device="cuda")
