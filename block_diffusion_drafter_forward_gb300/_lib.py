@@ -66,7 +66,8 @@ class dflash_weights(ctypes.Structure):
 
 EXPORTS = ("dflash_create", "dflash_destroy", "dflash_write_ctx_kv", "dflash_propose", "dflash_kv_layout",
            "dflash_device_status", "dflash_last_error", "dflash_fp8_lm_head", "dflash_profile",
-           "dflash_profile_kinds", "dflash_profile_read", "dflash_gemm_bf16")
+           "dflash_profile_kinds", "dflash_profile_read", "dflash_gemm_bf16",
+           "dflash_attention_check")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -103,6 +104,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_profile_read.restype = c.c_int
     lib.dflash_gemm_bf16.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp]
     lib.dflash_gemm_bf16.restype = c.c_int
+    lib.dflash_attention_check.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp]
+    lib.dflash_attention_check.restype = c.c_int
     lib.dflash_last_error.argtypes = [vp]
     lib.dflash_last_error.restype = c.c_char_p
     _lib = lib
@@ -193,3 +196,11 @@ def dflash_gemm_bf16(W: int, N: int, K: int, X: int, M: int, out: int, stream: i
     """out[M, N] fp32 = X[M, K] . W[N, K]^T on the tensor-core GEMM (device pointers)."""
     _check(load().dflash_gemm_bf16(ctypes.c_void_p(W), N, K, ctypes.c_void_p(X), M, ctypes.c_void_p(out), 1,
                                    ctypes.c_void_p(stream)), None)
+
+
+def dflash_attention_check(handle: int, layer: int, ctx_lens: int, page_tables: int, nb: int, max_ctx_len: int,
+                           out_cuda_core: int, out_tensor_core: int, stream: int = 0) -> None:
+    _check(load().dflash_attention_check(ctypes.c_void_p(handle), layer, ctypes.c_void_p(ctx_lens),
+                                         ctypes.c_void_p(page_tables), nb, max_ctx_len,
+                                         ctypes.c_void_p(out_cuda_core), ctypes.c_void_p(out_tensor_core),
+                                         ctypes.c_void_p(stream)), ctypes.c_void_p(handle))

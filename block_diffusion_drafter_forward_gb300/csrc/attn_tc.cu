@@ -1,0 +1,342 @@
+// Paged GQA block attention on the tensor cores (tcgen05 + TMEM).
+//
+// What it computes (memra-engine `dflash.rs` forward_round, `sdpa_naive(..., causal =
+// false)`; spark_model `from_weights.rs`: paged BF16 prefill kernel with the causal mask
+// off): for sequence s, query head h and block row r,
+//     o = softmax_j(q . k_j / sqrt(hd) + mask_j) v_j  over keys j = 0 .. ctx_len_s + 15,
+// with kv head h / (nh / nkv); on sliding layers key j is masked for the query at position
+// p = ctx_len_s + r iff p - j >= window.  Non-causal: every block row sees every block key.
+//
+// Work unit = (sequence, kv head): its 8 query heads x 16 block rows are the 128 rows of one
+// UMMA tile (M = 128), so every K/V byte read from HBM feeds 128 query rows.  Keys go in
+// chunks of 128 (8 pages): S = Q K^T and O = P V are each 8 tcgen05.mma into TMEM.  Pages
+// are fetched whole (4 KB bulk copies through the page table) into a 2-stage ring; the pool
+// stores each page tile in the 8x8-block operand layout, so no reshuffle is needed.
+// Softmax runs one query row per thread (no cross-thread reductions), online over chunks.
+// Split-KV: a unit's chunks are shared by several CTAs; each writes (O, m, l) partials and
+// the last one (atomic counter) combines them in split order.
+#include <float.h>
+
+#include <algorithm>
+
+#include "attn_tc.cuh"
+#include "dflash_internal.cuh"
+#include "tc_common.cuh"
+
+namespace dflash {
+namespace {
+
+using namespace tc;
+
+constexpr int kKC = 128;              // keys per chunk
+constexpr int kPagesPerChunk = kKC / kPage;
+constexpr int kTileBytes = kPage * 128 * 2;    // one page of one head: 16 x 128 bf16 = 4 KB
+constexpr int kQBytes = 128 * 128 * 2;         // 32 KB
+constexpr int kPBytes = 128 * kKC * 2;         // 32 KB
+constexpr int kKVStage = 2 * kPagesPerChunk * kTileBytes;  // K + V of one chunk: 64 KB
+constexpr int kStages = 2;
+constexpr int kSmem = kQBytes + kPBytes + kStages * kKVStage + 256 + 1024;
+
+// Chunks of 128 keys a sequence with `ctx` cached rows visits, starting at *first_key
+// (page aligned; on sliding layers the first key any block row can see).
+__host__ __device__ inline int chunk_range(int window, int ctx, int* first_key) {
+  const int nkeys = ctx + kGamma;
+  int k0 = 0;
+  if (window > 0) {
+    k0 = ctx - window + 1;
+    if (k0 < 0) k0 = 0;
+    k0 &= ~(kPage - 1);
+  }
+  *first_key = k0;
+  return (nkeys - k0 + kKC - 1) / kKC;
+}
+
+__global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sP = sQ + kQBytes;
+  uint8_t* sKV = sP + kPBytes;
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + kStages * kKVStage);
+  uint64_t* s_done = kv_full + kStages;
+  uint64_t* o_done = s_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int t = threadIdx.x, warp = t >> 5;
+  const int unit = blockIdx.x, split = blockIdx.y;
+  const int s = unit / p.nkv, g = unit % p.nkv;
+  const int group = p.nh / p.nkv;  // 8
+
+  pdl_wait();
+  const int ctx = p.ctx_lens[s];
+  if (ctx < 0 || ctx > p.max_ctx || ctx + kGamma > p.mpps * kPage) {
+    if (t == 0 && split == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
+    return;
+  }
+  int k0;
+  const int nch = chunk_range(p.window, ctx, &k0);
+  const int nsplit = (nch + p.chunks_per_split - 1) / p.chunks_per_split;
+  if (nsplit > (int)gridDim.y) {  // cannot happen for ctx <= max_ctx; never drop keys silently
+    if (t == 0 && split == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
+    return;
+  }
+  if (split >= nsplit) return;
+  const int c_begin = split * p.chunks_per_split;
+  const int c_end = min(nch, c_begin + p.chunks_per_split);
+  const int nkeys = ctx + kGamma;
+  const int32_t* pt = p.page_tables + (int64_t)s * p.mpps;
+  const int npages_seq = (nkeys + kPage - 1) / kPage;
+
+  if (t == 0) {
+    for (int i = 0; i < kStages; ++i) mbar_init(&kv_full[i], 1);
+    mbar_init(s_done, 1);
+    mbar_init(o_done, 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 128;
+
+  // issue the page loads of chunk c into stage st (thread 0)
+  auto load_chunk = [&](int c, int st) {
+    uint8_t* dK = sKV + st * kKVStage;
+    uint8_t* dV = dK + kPagesPerChunk * kTileBytes;
+    mbar_arrive_expect_tx(&kv_full[st], 2 * kPagesPerChunk * kTileBytes);
+    const int pg0 = (k0 + c * kKC) / kPage;
+    for (int i = 0; i < kPagesPerChunk; ++i) {
+      const int lp = pg0 + i;
+      int page = pt[lp < npages_seq ? lp : 0];
+      if (page < 0 || page >= p.g.num_pages) {
+        atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
+        page = 0;
+      }
+      const __nv_bfloat16* kt = p.pool + tile_base(p.g, p.layer, page, 0, g);
+      const __nv_bfloat16* vt = p.pool + tile_base(p.g, p.layer, page, 1, g);
+      bulk_load(dK + i * kTileBytes, kt, kTileBytes, &kv_full[st]);
+      bulk_load(dV + i * kTileBytes, vt, kTileBytes, &kv_full[st]);
+    }
+  };
+  if (t == 0) {
+    load_chunk(c_begin, 0);
+    if (c_begin + 1 < c_end) load_chunk(c_begin + 1, 1);
+  }
+
+  // Q tile: row i = hh * 16 + r  <-  q[s*16 + r, (g*group + hh) * 128 + :], 8x8-block layout
+  {
+    const int hh = t >> 4, r = t & 15;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)(s * kGamma + r) * p.nh + g * group + hh) * 128);
+#pragma unroll
+    for (int d8 = 0; d8 < 16; ++d8) {
+      const uint4 v = src[d8];
+      *reinterpret_cast<uint4*>(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16) = v;
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  const int r = t & 15;
+  const int pos_q = ctx + r;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+  float m_run = -FLT_MAX, l_run = 0.f;
+  float o[128];
+#pragma unroll
+  for (int i = 0; i < 128; ++i) o[i] = 0.f;
+  constexpr uint32_t idesc = idesc_bf16(128, 128);
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  bool ok = true;
+
+  for (int c = c_begin; c < c_end && ok; ++c) {
+    const int it = c - c_begin, st = it & 1;
+    uint8_t* sK = sKV + st * kKVStage;
+    uint8_t* sV = sK + kPagesPerChunk * kTileBytes;
+    if (t == 0) {
+      if (!mbar_wait(&kv_full[st], (it >> 1) & 1)) flags[0] = 1;
+      tc_fence_after();
+      if (!flags[0]) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_bf16(tS, desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048), idesc,
+                   k > 0 ? 1u : 0u);
+      }
+      mma_commit(s_done);
+    }
+    if (!mbar_wait(s_done, it & 1)) flags[0] = 1;
+    tc_fence_after();
+    // ---- softmax of this chunk, one query row per thread (two passes over the S row in
+    // TMEM: masked maximum, then probabilities written as the bf16 P operand)
+    const int kbase = k0 + c * kKC;
+    float mc = -FLT_MAX;
+#pragma unroll
+    for (int q4 = 0; q4 < kKC / 32; ++q4) {
+      float v[32];
+      tmem_ld32(tS + lane_off + q4 * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int key = kbase + q4 * 32 + j;
+        const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
+        if (vis) mc = fmaxf(mc, v[j] * scale_log2);
+      }
+    }
+    const float m_new = fmaxf(m_run, mc);
+    const float alpha = m_new == -FLT_MAX ? 1.f : exp2f(m_run - m_new);
+    float lsum = 0.f;
+#pragma unroll
+    for (int q4 = 0; q4 < kKC / 32; ++q4) {
+      float v[32];
+      tmem_ld32(tS + lane_off + q4 * 32, v);
+#pragma unroll
+      for (int j8 = 0; j8 < 4; ++j8) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float pr[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int jj = j8 * 8 + 2 * e + u;
+            const int key = kbase + q4 * 32 + jj;
+            const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
+            pr[u] = vis ? exp2f(v[jj] * scale_log2 - m_new) : 0.f;
+          }
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
+          lsum += __low2float(h2) + __high2float(h2);  // the normaliser sums what the MMA uses
+          pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(sP + ((t >> 3) * 16 + q4 * 4 + j8) * 128 + (t & 7) * 16) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    l_run = l_run * alpha + lsum;
+    m_run = m_new;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (t == 0) {
+      tc_fence_after();
+      if (!flags[0]) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_bf16(tO, desc_noswz(sP + k * 256, 128, 2048), desc_noswz(sV + k * kTileBytes, 128, 256), idesc,
+                   k > 0 ? 1u : 0u);
+      }
+      mma_commit(o_done);
+    }
+    if (!mbar_wait(o_done, it & 1)) flags[0] = 1;
+    tc_fence_after();
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float v[32];
+      tmem_ld32(tO + lane_off + q4 * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[q4 * 32 + j] = o[q4 * 32 + j] * alpha + v[j];
+    }
+    tc_fence_before();
+    __syncthreads();
+    // the stage is free again: prefetch chunk c + 2 into it
+    if (t == 0 && c + 2 < c_end && !flags[0]) load_chunk(c + 2, st);
+    ok = !flags[0];
+  }
+
+  const int hh = t >> 4;
+  __nv_bfloat16* dst = p.out + ((int64_t)(s * kGamma + r) * p.nh + g * group + hh) * 128;
+  if (!ok) {
+    if (t == 0) atomicOr(p.status, DFLASH_DEV_TIMEOUT);
+    for (int i = 0; i < 2000; ++i) __nanosleep(1000);
+  } else if (nsplit == 1) {
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+    for (int d8 = 0; d8 < 16; ++d8) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[d8 * 8 + 2 * e] * inv, o[d8 * 8 + 2 * e + 1] * inv);
+        pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      reinterpret_cast<uint4*>(dst)[d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  } else {
+    // partial (O unnormalised, m, l) of this split; the last split of the unit combines
+    const int64_t slot = (int64_t)unit * gridDim.y + split;
+    float* op = p.o_part + (slot * 128 + t) * 128;
+#pragma unroll
+    for (int i = 0; i < 128; i += 4) __stcg(reinterpret_cast<float4*>(op + i), make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
+    p.ml_part[(slot * 128 + t) * 2 + 0] = m_run;
+    p.ml_part[(slot * 128 + t) * 2 + 1] = l_run;
+    __threadfence();
+    __syncthreads();
+    if (t == 0) flags[1] = atomicAdd(&p.counters[unit], 1u) == (unsigned)(nsplit - 1);
+    __syncthreads();
+    if (flags[1]) {
+      __threadfence();
+      float mx = -FLT_MAX;
+      for (int q = 0; q < nsplit; ++q) mx = fmaxf(mx, __ldcg(p.ml_part + (((int64_t)unit * gridDim.y + q) * 128 + t) * 2));
+      float L = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) o[i] = 0.f;
+      for (int q = 0; q < nsplit; ++q) {
+        const int64_t sl = (int64_t)unit * gridDim.y + q;
+        const float mq = __ldcg(p.ml_part + (sl * 128 + t) * 2), lq = __ldcg(p.ml_part + (sl * 128 + t) * 2 + 1);
+        const float w = mq == -FLT_MAX ? 0.f : exp2f(mq - mx);
+        L += lq * w;
+        const float* src = p.o_part + (sl * 128 + t) * 128;
+#pragma unroll
+        for (int i = 0; i < 128; i += 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + i));
+          o[i] += v.x * w;
+          o[i + 1] += v.y * w;
+          o[i + 2] += v.z * w;
+          o[i + 3] += v.w * w;
+        }
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+      for (int d8 = 0; d8 < 16; ++d8) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[d8 * 8 + 2 * e] * inv, o[d8 * 8 + 2 * e + 1] * inv);
+          pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        reinterpret_cast<uint4*>(dst)[d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      if (t == 0) p.counters[unit] = 0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+}  // namespace
+
+// Partial slots any launch needs: units * splits <= num_sms + units (splits = ceil(nch / cps)
+// with cps = ceil(units * nch / num_sms)).
+int64_t attn_tc_partial_slots(int num_sms, int max_units) { return (int64_t)num_sms + max_units; }
+
+cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int units = nb * p.nkv;
+  // the most chunks any sequence with ctx <= max_ctx_len visits
+  int k0;
+  int nch = chunk_range(0, max_ctx_len, &k0);
+  if (p.window > 0) nch = std::min(nch, (p.window + kGamma + kPage + kKC - 1) / kKC);
+  int cps = (units * nch + num_sms - 1) / num_sms;
+  if (cps < 1) cps = 1;
+  const int splits = (nch + cps - 1) / cps;
+  p.chunks_per_split = cps;
+  p.max_ctx = max_ctx_len;
+  attn_tc_kernel<<<dim3(units, splits), 128, kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

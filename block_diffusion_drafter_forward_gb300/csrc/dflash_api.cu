@@ -9,6 +9,7 @@
 #include <string>
 
 #include "dflash_internal.cuh"
+#include "attn_tc.cuh"
 #include "gemm_tc.cuh"
 
 using namespace dflash;
@@ -43,24 +44,60 @@ cudaEvent_t ev_get(dflash_handle* h) {
   return e;
 }
 
+// Timing events: from the spare pool when launching eagerly; owned by the graph entry
+// (recorded as external event nodes) while capturing.
+cudaEvent_t ev_mark(dflash_handle* h, cudaStream_t st) {
+  cudaEvent_t e = nullptr;
+  if (h->cap_entry) {
+    cudaEventCreate(&e);
+    cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+  } else {
+    e = ev_get(h);
+    cudaEventRecord(e, st);
+  }
+  return e;
+}
+
 // Launch `call` as kernel kind `kind`: counted always, bracketed by events when profiling.
 #define KL(kind, call, where)                                                   \
   do {                                                                          \
-    cudaEvent_t e0_ = nullptr;                                                  \
-    if (h->prof.on) {                                                           \
-      e0_ = ev_get(h);                                                          \
-      cudaEventRecord(e0_, st);                                                 \
-    }                                                                           \
+    cudaEvent_t e0_ = h->prof.on ? ev_mark(h, st) : nullptr;                    \
     CK((call), where);                                                          \
-    h->prof.launches[kind]++;                                                   \
+    if (h->cap_entry)                                                           \
+      h->cap_entry->kind_counts[kind]++;                                        \
+    else                                                                        \
+      h->prof.launches[kind]++;                                                 \
     if (h->prof.on) {                                                           \
-      cudaEvent_t e1_ = ev_get(h);                                              \
-      cudaEventRecord(e1_, st);                                                 \
-      h->prof.pending.push_back({(int)(kind), {e0_, e1_}});                     \
+      cudaEvent_t e1_ = ev_mark(h, st);                                         \
+      auto& list_ = h->cap_entry ? h->cap_entry->evs : h->prof.pending;         \
+      list_.push_back({(int)(kind), {e0_, e1_}});                               \
     }                                                                           \
   } while (0)
 
+void graph_collect(dflash_handle* h) {
+  for (dflash::GraphEntry* g : h->graphs) {
+    if (!g->pending) continue;
+    for (auto& p : g->evs) {
+      float ms = 0.f;
+      if (cudaEventSynchronize(p.second.second) == cudaSuccess &&
+          cudaEventElapsedTime(&ms, p.second.first, p.second.second) == cudaSuccess)
+        h->prof.ms[p.first] += ms;
+    }
+    g->pending = false;
+  }
+}
+
+void graph_free(dflash::GraphEntry* g) {
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  for (auto& p : g->evs) {
+    cudaEventDestroy(p.second.first);
+    cudaEventDestroy(p.second.second);
+  }
+  delete g;
+}
+
 void prof_drain(dflash_handle* h) {
+  graph_collect(h);
   for (auto& p : h->prof.pending) {
     float ms = 0.f;
     if (cudaEventSynchronize(p.second.second) == cudaSuccess &&
@@ -87,6 +124,10 @@ void free_all(dflash_handle* h) {
   for (void* p : h->allocs) cudaFree(p);
   h->allocs.clear();
   prof_drain(h);
+  for (dflash::GraphEntry* g : h->graphs) graph_free(g);
+  h->graphs.clear();
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  h->cap_stream = nullptr;
   for (cudaEvent_t e : h->prof.spare) cudaEventDestroy(e);
   h->prof.spare.clear();
 }
@@ -194,7 +235,27 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.pool = static_cast<__nv_bfloat16*>(h->pool);
       KL(K_QKV, launch_gemm_tc(EPI_QKV, w.w_qkv, qkvd, H, h->xb, H, M, p, splits(qkvd, H), st, l > 0), "qkv");
     }
-    KL(K_ATTN, launch_attention(h, l, h->q, ctx_lens, page_tables, nb, max_ctx_len, h->attn, st), "attention");
+    if (h->tc_attn) {
+      AttnParams a;
+      a.q = static_cast<const __nv_bfloat16*>(h->q);
+      a.pool = static_cast<const __nv_bfloat16*>(h->pool);
+      a.g = h->geom;
+      a.layer = l;
+      a.ctx_lens = ctx_lens;
+      a.page_tables = page_tables;
+      a.mpps = c.max_pages_per_seq;
+      a.nh = c.n_q_heads;
+      a.nkv = c.n_kv_heads;
+      a.window = c.layer_sliding[l] ? c.sliding_window : 0;
+      a.o_part = h->attn_opart;
+      a.ml_part = h->attn_ml;
+      a.counters = h->attn_counters;
+      a.out = static_cast<__nv_bfloat16*>(h->attn);
+      a.status = h->d_status;
+      KL(K_ATTN, launch_attn_tc(a, nb, max_ctx_len, h->num_sms, st), "attention");
+    } else {
+      KL(K_ATTN, launch_attention(h, l, h->q, ctx_lens, page_tables, nb, max_ctx_len, h->attn, st), "attention");
+    }
     {
       GemmParams p = base;
       p.x = h->x;
@@ -240,6 +301,9 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
   }
   return DFLASH_OK;
 }
+
+int propose_graph(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens, const int32_t* page_tables,
+                  int nb, int max_ctx_len, int32_t* draft_tokens, void* logits, void* final_hidden, cudaStream_t st);
 
 }  // namespace
 
@@ -423,6 +487,22 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     }
     h->ws_floats = need;
     ALLOC(h->ws, need * 4);
+    h->tc_attn = (nh / nkv) == 8;
+    if (h->tc_attn) {
+      const int64_t units = (int64_t)c.max_batch * nkv;
+      const int64_t slots = attn_tc_partial_slots(h->num_sms, (int)units);
+      ALLOC(h->attn_opart, slots * 128 * 128 * 4);
+      ALLOC(h->attn_ml, slots * 128 * 2 * 4);
+      ALLOC(h->attn_counters, units * sizeof(unsigned));
+      if (cudaMemsetAsync(h->attn_counters, 0, units * sizeof(unsigned), st) != cudaSuccess) {
+        fail(h, DFLASH_ECUDA, "counter memset");
+        return bail(DFLASH_ECUDA);
+      }
+    }
+  }
+  if (cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    fail(h, DFLASH_ECUDA, "capture stream");
+    return bail(DFLASH_ECUDA);
   }
   ALLOC(h->d_status, sizeof(unsigned));
   if (cudaMemsetAsync(h->d_status, 0, sizeof(unsigned), st) != cudaSuccess) {
@@ -494,8 +574,18 @@ int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t*
     return fail(h, DFLASH_ECAPACITY, "max_ctx_len + gamma beyond the page-table capacity");
   if (!bonus_tokens || !ctx_lens || !page_tables || !draft_tokens) return fail(h, DFLASH_EINVAL, "null pointer");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (h->tc) return propose_tc(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits,
-                               final_hidden, st);
+  return propose_graph(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits, final_hidden,
+                       st);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The fp32 gamma-block forward on the CUDA-core kernels, launched eagerly on st.
+int propose_simple(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens, const int32_t* page_tables,
+                   int nb, int max_ctx_len, int32_t* draft_tokens, void* logits, void* final_hidden, cudaStream_t st) {
+  const dflash_cfg& c = h->cfg;
   const int M = nb * kGamma;
   const int H = c.hidden, F = c.n_ff, qd = c.n_q_heads * c.head_dim;
   const int qkvd = qd + 2 * c.n_kv_heads * c.head_dim;
@@ -522,6 +612,77 @@ int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t*
   KL(K_ARGMAX, launch_argmax(h, h->logits32, nb, draft_tokens, logits, st), "argmax");
   return DFLASH_OK;
 }
+
+int propose_eager(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens, const int32_t* page_tables,
+                  int nb, int max_ctx_len, int32_t* draft_tokens, void* logits, void* final_hidden, cudaStream_t st) {
+  if (h->tc)
+    return propose_tc(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits, final_hidden, st);
+  return propose_simple(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits, final_hidden,
+                        st);
+}
+
+// Replay the CUDA graph captured for these arguments (capturing it on first use on a private
+// stream); the whole forward is then one graph launch on the caller's stream.
+int propose_graph(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens, const int32_t* page_tables,
+                  int nb, int max_ctx_len, int32_t* draft_tokens, void* logits, void* final_hidden, cudaStream_t st) {
+  const void* args[6] = {bonus_tokens, ctx_lens, page_tables, draft_tokens, logits, final_hidden};
+  GraphEntry* e = nullptr;
+  for (GraphEntry* g : h->graphs)
+    if (g->nb == nb && g->max_ctx == max_ctx_len && g->prof == h->prof.on &&
+        memcmp(g->args, args, sizeof(args)) == 0) {
+      e = g;
+      break;
+    }
+  if (!e) {
+    if (h->graphs.size() >= 8) {
+      auto it = std::min_element(h->graphs.begin(), h->graphs.end(),
+                                 [](GraphEntry* a, GraphEntry* b) { return a->stamp < b->stamp; });
+      graph_collect(h);
+      CK(cudaStreamSynchronize(st), "graph evict sync");
+      graph_free(*it);
+      h->graphs.erase(it);
+    }
+    e = new GraphEntry();
+    e->nb = nb;
+    e->max_ctx = max_ctx_len;
+    memcpy(e->args, args, sizeof(args));
+    e->prof = h->prof.on;
+    cudaError_t err = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeRelaxed);
+    if (err != cudaSuccess) {
+      graph_free(e);
+      return cuda_fail(h, err, "begin capture");
+    }
+    h->cap_entry = e;
+    const int rc = propose_eager(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits,
+                                 final_hidden, h->cap_stream);
+    h->cap_entry = nullptr;
+    cudaGraph_t graph = nullptr;
+    err = cudaStreamEndCapture(h->cap_stream, &graph);
+    if (rc != DFLASH_OK || err != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      graph_free(e);
+      cudaGetLastError();
+      return rc != DFLASH_OK ? rc : cuda_fail(h, err, "end capture");
+    }
+    err = cudaGraphInstantiate(&e->exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (err != cudaSuccess) {
+      graph_free(e);
+      return cuda_fail(h, err, "graph instantiate");
+    }
+    h->graphs.push_back(e);
+  }
+  e->stamp = ++h->graph_clock;
+  if (h->prof.on) graph_collect(h);
+  for (int k = 0; k < K_COUNT; ++k) h->prof.launches[k] += e->kind_counts[k];
+  CK(cudaGraphLaunch(e->exec, st), "graph launch");
+  if (!e->evs.empty()) e->pending = true;
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
 
 int dflash_kv_layout(const dflash_handle* h, void** pool, size_t* bytes, int64_t strides[6]) {
   if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
@@ -571,6 +732,38 @@ int dflash_gemm_bf16(const void* W, int32_t N, int32_t K, const void* X, int32_t
   p.ldo = N;
   cudaError_t e = launch_gemm_tc(EPI_STORE, W, N, K, X, K, M, p, 1, reinterpret_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return fail(nullptr, DFLASH_ECUDA, std::string("gemm: ") + cudaGetErrorString(e));
+  return DFLASH_OK;
+}
+
+int dflash_attention_check(dflash_handle* h, int32_t layer, const int32_t* ctx_lens, const int32_t* page_tables,
+                           int32_t nb, int32_t max_ctx_len, void* out_cuda_core, void* out_tensor_core,
+                           dflash_stream stream) {
+  if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
+  const dflash_cfg& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers || nb < 1 || nb > c.max_batch || max_ctx_len < 0 ||
+      (int64_t)max_ctx_len + kGamma > (int64_t)kPage * c.max_pages_per_seq || !ctx_lens || !page_tables ||
+      !out_cuda_core || !out_tensor_core)
+    return fail(h, DFLASH_EINVAL, "bad argument");
+  if (!h->tc_attn) return fail(h, DFLASH_EUNSUPPORTED, "no tensor-core attention for this configuration");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  CK(launch_attention(h, layer, h->q, ctx_lens, page_tables, nb, max_ctx_len, out_cuda_core, st), "attention");
+  AttnParams a;
+  a.q = static_cast<const __nv_bfloat16*>(h->q);
+  a.pool = static_cast<const __nv_bfloat16*>(h->pool);
+  a.g = h->geom;
+  a.layer = layer;
+  a.ctx_lens = ctx_lens;
+  a.page_tables = page_tables;
+  a.mpps = c.max_pages_per_seq;
+  a.nh = c.n_q_heads;
+  a.nkv = c.n_kv_heads;
+  a.window = c.layer_sliding[layer] ? c.sliding_window : 0;
+  a.o_part = h->attn_opart;
+  a.ml_part = h->attn_ml;
+  a.counters = h->attn_counters;
+  a.out = static_cast<__nv_bfloat16*>(out_tensor_core);
+  a.status = h->d_status;
+  CK(launch_attn_tc(a, nb, max_ctx_len, h->num_sms, st), "attention tc");
   return DFLASH_OK;
 }
 

@@ -71,6 +71,18 @@ struct Prof {
   std::vector<cudaEvent_t> spare;
 };
 
+// One captured propose (CUDA graph) and the arguments it was captured with.
+struct GraphEntry {
+  int nb = 0, max_ctx = 0;
+  const void* args[6] = {};           // bonus, ctx_lens, page_tables, drafts, logits, hidden
+  bool prof = false;                  // captured with per-kernel timing events
+  cudaGraphExec_t exec = nullptr;
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> evs;  // owned timing events
+  int64_t kind_counts[K_COUNT] = {};
+  bool pending = false;               // events of the last launch not yet accumulated
+  uint64_t stamp = 0;
+};
+
 // ---------------------------------------------------------------- the handle
 struct LayerW {
   void* ln_in = nullptr;
@@ -133,10 +145,19 @@ struct dflash_handle {
   unsigned* counters = nullptr;        // split-K / argmax counters (zero between launches)
   float* amax_val = nullptr;           // [V/128 tiles, rows] per-tile argmax partials
   int* amax_idx = nullptr;
+  float* attn_opart = nullptr;         // attention split partials (O)
+  float* attn_ml = nullptr;            // attention split partials (max, sum)
+  unsigned* attn_counters = nullptr;   // per (sequence, kv head) unit
   bool tc = false;                     // bf16 tensor-core path in use
+  bool tc_attn = false;                // tensor-core attention (8 query heads per kv head)
 
   unsigned* d_status = nullptr;        // device status word
   dflash::Prof prof;
+  // CUDA graphs of dflash_propose, keyed by its arguments (small LRU)
+  std::vector<dflash::GraphEntry*> graphs;
+  uint64_t graph_clock = 0;
+  cudaStream_t cap_stream = nullptr;   // private stream used only for capture
+  dflash::GraphEntry* cap_entry = nullptr;  // non-null while capturing
   std::string err;
 };
 

@@ -203,6 +203,14 @@ int dflash_profile_read(dflash_handle* h, int kind, const char** name, double* t
 int dflash_gemm_bf16(const void* W, int32_t N, int32_t K, const void* X, int32_t M, float* out,
                      int32_t nsplit, dflash_stream stream);
 
+/* Attention cross-check (for tests, bf16 handles with 8 query heads per kv head): runs the
+ * CUDA-core and the tensor-core block attention of `layer` on the queries left in the
+ * handle by the last dflash_propose (its last layer's) and the pool, writing both
+ * [nb*gamma, nh*hd] bf16 outputs.  Arguments as in dflash_propose. */
+int dflash_attention_check(dflash_handle* h, int32_t layer, const int32_t* ctx_lens,
+                           const int32_t* page_tables, int32_t nb, int32_t max_ctx_len,
+                           void* out_cuda_core, void* out_tensor_core, dflash_stream stream);
+
 /* Synchronise `stream`, read the device status word into *flags (may be NULL) and clear
  * it.  Returns DFLASH_EDEVICE when any bit was set, else DFLASH_OK. */
 int dflash_device_status(dflash_handle* h, dflash_stream stream, uint32_t* flags);

@@ -4,7 +4,8 @@ import numpy as np
 import pytest
 import torch
 
-from block_diffusion_drafter_forward_gb300 import dflash_gemm_bf16
+from block_diffusion_drafter_forward_gb300 import dflash_attention_check, dflash_gemm_bf16
+from synth import CONFIGS, make_workload
 from synth.inputs import draw
 from synth.torch_io import to_torch
 
@@ -35,3 +36,27 @@ def test_gemm_bf16_matches_exact_product(N, K, M):
     # fp32 accumulation of K products: error well below 1e-5 of the output scale
     err = np.abs(got - ref).max() / np.abs(ref).max()
     assert np.isfinite(got).all() and err < 2e-5, err
+
+
+@pytest.mark.parametrize("cfgname,ctx", [("qwen3_8l_bf16", [4096]), ("qwen3_8l_bf16", [0, 17, 300, 129]),
+                                         ("wide_5l_yarn_bf16", [3000])])
+def test_tensor_core_attention_matches_cuda_core(cfgname, ctx):
+    """Same queries, same paged pool: the tcgen05 attention (split-KV, chunked online
+    softmax, bf16 probabilities) against the CUDA-core one (fp32 online softmax)."""
+    from helpers import Rig
+    cfg = CONFIGS[cfgname]
+    wl = make_workload(cfg, 61, ctx)
+    rig = Rig(wl)
+    rig.propose()
+    M = wl.nb * 16
+    layers = [cfg.n_layers - 1] + ([0] if cfg.sliding(0) else [])
+    for layer in layers:
+        a = torch.zeros((M, cfg.q_dim), dtype=torch.bfloat16, device="cuda")
+        b = torch.zeros_like(a)
+        dflash_attention_check(rig.drafter.handle, layer, rig.ctx_lens.data_ptr(), rig.page_tables.data_ptr(),
+                               wl.nb, wl.max_ctx_len, a.data_ptr(), b.data_ptr(),
+                               torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert rig.drafter.device_status() == 0
+        err = ((a.float() - b.float()).abs().max() / a.float().abs().max()).item()
+        assert err < 1e-2, (layer, err)
