@@ -14,7 +14,7 @@
 // stores each page tile in the 8x8-block operand layout, so no reshuffle is needed.
 // Softmax runs one query row per thread (no cross-thread reductions), online over chunks.
 // Split-KV: a unit's chunks are shared by several CTAs; each writes (O, m, l) partials and
-// the last one (atomic counter) combines them in split order.
+// attn_combine_kernel merges them (all units and rows in parallel, in split order).
 #include <float.h>
 
 #include <algorithm>
@@ -260,56 +260,58 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
       reinterpret_cast<uint4*>(dst)[d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   } else {
-    // partial (O unnormalised, m, l) of this split; the last split of the unit combines
+    // partial (O unnormalised, m, l) of this split; attn_combine_kernel merges the splits
     const int64_t slot = (int64_t)unit * gridDim.y + split;
     float* op = p.o_part + (slot * 128 + t) * 128;
 #pragma unroll
-    for (int i = 0; i < 128; i += 4) __stcg(reinterpret_cast<float4*>(op + i), make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
-    p.ml_part[(slot * 128 + t) * 2 + 0] = m_run;
-    p.ml_part[(slot * 128 + t) * 2 + 1] = l_run;
-    __threadfence();
-    __syncthreads();
-    if (t == 0) flags[1] = atomicAdd(&p.counters[unit], 1u) == (unsigned)(nsplit - 1);
-    __syncthreads();
-    if (flags[1]) {
-      __threadfence();
-      float mx = -FLT_MAX;
-      for (int q = 0; q < nsplit; ++q) mx = fmaxf(mx, __ldcg(p.ml_part + (((int64_t)unit * gridDim.y + q) * 128 + t) * 2));
-      float L = 0.f;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) o[i] = 0.f;
-      for (int q = 0; q < nsplit; ++q) {
-        const int64_t sl = (int64_t)unit * gridDim.y + q;
-        const float mq = __ldcg(p.ml_part + (sl * 128 + t) * 2), lq = __ldcg(p.ml_part + (sl * 128 + t) * 2 + 1);
-        const float w = mq == -FLT_MAX ? 0.f : exp2f(mq - mx);
-        L += lq * w;
-        const float* src = p.o_part + (sl * 128 + t) * 128;
-#pragma unroll
-        for (int i = 0; i < 128; i += 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + i));
-          o[i] += v.x * w;
-          o[i + 1] += v.y * w;
-          o[i + 2] += v.z * w;
-          o[i + 3] += v.w * w;
-        }
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-      for (int d8 = 0; d8 < 16; ++d8) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[d8 * 8 + 2 * e] * inv, o[d8 * 8 + 2 * e + 1] * inv);
-          pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        reinterpret_cast<uint4*>(dst)[d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
-      if (t == 0) p.counters[unit] = 0;
-    }
+    for (int i = 0; i < 128; i += 4)
+      __stcg(reinterpret_cast<float4*>(op + i), make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
+    __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// Merge the split partials of every (sequence, kv head) unit with more than one split:
+// o = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q, M = max_q m_q, in split order.
+// Block (unit, rb) owns rows 8 rb .. 8 rb + 7; 16 threads per row, 8 dims each.
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int splits_launched) {
+  pdl_wait();
+  const int unit = blockIdx.x, t = threadIdx.x;
+  const int s = unit / p.nkv, g = unit % p.nkv;
+  const int ctx = p.ctx_lens[s];
+  if (ctx < 0 || ctx > p.max_ctx || ctx + kGamma > p.mpps * kPage) return;
+  int k0;
+  const int nch = chunk_range(p.window, ctx, &k0);
+  const int nsplit = (nch + p.chunks_per_split - 1) / p.chunks_per_split;
+  if (nsplit <= 1 || nsplit > splits_launched) return;
+  const int row = blockIdx.y * 8 + (t >> 4), d0 = (t & 15) * 8;
+  const int64_t base = (int64_t)unit * splits_launched;
+  float mx = -FLT_MAX;
+  for (int q = 0; q < nsplit; ++q) mx = fmaxf(mx, __ldcg(p.ml_part + ((base + q) * 128 + row) * 2));
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float L = 0.f;
+  for (int q = 0; q < nsplit; ++q) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ml_part + ((base + q) * 128 + row) * 2));
+    const float w = ml.x == -FLT_MAX ? 0.f : exp2f(ml.x - mx);
+    L += ml.y * w;
+    const float* src = p.o_part + ((base + q) * 128 + row) * 128 + d0;
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
+    acc[0] += a.x * w; acc[1] += a.y * w; acc[2] += a.z * w; acc[3] += a.w * w;
+    acc[4] += b.x * w; acc[5] += b.y * w; acc[6] += b.z * w; acc[7] += b.w * w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint32_t pk[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+    pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  const int hh = row >> 4, r = row & 15;
+  __nv_bfloat16* dst = p.out + ((int64_t)(s * kGamma + r) * p.nh + g * (p.nh / p.nkv) + hh) * 128 + d0;
+  *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
 }
 
 }  // namespace
@@ -336,7 +338,18 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   p.chunks_per_split = cps;
   p.max_ctx = max_ctx_len;
   attn_tc_kernel<<<dim3(units, splits), 128, kSmem, st>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || splits == 1) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(units, 16);
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, splits);
 }
 
 }  // namespace dflash

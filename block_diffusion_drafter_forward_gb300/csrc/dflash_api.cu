@@ -286,18 +286,18 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
   }
   KL(K_NORM, launch_rmsnorm_f32in(h, h->x, h->norm, h->xn, M, H, st), "final norm");
   if (final_hidden) KL(K_COPY, launch_copy_hidden(h, h->xn, M, final_hidden, st), "final hidden");
-  if (c.lm_head_dtype == DFLASH_FP8E4M3_ROWSCALE) {
-    KL(K_LMHEAD, launch_gemm_fp8w(h, h->xn, H, h->lm_fp8, h->lm_scale, M, c.vocab, H, h->logits32, c.vocab, st),
-       "lm_head");
-    KL(K_ARGMAX, launch_argmax(h, h->logits32, nb, draft_tokens, logits, st), "argmax");
-  } else {
+  {
+    const bool fp8 = c.lm_head_dtype == DFLASH_FP8E4M3_ROWSCALE;
     GemmParams p = base;
     p.logits = static_cast<__nv_bfloat16*>(logits);
     p.amax_val = h->amax_val;
     p.amax_idx = h->amax_idx;
     p.amax_counter = h->counters + kCounters - 64;
     p.drafts = draft_tokens;
-    KL(K_LMHEAD, launch_gemm_tc(EPI_LMHEAD, h->lm_head, c.vocab, H, h->xn, H, M, p, 1, st, false), "lm_head");
+    p.row_scale = fp8 ? h->lm_scale : nullptr;
+    KL(K_LMHEAD, launch_gemm_tc(EPI_LMHEAD, fp8 ? (const void*)h->lm_fp8 : h->lm_head, c.vocab, H, h->xn, H, M, p, 1,
+                                st, false, fp8),
+       "lm_head");
   }
   return DFLASH_OK;
 }

@@ -22,6 +22,8 @@
 //   EPI_LMHEAD: logits (optional, bf16), per-row fp32 scale for the FP8 head, per-tile
 //               argmax partials and, in the last tile, the per-row argmax -> drafts.
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <float.h>
 
 #include <mutex>
@@ -211,20 +213,27 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, float (&v)[16],
   }
 }
 
-template <int EPI, int TN, int STAGES>
+// FP8A: the weight arrives as e4m3 codes (TMA, 64-byte rows) and warps 2-3 widen each
+// stage to the bf16 128-byte-swizzled A tile before the MMA reads it (the per-row scale is
+// applied in the epilogue), so the activations stay bf16 (weight-only FP8).
+template <int EPI, int TN, int STAGES, bool FP8A>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmParams p) {
   constexpr int A_BYTES = 128 * 64 * 2;
   constexpr int B_BYTES = TN * 64 * 2;
-  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr int A8_BYTES = FP8A ? 128 * 64 : 0;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES + A8_BYTES;
+  constexpr uint32_t LOAD_BYTES = (FP8A ? A8_BYTES : A_BYTES) + B_BYTES;
+  constexpr int W_OFF = FP8A ? A_BYTES + B_BYTES : 0;  // where the TMA puts the weight tile
   constexpr uint32_t TMEM_COLS = TN < 32 ? 32 : TN;
   static_assert(sizeof(EpiSmem) <= STAGES * STAGE_BYTES, "epilogue scratch must fit in the stages");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* accf = empty + STAGES;
+  uint64_t* conv = empty + STAGES;   // FP8A: widened A tile ready (64 arrivals)
+  uint64_t* accf = conv + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] timed out, [1] last split
 
@@ -238,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&conv[s], 64);
     }
     mbar_init(accf, 1);
     flags[0] = 0;
@@ -259,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
       const int pre = nloc < STAGES ? nloc : STAGES;
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], STAGE_BYTES);
-        tma_load_2d(smem + i * STAGE_BYTES, &tmW, &full[i], (kb0 + i) * 64, tile_n * 128, pol_w);
+        mbar_arrive_expect_tx(&full[i], LOAD_BYTES);
+        tma_load_2d(smem + i * STAGE_BYTES + W_OFF, &tmW, &full[i], (kb0 + i) * 64, tile_n * 128, pol_w);
       }
       pdl_wait();  // everything the previous kernel wrote is visible from here on
       for (int i = 0; i < pre; ++i)
@@ -271,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           flags[0] = 1;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-        tma_load_2d(smem + s * STAGE_BYTES, &tmW, &full[s], (kb0 + i) * 64, tile_n * 128, pol_w);
+        mbar_arrive_expect_tx(&full[s], LOAD_BYTES);
+        tma_load_2d(smem + s * STAGE_BYTES + W_OFF, &tmW, &full[s], (kb0 + i) * 64, tile_n * 128, pol_w);
         tma_load_2d(smem + s * STAGE_BYTES + A_BYTES, &tmX, &full[s], (kb0 + i) * 64, tile_m * TN, pol_x);
       }
     }
@@ -283,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16(128, TN);
       for (int i = 0; i < nloc; ++i) {
         const int s = i % STAGES;
-        if (!mbar_wait(&full[s], (i / STAGES) & 1)) {
+        if (!mbar_wait(FP8A ? &conv[s] : &full[s], (i / STAGES) & 1)) {
           flags[0] = 1;
           break;
         }
@@ -295,6 +305,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&empty[s]);
       }
       mma_commit(accf);
+    }
+    __syncwarp();
+  } else if (FP8A) {
+    // ---------------- e4m3 -> bf16 widening (warps 2-3): thread ct owns rows ct, ct + 64
+    const int ct = t - 64;
+    for (int i = 0; i < nloc; ++i) {
+      const int s = i % STAGES;
+      if (!mbar_wait(&full[s], (i / STAGES) & 1)) {
+        flags[0] = 1;
+        mbar_arrive(&conv[s]);
+        break;
+      }
+      const uint8_t* a8 = smem + s * STAGE_BYTES + W_OFF;
+      uint8_t* a = smem + s * STAGE_BYTES;
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int row = ct + rr * 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = *reinterpret_cast<const uint4*>(a8 + row * 64 + q * 16);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(
+                  (__nv_fp8x2_storage_t)((w[e] >> (16 * hf)) & 0xFFFFu), __NV_E4M3);
+              const __half2 hh = *reinterpret_cast<const __half2*>(&h2);
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__low2float(hh), __high2float(hh));
+              o[e * 2 + hf] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+          }
+          // 16 codes -> two 16-byte chunks (8 bf16 each) of the 128-byte swizzled row
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int chunk = q * 2 + cc;
+            *reinterpret_cast<uint4*>(a + row * 128 + ((chunk ^ (row & 7)) * 16)) =
+                make_uint4(o[cc * 4 + 0], o[cc * 4 + 1], o[cc * 4 + 2], o[cc * 4 + 3]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&conv[s]);
     }
     __syncwarp();
   }
@@ -427,11 +481,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int EPI, int TN, int STAGES>
+template <int EPI, int TN, int STAGES, bool FP8A>
 cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
                      cudaStream_t st, bool pdl) {
-  constexpr int smem = STAGES * (128 * 64 * 2 + TN * 64 * 2) + 1024 + 256;
-  auto kern = gemm_tc_kernel<EPI, TN, STAGES>;
+  constexpr int smem = STAGES * (128 * 64 * 2 + TN * 64 * 2 + (FP8A ? 128 * 64 : 0)) + 1024 + 256;
+  auto kern = gemm_tc_kernel<EPI, TN, STAGES, FP8A>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -453,21 +507,24 @@ cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPar
 
 template <int EPI, int TN>
 cudaError_t launch_tn(const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
-                      cudaStream_t st, bool pdl) {
+                      cudaStream_t st, bool pdl, bool fp8a) {
   // stages: keep two CTAs per SM possible for the skinny shapes
   constexpr int STAGES = TN <= 32 ? 6 : (TN <= 64 ? 5 : (TN <= 128 ? 4 : 3));
-  return launch_t<EPI, TN, STAGES>(tw, tx, p, grid, st, pdl);
+  if constexpr (EPI == EPI_LMHEAD) {
+    if (fp8a) return launch_t<EPI, TN, STAGES - 1, true>(tw, tx, p, grid, st, pdl);
+  }
+  return launch_t<EPI, TN, STAGES, false>(tw, tx, p, grid, st, pdl);
 }
 
 template <int EPI>
 cudaError_t launch_epi(int TN, const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
-                       cudaStream_t st, bool pdl) {
+                       cudaStream_t st, bool pdl, bool fp8a) {
   switch (TN) {
-    case 16: return launch_tn<EPI, 16>(tw, tx, p, grid, st, pdl);
-    case 32: return launch_tn<EPI, 32>(tw, tx, p, grid, st, pdl);
-    case 64: return launch_tn<EPI, 64>(tw, tx, p, grid, st, pdl);
-    case 128: return launch_tn<EPI, 128>(tw, tx, p, grid, st, pdl);
-    case 256: return launch_tn<EPI, 256>(tw, tx, p, grid, st, pdl);
+    case 16: return launch_tn<EPI, 16>(tw, tx, p, grid, st, pdl, fp8a);
+    case 32: return launch_tn<EPI, 32>(tw, tx, p, grid, st, pdl, fp8a);
+    case 64: return launch_tn<EPI, 64>(tw, tx, p, grid, st, pdl, fp8a);
+    case 128: return launch_tn<EPI, 128>(tw, tx, p, grid, st, pdl, fp8a);
+    case 256: return launch_tn<EPI, 256>(tw, tx, p, grid, st, pdl, fp8a);
   }
   return cudaErrorInvalidValue;
 }
@@ -503,11 +560,25 @@ int pick_splits(int tiles, int nkb, int num_sms) {
   return s < 1 ? 1 : s;
 }
 
+bool make_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, int ldx, int M, GemmParams p,
-                           int nsplit, cudaStream_t st, bool pdl) {
+                           int nsplit, cudaStream_t st, bool pdl, bool w_fp8) {
   const int TN = pick_tn(M);
   CUtensorMap tw, tx;
-  if (!make_tmap_bf16(&tw, W, N, K, K, 128)) return cudaErrorInvalidValue;
+  if (w_fp8 && epi != EPI_LMHEAD) return cudaErrorInvalidValue;
+  if (w_fp8 ? !make_tmap_u8(&tw, W, N, K) : !make_tmap_bf16(&tw, W, N, K, K, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tx, X, M, K, ldx, TN)) return cudaErrorInvalidValue;
   p.N = N;
   p.K = K;
@@ -516,11 +587,11 @@ cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, 
   p.nsplit = nsplit;
   dim3 grid((N + 127) / 128, (M + TN - 1) / TN, nsplit);
   switch (epi) {
-    case EPI_STORE: return launch_epi<EPI_STORE>(TN, tw, tx, p, grid, st, pdl);
-    case EPI_QKV: return launch_epi<EPI_QKV>(TN, tw, tx, p, grid, st, pdl);
-    case EPI_RESID: return launch_epi<EPI_RESID>(TN, tw, tx, p, grid, st, pdl);
-    case EPI_GATEUP: return launch_epi<EPI_GATEUP>(TN, tw, tx, p, grid, st, pdl);
-    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(TN, tw, tx, p, grid, st, pdl);
+    case EPI_STORE: return launch_epi<EPI_STORE>(TN, tw, tx, p, grid, st, pdl, false);
+    case EPI_QKV: return launch_epi<EPI_QKV>(TN, tw, tx, p, grid, st, pdl, false);
+    case EPI_RESID: return launch_epi<EPI_RESID>(TN, tw, tx, p, grid, st, pdl, false);
+    case EPI_GATEUP: return launch_epi<EPI_GATEUP>(TN, tw, tx, p, grid, st, pdl, false);
+    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(TN, tw, tx, p, grid, st, pdl, w_fp8);
   }
   return cudaErrorInvalidValue;
 }
