@@ -51,6 +51,10 @@ __device__ __forceinline__ void rope_cs(const double* inv_pi, int j, int pos, fl
   sincospif((float)t, s, c);
 }
 
+__device__ __forceinline__ void set_status(unsigned* status, unsigned bit) {
+  if (status) atomicOr(status, bit);
+}
+
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
@@ -160,13 +164,13 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, float (&v)[16],
       const int s = m / kGamma, r = m % kGamma;
       const int ctx = p.ctx_lens[s];
       if (ctx < 0 || ctx + kGamma > p.mpps * kPage) {
-        if (t == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
+        if (t == 0) set_status(p.status, DFLASH_DEV_BAD_CTX);
         continue;
       }
       const int li = ctx + r;
       const int page = p.page_tables[(int64_t)s * p.mpps + li / kPage];
       if (page < 0 || page >= p.g.num_pages) {
-        if (t == 0) atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
+        if (t == 0) set_status(p.status, DFLASH_DEV_BAD_PAGE);
         continue;
       }
       const int head = is_k ? hh - p.nh : hh - p.nh - p.nkv;
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (!ok || flags[0]) {
     // a wait gave up: record it, give copies still in flight time to land, unwind
-    if (t == 0) atomicOr(p.status, DFLASH_DEV_TIMEOUT);
+    if (t == 0) set_status(p.status, DFLASH_DEV_TIMEOUT);
     for (int i = 0; i < 2000; ++i) __nanosleep(1000);
   } else {
     EpiSmem& es = *reinterpret_cast<EpiSmem*>(smem);
