@@ -67,7 +67,7 @@ class dflash_weights(ctypes.Structure):
 EXPORTS = ("dflash_create", "dflash_destroy", "dflash_write_ctx_kv", "dflash_propose", "dflash_kv_layout",
            "dflash_device_status", "dflash_last_error", "dflash_fp8_lm_head", "dflash_profile",
            "dflash_profile_kinds", "dflash_profile_read", "dflash_gemm_bf16",
-           "dflash_attention_check")
+           "dflash_attention_check", "dflash_gemm_bf16_noalloc")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -106,6 +106,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_gemm_bf16.restype = c.c_int
     lib.dflash_attention_check.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp]
     lib.dflash_attention_check.restype = c.c_int
+    lib.dflash_gemm_bf16_noalloc.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp]
+    lib.dflash_gemm_bf16_noalloc.restype = c.c_int
     lib.dflash_last_error.argtypes = [vp]
     lib.dflash_last_error.restype = c.c_char_p
     _lib = lib
@@ -204,3 +206,13 @@ def dflash_attention_check(handle: int, layer: int, ctx_lens: int, page_tables: 
                                          ctypes.c_void_p(page_tables), nb, max_ctx_len,
                                          ctypes.c_void_p(out_cuda_core), ctypes.c_void_p(out_tensor_core),
                                          ctypes.c_void_p(stream)), ctypes.c_void_p(handle))
+
+
+def dflash_gemm_bf16_noalloc(W: int, N: int, K: int, X: int, M: int, out: int, nsplit: int,
+                             stream: int = 0) -> None:
+    """Split-K out[M, N] fp32 = X . W^T using the library's fixed device scratch (no
+    allocation; calls must not overlap on the GPU)."""
+    rc = load().dflash_gemm_bf16_noalloc(ctypes.c_void_p(W), N, K, ctypes.c_void_p(X), M, ctypes.c_void_p(out),
+                                         nsplit, ctypes.c_void_p(stream))
+    if rc != DFLASH_OK:
+        raise DflashError(rc, "dflash_gemm_bf16_noalloc failed")

@@ -203,6 +203,23 @@ int dflash_profile_read(dflash_handle* h, int kind, const char** name, double* t
 int dflash_gemm_bf16(const void* W, int32_t N, int32_t K, const void* X, int32_t M, float* out,
                      int32_t nsplit, dflash_stream stream);
 
+/* Split-K projection GEMM that allocates nothing (no counterpart in the paper: it exists
+ * for callers, not for the method).  Same product and kernel as dflash_gemm_bf16,
+ * out[m, n] = sum_k W[n, k] X[m, k] (W [N, K], X [M, K] bf16, out [M, N] fp32, K % 64 == 0),
+ * with the K dimension split `nsplit` ways (1..16, <= K/64) and summed in split order.
+ * For callers that cannot call cudaMalloc while running: a serving loop that reserved all
+ * device memory at start-up, a memory pool that owns the device, a runtime that forbids
+ * allocation after initialisation.  Its scratch (split-K partials, tile counters) is a
+ * fixed array in the library's device image: 8 MiB of partials and 4096 tiles, held on
+ * every GPU that loads the library until the process exits.  Shapes that need more
+ * (tiles * nsplit * 128 * TN floats, TN = 16/32/64/128/256 by M) return ECAPACITY.  All
+ * calls share that array: calls that overlap on the GPU (two streams, two threads) race
+ * and give wrong results, so serialise them.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Each call zeroes the counters it uses on `stream`. */
+int dflash_gemm_bf16_noalloc(const void* W, int32_t N, int32_t K, const void* X, int32_t M,
+                             float* out, int32_t nsplit, dflash_stream stream);
+
 /* Attention cross-check (for tests, bf16 handles with 8 query heads per kv head): runs the
  * CUDA-core and the tensor-core block attention of `layer` on the queries left in the
  * handle by the last dflash_propose (its last layer's) and the pool, writing both

@@ -1,0 +1,64 @@
+"""The allocation-free split-K GEMM entry point, for callers that cannot allocate device
+memory while running.  Checked through the C ABI against the regular GEMM entry point
+(same kernel without split-K), on two calls in a row so the shared fixed scratch is reused.
+This file is collected last on purpose."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_drafter_forward_gb300 import _lib
+from synth.inputs import draw
+from synth.torch_io import to_torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _regular(W, X, N, K, M, st):
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    rc = _lib.load().dflash_gemm_bf16(ctypes.c_void_p(W.data_ptr()), N, K, ctypes.c_void_p(X.data_ptr()), M,
+                                      ctypes.c_void_p(out.data_ptr()), 1, ctypes.c_void_p(st))
+    assert rc == 0
+    return out
+
+
+def _noalloc(W, X, N, K, M, nsplit, st):
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    rc = _lib.load().dflash_gemm_bf16_noalloc(ctypes.c_void_p(W.data_ptr()), N, K, ctypes.c_void_p(X.data_ptr()),
+                                              M, ctypes.c_void_p(out.data_ptr()), nsplit, ctypes.c_void_p(st))
+    assert rc == 0
+    return out
+
+
+@pytest.mark.parametrize("N,K,M,nsplit", [(5120, 2048, 16, 4), (2048, 6144, 48, 8), (1000, 512, 100, 3)])
+def test_noalloc_split_k_matches_regular_gemm_twice(N, K, M, nsplit):
+    st = torch.cuda.current_stream().cuda_stream
+    W = to_torch(draw(31, f"na_w{N}_{K}", (N, K), 0.0, 0.02, "bf16"), "bf16")
+    for call in range(2):
+        X = to_torch(draw(32 + call, f"na_x{M}_{K}", (M, K), 0.0, 1.0, "bf16"), "bf16")
+        ref = _regular(W, X, N, K, M, st)
+        got = _noalloc(W, X, N, K, M, nsplit, st)
+        torch.cuda.synchronize()
+        err = ((got - ref).abs().max() / ref.abs().max()).item()
+        assert torch.isfinite(got).all() and err < 1e-5, (call, err)
+
+
+def test_noalloc_rejects_shapes_beyond_the_fixed_scratch():
+    st = torch.cuda.current_stream().cuda_stream
+    W = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    X = torch.zeros((16, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((16, 128), dtype=torch.float32, device="cuda")
+    lib = _lib.load()
+    # 600 000 weight rows x 256 tokens x 2 splits needs far more than 8 MiB of partials
+    big = lib.dflash_gemm_bf16_noalloc(ctypes.c_void_p(W.data_ptr()), 600000, 128, ctypes.c_void_p(X.data_ptr()),
+                                       256, ctypes.c_void_p(out.data_ptr()), 2, ctypes.c_void_p(st))
+    assert big == _lib.DFLASH_ECAPACITY
+    assert lib.dflash_gemm_bf16_noalloc(ctypes.c_void_p(W.data_ptr()), 128, 64, ctypes.c_void_p(X.data_ptr()), 16,
+                                        ctypes.c_void_p(out.data_ptr()), 2, ctypes.c_void_p(st)) == _lib.DFLASH_EINVAL
