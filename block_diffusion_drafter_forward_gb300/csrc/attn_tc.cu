@@ -9,7 +9,10 @@
 //
 // Work unit = (sequence, kv head): its 8 query heads x 16 block rows are the 128 rows of one
 // UMMA tile (M = 128), so every K/V byte read from HBM feeds 128 query rows.  Keys go in
-// chunks of 128 (8 pages): S = Q K^T and O = P V are each 8 tcgen05.mma into TMEM.  Pages
+// chunks of 64 (4 pages): S = Q K^T is 8 tcgen05.mma (N = 64), O = P V 4 (K = 16 keys each),
+// accumulating in TMEM.  Shared memory stays under half an SM so a projection CTA can run
+// beside it.  Pages of context rows only are fetched before the wait on the QKV kernel
+// (programmatic dependent launch); the page with the block rows after it.  Pages
 // are fetched whole (4 KB bulk copies through the page table) into a 2-stage ring; the pool
 // stores each page tile in the 8x8-block operand layout, so no reshuffle is needed.
 // Softmax runs one query row per thread (no cross-thread reductions), online over chunks.
@@ -28,12 +31,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int kKC = 128;              // keys per chunk
+constexpr int kKC = 64;               // keys per chunk
 constexpr int kPagesPerChunk = kKC / kPage;
 constexpr int kTileBytes = kPage * 128 * 2;    // one page of one head: 16 x 128 bf16 = 4 KB
 constexpr int kQBytes = 128 * 128 * 2;         // 32 KB
-constexpr int kPBytes = 128 * kKC * 2;         // 32 KB
-constexpr int kKVStage = 2 * kPagesPerChunk * kTileBytes;  // K + V of one chunk: 64 KB
+constexpr int kPBytes = 128 * kKC * 2;         // 16 KB
+constexpr int kKVStage = 2 * kPagesPerChunk * kTileBytes;  // K + V of one chunk: 32 KB
 constexpr int kStages = 2;
 constexpr int kSmem = kQBytes + kPBytes + kStages * kKVStage + 256 + 1024;
 
@@ -68,8 +71,7 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
   const int s = unit / p.nkv, g = unit % p.nkv;
   const int group = p.nh / p.nkv;  // 8
 
-  pdl_wait();
-  const int ctx = p.ctx_lens[s];
+  const int ctx = p.ctx_lens[s];  // caller input: not written by the preceding kernel
   if (ctx < 0 || ctx > p.max_ctx || ctx + kGamma > p.mpps * kPage) {
     if (t == 0 && split == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
     return;
@@ -122,9 +124,24 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
       bulk_load(dV + i * kTileBytes, vt, kTileBytes, &kv_full[st]);
     }
   };
+  // Pages holding only cached context rows are not touched by the preceding QKV kernel (it
+  // writes the block rows ctx..ctx+15): fetch those chunks before waiting for it.
+  const int safe_keys = ctx & ~(kPage - 1);
+  bool early[2] = {false, false};
   if (t == 0) {
-    load_chunk(c_begin, 0);
-    if (c_begin + 1 < c_end) load_chunk(c_begin + 1, 1);
+    for (int i = 0; i < 2; ++i) {
+      const int c = c_begin + i;
+      if (c < c_end && k0 + (c + 1) * kKC <= safe_keys) {
+        load_chunk(c, i);
+        early[i] = true;
+      }
+    }
+  }
+  pdl_trigger();
+  pdl_wait();
+  if (t == 0) {
+    for (int i = 0; i < 2; ++i)
+      if (c_begin + i < c_end && !early[i]) load_chunk(c_begin + i, i);
   }
 
   // Q tile: row i = hh * 16 + r  <-  q[s*16 + r, (g*group + hh) * 128 + :], 8x8-block layout
@@ -147,6 +164,7 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
   float o[128];
 #pragma unroll
   for (int i = 0; i < 128; ++i) o[i] = 0.f;
+  constexpr uint32_t idesc_s = idesc_bf16(128, kKC);
   constexpr uint32_t idesc = idesc_bf16(128, 128);
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
   bool ok = true;
@@ -161,7 +179,7 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
       if (!flags[0]) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_bf16(tS, desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048), idesc,
+          mma_bf16(tS, desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048), idesc_s,
                    k > 0 ? 1u : 0u);
       }
       mma_commit(s_done);
@@ -207,7 +225,7 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
           lsum += __low2float(h2) + __high2float(h2);  // the normaliser sums what the MMA uses
           pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        *reinterpret_cast<uint4*>(sP + ((t >> 3) * 16 + q4 * 4 + j8) * 128 + (t & 7) * 16) =
+        *reinterpret_cast<uint4*>(sP + ((t >> 3) * (kKC / 8) + q4 * 4 + j8) * 128 + (t & 7) * 16) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
@@ -220,8 +238,8 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
       tc_fence_after();
       if (!flags[0]) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_bf16(tO, desc_noswz(sP + k * 256, 128, 2048), desc_noswz(sV + k * kTileBytes, 128, 256), idesc,
+        for (int k = 0; k < kPagesPerChunk; ++k)
+          mma_bf16(tO, desc_noswz(sP + k * 256, 128, kKC / 8 * 128), desc_noswz(sV + k * kTileBytes, 128, 256), idesc,
                    k > 0 ? 1u : 0u);
       }
       mma_commit(o_done);
@@ -273,10 +291,11 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// Merge the split partials of every (sequence, kv head) unit with more than one split:
-// o = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q, M = max_q m_q, in split order.
-// Block (unit, rb) owns rows 8 rb .. 8 rb + 7; 16 threads per row, 8 dims each.
+// Merge the split partials of every (sequence, kv head) unit with more than one split, in
+// split order with a running maximum: o = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
+// Block (unit, rb) owns rows 4 rb .. 4 rb + 3; a warp per row, 4 dims per thread.
 __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int splits_launched) {
+  pdl_trigger();  // the next projection may start streaming its weights
   pdl_wait();
   const int unit = blockIdx.x, t = threadIdx.x;
   const int s = unit / p.nkv, g = unit % p.nkv;
@@ -286,32 +305,39 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
   const int nch = chunk_range(p.window, ctx, &k0);
   const int nsplit = (nch + p.chunks_per_split - 1) / p.chunks_per_split;
   if (nsplit <= 1 || nsplit > splits_launched) return;
-  const int row = blockIdx.y * 8 + (t >> 4), d0 = (t & 15) * 8;
+  const int row = blockIdx.y * 4 + (t >> 5), d0 = (t & 31) * 4;
   const int64_t base = (int64_t)unit * splits_launched;
-  float mx = -FLT_MAX;
-  for (int q = 0; q < nsplit; ++q) mx = fmaxf(mx, __ldcg(p.ml_part + ((base + q) * 128 + row) * 2));
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float L = 0.f;
-  for (int q = 0; q < nsplit; ++q) {
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ml_part + ((base + q) * 128 + row) * 2));
-    const float w = ml.x == -FLT_MAX ? 0.f : exp2f(ml.x - mx);
-    L += ml.y * w;
-    const float* src = p.o_part + ((base + q) * 128 + row) * 128 + d0;
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
-    acc[0] += a.x * w; acc[1] += a.y * w; acc[2] += a.z * w; acc[3] += a.w * w;
-    acc[4] += b.x * w; acc[5] += b.y * w; acc[6] += b.z * w; acc[7] += b.w * w;
+  float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  for (int q0 = 0; q0 < nsplit; q0 += 4) {
+    float2 ml[4];
+    float4 ov[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t sl = base + q0 + u;
+      const bool v = q0 + u < nsplit;
+      ml[u] = v ? __ldcg(reinterpret_cast<const float2*>(p.ml_part + (sl * 128 + row) * 2)) : make_float2(-FLT_MAX, 0.f);
+      ov[u] = v ? __ldcg(reinterpret_cast<const float4*>(p.o_part + (sl * 128 + row) * 128 + d0))
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (ml[u].x > M) {
+        const float sc = M == -FLT_MAX ? 0.f : exp2f(M - ml[u].x);
+        a0 *= sc; a1 *= sc; a2 *= sc; a3 *= sc; L *= sc;
+        M = ml[u].x;
+      }
+      const float w = ml[u].x == -FLT_MAX ? 0.f : exp2f(ml[u].x - M);
+      a0 += ov[u].x * w; a1 += ov[u].y * w; a2 += ov[u].z * w; a3 += ov[u].w * w;
+      L += ml[u].y * w;
+    }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint32_t pk[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-    pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
-  }
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+  const __nv_bfloat162 h1 = __floats2bfloat162_rn(a2 * inv, a3 * inv);
   const int hh = row >> 4, r = row & 15;
   __nv_bfloat16* dst = p.out + ((int64_t)(s * kGamma + r) * p.nh + g * (p.nh / p.nkv) + hh) * 128 + d0;
-  *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
+                                              *reinterpret_cast<const uint32_t*>(&h1));
 }
 
 }  // namespace
@@ -337,11 +363,20 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   const int splits = (nch + cps - 1) / cps;
   p.chunks_per_split = cps;
   p.max_ctx = max_ctx_len;
-  attn_tc_kernel<<<dim3(units, splits), 128, kSmem, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t ac = {};
+  ac.gridDim = dim3(units, splits);
+  ac.blockDim = dim3(128);
+  ac.dynamicSmemBytes = kSmem;
+  ac.stream = st;
+  cudaLaunchAttribute aa[1];
+  aa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  aa[0].val.programmaticStreamSerializationAllowed = 1;
+  ac.attrs = aa;
+  ac.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
   if (e != cudaSuccess || splits == 1) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(units, 16);
+  cfg.gridDim = dim3(units, 32);
   cfg.blockDim = dim3(128);
   cfg.stream = st;
   cudaLaunchAttribute at[1];

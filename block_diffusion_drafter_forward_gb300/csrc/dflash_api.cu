@@ -263,7 +263,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.ss_out = h->ss_a;
       p.ln_next = static_cast<const __nv_bfloat16*>(w.ln_post);
       p.H = H;
-      KL(K_OPROJ, launch_gemm_tc(EPI_RESID, w.w_o, H, qd, h->attn, qd, M, p, splits(H, qd), st, false), "o_proj");
+      KL(K_OPROJ, launch_gemm_tc(EPI_RESID, w.w_o, H, qd, h->attn, qd, M, p, splits(H, qd), st, true), "o_proj");
     }
     {
       GemmParams p = base;

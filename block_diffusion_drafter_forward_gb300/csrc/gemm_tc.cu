@@ -51,6 +51,8 @@ __device__ __forceinline__ void rope_cs(const double* inv_pi, int j, int pos, fl
   sincospif((float)t, s, c);
 }
 
+__device__ __forceinline__ int m0_of(int tile_m, int tn) { return tile_m * tn; }
+
 __device__ __forceinline__ void set_status(unsigned* status, unsigned bit) {
   if (status) atomicOr(status, bit);
 }
@@ -63,20 +65,19 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 struct EpiSmem {
   float xch[kThreads][17];   // one 16-token chunk of the tile, transposed exchange
   float red[4][16];          // per-warp partial reductions for 16 tokens
-  float rsc[256];            // per-token input row scale
   float bv[4][16];
   int bi[4][16];
 };
 
 template <int EPI>
-__device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, float (&v)[16], int t, int n, int m0, int c0,
-                               int tile_n) {
+__device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rsc, float (&v)[16], int t, int n,
+                               int m0, int c0, int tile_n) {
   const int warp = t >> 5, lane = t & 31;
   if constexpr (EPI == EPI_STORE) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int m = m0 + c0 + c;
-      if (m < p.M && n < p.N) p.out[(int64_t)m * p.ldo + n] = v[c] * (p.ss_in ? es.rsc[c0 + c] : 1.f);
+      if (m < p.M && n < p.N) p.out[(int64_t)m * p.ldo + n] = v[c] * (p.ss_in ? rsc[c0 + c] : 1.f);
     }
   } else if constexpr (EPI == EPI_RESID) {
     float sq[16];
@@ -104,7 +105,7 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, float (&v)[16],
     __syncthreads();
   } else if constexpr (EPI == EPI_GATEUP) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * es.rsc[c0 + c];
+    for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * rsc[c0 + c];
     __syncthreads();
     const int f = tile_n * 64 + (t & 63);
     const int cb = (t >> 6) * 8;
@@ -121,7 +122,7 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, float (&v)[16],
     const int hh = tile_n;
     const bool is_q = hh < p.nh, is_k = !is_q && hh < p.nh + p.nkv;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) v[c] *= es.rsc[c0 + c];
+    for (int c = 0; c < 16; ++c) v[c] *= rsc[c0 + c];
     if (is_q || is_k) {
       // per-head RMSNorm over the 128 rows of the tile
       float sq[16];
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(sizeof(EpiSmem) <= STAGES * STAGE_BYTES, "epilogue scratch must fit in the stages");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);  // barriers: 1 KB, then EpiSmem
   uint64_t* empty = full + STAGES;
   uint64_t* conv = empty + STAGES;   // FP8A: widened A tile ready (64 arrivals)
   uint64_t* accf = conv + STAGES;
@@ -359,6 +360,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------- epilogue: all four warps
   pdl_wait();
+  // the exchange scratch aliases the drained stages; the row scales (needed while the
+  // stages are still filling) sit after the barriers
+  EpiSmem& es = *reinterpret_cast<EpiSmem*>(smem);
+  float* const rsc = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);
+  if (p.ss_in && warp >= 2) {
+    // input row scales 1/RMS(x_m) from the producer's per-128-column partials, computed by
+    // the warps that are idle during the mainloop
+    for (int c = t - 64; c < TN; c += 64) {
+      const int m = m0_of(tile_m, TN) + c;
+      float r = 1.f;
+      if (m < p.M) {
+        float part[8];
+        float ssum = 0.f;
+        for (int q0 = 0; q0 < p.ss_parts; q0 += 8) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) part[u] = q0 + u < p.ss_parts ? p.ss_in[(int64_t)(q0 + u) * p.Mp + m] : 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) ssum += part[u];
+        }
+        r = 1.f / sqrtf(ssum / (float)p.ss_n + p.eps);
+      }
+      rsc[c] = r;
+    }
+  }
   const bool ok = mbar_wait(accf, 0);
   tc_fence_after();
   __syncthreads();
@@ -367,24 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t == 0) set_status(p.status, DFLASH_DEV_TIMEOUT);
     for (int i = 0; i < 2000; ++i) __nanosleep(1000);
   } else {
-    EpiSmem& es = *reinterpret_cast<EpiSmem*>(smem);
     const int m0 = tile_m * TN;
     const int n = tile_n * 128 + t;
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
     const int64_t tile_lin = (int64_t)tile_n * gridDim.y + tile_m;
-    if (p.ss_in) {
-      for (int c = t; c < TN; c += kThreads) {
-        const int m = m0 + c;
-        float r = 1.f;
-        if (m < p.M) {
-          float ssum = 0.f;
-          for (int q = 0; q < p.ss_parts; ++q) ssum += p.ss_in[(int64_t)q * p.Mp + m];
-          r = 1.f / sqrtf(ssum / (float)p.ss_n + p.eps);
-        }
-        es.rsc[c] = r;
-      }
-    }
-    __syncthreads();
     bool last = true;
     if (p.nsplit > 1) {
       float* mine = p.ws + ((tile_lin * p.nsplit + split) * kThreads + t) * TN;
@@ -410,21 +421,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.nsplit > 1) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] = 0.f;
-          for (int s = 0; s < p.nsplit; ++s) {
-            const float* src = p.ws + ((tile_lin * p.nsplit + s) * kThreads + t) * TN + c0;
+          for (int s0 = 0; s0 < p.nsplit; s0 += 4) {
+            float4 q4[4][4];
 #pragma unroll
-            for (int c = 0; c < 16; c += 4) {
-              const float4 q4 = __ldcg(reinterpret_cast<const float4*>(src + c));
-              v[c] += q4.x;
-              v[c + 1] += q4.y;
-              v[c + 2] += q4.z;
-              v[c + 3] += q4.w;
+            for (int u = 0; u < 4; ++u) {
+              const float* src = p.ws + ((tile_lin * p.nsplit + (s0 + u)) * kThreads + t) * TN + c0;
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                q4[u][c] = s0 + u < p.nsplit ? __ldcg(reinterpret_cast<const float4*>(src) + c)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                v[4 * c] += q4[u][c].x;
+                v[4 * c + 1] += q4[u][c].y;
+                v[4 * c + 2] += q4[u][c].z;
+                v[4 * c + 3] += q4[u][c].w;
+              }
             }
           }
         } else {
           tmem_ld16(lane_addr + c0, v);
         }
-        epilogue_chunk<EPI>(p, es, v, t, n, m0, c0, tile_n);
+        epilogue_chunk<EPI>(p, es, rsc, v, t, n, m0, c0, tile_n);
       }
       if (p.nsplit > 1 && t == 0) p.counters[tile_lin] = 0;
       if constexpr (EPI == EPI_LMHEAD) {
@@ -488,7 +509,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 template <int EPI, int TN, int STAGES, bool FP8A>
 cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
                      cudaStream_t st, bool pdl) {
-  constexpr int smem = STAGES * (128 * 64 * 2 + TN * 64 * 2 + (FP8A ? 128 * 64 : 0)) + 1024 + 256;
+  constexpr int smem = STAGES * (128 * 64 * 2 + TN * 64 * 2 + (FP8A ? 128 * 64 : 0)) + 1024 + 256 + 1024;
   auto kern = gemm_tc_kernel<EPI, TN, STAGES, FP8A>;
   static bool attr_set = false;
   if (!attr_set) {
