@@ -340,6 +340,37 @@ def main():
            "h2d_bytes_per_step": int(h_bonus.numel() * 4 + h_ctx.numel() * 4 + h_pt.numel() * 4),
            "d2h_bytes_per_step": int(h_drafts.numel() * 4)}
 
+    # ---- context-K/V writer (the step before the path): rows/s at n = 16 and n = 4096,
+    # rewriting rows of sequence 0 with their own taps (same values), events on the stream
+    writer = {}
+    c0 = int(wl.ctx_lens[0])
+    tab = to_torch(taps_table(wl), cfg.dtype)
+    for n in (16, 4096):
+        n = min(n, c0)
+        if n <= 0:
+            continue
+        idx = (int(wl.tap_offsets[0]) + torch.arange(n, device="cuda")) % wl.taps_rows
+        taps0 = tab[idx].contiguous()
+        pos0 = to_torch(wl.ctx_positions(0, 0, n), "i32")
+        for _ in range(3):
+            drafter.write_ctx_kv(taps0, pos0, page_tables[0], 0)
+        reps = 20 if n <= 64 else 5
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            drafter.write_ctx_kv(taps0, pos0, page_tables[0], 0)
+        b.record(stream)
+        b.synchronize()
+        ms = a.elapsed_time(b) / reps
+        wbytes = (cfg.hidden * cfg.tap_dim + cfg.n_layers * 2 * cfg.kv_dim * cfg.hidden) * (4 if cfg.dtype == "f32" else 2)
+        wbytes += n * cfg.tap_dim * (4 if cfg.dtype == "f32" else 2) + n * cfg.n_layers * 2 * cfg.kv_dim * (4 if cfg.dtype == "f32" else 2)
+        wflops = 2.0 * n * (cfg.hidden * cfg.tap_dim + cfg.n_layers * 2 * cfg.kv_dim * cfg.hidden)
+        writer[f"n{n}"] = {"rows_per_s": n / (ms / 1e3), "us_per_call": 1e3 * ms,
+                           "hbm_frac": wbytes / (ms / 1e3) / (peaks()[0]["hbm_gbs"] * 1e9),
+                           "tensor_frac": wflops / (ms / 1e3) / (peaks()[0]["bf16_tflops"] * 1e12)}
+    del tab
+
     # ---- roofline of the dominant kernel
     pk, src = peaks()
     nbytes, flops, per_kernel = work_model(cfg, wl, logits_on)
@@ -378,6 +409,7 @@ def main():
         "kernels_ms_per_step": {k: v[0] / prof_steps for k, v in kernels.items()},
         "gpu_launches": int(launches),
         "e2e": e2e,
+        "writer": writer,
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["clocks"] = clk.summary()

@@ -111,9 +111,15 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
     uint8_t* dV = dK + kPagesPerChunk * kTileBytes;
     mbar_arrive_expect_tx(&kv_full[st], 2 * kPagesPerChunk * kTileBytes);
     const int pg0 = (k0 + c * kKC) / kPage;
-    for (int i = 0; i < kPagesPerChunk; ++i) {
+    int pages[kPagesPerChunk];
+#pragma unroll
+    for (int i = 0; i < kPagesPerChunk; ++i) {  // all page ids in flight together
       const int lp = pg0 + i;
-      int page = pt[lp < npages_seq ? lp : 0];
+      pages[i] = __ldg(pt + (lp < npages_seq ? lp : 0));
+    }
+#pragma unroll
+    for (int i = 0; i < kPagesPerChunk; ++i) {
+      int page = pages[i];
       if (page < 0 || page >= p.g.num_pages) {
         atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
         page = 0;

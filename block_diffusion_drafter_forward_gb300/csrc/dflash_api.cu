@@ -422,9 +422,14 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
   // ---- RoPE table
   std::vector<double> inv_pi;
   rope_table(c, inv_pi, h->rope_mscale);
-  ALLOC(h->rope_inv_pi, inv_pi.size() * sizeof(double));
+  std::vector<float2> inv_pi2(inv_pi.size());
+  for (size_t j = 0; j < inv_pi.size(); ++j) {
+    inv_pi2[j].x = (float)inv_pi[j];
+    inv_pi2[j].y = (float)(inv_pi[j] - (double)inv_pi2[j].x);
+  }
+  ALLOC(h->rope_inv_pi, inv_pi2.size() * sizeof(float2));
   {
-    cudaError_t e = cudaMemcpyAsync(h->rope_inv_pi, inv_pi.data(), inv_pi.size() * sizeof(double),
+    cudaError_t e = cudaMemcpyAsync(h->rope_inv_pi, inv_pi2.data(), inv_pi2.size() * sizeof(float2),
                                     cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) { cuda_fail(h, e, "rope table"); return bail(DFLASH_ECUDA); }
   }
@@ -470,20 +475,31 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
       fail(h, DFLASH_ECUDA, "counter memset");
       return bail(DFLASH_ECUDA);
     }
-    // split-K workspace: the largest need over every projection and batch size
+    // split-K workspace: the largest need over every projection and batch size, and over
+    // the writer's two GEMMs for every chunk size
     size_t need = 16;
-    const int64_t shapes[4][2] = {{qkvd, H}, {H, qd}, {2 * F, H}, {H, F}};
-    for (int64_t m = kGamma; m <= R; m += kGamma) {
+    auto account = [&](int64_t N, int64_t K, int64_t m) {
       const int tn = pick_tn((int)m);
-      for (auto& sh : shapes) {
-        const int64_t tiles = ((sh[0] + 127) / 128) * ((m + tn - 1) / tn);
-        const int ns = pick_splits((int)tiles, (int)(sh[1] / 64), h->num_sms);
-        if (tiles > kCounters - 64) {
-          fail(h, DFLASH_EUNSUPPORTED, "too many GEMM tiles");
-          return bail(DFLASH_EUNSUPPORTED);
-        }
-        if (ns > 1) need = std::max(need, (size_t)(tiles * ns * 128 * tn));
-      }
+      const int64_t tiles = ((N + 127) / 128) * ((m + tn - 1) / tn);
+      const int ns = pick_splits((int)tiles, (int)(K / 64), h->num_sms);
+      if (ns > 1) need = std::max(need, (size_t)(tiles * ns * 128 * tn));
+      return tiles <= kCounters - 64;
+    };
+    bool fits = true;
+    for (int64_t m = kGamma; m <= R; m += kGamma)
+      fits = account(qkvd, H, m) && account(H, qd, m) && account(2 * F, H, m) && account(H, F, m) && fits;
+    for (int64_t m = 1; m <= Rw; m = m < 256 ? m + 1 : m + 256)
+      fits = account(H, tapd, m) && account(L * 2 * kvd, 2 * H, m) && fits;
+    fits = account(H, tapd, Rw) && account(L * 2 * kvd, 2 * H, Rw) && fits;
+    if (!fits || tapd % 64) {
+      fail(h, DFLASH_EUNSUPPORTED, "GEMM tiling out of range (too many tiles or n_taps*target_hidden % 64 != 0)");
+      return bail(DFLASH_EUNSUPPORTED);
+    }
+    ALLOC(h->wf2, Rw * 2 * H * es);
+    ALLOC(h->w_ctxkv2, L * 2 * kvd * 2 * H * es);
+    if (launch_repeat_cols(h->w_ctxkv, (int)(L * 2 * kvd), (int)H, h->w_ctxkv2, st) != cudaSuccess) {
+      fail(h, DFLASH_ECUDA, "repeat context-K/V weight");
+      return bail(DFLASH_ECUDA);
     }
     h->ws_floats = need;
     ALLOC(h->ws, need * 4);
@@ -547,6 +563,46 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t H = c.hidden, tapd = (int64_t)c.n_taps * c.target_hidden;
   const int kvall = c.n_layers * 2 * c.n_kv_heads * c.head_dim;
+  if (h->tc) {
+    // tensor-core writer: fc GEMM -> hidden_norm (fp32) -> [hi | lo] bf16 -> one GEMM over
+    // [W | W] for every layer's K and V with the k_norm / RoPE / scatter epilogue
+    for (int32_t done = 0; done < n; done += c.max_write_rows) {
+      const int m = std::min<int32_t>(c.max_write_rows, n - done);
+      const void* tp = static_cast<const char*>(taps) + (int64_t)done * tapd * h->esz;
+      auto splits = [&](int64_t N, int64_t K) {
+        const int tn = pick_tn(m);
+        return pick_splits((int)(((N + 127) / 128) * ((m + tn - 1) / tn)), (int)(K / 64), h->num_sms);
+      };
+      GemmParams pf;
+      pf.ws = h->ws;
+      pf.counters = h->counters;
+      pf.status = h->d_status;
+      pf.out = h->wy;
+      pf.ldo = (int)H;
+      KL(K_W_FC, launch_gemm_tc(EPI_STORE, h->fc, (int)H, (int)tapd, tp, (int)tapd, m, pf, splits(H, tapd), st, false),
+         "writer fc");
+      KL(K_W_NORM, launch_rmsnorm_f32out(h, h->wy, h->hidden_norm, h->wf, m, (int)H, st), "writer hidden_norm");
+      KL(K_W_NORM, launch_split_hi_lo(h->wf, m, (int)H, h->wf2, st), "writer split");
+      GemmParams pk;
+      pk.ws = h->ws;
+      pk.counters = h->counters;
+      pk.status = h->d_status;
+      pk.eps = c.rms_eps;
+      pk.k_norm = static_cast<const __nv_bfloat16*>(h->kn_all);
+      pk.inv_pi = h->rope_inv_pi;
+      pk.mscale = h->rope_mscale;
+      pk.nkv = c.n_kv_heads;
+      pk.positions = positions + done;
+      pk.page_tables = page_table;
+      pk.first = first + done;
+      pk.g = h->geom;
+      pk.pool = static_cast<__nv_bfloat16*>(h->pool);
+      KL(K_W_KV, launch_gemm_tc(EPI_CTXKV, h->w_ctxkv2, kvall, (int)(2 * H), h->wf2, (int)(2 * H), m, pk,
+                                splits(kvall, 2 * H), st, false),
+         "writer kv");
+    }
+    return DFLASH_OK;
+  }
   for (int32_t done = 0; done < n; done += c.max_write_rows) {
     const int m = std::min<int32_t>(c.max_write_rows, n - done);
     const void* tp = static_cast<const char*>(taps) + (int64_t)done * tapd * h->esz;

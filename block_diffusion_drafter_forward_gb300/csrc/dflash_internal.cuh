@@ -115,7 +115,7 @@ struct dflash_handle {
   void* w_ctxkv = nullptr;             // [L * 2 * kv, H]: K_0, V_0, K_1, V_1, ...
   void* kn_all = nullptr;              // [L, hd] every layer's k_norm (writer epilogue)
   dflash::LayerW layer[64];
-  double* rope_inv_pi = nullptr;       // [hd/2] inv_freq_j / pi (float64)
+  float2* rope_inv_pi = nullptr;       // [hd/2] inv_freq_j / pi split as (hi, lo) floats
   float rope_mscale = 1.f;
 
   // paged K/V pool
@@ -135,6 +135,8 @@ struct dflash_handle {
   // writer scratch (rows = max_write_rows)
   float* wy = nullptr;                 // [Rw, max(H, L*2*kv)] fp32
   float* wf = nullptr;                 // [Rw, H] ctx features (fp32)
+  void* wf2 = nullptr;                 // [Rw, 2H] ctx features as bf16 [hi | lo] (tensor-core writer)
+  void* w_ctxkv2 = nullptr;            // [L * 2 * kv, 2H] fused context-K/V weight repeated [W | W]
 
   // tensor-core (bf16) path scratch
   void* xb = nullptr;                  // [rows, H] bf16 copy of the residual stream
@@ -190,6 +192,8 @@ cudaError_t launch_copy_hidden(const dflash_handle* h, const void* src, int rows
 cudaError_t launch_ctxkv_post(const dflash_handle* h, const float* ykv, int n, const int32_t* positions,
                               const int32_t* page_table, int first, cudaStream_t st);
 cudaError_t launch_embed_tc(const dflash_handle* h, const int32_t* bonus, int nb, cudaStream_t st);
+cudaError_t launch_split_hi_lo(const float* x, int rows, int n, void* out, cudaStream_t st);
+cudaError_t launch_repeat_cols(const void* w, int rows, int cols, void* out, cudaStream_t st);
 cudaError_t launch_fold_norm(const void* A, const void* B, int mode, int rows, int cols, const void* ln, void* out,
                              cudaStream_t st);
 cudaError_t launch_quantize_fp8(const void* w, int rows, int cols, int dtype, uint8_t* codes,

@@ -21,6 +21,9 @@
 //   EPI_GATEUP: tile = 64 gate rows + 64 up rows; act = silu(r_m g) * (r_m u).
 //   EPI_LMHEAD: logits (optional, bf16), per-row fp32 scale for the FP8 head, per-tile
 //               argmax partials and, in the last tile, the per-row argmax -> drafts.
+//   EPI_CTXKV : context-K/V writer (dflash.rs ingest_ctx): tile = one head of one layer's
+//               K or V; K gets k_norm, RoPE at the row's position and mscale; both are
+//               scattered to the row's paged slot.
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -45,10 +48,19 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ void rope_cs(const double* inv_pi, int j, int pos, float* c, float* s) {
-  double t = (double)pos * inv_pi[j];
-  t -= 2.0 * rint(0.5 * t);
-  sincospif((float)t, s, c);
+// RoPE angle of pair j at position pos (from_weights.rs inv_freq table; YaRN divisors
+// already folded into inv_freq), as half-turns t = pos * inv_freq_j / pi reduced to [-1, 1],
+// then sin/cos(pi t) in fp32.  ip[j] = (hi, lo) splits inv_freq_j / pi into two floats;
+// fmaf gives the exact rounding error of pos * hi, and subtracting the nearest even integer
+// is exact below 2^24, so t carries ~1e-7 absolute error without float64 arithmetic.
+__device__ __forceinline__ void rope_cs(const float2* ip, int j, int pos, float* c, float* s) {
+  const float p = (float)pos;
+  const float2 v = ip[j];
+  const float a = p * v.x;
+  const float e = fmaf(p, v.x, -a);
+  const float k = 2.f * rintf(0.5f * a);
+  const float t = (a - k) + fmaf(p, v.y, e);
+  sincospif(t, s, c);
 }
 
 __device__ __forceinline__ int m0_of(int tile_m, int tn) { return tile_m * tn; }
@@ -179,6 +191,54 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
       p.pool[base + (is_k ? k_in_tile(li % kPage, t, 128) : v_in_tile(li % kPage, t, 128))] =
           __float2bfloat16_rn(v[c]);
     }
+  } else if constexpr (EPI == EPI_CTXKV) {
+    // one tile = one head of one layer's K or V in the fused context-K/V weight
+    // [K_0; V_0; K_1; V_1; ...]; token m is context row first + m at position positions[m]
+    const int l = tile_n / (2 * p.nkv), rem = tile_n % (2 * p.nkv);
+    const bool is_k = rem < p.nkv;
+    const int head = is_k ? rem : rem - p.nkv;
+    if (is_k) {
+      float sq[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sq[c] = warp_sum(v[c] * v[c]);
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) es.red[warp][c] = sq[c];
+      }
+      __syncthreads();
+      const float w = __bfloat162float(p.k_norm[l * 128 + t]);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float ss = es.red[0][c] + es.red[1][c] + es.red[2][c] + es.red[3][c];
+        es.xch[t][c] = v[c] * (1.f / sqrtf(ss * (1.f / 128.f) + p.eps)) * w;
+      }
+      __syncthreads();
+      const int j = t & 63;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c0 + c;
+        const int pos = m < p.M ? p.positions[m] : 0;
+        float cs, sn;
+        rope_cs(p.inv_pi, j, pos, &cs, &sn);
+        const float a = es.xch[j][c], b = es.xch[j + 64][c];
+        v[c] = (t < 64 ? a * cs - b * sn : b * cs + a * sn) * p.mscale;
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int m = m0 + c0 + c;
+      if (m >= p.M) continue;
+      const int li = p.first + m;
+      const int page = p.page_tables[li / kPage];
+      if (page < 0 || page >= p.g.num_pages) {
+        if (t == 0) set_status(p.status, DFLASH_DEV_BAD_PAGE);
+        continue;
+      }
+      const int64_t base = tile_base(p.g, l, page, is_k ? 0 : 1, head);
+      p.pool[base + (is_k ? k_in_tile(li % kPage, t, 128) : v_in_tile(li % kPage, t, 128))] =
+          __float2bfloat16_rn(v[c]);
+    }
   } else if constexpr (EPI == EPI_LMHEAD) {
     const bool valid_row = n < p.N;
     const float sc = (p.row_scale && valid_row) ? p.row_scale[n] : 1.f;
@@ -243,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] timed out, [1] last split
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
+  const int tile_m = blockIdx.x, tile_n = blockIdx.y, split = blockIdx.z;
   const int kb0 = (int)((int64_t)split * p.nkb / p.nsplit);
   const int kb1 = (int)((int64_t)(split + 1) * p.nkb / p.nsplit);
   const int nloc = kb1 - kb0;
@@ -395,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m0 = tile_m * TN;
     const int n = tile_n * 128 + t;
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    const int64_t tile_lin = (int64_t)tile_n * gridDim.y + tile_m;
+    const int64_t tile_lin = (int64_t)tile_n * gridDim.x + tile_m;
     bool last = true;
     if (p.nsplit > 1) {
       float* mine = p.ws + ((tile_lin * p.nsplit + split) * kThreads + t) * TN;
@@ -452,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the last vocabulary tile of this token tile reduces the per-tile argmaxes
         __threadfence();
         __syncthreads();
-        if (t == 0) flags[1] = atomicAdd(&p.amax_counter[tile_m], 1u) == (unsigned)(gridDim.x - 1);
+        if (t == 0) flags[1] = atomicAdd(&p.amax_counter[tile_m], 1u) == (unsigned)(gridDim.y - 1);
         __syncthreads();
         if (flags[1]) {
           __threadfence();
@@ -463,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float b = -FLT_MAX;
             int bi = 0x7fffffff;
             if (m < p.M) {
-              for (int q = sub; q < (int)gridDim.x; q += 8) {
+              for (int q = sub; q < (int)gridDim.y; q += 8) {
                 const float vv = __ldcg(p.amax_val + (int64_t)q * p.Mp + m);
                 const int ii = __ldcg(p.amax_idx + (int64_t)q * p.Mp + m);
                 if (better(vv, ii, b, bi)) { b = vv; bi = ii; }
@@ -574,8 +634,7 @@ int pick_tn(int M) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
-  if (M <= 128) return 128;
-  return 256;
+  return 128;  // larger batches: several 128-token tiles, consecutive in the grid (weight tile reuse in L2)
 }
 
 int pick_splits(int tiles, int nkb, int num_sms) {
@@ -610,13 +669,14 @@ cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, 
   p.M = M;
   p.nkb = K / 64;
   p.nsplit = nsplit;
-  dim3 grid((N + 127) / 128, (M + TN - 1) / TN, nsplit);
+  dim3 grid((M + TN - 1) / TN, (N + 127) / 128, nsplit);
   switch (epi) {
     case EPI_STORE: return launch_epi<EPI_STORE>(TN, tw, tx, p, grid, st, pdl, false);
     case EPI_QKV: return launch_epi<EPI_QKV>(TN, tw, tx, p, grid, st, pdl, false);
     case EPI_RESID: return launch_epi<EPI_RESID>(TN, tw, tx, p, grid, st, pdl, false);
     case EPI_GATEUP: return launch_epi<EPI_GATEUP>(TN, tw, tx, p, grid, st, pdl, false);
     case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(TN, tw, tx, p, grid, st, pdl, w_fp8);
+    case EPI_CTXKV: return launch_epi<EPI_CTXKV>(TN, tw, tx, p, grid, st, pdl, false);
   }
   return cudaErrorInvalidValue;
 }

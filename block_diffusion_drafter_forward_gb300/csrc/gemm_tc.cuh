@@ -10,7 +10,7 @@
 
 namespace dflash {
 
-enum GemmEpi { EPI_STORE = 0, EPI_QKV = 1, EPI_RESID = 2, EPI_GATEUP = 3, EPI_LMHEAD = 4 };
+enum GemmEpi { EPI_STORE = 0, EPI_QKV = 1, EPI_RESID = 2, EPI_GATEUP = 3, EPI_LMHEAD = 4, EPI_CTXKV = 5 };
 constexpr int kMaxSplits = 16;
 
 // Everything an epilogue may need; fields an epilogue does not use stay zero.
@@ -30,13 +30,16 @@ struct GemmParams {
   __nv_bfloat16* q = nullptr;
   const __nv_bfloat16* q_norm = nullptr;
   const __nv_bfloat16* k_norm = nullptr;
-  const double* inv_pi = nullptr;
+  const float2* inv_pi = nullptr;        // RoPE inv_freq / pi as (hi, lo) floats
   float mscale = 1.f;
   int nh = 0, nkv = 0, mpps = 0, layer = 0;
   const int32_t* ctx_lens = nullptr;
   const int32_t* page_tables = nullptr;
   PoolGeom g{};
   __nv_bfloat16* pool = nullptr;
+  // EPI_CTXKV (k_norm: every layer's k_norm [L, 128]; page_tables: one sequence's table)
+  const int32_t* positions = nullptr;
+  int first = 0;
   // EPI_RESID
   float* x = nullptr;
   __nv_bfloat16* xb = nullptr;

@@ -39,12 +39,18 @@ __device__ float block_sum(float v) {
 }
 
 // RoPE angle of pair j at position pos (from_weights.rs inv_freq table; YaRN divisors
-// already folded into inv_freq).  theta = pos * inv_freq_j is formed in float64 as a
-// multiple of pi, reduced to [-1, 1] half-turns, then sin/cos(pi t) in fp32.
-__device__ __forceinline__ void rope_cs(const double* inv_pi, int j, int pos, float* c, float* s) {
-  double t = (double)pos * inv_pi[j];
-  t -= 2.0 * rint(0.5 * t);
-  sincospif((float)t, s, c);
+// already folded into inv_freq), as half-turns t = pos * inv_freq_j / pi reduced to [-1, 1],
+// then sin/cos(pi t) in fp32.  ip[j] = (hi, lo) splits inv_freq_j / pi into two floats;
+// fmaf gives the exact rounding error of pos * hi, and subtracting the nearest even integer
+// is exact below 2^24, so t carries ~1e-7 absolute error without float64 arithmetic.
+__device__ __forceinline__ void rope_cs(const float2* ip, int j, int pos, float* c, float* s) {
+  const float p = (float)pos;
+  const float2 v = ip[j];
+  const float a = p * v.x;
+  const float e = fmaf(p, v.x, -a);
+  const float k = 2.f * rintf(0.5f * a);
+  const float t = (a - k) + fmaf(p, v.y, e);
+  sincospif(t, s, c);
 }
 
 __device__ __forceinline__ void flag(unsigned* status, unsigned bit) { atomicOr(status, bit); }
@@ -146,7 +152,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const TX* __restrict__ X, int
 // ctx_len + r of the sequence (the transient block K/V).
 template <typename T>
 __global__ void qkv_post_kernel(const float* __restrict__ y, int ldy, const T* __restrict__ qn_w,
-                                const T* __restrict__ kn_w, const double* __restrict__ inv_pi, float mscale,
+                                const T* __restrict__ kn_w, const float2* __restrict__ inv_pi, float mscale,
                                 float eps, int nh, int nkv, int hd, const int32_t* __restrict__ ctx_lens,
                                 const int32_t* __restrict__ page_tables, int mpps, PoolGeom g, int layer,
                                 T* __restrict__ pool, T* __restrict__ qout, unsigned* status) {
@@ -293,7 +299,7 @@ __global__ void argmax_kernel(const float* __restrict__ z, int V, int32_t* __res
 // first + i (dflash.rs ingest_ctx).
 template <typename T>
 __global__ void ctxkv_post_kernel(const float* __restrict__ ykv, int ldy, const T* __restrict__ kn_all,
-                                  const double* __restrict__ inv_pi, float mscale, float eps, int nkv, int hd,
+                                  const float2* __restrict__ inv_pi, float mscale, float eps, int nkv, int hd,
                                   const int32_t* __restrict__ positions, const int32_t* __restrict__ page_table,
                                   int first, PoolGeom g, T* __restrict__ pool, unsigned* status) {
   extern __shared__ float sm[];
@@ -397,7 +403,41 @@ __global__ void fold_norm_kernel(const __nv_bfloat16* __restrict__ A, const __nv
     out[(int64_t)p * cols + k] = ln ? __float2bfloat16_rn(__bfloat162float(src[k]) * __bfloat162float(ln[k])) : src[k];
 }
 
+// x (fp32) -> [hi | lo] bf16 with hi = bf16(x), lo = bf16(x - hi): a GEMM over the doubled
+// K with the weight repeated ([W | W]) then sees x to ~16 mantissa bits.
+__global__ void split_hi_lo_kernel(const float* __restrict__ x, int n, __nv_bfloat16* __restrict__ out) {
+  const float* xr = x + (int64_t)blockIdx.x * n;
+  __nv_bfloat16* o = out + (int64_t)blockIdx.x * 2 * n;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float v = xr[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    o[i] = hi;
+    o[n + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  }
+}
+
+// out[r] = [w[r] | w[r]] (rows x 2 cols), bf16
+__global__ void repeat_cols_kernel(const __nv_bfloat16* __restrict__ w, int cols, __nv_bfloat16* __restrict__ out) {
+  const __nv_bfloat16* src = w + (int64_t)blockIdx.x * cols;
+  __nv_bfloat16* dst = out + (int64_t)blockIdx.x * 2 * cols;
+  for (int k = threadIdx.x; k < cols; k += blockDim.x) {
+    dst[k] = src[k];
+    dst[cols + k] = src[k];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_split_hi_lo(const float* x, int rows, int n, void* out, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  split_hi_lo_kernel<<<rows, 256, 0, st>>>(x, n, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repeat_cols(const void* w, int rows, int cols, void* out, cudaStream_t st) {
+  repeat_cols_kernel<<<rows, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w), cols, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_embed_tc(const dflash_handle* h, const int32_t* bonus, int nb, cudaStream_t st) {
   const dflash_cfg& c = h->cfg;
