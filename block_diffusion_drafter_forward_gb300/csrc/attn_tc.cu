@@ -297,6 +297,269 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// ---------------------------------------------------------------------------------------
+// Pipelined variant for long key ranges (many chunks per CTA).  Warp 4 only streams K/V
+// pages into a 3-stage ring; warps 0-3 run the softmax while the tensor cores work ahead:
+// S of chunk c+1 (second TMEM buffer) is computed during the softmax of chunk c, P is
+// double-buffered in shared memory, and O accumulates in TMEM across chunks.  O is rescaled
+// only when a row's running maximum grows by more than 2^8 (probabilities stay <= 256, so
+// fp32 sums are safe), which after the first chunks is rare; the normaliser l uses the
+// same stale maximum, so the result is unchanged.
+constexpr int kPipeStages = 3;
+constexpr int kPipeSmem = kQBytes + 2 * kPBytes + kPipeStages * kKVStage + 256 + 1024;
+
+__global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sP = sQ + kQBytes;                      // two buffers of kPBytes
+  uint8_t* sKV = sP + 2 * kPBytes;
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + kPipeStages * kKVStage);
+  uint64_t* kv_empty = kv_full + kPipeStages;
+  uint64_t* s_done = kv_empty + kPipeStages;       // [2]
+  uint64_t* o_done = s_done + 2;                   // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int unit = blockIdx.x, split = blockIdx.y;
+  const int s = unit / p.nkv, g = unit % p.nkv;
+  const int group = p.nh / p.nkv;
+  const int ctx = p.ctx_lens[s];
+  if (ctx < 0 || ctx > p.max_ctx || ctx + kGamma > p.mpps * kPage) {
+    if (t == 0 && split == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
+    return;
+  }
+  int k0;
+  const int nch = chunk_range(p.window, ctx, &k0);
+  const int nsplit = (nch + p.chunks_per_split - 1) / p.chunks_per_split;
+  if (nsplit > (int)gridDim.y) {
+    if (t == 0 && split == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
+    return;
+  }
+  if (split >= nsplit) return;
+  const int c_begin = split * p.chunks_per_split;
+  const int n = min(nch, c_begin + p.chunks_per_split) - c_begin;
+  const int nkeys = ctx + kGamma;
+  const int32_t* pt = p.page_tables + (int64_t)s * p.mpps;
+  const int npages_seq = (nkeys + kPage - 1) / kPage;
+  const int safe_keys = ctx & ~(kPage - 1);
+
+  if (t == 0) {
+    for (int i = 0; i < kPipeStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_done[i], 1);
+      mbar_init(&o_done[i], 1);
+    }
+    flags[0] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS[2] = {tmem, tmem + 64}, tO = tmem + 128;
+  pdl_trigger();
+
+  if (warp == 4) {
+    // ---------------- K/V page producer
+    if (lane == 0) {
+      bool waited = false;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % kPipeStages, c = c_begin + i;
+        if (i >= kPipeStages && !mbar_wait(&kv_empty[st], ((i / kPipeStages) - 1) & 1)) {
+          flags[0] = 1;
+          break;
+        }
+        if (!waited && k0 + (c + 1) * kKC > safe_keys) {  // chunk holds block rows
+          pdl_wait();
+          waited = true;
+        }
+        uint8_t* dK = sKV + st * kKVStage;
+        uint8_t* dV = dK + kPagesPerChunk * kTileBytes;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * kPagesPerChunk * kTileBytes);
+        const int pg0 = (k0 + c * kKC) / kPage;
+        int pages[kPagesPerChunk];
+#pragma unroll
+        for (int q = 0; q < kPagesPerChunk; ++q) pages[q] = __ldg(pt + (pg0 + q < npages_seq ? pg0 + q : 0));
+#pragma unroll
+        for (int q = 0; q < kPagesPerChunk; ++q) {
+          int page = pages[q];
+          if (page < 0 || page >= p.g.num_pages) {
+            atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
+            page = 0;
+          }
+          bulk_load(dK + q * kTileBytes, p.pool + tile_base(p.g, p.layer, page, 0, g), kTileBytes, &kv_full[st]);
+          bulk_load(dV + q * kTileBytes, p.pool + tile_base(p.g, p.layer, page, 1, g), kTileBytes, &kv_full[st]);
+        }
+      }
+      if (!waited) pdl_wait();
+    }
+    __syncwarp();
+  } else {
+    // ---------------- warps 0-3: queries, softmax, MMA issue (thread 0)
+    pdl_wait();
+    {
+      const int hh = t >> 4, r = t & 15;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(p.q + ((int64_t)(s * kGamma + r) * p.nh + g * group + hh) * 128);
+#pragma unroll
+      for (int d8 = 0; d8 < 16; ++d8)
+        *reinterpret_cast<uint4*>(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16) = src[d8];
+    }
+    fence_proxy_async_smem();
+    named_barrier(1, 128);
+    constexpr uint32_t idesc_s = idesc_bf16(128, kKC);
+    constexpr uint32_t idesc_o = idesc_bf16(128, 128);
+    auto issue_s = [&](int i) {  // thread 0: S(i) = Q K(i)^T into tS[i & 1]
+      const int st = i % kPipeStages;
+      if (!mbar_wait(&kv_full[st], (i / kPipeStages) & 1)) flags[0] = 1;
+      tc_fence_after();
+      if (!flags[0]) {
+        const uint8_t* sK = sKV + st * kKVStage;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_bf16(tS[i & 1], desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048), idesc_s,
+                   k > 0 ? 1u : 0u);
+      }
+      mma_commit(&s_done[i & 1]);
+    };
+    if (t == 0) issue_s(0);
+    const int r = t & 15;
+    const int pos_q = ctx + r;
+    const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    float m_used = -FLT_MAX, l_run = 0.f;
+    for (int i = 0; i < n; ++i) {
+      const int b = i & 1, st = i % kPipeStages;
+      if (!mbar_wait(&s_done[b], (i >> 1) & 1)) flags[0] = 1;
+      tc_fence_after();
+      const int kbase = k0 + (c_begin + i) * kKC;
+      float mc = -FLT_MAX;
+#pragma unroll
+      for (int q4 = 0; q4 < kKC / 32; ++q4) {
+        float v[32];
+        tmem_ld32(tS[b] + lane_off + q4 * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int key = kbase + q4 * 32 + j;
+          if (key < nkeys && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[j] * scale_log2);
+        }
+      }
+      // lazy rescale: move the reference maximum only when it grew by more than 2^8
+      float m_new = m_used;
+      if (mc > m_used + 8.f || (m_used == -FLT_MAX && mc > -FLT_MAX)) m_new = mc;
+      // P buffer b was read by PV(i-2); O is about to be rescaled only after PV(i-1)
+      if (i >= 2 && !mbar_wait(&o_done[b], ((i - 2) >> 1) & 1)) flags[0] = 1;
+      const bool rescale = m_new != m_used && m_used != -FLT_MAX && i > 0;
+      if (rescale) {
+        if (!mbar_wait(&o_done[b ^ 1], ((i - 1) >> 1) & 1)) flags[0] = 1;
+        tc_fence_after();
+        const float a = exp2f(m_used - m_new);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float v[32];
+          tmem_ld32(tO + lane_off + q4 * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= a;
+          tmem_st32(tO + lane_off + q4 * 32, v);
+        }
+        l_run *= a;
+      }
+      m_used = m_new;
+      float lsum = 0.f;
+      uint8_t* pb = sP + b * kPBytes;
+#pragma unroll
+      for (int q4 = 0; q4 < kKC / 32; ++q4) {
+        float v[32];
+        tmem_ld32(tS[b] + lane_off + q4 * 32, v);
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float pr[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int jj = j8 * 8 + 2 * e + u;
+              const int key = kbase + q4 * 32 + jj;
+              const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
+              pr[u] = vis ? exp2f(v[jj] * scale_log2 - m_used) : 0.f;
+            }
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
+            lsum += __low2float(h2) + __high2float(h2);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(pb + ((t >> 3) * (kKC / 8) + q4 * 4 + j8) * 128 + (t & 7) * 16) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      l_run += lsum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_barrier(1, 128);
+      if (t == 0) {
+        tc_fence_after();
+        if (!flags[0]) {
+          const uint8_t* sV = sKV + st * kKVStage + kPagesPerChunk * kTileBytes;
+#pragma unroll
+          for (int k = 0; k < kPagesPerChunk; ++k)
+            mma_bf16(tO, desc_noswz(pb + k * 256, 128, kKC / 8 * 128), desc_noswz(sV + k * kTileBytes, 128, 256),
+                     idesc_o, (i > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(&o_done[b]);
+        mma_commit(&kv_empty[st]);
+        if (i + 1 < n) issue_s(i + 1);
+      }
+    }
+    if (n > 0 && !mbar_wait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) flags[0] = 1;
+    tc_fence_after();
+    named_barrier(1, 128);
+    const int hh = t >> 4;
+    __nv_bfloat16* dst = p.out + ((int64_t)(s * kGamma + r) * p.nh + g * group + hh) * 128;
+    if (flags[0]) {
+      if (t == 0) atomicOr(p.status, DFLASH_DEV_TIMEOUT);
+      for (int i = 0; i < 2000; ++i) __nanosleep(1000);
+    } else if (nsplit == 1) {
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float v[32];
+        tmem_ld32(tO + lane_off + q4 * 32, v);
+#pragma unroll
+        for (int d8 = 0; d8 < 4; ++d8) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[d8 * 8 + 2 * e] * inv, v[d8 * 8 + 2 * e + 1] * inv);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          reinterpret_cast<uint4*>(dst)[q4 * 4 + d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+    } else {
+      const int64_t slot = (int64_t)unit * gridDim.y + split;
+      float* op = p.o_part + (slot * 128 + t) * 128;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float v[32];
+        tmem_ld32(tO + lane_off + q4 * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          __stcg(reinterpret_cast<float4*>(op + q4 * 32 + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+      }
+      __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_used, l_run));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 // Merge the split partials of every (sequence, kv head) unit with more than one split, in
 // split order with a running maximum: o = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
 // Block (unit, rb) owns rows 4 rb .. 4 rb + 3; a warp per row, 4 dims per thread.
@@ -369,17 +632,26 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   const int splits = (nch + cps - 1) / cps;
   p.chunks_per_split = cps;
   p.max_ctx = max_ctx_len;
+  static bool attr2 = false;
+  if (!attr2) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmem);
+    if (e != cudaSuccess) return e;
+    attr2 = true;
+  }
+  // many chunks per CTA: the pipelined kernel; a few: the compact one (it fits beside a
+  // projection CTA on one SM, so it overlaps the QKV kernel under programmatic launch)
+  const bool pipe = cps >= 4;
   cudaLaunchConfig_t ac = {};
   ac.gridDim = dim3(units, splits);
-  ac.blockDim = dim3(128);
-  ac.dynamicSmemBytes = kSmem;
+  ac.blockDim = dim3(pipe ? 160 : 128);
+  ac.dynamicSmemBytes = pipe ? kPipeSmem : kSmem;
   ac.stream = st;
   cudaLaunchAttribute aa[1];
   aa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   aa[0].val.programmaticStreamSerializationAllowed = 1;
   ac.attrs = aa;
   ac.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
+  cudaError_t e = pipe ? cudaLaunchKernelEx(&ac, attn_tc_pipe_kernel, p) : cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
   if (e != cudaSuccess || splits == 1) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units, 32);
