@@ -186,6 +186,21 @@ def oracle_timing(wl, budget_s: float = 20.0):
 # ----------------------------------------------------------------------------- main
 
 
+def aggregate_over_ranks(local_ms: float, tokens_per_rank: int, dist=None, device="cpu"):
+    """Replicas: each rank timed its own batch.  Returns (max over ranks of the timed region in
+    ms, whole-job tokens/s = tokens of all ranks / that max)."""
+    import torch
+
+    world = 1
+    t = local_ms
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        buf = torch.tensor([local_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(buf, op=dist.ReduceOp.MAX)
+        t = float(buf.item())
+    return t, world * tokens_per_rank / (t / 1e3)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -289,14 +304,9 @@ def main():
             evs[i][1].record(stream)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
     tokens_per_step = wl.nb * (cfg.gamma - 1)
-    value = world * tokens_per_step * args.steps / (total_ms / 1e3)
+    total_ms, value = aggregate_over_ranks(sum(step_ms), tokens_per_step * args.steps, dist, "cuda")
+    ms_per_step = total_ms / args.steps
 
     # ---- per-kernel durations: the same K steps again, replaying the graph captured with
     # CUDA events around every kernel (the events serialise the kernels, so this pass is
@@ -332,11 +342,8 @@ def main():
         b.record(stream)
         b.synchronize()
         e2e_ms += a.elapsed_time(b)
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * tokens_per_step * args.steps / (e2e_ms / 1e3), "unit": "draft tokens/s",
+    e2e_ms, e2e_value = aggregate_over_ranks(e2e_ms, tokens_per_step * args.steps, dist, "cuda")
+    e2e = {"value": e2e_value, "unit": "draft tokens/s",
            "h2d_bytes_per_step": int(h_bonus.numel() * 4 + h_ctx.numel() * 4 + h_pt.numel() * 4),
            "d2h_bytes_per_step": int(h_drafts.numel() * 4)}
 

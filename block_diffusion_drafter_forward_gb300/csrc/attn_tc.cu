@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
   uint64_t* s_done = kv_empty + kPipeStages;       // [2]
   uint64_t* o_done = s_done + 2;                   // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
-  int* flags = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int unit = blockIdx.x, split = blockIdx.y;
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
       bool waited = false;
       for (int i = 0; i < n; ++i) {
         const int st = i % kPipeStages, c = c_begin + i;
-        if (i >= kPipeStages && !mbar_wait(&kv_empty[st], ((i / kPipeStages) - 1) & 1)) {
+        if (i >= kPipeStages && !mbar_wait_ab(&kv_empty[st], ((i / kPipeStages) - 1) & 1, flags)) {
           flags[0] = 1;
           break;
         }
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
     constexpr uint32_t idesc_o = idesc_bf16(128, 128);
     auto issue_s = [&](int i) {  // thread 0: S(i) = Q K(i)^T into tS[i & 1]
       const int st = i % kPipeStages;
-      if (!mbar_wait(&kv_full[st], (i / kPipeStages) & 1)) flags[0] = 1;
+      if (!mbar_wait_ab(&kv_full[st], (i / kPipeStages) & 1, flags)) flags[0] = 1;
       tc_fence_after();
       if (!flags[0]) {
         const uint8_t* sK = sKV + st * kKVStage;
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
     float m_used = -FLT_MAX, l_run = 0.f;
     for (int i = 0; i < n; ++i) {
       const int b = i & 1, st = i % kPipeStages;
-      if (!mbar_wait(&s_done[b], (i >> 1) & 1)) flags[0] = 1;
+      if (!mbar_wait_ab(&s_done[b], (i >> 1) & 1, flags)) flags[0] = 1;
       tc_fence_after();
       const int kbase = k0 + (c_begin + i) * kKC;
       float mc = -FLT_MAX;
@@ -454,12 +454,14 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
       float m_new = m_used;
       if (mc > m_used + 8.f || (m_used == -FLT_MAX && mc > -FLT_MAX)) m_new = mc;
       // P buffer b was read by PV(i-2); O is about to be rescaled only after PV(i-1)
-      if (i >= 2 && !mbar_wait(&o_done[b], ((i - 2) >> 1) & 1)) flags[0] = 1;
+      if (i >= 2 && !mbar_wait_ab(&o_done[b], ((i - 2) >> 1) & 1, flags)) flags[0] = 1;
+      // TMEM loads/stores are warp-collective: rescale a warp's rows together (factor 1 for
+      // rows whose reference maximum did not move)
       const bool rescale = m_new != m_used && m_used != -FLT_MAX && i > 0;
-      if (rescale) {
-        if (!mbar_wait(&o_done[b ^ 1], ((i - 1) >> 1) & 1)) flags[0] = 1;
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!mbar_wait_ab(&o_done[b ^ 1], ((i - 1) >> 1) & 1, flags)) flags[0] = 1;
         tc_fence_after();
-        const float a = exp2f(m_used - m_new);
+        const float a = rescale ? exp2f(m_used - m_new) : 1.f;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           float v[32];
@@ -516,7 +518,7 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
         if (i + 1 < n) issue_s(i + 1);
       }
     }
-    if (n > 0 && !mbar_wait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) flags[0] = 1;
+    if (n > 0 && !mbar_wait_ab(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, flags)) flags[0] = 1;
     tc_fence_after();
     named_barrier(1, 128);
     const int hh = t >> 4;
