@@ -299,21 +299,21 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
 
 // ---------------------------------------------------------------------------------------
 // Pipelined variant for long key ranges (many chunks per CTA).  Warp 4 only streams K/V
-// pages into a 3-stage ring; warps 0-3 run the softmax while the tensor cores work ahead:
+// pages into a 2-stage ring; warps 0-3 run the softmax while the tensor cores work ahead:
 // S of chunk c+1 (second TMEM buffer) is computed during the softmax of chunk c, P is
-// double-buffered in shared memory, and O accumulates in TMEM across chunks.  O is rescaled
+// written as bf16 over its own S columns in TMEM and read from there by the P V MMA, and O
+// accumulates in TMEM across chunks.  ~96 KB of shared memory: two CTAs share an SM.  O is rescaled
 // only when a row's running maximum grows by more than 2^8 (probabilities stay <= 256, so
 // fp32 sums are safe), which after the first chunks is rare; the normaliser l uses the
 // same stale maximum, so the result is unchanged.
-constexpr int kPipeStages = 3;
-constexpr int kPipeSmem = kQBytes + 2 * kPBytes + kPipeStages * kKVStage + 256 + 1024;
+constexpr int kPipeStages = 2;
+constexpr int kPipeSmem = kQBytes + kPipeStages * kKVStage + 256 + 1024;
 
 __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sP = sQ + kQBytes;                      // two buffers of kPBytes
-  uint8_t* sKV = sP + 2 * kPBytes;
+  uint8_t* sKV = sQ + kQBytes;
   uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + kPipeStages * kKVStage);
   uint64_t* kv_empty = kv_full + kPipeStages;
   uint64_t* s_done = kv_empty + kPipeStages;       // [2]
@@ -453,8 +453,7 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
       // lazy rescale: move the reference maximum only when it grew by more than 2^8
       float m_new = m_used;
       if (mc > m_used + 8.f || (m_used == -FLT_MAX && mc > -FLT_MAX)) m_new = mc;
-      // P buffer b was read by PV(i-2); O is about to be rescaled only after PV(i-1)
-      if (i >= 2 && !mbar_wait_ab(&o_done[b], ((i - 2) >> 1) & 1, flags)) flags[0] = 1;
+      // (P of chunk i goes over S[b]; S(i) already overwrote P(i-2) after PV(i-2) in order)
       // TMEM loads/stores are warp-collective: rescale a warp's rows together (factor 1 for
       // rows whose reference maximum did not move)
       const bool rescale = m_new != m_used && m_used != -FLT_MAX && i > 0;
@@ -474,34 +473,28 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
       }
       m_used = m_new;
       float lsum = 0.f;
-      uint8_t* pb = sP + b * kPBytes;
+      uint32_t pw[kKC / 2];
 #pragma unroll
       for (int q4 = 0; q4 < kKC / 32; ++q4) {
         float v[32];
         tmem_ld32(tS[b] + lane_off + q4 * 32, v);
 #pragma unroll
-        for (int j8 = 0; j8 < 4; ++j8) {
-          uint32_t pk[4];
+        for (int e = 0; e < 16; ++e) {
+          float pr[2];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float pr[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int jj = j8 * 8 + 2 * e + u;
-              const int key = kbase + q4 * 32 + jj;
-              const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
-              pr[u] = vis ? exp2f(v[jj] * scale_log2 - m_used) : 0.f;
-            }
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
-            lsum += __low2float(h2) + __high2float(h2);
-            pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          for (int u = 0; u < 2; ++u) {
+            const int jj = 2 * e + u;
+            const int key = kbase + q4 * 32 + jj;
+            const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
+            pr[u] = vis ? exp2f(v[jj] * scale_log2 - m_used) : 0.f;
           }
-          *reinterpret_cast<uint4*>(pb + ((t >> 3) * (kKC / 8) + q4 * 4 + j8) * 128 + (t & 7) * 16) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
+          lsum += __low2float(h2) + __high2float(h2);
+          pw[q4 * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
       }
+      tmem_st32u(tS[b] + lane_off, pw);  // P(i): 64 bf16 per row in S[b] columns 0..31
       l_run += lsum;
-      fence_proxy_async_smem();
       tc_fence_before();
       named_barrier(1, 128);
       if (t == 0) {
@@ -509,9 +502,9 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
         if (!flags[0]) {
           const uint8_t* sV = sKV + st * kKVStage + kPagesPerChunk * kTileBytes;
 #pragma unroll
-          for (int k = 0; k < kPagesPerChunk; ++k)
-            mma_bf16(tO, desc_noswz(pb + k * 256, 128, kKC / 8 * 128), desc_noswz(sV + k * kTileBytes, 128, 256),
-                     idesc_o, (i > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kPagesPerChunk; ++k)  // K = 16 keys = 8 TMEM columns of P each
+            mma_bf16_tmem_a(tO, tS[b] + k * 8, desc_noswz(sV + k * kTileBytes, 128, 256), idesc_o,
+                            (i > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(&o_done[b]);
         mma_commit(&kv_empty[st]);
@@ -613,9 +606,9 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
 
 }  // namespace
 
-// Partial slots any launch needs: units * splits <= num_sms + units (splits = ceil(nch / cps)
-// with cps = ceil(units * nch / num_sms)).
-int64_t attn_tc_partial_slots(int num_sms, int max_units) { return (int64_t)num_sms + max_units; }
+// Partial slots any launch needs: units * splits <= 2 * num_sms + units (splits =
+// ceil(nch / cps) with cps >= units * nch / (2 * num_sms)).
+int64_t attn_tc_partial_slots(int num_sms, int max_units) { return 2 * (int64_t)num_sms + max_units; }
 
 cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, cudaStream_t st) {
   static bool attr = false;
@@ -631,8 +624,6 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   if (p.window > 0) nch = std::min(nch, (p.window + kGamma + kPage + kKC - 1) / kKC);
   int cps = (units * nch + num_sms - 1) / num_sms;
   if (cps < 1) cps = 1;
-  const int splits = (nch + cps - 1) / cps;
-  p.chunks_per_split = cps;
   p.max_ctx = max_ctx_len;
   static bool attr2 = false;
   if (!attr2) {
@@ -643,8 +634,13 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   // many chunks per CTA: the pipelined kernel; a few: the compact one (it fits beside a
   // projection CTA on one SM, so it overlaps the QKV kernel under programmatic launch)
   const bool pipe = cps >= 4;
+  if (pipe) {  // two pipelined CTAs fit on an SM: size the split for 2 x num_sms CTAs
+    cps = std::max(4, (units * nch + 2 * num_sms - 1) / (2 * num_sms));
+  }
+  const int splits_l = (nch + cps - 1) / cps;
+  p.chunks_per_split = cps;
   cudaLaunchConfig_t ac = {};
-  ac.gridDim = dim3(units, splits);
+  ac.gridDim = dim3(units, splits_l);
   ac.blockDim = dim3(pipe ? 160 : 128);
   ac.dynamicSmemBytes = pipe ? kPipeSmem : kSmem;
   ac.stream = st;
@@ -654,7 +650,7 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   ac.attrs = aa;
   ac.numAttrs = 1;
   cudaError_t e = pipe ? cudaLaunchKernelEx(&ac, attn_tc_pipe_kernel, p) : cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
-  if (e != cudaSuccess || splits == 1) return e;
+  if (e != cudaSuccess || splits_l == 1) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units, 32);
   cfg.blockDim = dim3(128);
@@ -664,7 +660,7 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, splits);
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, splits_l);
 }
 
 }  // namespace dflash

@@ -77,9 +77,28 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 struct EpiSmem {
   float xch[kThreads][17];   // one 16-token chunk of the tile, transposed exchange
   float red[4][16];          // per-warp partial reductions for 16 tokens
+  float tot[16];             // per-token totals over the tile's 128 rows
   float bv[4][16];
   int bi[4][16];
 };
+
+// Sum over the tile's 128 rows of w[row][c] for each of the chunk's 16 tokens, into es.tot.
+// Transposed through shared memory: thread (token c = t % 16, group g = t / 16) adds rows
+// 16g..16g+15 of token c, then one shuffle and a 4-warp combine.
+__device__ __forceinline__ void rowsum16(EpiSmem& es, const float (&w)[16], int t) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c) es.xch[t][c] = w[c];
+  __syncthreads();
+  const int c = t & 15, g = t >> 4;
+  float a = 0.f;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) a += es.xch[g * 16 + r][c];
+  a += __shfl_xor_sync(0xffffffffu, a, 16);
+  if ((t & 31) < 16) es.red[t >> 5][c] = a;
+  __syncthreads();
+  if (t < 16) es.tot[t] = (es.red[0][t] + es.red[1][t]) + (es.red[2][t] + es.red[3][t]);
+  __syncthreads();
+}
 
 template <int EPI>
 __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rsc, float (&v)[16], int t, int n,
@@ -93,28 +112,27 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
     }
   } else if constexpr (EPI == EPI_RESID) {
     float sq[16];
+    const float lnw = p.ln_next ? __bfloat162float(p.ln_next[n]) : 1.f;
+    float xo[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) xo[c] = m0 + c0 + c < p.M ? p.x[(int64_t)(m0 + c0 + c) * p.H + n] : 0.f;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int m = m0 + c0 + c;
       float xv = 0.f;
       if (m < p.M) {
         const int64_t o = (int64_t)m * p.H + n;
-        xv = p.x[o] + v[c];
+        xv = xo[c] + v[c];
         p.x[o] = xv;
-        p.xb[o] = __float2bfloat16_rn(p.ln_next ? xv * __bfloat162float(p.ln_next[n]) : xv);
+        p.xb[o] = __float2bfloat16_rn(xv * lnw);
       }
-      sq[c] = warp_sum(xv * xv);
+      sq[c] = xv * xv;
     }
-    if (lane == 0) {
-#pragma unroll
-      for (int c = 0; c < 16; ++c) es.red[warp][c] = sq[c];
-    }
-    __syncthreads();
+    rowsum16(es, sq, t);
     if (t < 16) {
       const int m = m0 + c0 + t;
-      if (m < p.M) p.ss_out[(int64_t)tile_n * p.Mp + m] = es.red[0][t] + es.red[1][t] + es.red[2][t] + es.red[3][t];
+      if (m < p.M) p.ss_out[(int64_t)tile_n * p.Mp + m] = es.tot[t];
     }
-    __syncthreads();
   } else if constexpr (EPI == EPI_GATEUP) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * rsc[c0 + c];
@@ -139,18 +157,11 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
       // per-head RMSNorm over the 128 rows of the tile
       float sq[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) sq[c] = warp_sum(v[c] * v[c]);
-      if (lane == 0) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) es.red[warp][c] = sq[c];
-      }
-      __syncthreads();
+      for (int c = 0; c < 16; ++c) sq[c] = v[c] * v[c];
+      rowsum16(es, sq, t);
       const float w = __bfloat162float((is_q ? p.q_norm : p.k_norm)[t]);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float ss = es.red[0][c] + es.red[1][c] + es.red[2][c] + es.red[3][c];
-        es.xch[t][c] = v[c] * (1.f / sqrtf(ss * (1.f / 128.f) + p.eps)) * w;
-      }
+      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * (1.f / sqrtf(es.tot[c] * (1.f / 128.f) + p.eps)) * w;
       __syncthreads();
       // RoPE: pair (j, j + 64), NeoX rotate-half
       const int j = t & 63;
@@ -200,18 +211,11 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
     if (is_k) {
       float sq[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) sq[c] = warp_sum(v[c] * v[c]);
-      if (lane == 0) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) es.red[warp][c] = sq[c];
-      }
-      __syncthreads();
+      for (int c = 0; c < 16; ++c) sq[c] = v[c] * v[c];
+      rowsum16(es, sq, t);
       const float w = __bfloat162float(p.k_norm[l * 128 + t]);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float ss = es.red[0][c] + es.red[1][c] + es.red[2][c] + es.red[3][c];
-        es.xch[t][c] = v[c] * (1.f / sqrtf(ss * (1.f / 128.f) + p.eps)) * w;
-      }
+      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * (1.f / sqrtf(es.tot[c] * (1.f / 128.f) + p.eps)) * w;
       __syncthreads();
       const int j = t & 63;
 #pragma unroll
@@ -242,36 +246,41 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
   } else if constexpr (EPI == EPI_LMHEAD) {
     const bool valid_row = n < p.N;
     const float sc = (p.row_scale && valid_row) ? p.row_scale[n] : 1.f;
-    float bv[16];
-    int bi[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int m = m0 + c0 + c;
       const float z = v[c] * sc;
       if (p.logits && valid_row && m < p.M) p.logits[(int64_t)m * p.N + n] = __float2bfloat16_rn(z);
-      bv[c] = valid_row ? z : -FLT_MAX;
-      bi[c] = valid_row ? n : 0x7fffffff;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv[c], o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi[c], o);
-        if (better(ov, oi, bv[c], bi[c])) { bv[c] = ov; bi[c] = oi; }
-      }
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int c = 0; c < 16; ++c) { es.bv[warp][c] = bv[c]; es.bi[warp][c] = bi[c]; }
+      es.xch[t][c] = valid_row ? z : -FLT_MAX;
     }
     __syncthreads();
+    // thread (token c, group g) scans rows 16g..16g+15 (ties -> lowest row), then combine
+    const int c = t & 15, g = t >> 4;
+    float b = -FLT_MAX;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float z = es.xch[g * 16 + r][c];
+      const int idx = tile_n * 128 + g * 16 + r;
+      if (z > b) { b = z; bi = idx; }
+    }
+    if (b == -FLT_MAX) bi = 0x7fffffff;
+    {
+      const float ob = __shfl_xor_sync(0xffffffffu, b, 16);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, 16);
+      if (better(ob, oi, b, bi)) { b = ob; bi = oi; }
+    }
+    if ((t & 31) < 16) { es.bv[t >> 5][c] = b; es.bi[t >> 5][c] = bi; }
+    __syncthreads();
     if (t < 16) {
-      float b = es.bv[0][t];
-      int i = es.bi[0][t];
+      float bb = es.bv[0][t];
+      int ii = es.bi[0][t];
       for (int w2 = 1; w2 < 4; ++w2)
-        if (better(es.bv[w2][t], es.bi[w2][t], b, i)) { b = es.bv[w2][t]; i = es.bi[w2][t]; }
+        if (better(es.bv[w2][t], es.bi[w2][t], bb, ii)) { bb = es.bv[w2][t]; ii = es.bi[w2][t]; }
       const int m = m0 + c0 + t;
       if (m < p.M) {
-        p.amax_val[(int64_t)tile_n * p.Mp + m] = b;
-        p.amax_idx[(int64_t)tile_n * p.Mp + m] = i;
+        p.amax_val[(int64_t)tile_n * p.Mp + m] = bb;
+        p.amax_idx[(int64_t)tile_n * p.Mp + m] = ii;
       }
     }
     __syncthreads();
