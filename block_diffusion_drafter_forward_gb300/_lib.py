@@ -67,7 +67,7 @@ class dflash_weights(ctypes.Structure):
 EXPORTS = ("dflash_create", "dflash_destroy", "dflash_write_ctx_kv", "dflash_propose", "dflash_kv_layout",
            "dflash_device_status", "dflash_last_error", "dflash_fp8_lm_head", "dflash_profile",
            "dflash_profile_kinds", "dflash_profile_read", "dflash_gemm_bf16",
-           "dflash_attention_check", "dflash_gemm_bf16_noalloc")
+           "dflash_attention_check", "dflash_gemm_bf16_noalloc", "dflash_set_persistent", "dflash_persistent")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -108,6 +108,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_attention_check.restype = c.c_int
     lib.dflash_gemm_bf16_noalloc.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp]
     lib.dflash_gemm_bf16_noalloc.restype = c.c_int
+    lib.dflash_set_persistent.argtypes = [vp, c.c_int]
+    lib.dflash_set_persistent.restype = c.c_int
+    lib.dflash_persistent.argtypes = [vp]
+    lib.dflash_persistent.restype = c.c_int
     lib.dflash_last_error.argtypes = [vp]
     lib.dflash_last_error.restype = c.c_char_p
     _lib = lib
@@ -176,6 +180,14 @@ def dflash_fp8_lm_head(handle: int) -> Tuple[int, int]:
     _check(load().dflash_fp8_lm_head(ctypes.c_void_p(handle), ctypes.byref(codes), ctypes.byref(scales)),
            ctypes.c_void_p(handle))
     return codes.value, scales.value
+
+
+def dflash_set_persistent(handle: int, enable: bool) -> None:
+    _check(load().dflash_set_persistent(ctypes.c_void_p(handle), 1 if enable else 0), ctypes.c_void_p(handle))
+
+
+def dflash_persistent(handle: int) -> bool:
+    return bool(load().dflash_persistent(ctypes.c_void_p(handle)))
 
 
 def dflash_profile(handle: int, enable: bool) -> None:

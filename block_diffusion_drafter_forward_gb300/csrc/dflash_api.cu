@@ -11,6 +11,7 @@
 #include "dflash_internal.cuh"
 #include "attn_tc.cuh"
 #include "gemm_tc.cuh"
+#include "persist_tc.cuh"
 
 using namespace dflash;
 
@@ -189,6 +190,60 @@ int check_cfg(const dflash_cfg& c) {
   return DFLASH_OK;
 }
 
+// The bf16 gamma-block forward of one sequence as ONE persistent kernel (persist_tc.cu):
+// same arithmetic as propose_tc's per-projection kernels, no launch or grid-drain gaps
+// between the projections.
+int propose_persist(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens,
+                    const int32_t* page_tables, int nb, int max_ctx_len, int32_t* draft_tokens, void* logits,
+                    void* final_hidden, cudaStream_t st) {
+  const dflash_cfg& c = h->cfg;
+  PersistParams p{};
+  p.L = c.n_layers;
+  p.M = nb * kGamma;
+  p.H = c.hidden;
+  p.F = c.n_ff;
+  p.nh = c.n_q_heads;
+  p.nkv = c.n_kv_heads;
+  p.V = c.vocab;
+  p.mpps = c.max_pages_per_seq;
+  p.mask = c.mask_token_id;
+  p.max_ctx = max_ctx_len;
+  p.G = h->num_sms;
+  p.eps = c.rms_eps;
+  p.mscale = h->rope_mscale;
+  const int units = nb * c.n_kv_heads;
+  persist_attn_split(units, max_ctx_len, 0, p.G, &p.attn_cps[0], &p.attn_splits[0]);
+  persist_attn_split(units, max_ctx_len, c.sliding_window, p.G, &p.attn_cps[1], &p.attn_splits[1]);
+  p.bonus = bonus_tokens;
+  p.ctx_lens = ctx_lens;
+  p.page_tables = page_tables;
+  p.embed = static_cast<const __nv_bfloat16*>(h->embed);
+  p.norm = static_cast<const __nv_bfloat16*>(h->norm);
+  p.inv_pi = h->rope_inv_pi;
+  p.layers = static_cast<const PersistLayer*>(h->p_layers);
+  p.maps = static_cast<const CUtensorMap*>(h->p_maps);
+  p.x = h->x;
+  p.xb = static_cast<__nv_bfloat16*>(h->xb);
+  p.ss_a = h->ss_a;
+  p.ss_b = h->ss_b;
+  p.q = static_cast<__nv_bfloat16*>(h->q);
+  p.attn = static_cast<__nv_bfloat16*>(h->attn);
+  p.act = static_cast<__nv_bfloat16*>(h->act);
+  p.pool = static_cast<__nv_bfloat16*>(h->pool);
+  p.g = h->geom;
+  p.ws = h->ws;
+  p.o_part = h->attn_opart;
+  p.ml_part = h->attn_ml;
+  p.drafts = draft_tokens;
+  p.logits = static_cast<__nv_bfloat16*>(logits);
+  p.final_hidden = static_cast<__nv_bfloat16*>(final_hidden);
+  p.status = h->d_status;
+  persist_bind_ctl(p, h->p_ctl);
+  CK(cudaMemsetAsync(h->p_ctl, 0, h->p_ctl_words * sizeof(unsigned), st), "persistent control reset");
+  KL(K_PERSIST, launch_persist(p, st), "persistent forward");
+  return DFLASH_OK;
+}
+
 // The bf16 gamma-block forward on the tensor-core kernels (dflash.rs forward_round +
 // final norm + lm_head + argmax).  Every projection is one tcgen05 GEMM launch with its
 // epilogue fused; launches after the first may start early (programmatic dependent launch)
@@ -197,6 +252,9 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
                int nb, int max_ctx_len, int32_t* draft_tokens, void* logits, void* final_hidden, cudaStream_t st) {
   const dflash_cfg& c = h->cfg;
   const int M = nb * kGamma;
+  if (h->persist_on && M <= kPersistMaxM)
+    return propose_persist(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits,
+                           final_hidden, st);
   const int H = c.hidden, F = c.n_ff, qd = c.n_q_heads * c.head_dim;
   const int qkvd = qd + 2 * c.n_kv_heads * c.head_dim;
   const int Mp = h->rows_max;
@@ -290,8 +348,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
     const bool fp8 = c.lm_head_dtype == DFLASH_FP8E4M3_ROWSCALE;
     GemmParams p = base;
     p.logits = static_cast<__nv_bfloat16*>(logits);
-    p.amax_val = h->amax_val;
-    p.amax_idx = h->amax_idx;
+    p.amax_best = h->amax_best;
     p.amax_counter = h->counters + kCounters - 64;
     p.drafts = draft_tokens;
     p.row_scale = fp8 ? h->lm_scale : nullptr;
@@ -468,8 +525,11 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     ALLOC(h->xb, R * H * es);
     ALLOC(h->ss_a, (H / 128) * R * 4);
     ALLOC(h->ss_b, (H / 128) * R * 4);
-    ALLOC(h->amax_val, ((V + 127) / 128) * R * 4);
-    ALLOC(h->amax_idx, ((V + 127) / 128) * R * 4);
+    ALLOC(h->amax_best, R * sizeof(unsigned long long));
+    if (cudaMemsetAsync(h->amax_best, 0, R * sizeof(unsigned long long), st) != cudaSuccess) {
+      fail(h, DFLASH_ECUDA, "argmax memset");
+      return bail(DFLASH_ECUDA);
+    }
     ALLOC(h->counters, kCounters * sizeof(unsigned));
     if (cudaMemsetAsync(h->counters, 0, kCounters * sizeof(unsigned), st) != cudaSuccess) {
       fail(h, DFLASH_ECUDA, "counter memset");
@@ -501,9 +561,57 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
       fail(h, DFLASH_ECUDA, "repeat context-K/V weight");
       return bail(DFLASH_ECUDA);
     }
+    h->tc_attn = (nh / nkv) == 8;
+    // single-launch persistent forward for batch 1: needs the tensor-core attention, a bf16
+    // lm_head and one resident CTA per SM
+    if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && H <= persist_max_hidden()) {
+      int per_sm = 0;
+      if (persist_occupancy(&per_sm) == cudaSuccess && per_sm >= 1) h->persist_ok = true;
+      cudaGetLastError();
+    }
+    if (h->persist_ok) {
+      need = std::max(need, persist_ws_floats((int)H, (int)F, (int)nh, (int)nkv, (int)V, h->num_sms));
+      std::vector<CUtensorMap> maps(4 * L + 4);
+      bool ok = true;
+      for (int l = 0; l < L && ok; ++l) {
+        const LayerW& d = h->layer[l];
+        ok = make_tmap_bf16(&maps[4 * l + 0], d.w_qkv, qkvd, H, H, 128) &&
+             make_tmap_bf16(&maps[4 * l + 1], d.w_o, H, qd, qd, 128) &&
+             make_tmap_bf16(&maps[4 * l + 2], d.w_gu, 2 * F, H, H, 128) &&
+             make_tmap_bf16(&maps[4 * l + 3], d.w_down, H, F, F, 128);
+      }
+      ok = ok && make_tmap_bf16(&maps[4 * L], h->lm_head, V, H, H, 128) &&
+           make_tmap_bf16(&maps[4 * L + 1], h->xb, kGamma, H, H, kGamma) &&
+           make_tmap_bf16(&maps[4 * L + 2], h->attn, kGamma, qd, qd, kGamma) &&
+           make_tmap_bf16(&maps[4 * L + 3], h->act, kGamma, F, F, kGamma);
+      if (!ok) {
+        fail(h, DFLASH_ECUDA, "tensor maps of the persistent forward");
+        return bail(DFLASH_ECUDA);
+      }
+      ALLOC(h->p_maps, maps.size() * sizeof(CUtensorMap));
+      std::vector<PersistLayer> pl(L);
+      for (int l = 0; l < L; ++l) {
+        const LayerW& d = h->layer[l];
+        pl[l].q_norm = static_cast<const __nv_bfloat16*>(d.q_norm);
+        pl[l].k_norm = static_cast<const __nv_bfloat16*>(d.k_norm);
+        pl[l].ln_in = static_cast<const __nv_bfloat16*>(d.ln_in);
+        pl[l].ln_post = static_cast<const __nv_bfloat16*>(d.ln_post);
+        pl[l].window = c.layer_sliding[l] ? c.sliding_window : 0;
+      }
+      ALLOC(h->p_layers, pl.size() * sizeof(PersistLayer));
+      h->p_ctl_words = persist_ctl_words((int)L, (int)H, (int)F, (int)nh, (int)nkv, (int)V);
+      ALLOC(h->p_ctl, h->p_ctl_words * sizeof(unsigned));
+      cudaError_t e1 = cudaMemcpy(h->p_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
+      if (e1 == cudaSuccess)
+        e1 = cudaMemcpy(h->p_layers, pl.data(), pl.size() * sizeof(PersistLayer), cudaMemcpyHostToDevice);
+      if (e1 != cudaSuccess) {
+        cuda_fail(h, e1, "persistent forward tables");
+        return bail(DFLASH_ECUDA);
+      }
+      h->persist_on = true;
+    }
     h->ws_floats = need;
     ALLOC(h->ws, need * 4);
-    h->tc_attn = (nh / nkv) == 8;
     if (h->tc_attn) {
       const int64_t units = (int64_t)c.max_batch * nkv;
       const int64_t slots = attn_tc_partial_slots(h->num_sms, (int)units);
@@ -684,7 +792,7 @@ int propose_graph(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* 
   const void* args[6] = {bonus_tokens, ctx_lens, page_tables, draft_tokens, logits, final_hidden};
   GraphEntry* e = nullptr;
   for (GraphEntry* g : h->graphs)
-    if (g->nb == nb && g->max_ctx == max_ctx_len && g->prof == h->prof.on &&
+    if (g->nb == nb && g->max_ctx == max_ctx_len && g->prof == h->prof.on && g->persist == h->persist_on &&
         memcmp(g->args, args, sizeof(args)) == 0) {
       e = g;
       break;
@@ -703,6 +811,7 @@ int propose_graph(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* 
     e->max_ctx = max_ctx_len;
     memcpy(e->args, args, sizeof(args));
     e->prof = h->prof.on;
+    e->persist = h->persist_on;
     cudaError_t err = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeRelaxed);
     if (err != cudaSuccess) {
       graph_free(e);
@@ -767,6 +876,16 @@ int dflash_profile(dflash_handle* h, int enable) {
 }
 
 int dflash_profile_kinds(void) { return K_COUNT; }
+
+int dflash_set_persistent(dflash_handle* h, int enable) {
+  if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
+  if (enable && !h->persist_ok)
+    return fail(h, DFLASH_EUNSUPPORTED, "no persistent forward for this configuration or device");
+  h->persist_on = enable != 0;
+  return DFLASH_OK;
+}
+
+int dflash_persistent(const dflash_handle* h) { return h && h->persist_on ? 1 : 0; }
 
 int dflash_profile_read(dflash_handle* h, int kind, const char** name, double* total_ms, int64_t* launches) {
   if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");

@@ -57,11 +57,12 @@ template <> struct Elem<__nv_bfloat16> {
 // ---------------------------------------------------------------- profiling
 enum Kind {
   K_EMBED, K_NORM, K_QKV, K_QKV_POST, K_ATTN, K_OPROJ, K_GATEUP, K_SILU, K_DOWN, K_LMHEAD, K_ARGMAX,
-  K_COPY, K_W_FC, K_W_NORM, K_W_KV, K_W_POST, K_COUNT
+  K_COPY, K_W_FC, K_W_NORM, K_W_KV, K_W_POST, K_PERSIST, K_COUNT
 };
 static const char* const kKindNames[K_COUNT] = {
     "embed", "rmsnorm", "qkv_gemm", "qkv_post", "attention", "o_proj_gemm", "gate_up_gemm", "silu_mul",
-    "down_gemm", "lm_head", "argmax", "copy", "writer_fc_gemm", "writer_norm", "writer_kv_gemm", "writer_post"};
+    "down_gemm", "lm_head", "argmax", "copy", "writer_fc_gemm", "writer_norm", "writer_kv_gemm", "writer_post",
+    "persistent_forward"};
 
 struct Prof {
   bool on = false;
@@ -76,6 +77,7 @@ struct GraphEntry {
   int nb = 0, max_ctx = 0;
   const void* args[6] = {};           // bonus, ctx_lens, page_tables, drafts, logits, hidden
   bool prof = false;                  // captured with per-kernel timing events
+  bool persist = false;               // captured on the single-launch persistent forward
   cudaGraphExec_t exec = nullptr;
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> evs;  // owned timing events
   int64_t kind_counts[K_COUNT] = {};
@@ -145,13 +147,19 @@ struct dflash_handle {
   float* ws = nullptr;                 // split-K partials
   size_t ws_floats = 0;
   unsigned* counters = nullptr;        // split-K / argmax counters (zero between launches)
-  float* amax_val = nullptr;           // [V/128 tiles, rows] per-tile argmax partials
-  int* amax_idx = nullptr;
+  unsigned long long* amax_best = nullptr;  // [rows] packed running argmax (zero between launches)
   float* attn_opart = nullptr;         // attention split partials (O)
   float* attn_ml = nullptr;            // attention split partials (max, sum)
   unsigned* attn_counters = nullptr;   // per (sequence, kv head) unit
   bool tc = false;                     // bf16 tensor-core path in use
   bool tc_attn = false;                // tensor-core attention (8 query heads per kv head)
+  // single-launch persistent forward (batch 1, bf16 lm_head)
+  bool persist_ok = false;             // available for this configuration and device
+  bool persist_on = false;             // used by dflash_propose (dflash_set_persistent)
+  void* p_maps = nullptr;              // device CUtensorMap table
+  void* p_layers = nullptr;            // device per-layer table
+  unsigned* p_ctl = nullptr;           // control words, zeroed before each launch
+  size_t p_ctl_words = 0;
 
   unsigned* d_status = nullptr;        // device status word
   dflash::Prof prof;

@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "dflash_internal.cuh"
+#include "gemm_epi.cuh"
 #include "gemm_tc.cuh"
 #include "tc_common.cuh"
 
@@ -39,253 +40,6 @@ namespace dflash {
 namespace {
 
 using namespace tc;
-
-constexpr int kThreads = 128;
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// RoPE angle of pair j at position pos (from_weights.rs inv_freq table; YaRN divisors
-// already folded into inv_freq), as half-turns t = pos * inv_freq_j / pi reduced to [-1, 1],
-// then sin/cos(pi t) in fp32.  ip[j] = (hi, lo) splits inv_freq_j / pi into two floats;
-// fmaf gives the exact rounding error of pos * hi, and subtracting the nearest even integer
-// is exact below 2^24, so t carries ~1e-7 absolute error without float64 arithmetic.
-__device__ __forceinline__ void rope_cs(const float2* ip, int j, int pos, float* c, float* s) {
-  const float p = (float)pos;
-  const float2 v = ip[j];
-  const float a = p * v.x;
-  const float e = fmaf(p, v.x, -a);
-  const float k = 2.f * rintf(0.5f * a);
-  const float t = (a - k) + fmaf(p, v.y, e);
-  sincospif(t, s, c);
-}
-
-__device__ __forceinline__ int m0_of(int tile_m, int tn) { return tile_m * tn; }
-
-__device__ __forceinline__ void set_status(unsigned* status, unsigned bit) {
-  if (status) atomicOr(status, bit);
-}
-
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
-
-// Shared-memory carve-up of the epilogue (aliases the drained pipeline stages).
-struct EpiSmem {
-  float xch[kThreads][17];   // one 16-token chunk of the tile, transposed exchange
-  float red[4][16];          // per-warp partial reductions for 16 tokens
-  float tot[16];             // per-token totals over the tile's 128 rows
-  float bv[4][16];
-  int bi[4][16];
-};
-
-// Sum over the tile's 128 rows of w[row][c] for each of the chunk's 16 tokens, into es.tot.
-// Transposed through shared memory: thread (token c = t % 16, group g = t / 16) adds rows
-// 16g..16g+15 of token c, then one shuffle and a 4-warp combine.
-__device__ __forceinline__ void rowsum16(EpiSmem& es, const float (&w)[16], int t) {
-#pragma unroll
-  for (int c = 0; c < 16; ++c) es.xch[t][c] = w[c];
-  __syncthreads();
-  const int c = t & 15, g = t >> 4;
-  float a = 0.f;
-#pragma unroll
-  for (int r = 0; r < 16; ++r) a += es.xch[g * 16 + r][c];
-  a += __shfl_xor_sync(0xffffffffu, a, 16);
-  if ((t & 31) < 16) es.red[t >> 5][c] = a;
-  __syncthreads();
-  if (t < 16) es.tot[t] = (es.red[0][t] + es.red[1][t]) + (es.red[2][t] + es.red[3][t]);
-  __syncthreads();
-}
-
-template <int EPI>
-__device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rsc, float (&v)[16], int t, int n,
-                               int m0, int c0, int tile_n) {
-  const int warp = t >> 5, lane = t & 31;
-  if constexpr (EPI == EPI_STORE) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int m = m0 + c0 + c;
-      if (m < p.M && n < p.N) p.out[(int64_t)m * p.ldo + n] = v[c] * (p.ss_in ? rsc[c0 + c] : 1.f);
-    }
-  } else if constexpr (EPI == EPI_RESID) {
-    float sq[16];
-    const float lnw = p.ln_next ? __bfloat162float(p.ln_next[n]) : 1.f;
-    float xo[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) xo[c] = m0 + c0 + c < p.M ? p.x[(int64_t)(m0 + c0 + c) * p.H + n] : 0.f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int m = m0 + c0 + c;
-      float xv = 0.f;
-      if (m < p.M) {
-        const int64_t o = (int64_t)m * p.H + n;
-        xv = xo[c] + v[c];
-        p.x[o] = xv;
-        p.xb[o] = __float2bfloat16_rn(xv * lnw);
-      }
-      sq[c] = xv * xv;
-    }
-    rowsum16(es, sq, t);
-    if (t < 16) {
-      const int m = m0 + c0 + t;
-      if (m < p.M) p.ss_out[(int64_t)tile_n * p.Mp + m] = es.tot[t];
-    }
-  } else if constexpr (EPI == EPI_GATEUP) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * rsc[c0 + c];
-    __syncthreads();
-    const int f = tile_n * 64 + (t & 63);
-    const int cb = (t >> 6) * 8;
-#pragma unroll
-    for (int c = cb; c < cb + 8; ++c) {
-      const int m = m0 + c0 + c;
-      if (m < p.M) {
-        const float g = es.xch[t & 63][c], u = es.xch[(t & 63) + 64][c];
-        p.act[(int64_t)m * p.F + f] = __float2bfloat16_rn(g / (1.f + __expf(-g)) * u);
-      }
-    }
-    __syncthreads();
-  } else if constexpr (EPI == EPI_QKV) {
-    const int hh = tile_n;
-    const bool is_q = hh < p.nh, is_k = !is_q && hh < p.nh + p.nkv;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) v[c] *= rsc[c0 + c];
-    if (is_q || is_k) {
-      // per-head RMSNorm over the 128 rows of the tile
-      float sq[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) sq[c] = v[c] * v[c];
-      rowsum16(es, sq, t);
-      const float w = __bfloat162float((is_q ? p.q_norm : p.k_norm)[t]);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * (1.f / sqrtf(es.tot[c] * (1.f / 128.f) + p.eps)) * w;
-      __syncthreads();
-      // RoPE: pair (j, j + 64), NeoX rotate-half
-      const int j = t & 63;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int m = m0 + c0 + c;
-        const int s = m / kGamma, r = m % kGamma;
-        const int ctx = m < p.M ? p.ctx_lens[s] : 0;
-        float cs, sn;
-        rope_cs(p.inv_pi, j, ctx + r, &cs, &sn);
-        const float a = es.xch[j][c], b = es.xch[j + 64][c];
-        v[c] = (t < 64 ? a * cs - b * sn : b * cs + a * sn) * p.mscale;
-      }
-      __syncthreads();
-    }
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int m = m0 + c0 + c;
-      if (m >= p.M) continue;
-      if (is_q) {
-        p.q[(int64_t)m * p.nh * 128 + hh * 128 + t] = __float2bfloat16_rn(v[c]);
-        continue;
-      }
-      const int s = m / kGamma, r = m % kGamma;
-      const int ctx = p.ctx_lens[s];
-      if (ctx < 0 || ctx + kGamma > p.mpps * kPage) {
-        if (t == 0) set_status(p.status, DFLASH_DEV_BAD_CTX);
-        continue;
-      }
-      const int li = ctx + r;
-      const int page = p.page_tables[(int64_t)s * p.mpps + li / kPage];
-      if (page < 0 || page >= p.g.num_pages) {
-        if (t == 0) set_status(p.status, DFLASH_DEV_BAD_PAGE);
-        continue;
-      }
-      const int head = is_k ? hh - p.nh : hh - p.nh - p.nkv;
-      const int64_t base = tile_base(p.g, p.layer, page, is_k ? 0 : 1, head);
-      p.pool[base + (is_k ? k_in_tile(li % kPage, t, 128) : v_in_tile(li % kPage, t, 128))] =
-          __float2bfloat16_rn(v[c]);
-    }
-  } else if constexpr (EPI == EPI_CTXKV) {
-    // one tile = one head of one layer's K or V in the fused context-K/V weight
-    // [K_0; V_0; K_1; V_1; ...]; token m is context row first + m at position positions[m]
-    const int l = tile_n / (2 * p.nkv), rem = tile_n % (2 * p.nkv);
-    const bool is_k = rem < p.nkv;
-    const int head = is_k ? rem : rem - p.nkv;
-    if (is_k) {
-      float sq[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) sq[c] = v[c] * v[c];
-      rowsum16(es, sq, t);
-      const float w = __bfloat162float(p.k_norm[l * 128 + t]);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * (1.f / sqrtf(es.tot[c] * (1.f / 128.f) + p.eps)) * w;
-      __syncthreads();
-      const int j = t & 63;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int m = m0 + c0 + c;
-        const int pos = m < p.M ? p.positions[m] : 0;
-        float cs, sn;
-        rope_cs(p.inv_pi, j, pos, &cs, &sn);
-        const float a = es.xch[j][c], b = es.xch[j + 64][c];
-        v[c] = (t < 64 ? a * cs - b * sn : b * cs + a * sn) * p.mscale;
-      }
-      __syncthreads();
-    }
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int m = m0 + c0 + c;
-      if (m >= p.M) continue;
-      const int li = p.first + m;
-      const int page = p.page_tables[li / kPage];
-      if (page < 0 || page >= p.g.num_pages) {
-        if (t == 0) set_status(p.status, DFLASH_DEV_BAD_PAGE);
-        continue;
-      }
-      const int64_t base = tile_base(p.g, l, page, is_k ? 0 : 1, head);
-      p.pool[base + (is_k ? k_in_tile(li % kPage, t, 128) : v_in_tile(li % kPage, t, 128))] =
-          __float2bfloat16_rn(v[c]);
-    }
-  } else if constexpr (EPI == EPI_LMHEAD) {
-    const bool valid_row = n < p.N;
-    const float sc = (p.row_scale && valid_row) ? p.row_scale[n] : 1.f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int m = m0 + c0 + c;
-      const float z = v[c] * sc;
-      if (p.logits && valid_row && m < p.M) p.logits[(int64_t)m * p.N + n] = __float2bfloat16_rn(z);
-      es.xch[t][c] = valid_row ? z : -FLT_MAX;
-    }
-    __syncthreads();
-    // thread (token c, group g) scans rows 16g..16g+15 (ties -> lowest row), then combine
-    const int c = t & 15, g = t >> 4;
-    float b = -FLT_MAX;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float z = es.xch[g * 16 + r][c];
-      const int idx = tile_n * 128 + g * 16 + r;
-      if (z > b) { b = z; bi = idx; }
-    }
-    if (b == -FLT_MAX) bi = 0x7fffffff;
-    {
-      const float ob = __shfl_xor_sync(0xffffffffu, b, 16);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, 16);
-      if (better(ob, oi, b, bi)) { b = ob; bi = oi; }
-    }
-    if ((t & 31) < 16) { es.bv[t >> 5][c] = b; es.bi[t >> 5][c] = bi; }
-    __syncthreads();
-    if (t < 16) {
-      float bb = es.bv[0][t];
-      int ii = es.bi[0][t];
-      for (int w2 = 1; w2 < 4; ++w2)
-        if (better(es.bv[w2][t], es.bi[w2][t], bb, ii)) { bb = es.bv[w2][t]; ii = es.bi[w2][t]; }
-      const int m = m0 + c0 + t;
-      if (m < p.M) {
-        p.amax_val[(int64_t)tile_n * p.Mp + m] = bb;
-        p.amax_idx[(int64_t)tile_n * p.Mp + m] = ii;
-      }
-    }
-    __syncthreads();
-  }
-}
 
 // FP8A: the weight arrives as e4m3 codes (TMA, 64-byte rows) and warps 2-3 widen each
 // stage to the bf16 128-byte-swizzled A tile before the MMA reads it (the per-row scale is
@@ -444,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ssum = 0.f;
         for (int q0 = 0; q0 < p.ss_parts; q0 += 8) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) part[u] = q0 + u < p.ss_parts ? p.ss_in[(int64_t)(q0 + u) * p.Mp + m] : 0.f;
+          for (int u = 0; u < 8; ++u) part[u] = q0 + u < p.ss_parts ? __ldcg(p.ss_in + (int64_t)(q0 + u) * p.Mp + m) : 0.f;
 #pragma unroll
           for (int u = 0; u < 8; ++u) ssum += part[u];
         }
@@ -524,29 +278,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0) flags[1] = atomicAdd(&p.amax_counter[tile_m], 1u) == (unsigned)(gridDim.y - 1);
         __syncthreads();
         if (flags[1]) {
+          // every vocabulary tile of these tokens has folded its best into amax_best
           __threadfence();
-          // 8 threads per token, 16 tokens per pass
-          for (int cb = 0; cb < TN; cb += 16) {
-            const int c = cb + (t >> 3), sub = t & 7;
+          for (int c = t; c < TN; c += kThreads) {
             const int m = m0 + c;
-            float b = -FLT_MAX;
-            int bi = 0x7fffffff;
             if (m < p.M) {
-              for (int q = sub; q < (int)gridDim.y; q += 8) {
-                const float vv = __ldcg(p.amax_val + (int64_t)q * p.Mp + m);
-                const int ii = __ldcg(p.amax_idx + (int64_t)q * p.Mp + m);
-                if (better(vv, ii, b, bi)) { b = vv; bi = ii; }
-              }
-            }
-#pragma unroll
-            for (int o = 4; o > 0; o >>= 1) {
-              const float ov = __shfl_xor_sync(0xffffffffu, b, o);
-              const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-              if (better(ov, oi, b, bi)) { b = ov; bi = oi; }
-            }
-            if (sub == 0 && m < p.M) {
+              const unsigned long long k = atomicExch(p.amax_best + m, 0ull);  // read and re-arm
               const int r = m % kGamma;
-              if (r > 0) p.drafts[(m / kGamma) * (kGamma - 1) + r - 1] = bi;
+              if (r > 0) p.drafts[(m / kGamma) * (kGamma - 1) + r - 1] = argmax_key_index(k);
             }
           }
           if (t == 0) p.amax_counter[tile_m] = 0;

@@ -52,8 +52,9 @@ struct GemmParams {
   // EPI_LMHEAD
   __nv_bfloat16* logits = nullptr;
   const float* row_scale = nullptr;
-  float* amax_val = nullptr;
-  int* amax_idx = nullptr;
+  // per token row: max over vocabulary tiles of (orderable logit << 32 | ~index), combined
+  // with 64-bit atomicMax (order-independent, so deterministic); zero between launches
+  unsigned long long* amax_best = nullptr;
   unsigned* amax_counter = nullptr;
   int32_t* drafts = nullptr;
 };

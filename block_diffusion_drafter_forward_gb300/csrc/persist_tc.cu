@@ -1,0 +1,946 @@
+// The whole bf16 gamma-block forward for one small batch (16 tokens) in ONE persistent
+// kernel: one CTA per SM, resident for the entire forward (cooperative launch).
+//
+// Why: at batch 1 each projection streams 17-50 MB of weights (2.5-7.4 us at HBM speed), but
+// as separate kernels every projection also pays grid completion, launch and activation-load
+// latency on the dependency chain.  Here the phases of the forward
+//     embed | per layer: QKV, attention, split combine, o_proj, gate/up, down | lm_head
+// run back to back inside one launch, separated by grid-wide arrival counters, and the
+// weight-tile producer runs ahead across those barriers: weights depend on nothing, so the
+// next projection's weights stream while the current phase finishes.  The final RMSNorm is
+// folded into the last down projection's epilogue (operand bf16(x * norm), per-token 1/RMS
+// applied to the logits) the same way every other norm of the forward is.
+//
+// Roles (224 threads):
+//   warp 4 lane 0: weight TMA producer (runs ahead, bounded by the smem ring)
+//   warp 5 lane 0: tcgen05.mma issuer (double-buffered TMEM accumulators)
+//   warp 6 lane 0: activation TMA producer (waits for the phase the activation comes from)
+//   warps 0-3:     epilogues (gemm_epi.cuh), block attention, split combine, embedding
+// Every projection is split evenly over the CTAs by k-blocks (stream-K): CTA c owns k-blocks
+// [c T/G, (c+1) T/G) of the T = tiles x k-blocks of the projection; a tile covered by several
+// CTAs is summed from fp32 partials in CTA order by the last one to arrive (deterministic).
+// The arithmetic of every phase is the same as the per-projection kernels'.
+#include <cudaTypedefs.h>
+#include <float.h>
+
+#include <algorithm>
+
+#include "dflash_internal.cuh"
+#include "gemm_epi.cuh"
+#include "gemm_tc.cuh"
+#include "persist_tc.cuh"
+#include "tc_common.cuh"
+
+namespace dflash {
+namespace {
+
+using namespace tc;
+
+constexpr int TN = 16;                        // tokens: one accumulator chunk
+constexpr int kS = 6;                         // ring stages
+constexpr int kAB = 128 * 64 * 2;             // weight tile (bf16, 128 rows x 64 k)
+constexpr int kBB = TN * 64 * 2;              // activation tile
+constexpr int kStage = kAB + kBB;
+constexpr int kRing = kS * kStage;
+// attention region: P (the epilogue scratch aliases it), then Q and two K/V stages; Q and the
+// K/V stages double as the landing buffer of split-K partials during projection phases
+constexpr int kAKC = 64, kAPages = 4, kATile = 4096;
+constexpr int kAP = 128 * kAKC * 2, kAQ = 128 * 128 * 2, kAKVStage = 2 * kAPages * kATile;
+constexpr int kAttn = kAP + kAQ + 2 * kAKVStage;
+constexpr int kPartBytes = 128 * TN * 4;                     // one contributor's partial tile
+constexpr int kRedMax = (kAQ + 2 * kAKVStage) / kPartBytes;  // partials that fit at once
+constexpr int kBarOff = kRing + kAttn;
+constexpr int kSmemP = kBarOff + 512 + 256 + 1024;
+constexpr uint32_t kAccCols = 32;             // per accumulator buffer (16 used)
+constexpr uint32_t kTS = 64, kTO = 128;       // attention S and O columns
+constexpr long long kGridSpin = 20000000ll;   // polls of a phase counter before giving up
+constexpr int kEThreads = 128;
+constexpr int kBlockThreads = 224;
+constexpr int kMaxHGroups = 48;               // H / 128 the final-hidden pass holds in registers
+
+static_assert(sizeof(EpiSmem) <= kAP, "epilogue scratch must fit in the attention P area");
+
+struct Bars {
+  uint64_t full[kS], empty[kS];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t kv_full[2], s_done, o_done, red_full;
+  uint32_t tmem;
+  volatile int abort;
+  int flag;
+};
+static_assert(sizeof(Bars) <= 512, "barrier block overflows its slot");
+
+enum { PH_EMBED, PH_GEMM, PH_ATTN, PH_COMB };
+
+__device__ __forceinline__ int phase_kind(int ph, int L) {
+  if (ph == 0) return PH_EMBED;
+  if (ph == 1 + 6 * L) return PH_GEMM;
+  const int k = (ph - 1) % 6;
+  return k == 1 ? PH_ATTN : (k == 2 ? PH_COMB : PH_GEMM);
+}
+
+struct GPh {
+  int epi, wmap, xmap, N, K, layer, kind;  // kind: 0 qkv, 3 o, 4 gate/up, 5 down, 6 lm_head
+};
+
+__device__ __forceinline__ GPh gemm_of(int ph, const PersistParams& p) {
+  GPh g;
+  const int qkvd = (p.nh + 2 * p.nkv) * 128, qd = p.nh * 128;
+  if (ph == 1 + 6 * p.L) {
+    g.epi = EPI_LMHEAD; g.wmap = 4 * p.L; g.xmap = 0; g.N = p.V; g.K = p.H; g.layer = p.L - 1; g.kind = 6;
+    return g;
+  }
+  const int l = (ph - 1) / 6, k = (ph - 1) % 6;
+  g.layer = l;
+  g.kind = k;
+  if (k == 0) { g.epi = EPI_QKV; g.wmap = 4 * l; g.xmap = 0; g.N = qkvd; g.K = p.H; }
+  else if (k == 3) { g.epi = EPI_RESID; g.wmap = 4 * l + 1; g.xmap = 1; g.N = p.H; g.K = qd; }
+  else if (k == 4) { g.epi = EPI_GATEUP; g.wmap = 4 * l + 2; g.xmap = 0; g.N = 2 * p.F; g.K = p.H; }
+  else { g.epi = EPI_RESID; g.wmap = 4 * l + 3; g.xmap = 2; g.N = p.H; g.K = p.F; }
+  return g;
+}
+
+// ---------------------------------------------------------------- stream-K segments
+struct Seg {
+  int tile, kb0, nkb, rank, ncontrib;
+};
+
+// Owner CTA of global k-block k when `total` k-blocks are split over G CTAs with CTA c
+// starting at floor(c * total / G).
+__device__ __forceinline__ int owner_of(int64_t k, int64_t total, int G) {
+  return (int)(((k + 1) * G + total - 1) / total) - 1;
+}
+
+struct SegIter {
+  int64_t k, hi, total;
+  int nkb, G, c;
+  __device__ SegIter(int tiles, int nkb_, int G_, int c_) : nkb(nkb_), G(G_), c(c_) {
+    total = (int64_t)tiles * nkb_;
+    k = (int64_t)c_ * total / G_;
+    hi = (int64_t)(c_ + 1) * total / G_;
+  }
+  __device__ bool next(Seg& s) {
+    if (k >= hi) return false;
+    const int tile = (int)(k / nkb);
+    const int64_t tb = (int64_t)tile * nkb, te = tb + nkb;
+    const int64_t end = hi < te ? hi : te;
+    const int first = owner_of(tb, total, G), last = owner_of(te - 1, total, G);
+    s.tile = tile;
+    s.kb0 = (int)(k - tb);
+    s.nkb = (int)(end - k);
+    s.rank = c - first;
+    s.ncontrib = last - first + 1;
+    k = end;
+    return true;
+  }
+};
+
+// Most CTAs that can share one tile: each CTA covers at least floor(T / G) k-blocks.
+__host__ __device__ __forceinline__ int max_contrib(int tiles, int nkb, int G) {
+  const int64_t total = (int64_t)tiles * nkb;
+  const int64_t per = total / G;
+  return (int)(per > 0 ? (nkb + per - 1) / per + 1 : G);
+}
+
+// ---------------------------------------------------------------- grid-wide phase counters
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* ptr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until every CTA arrived on counter `ctr`.  Gives up (and raises the grid abort flag) after
+// kGridSpin polls, or early when another CTA gave up.
+__device__ bool grid_wait(const unsigned* ctr, unsigned target, volatile int* labort, int* gabort) {
+  for (long long i = 0; i < kGridSpin; ++i) {
+    if (ld_acquire(ctr) >= target) {
+      fence_proxy_async_global();
+      return true;
+    }
+    if ((i & 127) == 127 && (*labort || *reinterpret_cast<volatile int*>(gabort))) return false;
+    __nanosleep(32);
+  }
+  *labort = 1;
+  atomicExch(gabort, 1);
+  return false;
+}
+
+__device__ __forceinline__ void grid_arrive(unsigned* ctr) {
+  fence_proxy_async_global();
+  __threadfence();
+  atomicAdd(ctr, 1u);
+}
+
+__device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort, int* gabort) {
+  if (*abort) return false;
+  for (long long i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && (*abort || *reinterpret_cast<volatile int*>(gabort))) {
+      *abort = 1;
+      return false;
+    }
+  }
+  *abort = 1;
+  atomicExch(gabort, 1);
+  return false;
+}
+
+// ---------------------------------------------------------------- embedding (warps 0-3)
+// One warp per (token row, 128-column group): x = E[token], xb = bf16(x * ln_in_0) and the
+// group's sum of x^2 into ss_b.  No block-wide barrier.
+__device__ void embed_phase(const PersistParams& p, int c, int warp, int lane) {
+  const int ngr = p.H / 128;
+  const int items = p.M * ngr;
+  const __nv_bfloat16* ln = p.layers[0].ln_in;
+  for (int i = c * 4 + warp; i < items; i += p.G * 4) {
+    const int row = i / ngr, gi = i % ngr;
+    const int r = row % kGamma, s = row / kGamma;
+    const int tok = r == 0 ? __ldg(p.bonus + s) : p.mask;
+    const bool ok = tok >= 0 && tok < p.V;
+    if (!ok && gi == 0 && lane == 0) atomicOr(p.status, DFLASH_DEV_BAD_TOKEN);
+    const int col = gi * 128 + lane * 4;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) {
+      const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.embed + (int64_t)tok * p.H + col));
+      const __nv_bfloat162 e0 = *reinterpret_cast<const __nv_bfloat162*>(&e.x);
+      const __nv_bfloat162 e1 = *reinterpret_cast<const __nv_bfloat162*>(&e.y);
+      v[0] = __low2float(e0); v[1] = __high2float(e0); v[2] = __low2float(e1); v[3] = __high2float(e1);
+    }
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(ln + col));
+    const __nv_bfloat162 w0 = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+    const __nv_bfloat162 w1 = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+    *reinterpret_cast<float4*>(p.x + (int64_t)row * p.H + col) = make_float4(v[0], v[1], v[2], v[3]);
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0] * __low2float(w0), v[1] * __high2float(w0));
+    const __nv_bfloat162 b1 = __floats2bfloat162_rn(v[2] * __low2float(w1), v[3] * __high2float(w1));
+    *reinterpret_cast<uint2*>(p.xb + (int64_t)row * p.H + col) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+    const float ss = warp_sum(v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3]);
+    if (lane == 0) p.ss_b[(int64_t)gi * p.M + row] = ss;
+  }
+}
+
+// Per-token input scale 1/RMS(x_m) from the per-128-column partial sums.
+__device__ __forceinline__ float row_rscale(const PersistParams& p, const float* ss_in, int m) {
+  const int parts = p.H / 128;
+  float ssum = 0.f;
+  for (int q0 = 0; q0 < parts; q0 += 8) {
+    float part[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) part[u] = q0 + u < parts ? __ldcg(ss_in + (int64_t)(q0 + u) * p.M + m) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) ssum += part[u];
+  }
+  return 1.f / sqrtf(ssum / (float)p.H + p.eps);
+}
+
+// Final hidden state of token `row`: RMSNorm(x) * norm in bf16 (rs = 1/RMS(x_row)).
+__device__ void final_hidden_row(const PersistParams& p, int row, float rs, int t) {
+  const int ngr = p.H / 128;
+  float xv[kMaxHGroups];
+#pragma unroll
+  for (int k = 0; k < kMaxHGroups; ++k) xv[k] = k < ngr ? __ldcg(p.x + (int64_t)row * p.H + k * 128 + t) : 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxHGroups; ++k)
+    if (k < ngr)
+      p.final_hidden[(int64_t)row * p.H + k * 128 + t] =
+          __float2bfloat16_rn(xv[k] * rs * __bfloat162float(p.norm[k * 128 + t]));
+}
+
+// ---------------------------------------------------------------- attention (warps 0-3)
+struct AttnUse {
+  int kv[2], s, o;
+};
+
+// Geometry of one attention work item (unit = sequence x kv head, split of its key chunks).
+struct AItem {
+  int s, g, ctx, k0, nch, c_begin, c_end, nsplit, splits, window;
+  bool bad;  // context length out of range (reported once per unit)
+  bool run;  // false: nothing to do (bad context, or a split beyond the sequence's chunks)
+};
+
+__device__ __forceinline__ int chunk_range_p(int window, int ctx, int* first_key) {
+  const int nkeys = ctx + kGamma;
+  int k0 = 0;
+  if (window > 0) {
+    k0 = ctx - window + 1;
+    if (k0 < 0) k0 = 0;
+    k0 &= ~(kPage - 1);
+  }
+  *first_key = k0;
+  return (nkeys - k0 + kAKC - 1) / kAKC;
+}
+
+__device__ AItem attn_geom(const PersistParams& p, int layer, int unit, int split) {
+  AItem a;
+  a.window = p.layers[layer].window;
+  a.s = unit / p.nkv;
+  a.g = unit % p.nkv;
+  a.ctx = __ldg(p.ctx_lens + a.s);
+  const int wi = a.window > 0;
+  const int cps = p.attn_cps[wi];
+  a.splits = p.attn_splits[wi];
+  a.run = false;
+  a.bad = false;
+  a.nch = a.k0 = a.nsplit = a.c_begin = a.c_end = 0;
+  if (a.ctx < 0 || a.ctx > p.max_ctx || a.ctx + kGamma > p.mpps * kPage) {
+    a.bad = true;
+    return a;
+  }
+  a.nch = chunk_range_p(a.window, a.ctx, &a.k0);
+  a.nsplit = (a.nch + cps - 1) / cps;
+  if (a.nsplit > a.splits) {  // cannot happen for ctx <= max_ctx; never drop keys silently
+    a.bad = true;
+    return a;
+  }
+  if (split >= a.nsplit) return a;
+  a.c_begin = split * cps;
+  a.c_end = min(a.nch, a.c_begin + cps);
+  a.run = true;
+  return a;
+}
+
+// K and V pages of key chunk c into K/V stage st (one thread).
+__device__ void attn_load_chunk(const PersistParams& p, int layer, const AItem& a, int c, int st, uint8_t* sKV,
+                                Bars& B) {
+  uint8_t* dK = sKV + st * kAKVStage;
+  uint8_t* dV = dK + kAPages * kATile;
+  const int32_t* pt = p.page_tables + (int64_t)a.s * p.mpps;
+  const int npages_seq = (a.ctx + kGamma + kPage - 1) / kPage;
+  mbar_arrive_expect_tx(&B.kv_full[st], 2 * kAPages * kATile);
+  const int pg0 = (a.k0 + c * kAKC) / kPage;
+  int pages[kAPages];
+#pragma unroll
+  for (int i = 0; i < kAPages; ++i) pages[i] = __ldg(pt + (pg0 + i < npages_seq ? pg0 + i : 0));
+#pragma unroll
+  for (int i = 0; i < kAPages; ++i) {
+    int page = pages[i];
+    if (page < 0 || page >= p.g.num_pages) {
+      atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
+      page = 0;
+    }
+    bulk_load(dK + i * kATile, p.pool + tile_base(p.g, layer, page, 0, a.g), kATile, &B.kv_full[st]);
+    bulk_load(dV + i * kATile, p.pool + tile_base(p.g, layer, page, 1, a.g), kATile, &B.kv_full[st]);
+  }
+}
+
+// Chunk c holds context keys only (pages written before this forward), so it may be copied
+// before this forward's QKV phase has finished.
+__device__ __forceinline__ bool chunk_is_context(const AItem& a, int c) {
+  return a.k0 + (c + 1) * kAKC <= (a.ctx / kPage) * kPage;
+}
+
+// Before the QKV phase completes: copy the first two chunks of this CTA's first item if they
+// hold context keys only.  Returns the stages loaded (bit st).  One thread.
+__device__ int attn_prefetch(const PersistParams& p, int layer, int unit, int split, uint8_t* sKV, Bars& B) {
+  const AItem a = attn_geom(p, layer, unit, split);
+  if (!a.run) return 0;
+  fence_proxy_async_smem();
+  int pre = 0;
+  for (int i = 0; i < 2; ++i) {
+    const int c = a.c_begin + i;
+    if (c < a.c_end && chunk_is_context(a, c)) {
+      attn_load_chunk(p, layer, a, c, i, sKV, B);
+      pre |= 1 << i;
+    }
+  }
+  return pre;
+}
+
+// One attention work item on warps 0-3: the 8 query heads x 16 rows of one kv head against
+// key chunks [c_begin, c_end), S and P.V on the tensor cores, online softmax in registers.
+// Warp 0 waits for the K/V copies and issues the MMAs (lane 0) with the warp converged.
+__device__ void attn_item(const PersistParams& p, int layer, int unit, int split, int pre, uint8_t* sA, Bars& B,
+                          AttnUse& use, int t) {
+  const int warp = t >> 5, lane = t & 31;
+  const AItem a = attn_geom(p, layer, unit, split);
+  if (!a.run) {
+    if (a.bad && split == 0 && t == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
+    return;
+  }
+  const int group = p.nh / p.nkv;
+  const int nkeys = a.ctx + kGamma;
+  uint8_t* sP = sA;
+  uint8_t* sQ = sP + kAP;
+  uint8_t* sKV = sQ + kAQ;
+  const uint32_t tS = B.tmem + kTS, tO = B.tmem + kTO;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      if (!(pre & 1)) attn_load_chunk(p, layer, a, a.c_begin, 0, sKV, B);
+      if (a.c_begin + 1 < a.c_end && !(pre & 2)) attn_load_chunk(p, layer, a, a.c_begin + 1, 1, sKV, B);
+    }
+    __syncwarp();
+  }
+  {
+    const int hh = t >> 4, r = t & 15;
+    const uint4* src =
+        reinterpret_cast<const uint4*>(p.q + ((int64_t)(a.s * kGamma + r) * p.nh + a.g * group + hh) * 128);
+    uint4 qv[16];
+#pragma unroll
+    for (int d8 = 0; d8 < 16; ++d8) qv[d8] = __ldcg(src + d8);
+#pragma unroll
+    for (int d8 = 0; d8 < 16; ++d8) *reinterpret_cast<uint4*>(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16) = qv[d8];
+  }
+  fence_proxy_async_smem();
+  epi_sync();
+
+  const int r = t & 15;
+  const int pos_q = a.ctx + r;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+  float m_run = -FLT_MAX, l_run = 0.f;
+  float o[128];
+#pragma unroll
+  for (int i = 0; i < 128; ++i) o[i] = 0.f;
+  constexpr uint32_t idesc_s = idesc_bf16(128, kAKC);
+  constexpr uint32_t idesc_o = idesc_bf16(128, 128);
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  volatile int* ab = &B.abort;
+
+  for (int c = a.c_begin; c < a.c_end; ++c) {
+    const int st = (c - a.c_begin) & 1;
+    uint8_t* sK = sKV + st * kAKVStage;
+    uint8_t* sV = sK + kAPages * kATile;
+    if (warp == 0) {
+      wait_ab(&B.kv_full[st], use.kv[st] & 1, ab, p.gabort);
+      tc_fence_after();
+      if (lane == 0) {
+        if (!*ab) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_bf16(tS, desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048), idesc_s,
+                     k > 0 ? 1u : 0u);
+        }
+        mma_commit(&B.s_done);
+      }
+      __syncwarp();
+    }
+    use.kv[st]++;
+    wait_ab(&B.s_done, use.s & 1, ab, p.gabort);
+    use.s++;
+    tc_fence_after();
+    const int kbase = a.k0 + c * kAKC;
+    float mc = -FLT_MAX;
+#pragma unroll
+    for (int q4 = 0; q4 < kAKC / 32; ++q4) {
+      float v[32];
+      tmem_ld32(tS + lane_off + q4 * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int key = kbase + q4 * 32 + j;
+        if (key < nkeys && (a.window <= 0 || pos_q - key < a.window)) mc = fmaxf(mc, v[j] * scale_log2);
+      }
+    }
+    const float m_new = fmaxf(m_run, mc);
+    const float alpha = m_new == -FLT_MAX ? 1.f : exp2f(m_run - m_new);
+    float lsum = 0.f;
+#pragma unroll
+    for (int q4 = 0; q4 < kAKC / 32; ++q4) {
+      float v[32];
+      tmem_ld32(tS + lane_off + q4 * 32, v);
+#pragma unroll
+      for (int j8 = 0; j8 < 4; ++j8) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float pr[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int jj = j8 * 8 + 2 * e + u;
+            const int key = kbase + q4 * 32 + jj;
+            const bool vis = key < nkeys && (a.window <= 0 || pos_q - key < a.window);
+            pr[u] = vis ? exp2f(v[jj] * scale_log2 - m_new) : 0.f;
+          }
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
+          lsum += __low2float(h2) + __high2float(h2);
+          pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(sP + ((t >> 3) * (kAKC / 8) + q4 * 4 + j8) * 128 + (t & 7) * 16) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    l_run = l_run * alpha + lsum;
+    m_run = m_new;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    epi_sync();
+    if (warp == 0) {
+      if (lane == 0) {
+        tc_fence_after();
+        if (!*ab) {
+#pragma unroll
+          for (int k = 0; k < kAPages; ++k)
+            mma_bf16(tO, desc_noswz(sP + k * 256, 128, kAKC / 8 * 128), desc_noswz(sV + k * kATile, 128, 256),
+                     idesc_o, k > 0 ? 1u : 0u);
+        }
+        mma_commit(&B.o_done);
+      }
+      __syncwarp();
+    }
+    wait_ab(&B.o_done, use.o & 1, ab, p.gabort);
+    use.o++;
+    tc_fence_after();
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float v[32];
+      tmem_ld32(tO + lane_off + q4 * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[q4 * 32 + j] = o[q4 * 32 + j] * alpha + v[j];
+    }
+    tc_fence_before();
+    epi_sync();
+    if (warp == 0) {
+      if (lane == 0 && c + 2 < a.c_end && !*ab) attn_load_chunk(p, layer, a, c + 2, st, sKV, B);
+      __syncwarp();
+    }
+  }
+  const int hh = t >> 4;
+  __nv_bfloat16* dst = p.attn + ((int64_t)(a.s * kGamma + r) * p.nh + a.g * group + hh) * 128;
+  if (a.nsplit == 1) {
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+    for (int d8 = 0; d8 < 16; ++d8) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[d8 * 8 + 2 * e] * inv, o[d8 * 8 + 2 * e + 1] * inv);
+        pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      reinterpret_cast<uint4*>(dst)[d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  } else {
+    const int64_t slot = (int64_t)unit * a.splits + split;
+    float* op = p.o_part + (slot * 128 + t) * 128;
+#pragma unroll
+    for (int i = 0; i < 128; i += 4)
+      __stcg(reinterpret_cast<float4*>(op + i), make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
+    __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
+  }
+}
+
+// Merge the split partials of rows 4 rb .. 4 rb + 3 of one unit (a warp per row, loads of 8
+// splits in flight at a time).
+__device__ void combine_item(const PersistParams& p, int layer, int unit, int rb, int t) {
+  const AItem a = attn_geom(p, layer, unit, 0);
+  if (!a.run || a.nsplit <= 1) return;
+  const int row = rb * 4 + (t >> 5), d0 = (t & 31) * 4;
+  const int64_t base = (int64_t)unit * a.splits;
+  float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  for (int q0 = 0; q0 < a.nsplit; q0 += 8) {
+    float2 ml[8];
+    float4 ov[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + u < a.nsplit ? q0 + u : q0;
+      ml[u] = __ldcg(reinterpret_cast<const float2*>(p.ml_part + ((base + q) * 128 + row) * 2));
+      ov[u] = __ldcg(reinterpret_cast<const float4*>(p.o_part + ((base + q) * 128 + row) * 128 + d0));
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (q0 + u >= a.nsplit) break;
+      if (ml[u].x > M) {
+        const float sc = M == -FLT_MAX ? 0.f : exp2f(M - ml[u].x);
+        a0 *= sc; a1 *= sc; a2 *= sc; a3 *= sc; L *= sc;
+        M = ml[u].x;
+      }
+      const float w = ml[u].x == -FLT_MAX ? 0.f : exp2f(ml[u].x - M);
+      a0 += ov[u].x * w; a1 += ov[u].y * w; a2 += ov[u].z * w; a3 += ov[u].w * w;
+      L += ml[u].y * w;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+  const __nv_bfloat162 h1 = __floats2bfloat162_rn(a2 * inv, a3 * inv);
+  const int hh = row >> 4, r = row & 15;
+  __nv_bfloat16* dst = p.attn + ((int64_t)(a.s * kGamma + r) * p.nh + a.g * (p.nh / p.nkv) + hh) * 128 + d0;
+  *reinterpret_cast<uint2*>(dst) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+}
+
+// ---------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const PersistParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* sA = smem + kRing;
+  uint8_t* sRed = sA + kAP;  // split-K partial landing buffer (the attention Q + K/V area)
+  Bars& B = *reinterpret_cast<Bars*>(smem + kBarOff);
+  float* rsc = reinterpret_cast<float*>(smem + kBarOff + 512);
+  EpiSmem& es = *reinterpret_cast<EpiSmem*>(sA);  // aliases the attention P area
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int G = p.G, c = blockIdx.x;
+  const int P = 2 + 6 * p.L;
+
+  if (t == 0) {
+    for (int i = 0; i < kS; ++i) {
+      mbar_init(&B.full[i], 1);
+      mbar_init(&B.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.acc_full[i], 1);
+      mbar_init(&B.acc_empty[i], 1);
+      mbar_init(&B.kv_full[i], 1);
+    }
+    mbar_init(&B.s_done, 1);
+    mbar_init(&B.o_done, 1);
+    mbar_init(&B.red_full, 1);
+    B.abort = 0;
+    B.flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(&B.tmem, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  volatile int* ab = &B.abort;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      // ---------------- weight producer: runs ahead over every projection of the forward
+      const uint64_t pol = policy_evict_first();
+      int j = 0;
+      for (int ph = 0; ph < P && !*ab; ++ph) {
+        if (phase_kind(ph, p.L) != PH_GEMM) continue;
+        const GPh gp = gemm_of(ph, p);
+        const CUtensorMap* wm = p.maps + gp.wmap;
+        SegIter it((gp.N + 127) / 128, gp.K / 64, G, c);
+        Seg sg;
+        while (it.next(sg) && !*ab) {
+          for (int kk = 0; kk < sg.nkb; ++kk, ++j) {
+            const int s = j % kS;
+            if (j >= kS && !wait_ab(&B.empty[s], ((j / kS) - 1) & 1, ab, p.gabort)) break;
+            // arm the stage for the weight and the activation tile (the activation producer
+            // adds its copy to the same phase, before or after this arrive)
+            mbar_arrive_expect_tx(&B.full[s], kStage);
+            tma_load_2d(ring + s * kStage, wm, &B.full[s], (sg.kb0 + kk) * 64, sg.tile * 128, pol);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    if (lane == 0) {
+      // ---------------- activation producer: X tiles once the phase they come from is complete
+      const uint64_t pol = policy_evict_last();
+      int j = 0;
+      for (int ph = 0; ph < P && !*ab; ++ph) {
+        if (phase_kind(ph, p.L) != PH_GEMM) continue;
+        const GPh gp = gemm_of(ph, p);
+        const CUtensorMap* xm = p.maps + 4 * p.L + 1 + gp.xmap;
+        SegIter it((gp.N + 127) / 128, gp.K / 64, G, c);
+        Seg sg;
+        bool waited = false;
+        while (it.next(sg) && !*ab) {
+          if (!waited) {
+            grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+            waited = true;
+          }
+          for (int kk = 0; kk < sg.nkb && !*ab; ++kk, ++j) {
+            const int s = j % kS;
+            // use j of stage s starts once the MMA released use j - kS; the release of use j
+            // needs this copy, so the stage cannot run a phase ahead of it
+            if (j >= kS && !wait_ab(&B.empty[s], ((j / kS) - 1) & 1, ab, p.gabort)) break;
+            tma_load_2d(ring + s * kStage + kAB, xm, &B.full[s], (sg.kb0 + kk) * 64, 0, pol);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16(128, TN);
+      int j = 0, segc = 0;
+      for (int ph = 0; ph < P && !*ab; ++ph) {
+        if (phase_kind(ph, p.L) != PH_GEMM) continue;
+        const GPh gp = gemm_of(ph, p);
+        SegIter it((gp.N + 127) / 128, gp.K / 64, G, c);
+        Seg sg;
+        while (it.next(sg) && !*ab) {
+          const int buf = segc & 1;
+          if (segc >= 2) wait_ab(&B.acc_empty[buf], ((segc >> 1) - 1) & 1, ab, p.gabort);
+          tc_fence_after();
+          const uint32_t d = B.tmem + buf * kAccCols;
+          for (int kk = 0; kk < sg.nkb; ++kk, ++j) {
+            const int s = j % kS;
+            wait_ab(&B.full[s], (j / kS) & 1, ab, p.gabort);
+            tc_fence_after();
+            if (!*ab) {
+              const uint64_t ad = desc_sw128(ring + s * kStage);
+              const uint64_t bd = desc_sw128(ring + s * kStage + kAB);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(&B.empty[s]);
+          }
+          mma_commit(&B.acc_full[buf]);
+          ++segc;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- warps 0-3: epilogues and the non-GEMM phases
+    AttnUse use = {{0, 0}, 0, 0};
+    int segc = 0, red_use = 0;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    for (int ph = 0; ph < P; ++ph) {
+      const int kind = phase_kind(ph, p.L);
+      if (kind == PH_EMBED) {
+        embed_phase(p, c, warp, lane);
+      } else if (kind == PH_ATTN || kind == PH_COMB) {
+        const int l = (ph - 1) / 6;
+        const int units = (p.M / kGamma) * p.nkv;
+        const int splits = p.attn_splits[p.layers[l].window > 0];
+        const int items = kind == PH_ATTN ? units * splits : units * 32;
+        if (c < items) {
+          int pre = 0;
+          if (kind == PH_ATTN && t == 0) pre = attn_prefetch(p, l, c / splits, c % splits, sA + kAP + kAQ, B);
+          if (t == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+          epi_sync();
+          for (int i = c; i < items && !*ab; i += G) {
+            if (kind == PH_ATTN) {
+              // `pre` is only read by thread 0, which computed it
+              attn_item(p, l, i / splits, i % splits, i == c ? pre : 0, sA, B, use, t);
+              epi_sync();
+            } else {
+              combine_item(p, l, i / 32, i % 32, t);
+            }
+          }
+        }
+      } else {
+        // GEMM epilogues of this CTA's segments
+        const GPh gp = gemm_of(ph, p);
+        const int tiles = (gp.N + 127) / 128, nkb = gp.K / 64;
+        const int maxc = max_contrib(tiles, nkb, G);
+        SegIter it(tiles, nkb, G, c);
+        Seg sg;
+        bool first = true;
+        GemmParams e;
+        e.N = gp.N; e.K = gp.K; e.M = p.M; e.Mp = p.M; e.eps = p.eps; e.status = p.status;
+        e.ss_n = p.H; e.ss_parts = p.H / 128;
+        e.q = p.q; e.inv_pi = p.inv_pi; e.mscale = p.mscale; e.nh = p.nh; e.nkv = p.nkv;
+        e.ctx_lens = p.ctx_lens; e.page_tables = p.page_tables; e.mpps = p.mpps; e.g = p.g;
+        e.layer = gp.layer; e.pool = p.pool; e.x = p.x; e.xb = p.xb; e.H = p.H; e.act = p.act; e.F = p.F;
+        e.logits = p.logits; e.amax_best = p.amax_best;
+        const PersistLayer& Ly = p.layers[gp.layer];
+        if (gp.epi == EPI_QKV) {
+          e.ss_in = p.ss_b; e.q_norm = Ly.q_norm; e.k_norm = Ly.k_norm;
+        } else if (gp.epi == EPI_GATEUP) {
+          e.ss_in = p.ss_a;
+        } else if (gp.epi == EPI_LMHEAD) {
+          e.ss_in = p.ss_b;  // the final RMSNorm's 1/RMS, applied to the logits
+        } else {
+          const bool is_o = gp.kind == 3;
+          e.ss_out = is_o ? p.ss_a : p.ss_b;
+          // the last down projection prepares the lm_head operand bf16(x * norm)
+          e.ln_next = is_o ? Ly.ln_post : (gp.layer + 1 < p.L ? p.layers[gp.layer + 1].ln_in : p.norm);
+        }
+        if (gp.epi == EPI_LMHEAD && p.final_hidden && c < p.M) {
+          // side job (nothing waits for it): the final hidden state of token c
+          if (t == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+          epi_sync();
+          if (t == 0) rsc[0] = row_rscale(p, p.ss_b, c);
+          epi_sync();
+          final_hidden_row(p, c, rsc[0], t);
+          epi_sync();
+        }
+        while (it.next(sg)) {
+          if (first) {
+            if (t == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+            epi_sync();
+            if (e.ss_in && t < TN) rsc[t] = t < p.M ? row_rscale(p, e.ss_in, t) : 1.f;
+            epi_sync();
+            first = false;
+          }
+          const int buf = segc & 1;
+          wait_ab(&B.acc_full[buf], (segc >> 1) & 1, ab, p.gabort);
+          tc_fence_after();
+          const uint32_t acc = B.tmem + buf * kAccCols + lane_off;
+          const int n = sg.tile * 128 + t;
+          float v[16];
+          tmem_ld16(acc, v);
+          tc_fence_before();
+          epi_sync();
+          if (t == 0) mbar_arrive(&B.acc_empty[buf]);  // accumulator copied: MMA may reuse it
+          ++segc;
+          bool last = true;
+          if (sg.ncontrib > 1) {
+            // fp32 partial of this CTA's k-range; the last contributor sums all in CTA order
+            float* tile_ws = p.ws + (int64_t)sg.tile * maxc * (kEThreads * TN);
+            float* mine = tile_ws + ((int64_t)sg.rank * kEThreads + t) * TN;
+#pragma unroll
+            for (int q = 0; q < 16; q += 4)
+              __stcg(reinterpret_cast<float4*>(mine + q), make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]));
+            fence_proxy_async_global();
+            __threadfence();
+            epi_sync();
+            if (t == 0) B.flag = atomicAdd(&p.counters[sg.tile], 1u) == (unsigned)(sg.ncontrib - 1);
+            epi_sync();
+            last = B.flag != 0;
+            if (last) {
+              __threadfence();
+#pragma unroll
+              for (int q = 0; q < 16; ++q) v[q] = 0.f;
+              if (sg.ncontrib <= kRedMax) {
+                // every partial of the tile in one bulk copy, then summed from shared memory
+                if (t == 0) {
+                  fence_proxy_async_global();
+                  fence_proxy_async_smem();
+                  mbar_arrive_expect_tx(&B.red_full, sg.ncontrib * kPartBytes);
+                  bulk_load(sRed, tile_ws, sg.ncontrib * kPartBytes, &B.red_full);
+                }
+                wait_ab(&B.red_full, red_use & 1, ab, p.gabort);
+                ++red_use;
+                for (int rk = 0; rk < sg.ncontrib; ++rk) {
+                  const float4* src = reinterpret_cast<const float4*>(sRed + (size_t)(rk * kEThreads + t) * TN * 4);
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) {
+                    const float4 f = src[q];
+                    v[4 * q] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
+                  }
+                }
+              } else {
+                for (int rk0 = 0; rk0 < sg.ncontrib; rk0 += 4) {
+                  float4 q4[4][4];
+#pragma unroll
+                  for (int u = 0; u < 4; ++u) {
+                    const int rk = rk0 + u < sg.ncontrib ? rk0 + u : rk0;
+                    const float4* src = reinterpret_cast<const float4*>(tile_ws + ((int64_t)rk * kEThreads + t) * TN);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) q4[u][q] = __ldcg(src + q);
+                  }
+#pragma unroll
+                  for (int u = 0; u < 4; ++u) {
+                    if (rk0 + u >= sg.ncontrib) break;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                      v[4 * q] += q4[u][q].x; v[4 * q + 1] += q4[u][q].y;
+                      v[4 * q + 2] += q4[u][q].z; v[4 * q + 3] += q4[u][q].w;
+                    }
+                  }
+                }
+              }
+              if (t == 0) p.counters[sg.tile] = 0;
+            }
+          }
+          if (last) {
+            switch (gp.epi) {
+              case EPI_QKV: epilogue_chunk<EPI_QKV>(e, es, rsc, v, t, n, 0, 0, sg.tile); break;
+              case EPI_RESID: epilogue_chunk<EPI_RESID>(e, es, rsc, v, t, n, 0, 0, sg.tile); break;
+              case EPI_GATEUP: epilogue_chunk<EPI_GATEUP>(e, es, rsc, v, t, n, 0, 0, sg.tile); break;
+              default: epilogue_chunk<EPI_LMHEAD>(e, es, rsc, v, t, n, 0, 0, sg.tile); break;
+            }
+            if (gp.epi == EPI_LMHEAD) {
+              // the last vocabulary tile to finish turns the running argmaxes into drafts
+              __threadfence();
+              epi_sync();
+              if (t == 0) B.flag = atomicAdd(p.amax_counter, 1u) == (unsigned)(tiles - 1);
+              epi_sync();
+              if (B.flag) {
+                __threadfence();
+                if (t < p.M && (t % kGamma) > 0) {
+                  const unsigned long long k = __ldcg(p.amax_best + t);
+                  p.drafts[(t / kGamma) * (kGamma - 1) + (t % kGamma) - 1] = argmax_key_index(k);
+                }
+              }
+            }
+          }
+        }
+      }
+      // phase done on this CTA
+      epi_sync();
+      if (t == 0) grid_arrive(&p.bar[ph]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (t == 0 && *ab) atomicOr(p.status, DFLASH_DEV_TIMEOUT);
+  if (*ab) {  // copies issued before a wait gave up: give them time to land
+    for (int i = 0; i < 2000; ++i) __nanosleep(1000);
+  }
+  if (warp == 0) tmem_dealloc(B.tmem, 256);
+}
+
+}  // namespace
+
+int persist_smem_bytes() { return kSmemP; }
+
+int persist_max_hidden() { return kMaxHGroups * 128; }
+
+size_t persist_ws_floats(int H, int F, int nh, int nkv, int V, int num_sms) {
+  const int shapes[5][2] = {{(nh + 2 * nkv) * 128, H}, {H, nh * 128}, {2 * F, H}, {H, F}, {V, H}};
+  size_t need = 16;
+  for (auto& s : shapes) {
+    const int tiles = (s[0] + 127) / 128, nkb = s[1] / 64;
+    need = std::max(need, (size_t)tiles * max_contrib(tiles, nkb, num_sms) * 128 * TN);
+  }
+  return need;
+}
+
+static int max_tiles_of(int H, int F, int nh, int nkv, int V) {
+  return std::max(std::max((nh + 2 * nkv) * 128, H), std::max(2 * F, V)) / 128 + 1;
+}
+
+// Control words: the packed argmax of every token (2 words each, first, so 8-byte aligned),
+// the phase counters, the abort flag, the lm_head tile counter, the split-K tile counters.
+size_t persist_ctl_words(int L, int H, int F, int nh, int nkv, int V) {
+  return 2 * (size_t)kPersistMaxM + (size_t)(2 + 6 * L) + 2 + (size_t)max_tiles_of(H, F, nh, nkv, V);
+}
+
+void persist_bind_ctl(PersistParams& p, unsigned* ctl) {
+  const int nbar = 2 + 6 * p.L;
+  p.amax_best = reinterpret_cast<unsigned long long*>(ctl);
+  unsigned* w = ctl + 2 * kPersistMaxM;
+  p.bar = w;
+  p.gabort = reinterpret_cast<int*>(w + nbar);
+  p.amax_counter = w + nbar + 1;
+  p.counters = w + nbar + 2;
+}
+
+void persist_attn_split(int units, int max_ctx, int window, int G, int* cps, int* splits) {
+  int nch = (max_ctx + kGamma + kAKC - 1) / kAKC;
+  if (window > 0) nch = std::min(nch, (window + kGamma + kPage + kAKC - 1) / kAKC);
+  int c = (units * nch + G - 1) / G;
+  if (c < 1) c = 1;
+  *cps = c;
+  *splits = (nch + c - 1) / c;
+}
+
+static cudaError_t persist_attr() {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemP);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t persist_occupancy(int* per_sm) {
+  cudaError_t e = persist_attr();
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, persist_kernel, kBlockThreads, kSmemP);
+}
+
+cudaError_t launch_persist(const PersistParams& p, cudaStream_t st) {
+  cudaError_t e0 = persist_attr();
+  if (e0 != cudaSuccess) return e0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.G);
+  cfg.blockDim = dim3(kBlockThreads);
+  cfg.dynamicSmemBytes = kSmemP;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the phase counters need it
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, persist_kernel, p);
+}
+
+}  // namespace dflash

@@ -1,0 +1,78 @@
+// Host interface of the persistent single-launch propose kernel (persist_tc.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dflash_internal.cuh"
+
+namespace dflash {
+
+struct PersistLayer {
+  const __nv_bfloat16* q_norm;
+  const __nv_bfloat16* k_norm;
+  const __nv_bfloat16* ln_in;
+  const __nv_bfloat16* ln_post;
+  int window;        // 0: full attention
+};
+
+struct PersistParams {
+  int L, M, H, F, nh, nkv, V, mpps, mask, max_ctx, G;
+  float eps, mscale;
+  int attn_cps[2];      // attention: 64-key chunks per work item (full layers, windowed layers)
+  int attn_splits[2];   // attention: work items per (sequence, kv head)
+  const int32_t* bonus;
+  const int32_t* ctx_lens;
+  const int32_t* page_tables;
+  const __nv_bfloat16* embed;
+  const __nv_bfloat16* norm;
+  const float2* inv_pi;
+  const PersistLayer* layers;       // [L], device
+  const CUtensorMap* maps;          // [4L + 1] weights (qkv, o, gate/up, down per layer; lm_head),
+                                    // then [3] activations (xb, attn, act), device, 64-B aligned
+  float* x;
+  __nv_bfloat16* xb;
+  float* ss_a;
+  float* ss_b;
+  __nv_bfloat16* q;
+  __nv_bfloat16* attn;
+  __nv_bfloat16* act;
+  __nv_bfloat16* pool;
+  PoolGeom g;
+  float* ws;
+  unsigned* counters;
+  unsigned long long* amax_best;    // [16] packed running argmax per token (control buffer)
+  unsigned* amax_counter;
+  float* o_part;
+  float* ml_part;
+  int32_t* drafts;
+  __nv_bfloat16* logits;
+  __nv_bfloat16* final_hidden;
+  // One control buffer, zeroed before each launch (persist_ctl_words words):
+  unsigned* bar;                    // [3 + 6L] phase arrival counters
+  int* gabort;                      // grid-wide "a wait gave up" flag
+  unsigned* status;
+};
+
+// Tokens (M = 16 * nb) the persistent kernel handles (bf16 lm_head only); larger batches and
+// the FP8 lm_head use the per-projection kernels.
+constexpr int kPersistMaxM = 16;
+
+// Shared memory and split-K workspace the persistent kernel needs; the largest hidden size.
+int persist_smem_bytes();
+int persist_max_hidden();
+size_t persist_ws_floats(int H, int F, int nh, int nkv, int V, int num_sms);
+// Control words: phase counters, abort flag, lm_head tile counter, split-K tile counters.
+size_t persist_ctl_words(int L, int H, int F, int nh, int nkv, int V);
+// Point p.bar / p.gabort / p.amax_counter / p.counters into `ctl`.
+void persist_bind_ctl(PersistParams& p, unsigned* ctl);
+// Attention work split for `units` (sequence, kv head) pairs over G CTAs.
+void persist_attn_split(int units, int max_ctx, int window, int G, int* cps, int* splits);
+// Resident CTAs of the persistent kernel per SM (1 when it can run).
+cudaError_t persist_occupancy(int* per_sm);
+// Launch (cooperative, one CTA per SM).  The control buffer must be zero (memset it on `st`).
+cudaError_t launch_persist(const PersistParams& p, cudaStream_t st);
+
+}  // namespace dflash

@@ -92,6 +92,13 @@ class Drafter:
                          hidden.data_ptr() if hidden is not None else 0, _stream(stream))
         return drafts
 
+    def set_persistent(self, enable: bool) -> None:
+        L.dflash_set_persistent(self.handle, enable)
+
+    @property
+    def persistent(self) -> bool:
+        return L.dflash_persistent(self.handle)
+
     def kv_layout(self) -> Tuple[int, int, Tuple[int, ...]]:
         return L.dflash_kv_layout(self.handle)
 

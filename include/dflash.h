@@ -197,6 +197,16 @@ int dflash_profile_kinds(void);
 int dflash_profile_read(dflash_handle* h, int kind, const char** name, double* total_ms,
                         int64_t* launches);
 
+/* Single-launch forward.  On bf16 handles with a bf16 lm_head and 8 query heads per kv
+ * head, dflash_propose with nb == 1 runs the whole gamma-block forward (embedding, every
+ * layer, final norm, lm_head and argmax) as ONE persistent kernel with one CTA per SM;
+ * larger batches launch one kernel per projection.  Both give the same result up to the
+ * summation order of the split-K partial sums.  dflash_set_persistent(h, 0) makes nb == 1
+ * use the per-projection kernels too (for comparisons); enabling it where it is not
+ * available returns DFLASH_EUNSUPPORTED.  dflash_persistent(h) is 1 when it is in use. */
+int dflash_set_persistent(dflash_handle* h, int enable);
+int dflash_persistent(const dflash_handle* h);
+
 /* The tensor-core projection GEMM on its own (for tests): out[m, n] = sum_k W[n, k] X[m, k]
  * with W [N, K] and X [M, K] bf16 row-major device arrays, out [M, N] fp32.  K % 64 == 0,
  * nsplit must be 1.  Same kernel as every bf16 projection of dflash_propose. */
