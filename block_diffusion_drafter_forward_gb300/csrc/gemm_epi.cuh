@@ -154,15 +154,21 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
 #pragma unroll
       for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * (1.f / sqrtf(es.tot[c] * (1.f / 128.f) + p.eps)) * w;
       epi_sync();
-      // RoPE: pair (j, j + 64), NeoX rotate-half
+      // RoPE: pair (j, j + 64), NeoX rotate-half.  The block's positions are consecutive, so
+      // the angle at ctx + c comes from the one at ctx by c rotations through one position's
+      // angle (fp32 error ~c * 6e-8, far below the bf16 rounding of the result).
       const int j = t & 63;
       const float2 ipj = p.inv_pi[j];
+      float cs, sn, c1, s1;
+      rope_cs(ipj, ctx, &cs, &sn);
+      rope_cs(ipj, 1, &c1, &s1);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        float cs, sn;
-        rope_cs(ipj, ctx + c, &cs, &sn);
         const float a = es.xch[j][c], b = es.xch[j + 64][c];
         v[c] = (t < 64 ? a * cs - b * sn : b * cs + a * sn) * p.mscale;
+        const float cn = cs * c1 - sn * s1;
+        sn = fmaf(sn, c1, cs * s1);
+        cs = cn;
       }
       epi_sync();
     }

@@ -42,8 +42,8 @@ constexpr int kAB = 128 * 64 * 2;             // weight tile (bf16, 128 rows x 6
 constexpr int kBB = TN * 64 * 2;              // activation tile
 constexpr int kStage = kAB + kBB;
 constexpr int kRing = kS * kStage;
-// attention region: P (the epilogue scratch aliases it), then Q and two K/V stages; Q and the
-// K/V stages double as the landing buffer of split-K partials during projection phases
+// attention region: the epilogue scratch, then Q and two K/V stages; Q and the K/V stages
+// double as the landing buffer of split-K partials during projection phases
 constexpr int kAKC = 64, kAPages = 4, kATile = 4096;
 constexpr int kAP = 128 * kAKC * 2, kAQ = 128 * 128 * 2, kAKVStage = 2 * kAPages * kATile;
 constexpr int kAttn = kAP + kAQ + 2 * kAKVStage;
@@ -52,13 +52,14 @@ constexpr int kRedMax = (kAQ + 2 * kAKVStage) / kPartBytes;  // partials that fi
 constexpr int kBarOff = kRing + kAttn;
 constexpr int kSmemP = kBarOff + 512 + 256 + 1024;
 constexpr uint32_t kAccCols = 32;             // per accumulator buffer (16 used)
-constexpr uint32_t kTS = 64, kTO = 128;       // attention S and O columns
+constexpr uint32_t kTS = 128, kTO = 256;      // attention S/P and O columns (128 each)
+constexpr uint32_t kTmemCols = 512;
 constexpr long long kGridSpin = 20000000ll;   // polls of a phase counter before giving up
 constexpr int kEThreads = 128;
 constexpr int kBlockThreads = 224;
 constexpr int kMaxHGroups = 48;               // H / 128 the final-hidden pass holds in registers
 
-static_assert(sizeof(EpiSmem) <= kAP, "epilogue scratch must fit in the attention P area");
+static_assert(sizeof(EpiSmem) <= kAP, "epilogue scratch overflows its area");
 
 struct Bars {
   uint64_t full[kS], empty[kS];
@@ -350,9 +351,19 @@ __device__ int attn_prefetch(const PersistParams& p, int layer, int unit, int sp
   return pre;
 }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // One attention work item on warps 0-3: the 8 query heads x 16 rows of one kv head against
-// key chunks [c_begin, c_end), S and P.V on the tensor cores, online softmax in registers.
-// Warp 0 waits for the K/V copies and issues the MMAs (lane 0) with the warp converged.
+// key chunks [c_begin, c_end), taken two chunks (128 keys) at a time: S = Q K^T for both
+// chunks on the tensor cores, one max pass and one exp pass over the 128 scores, P (bf16) back
+// into the S columns of TMEM, O += P V with P read from TMEM.  O stays in TMEM (rescaled
+// there when a row's running max grows) and is read once at the end.  Warp 0 waits for the
+// K/V copies and issues the MMAs (lane 0) with the warp converged.  The loops are kept
+// rolled: straight-line code this large would run from a cold instruction cache every time.
 __device__ void attn_item(const PersistParams& p, int layer, int unit, int split, int pre, uint8_t* sA, Bars& B,
                           AttnUse& use, int t) {
   const int warp = t >> 5, lane = t & 31;
@@ -363,10 +374,11 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
   }
   const int group = p.nh / p.nkv;
   const int nkeys = a.ctx + kGamma;
-  uint8_t* sP = sA;
-  uint8_t* sQ = sP + kAP;
+  uint8_t* sQ = sA + kAP;
   uint8_t* sKV = sQ + kAQ;
-  const uint32_t tS = B.tmem + kTS, tO = B.tmem + kTO;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  const uint32_t tS = B.tmem + kTS + lane_off, tO = B.tmem + kTO + lane_off;
+  volatile int* ab = &B.abort;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -389,93 +401,120 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
   fence_proxy_async_smem();
   epi_sync();
 
-  const int r = t & 15;
-  const int pos_q = a.ctx + r;
+  const int pos_q = a.ctx + (t & 15);
   const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
   float m_run = -FLT_MAX, l_run = 0.f;
-  float o[128];
-#pragma unroll
-  for (int i = 0; i < 128; ++i) o[i] = 0.f;
   constexpr uint32_t idesc_s = idesc_bf16(128, kAKC);
   constexpr uint32_t idesc_o = idesc_bf16(128, 128);
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  volatile int* ab = &B.abort;
 
-  for (int c = a.c_begin; c < a.c_end; ++c) {
-    const int st = (c - a.c_begin) & 1;
-    uint8_t* sK = sKV + st * kAKVStage;
-    uint8_t* sV = sK + kAPages * kATile;
+#pragma unroll 1
+  for (int sc = a.c_begin; sc < a.c_end; sc += 2) {
+    const int nchk = min(2, a.c_end - sc);
     if (warp == 0) {
-      wait_ab(&B.kv_full[st], use.kv[st] & 1, ab, p.gabort);
-      tc_fence_after();
-      if (lane == 0) {
-        if (!*ab) {
+#pragma unroll 1
+      for (int i = 0; i < nchk; ++i) {
+        wait_ab(&B.kv_full[i], use.kv[i] & 1, ab, p.gabort);
+        tc_fence_after();
+        if (lane == 0 && !*ab) {
+          uint8_t* sK = sKV + i * kAKVStage;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_bf16(tS, desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048), idesc_s,
-                     k > 0 ? 1u : 0u);
+            mma_bf16(B.tmem + kTS + i * kAKC, desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048),
+                     idesc_s, k > 0 ? 1u : 0u);
         }
-        mma_commit(&B.s_done);
+        __syncwarp();
       }
+      if (lane == 0) mma_commit(&B.s_done);
       __syncwarp();
     }
-    use.kv[st]++;
+    use.kv[0]++;
+    if (nchk > 1) use.kv[1]++;
     wait_ab(&B.s_done, use.s & 1, ab, p.gabort);
     use.s++;
     tc_fence_after();
-    const int kbase = a.k0 + c * kAKC;
+
+    // every key of the super-chunk visible to every row: no masking
+    const int kb = a.k0 + sc * kAKC, nk = nchk * kAKC;
+    const bool full = kb + nk <= nkeys && (a.window <= 0 || a.ctx + kGamma - 1 - kb < a.window);
     float mc = -FLT_MAX;
-#pragma unroll
-    for (int q4 = 0; q4 < kAKC / 32; ++q4) {
+#pragma unroll 1
+    for (int q4 = 0; q4 < 2 * nchk; ++q4) {
       float v[32];
-      tmem_ld32(tS + lane_off + q4 * 32, v);
+      tmem_ld32(tS + q4 * 32, v);
+      if (full) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int key = kbase + q4 * 32 + j;
-        if (key < nkeys && (a.window <= 0 || pos_q - key < a.window)) mc = fmaxf(mc, v[j] * scale_log2);
+        for (int j = 0; j < 32; ++j) mc = fmaxf(mc, v[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int key = kb + q4 * 32 + j;
+          if (key < nkeys && (a.window <= 0 || pos_q - key < a.window)) mc = fmaxf(mc, v[j]);
+        }
       }
     }
-    const float m_new = fmaxf(m_run, mc);
-    const float alpha = m_new == -FLT_MAX ? 1.f : exp2f(m_run - m_new);
-    float lsum = 0.f;
+    // max(s) * c == max(s * c) for c > 0 (rounding is monotonic)
+    const float m_new = fmaxf(m_run, mc == -FLT_MAX ? -FLT_MAX : mc * scale_log2);
+    const float alpha = m_run == -FLT_MAX ? 1.f : ex2(m_run - m_new);
+    if (sc > a.c_begin && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // O (complete: the previous P V was waited for) times alpha, in TMEM
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float v[32];
+        tmem_ld32(tO + q4 * 32, v);
 #pragma unroll
-    for (int q4 = 0; q4 < kAKC / 32; ++q4) {
-      float v[32];
-      tmem_ld32(tS + lane_off + q4 * 32, v);
-#pragma unroll
-      for (int j8 = 0; j8 < 4; ++j8) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float pr[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int jj = j8 * 8 + 2 * e + u;
-            const int key = kbase + q4 * 32 + jj;
-            const bool vis = key < nkeys && (a.window <= 0 || pos_q - key < a.window);
-            pr[u] = vis ? exp2f(v[jj] * scale_log2 - m_new) : 0.f;
-          }
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
-          lsum += __low2float(h2) + __high2float(h2);
-          pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        *reinterpret_cast<uint4*>(sP + ((t >> 3) * (kAKC / 8) + q4 * 4 + j8) * 128 + (t & 7) * 16) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int j = 0; j < 32; ++j) v[j] *= alpha;
+        tmem_st32(tO + q4 * 32, v);
       }
+    }
+    // P = exp2(s * c - m) as bf16 pairs; keys 64 h .. 64 h + 63 go to columns 32 h .. 32 h + 31,
+    // over scores already read
+    float lsum = 0.f;
+#pragma unroll 1
+    for (int h = 0; h < nchk; ++h) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        float v[32];
+        tmem_ld32(tS + (2 * h + q) * 32, v);
+        if (full) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2(fmaf(v[2 * e], scale_log2, -m_new)),
+                                                            ex2(fmaf(v[2 * e + 1], scale_log2, -m_new)));
+            lsum += __low2float(h2) + __high2float(h2);
+            pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float pr[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int key = kb + (2 * h + q) * 32 + 2 * e + u;
+              const bool vis = key < nkeys && (a.window <= 0 || pos_q - key < a.window);
+              pr[u] = vis ? ex2(fmaf(v[2 * e + u], scale_log2, -m_new)) : 0.f;
+            }
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
+            lsum += __low2float(h2) + __high2float(h2);
+            pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+        }
+      }
+      tmem_st32u(tS + h * 32, pk);
     }
     l_run = l_run * alpha + lsum;
     m_run = m_new;
-    fence_proxy_async_smem();
     tc_fence_before();
     epi_sync();
     if (warp == 0) {
       if (lane == 0) {
         tc_fence_after();
         if (!*ab) {
-#pragma unroll
-          for (int k = 0; k < kAPages; ++k)
-            mma_bf16(tO, desc_noswz(sP + k * 256, 128, kAKC / 8 * 128), desc_noswz(sV + k * kATile, 128, 256),
-                     idesc_o, k > 0 ? 1u : 0u);
+#pragma unroll 1
+          for (int kk = 0; kk < 4 * nchk; ++kk)
+            mma_bf16_tmem_a(B.tmem + kTO, B.tmem + kTS + kk * 8,
+                            desc_noswz(sKV + (kk >> 2) * kAKVStage + kAPages * kATile + (kk & 3) * kATile, 128, 256),
+                            idesc_o, (sc > a.c_begin || kk > 0) ? 1u : 0u);
         }
         mma_commit(&B.o_done);
       }
@@ -484,42 +523,44 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
     wait_ab(&B.o_done, use.o & 1, ab, p.gabort);
     use.o++;
     tc_fence_after();
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float v[32];
-      tmem_ld32(tO + lane_off + q4 * 32, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[q4 * 32 + j] = o[q4 * 32 + j] * alpha + v[j];
-    }
-    tc_fence_before();
-    epi_sync();
-    if (warp == 0) {
-      if (lane == 0 && c + 2 < a.c_end && !*ab) attn_load_chunk(p, layer, a, c + 2, st, sKV, B);
+    if (sc + 2 < a.c_end && warp == 0) {
+      // the MMAs that read both stages are complete: refill them
+      if (lane == 0 && !*ab) {
+        attn_load_chunk(p, layer, a, sc + 2, 0, sKV, B);
+        if (sc + 3 < a.c_end) attn_load_chunk(p, layer, a, sc + 3, 1, sKV, B);
+      }
       __syncwarp();
     }
   }
+  // O out of TMEM: normalised bf16 rows, or the split's fp32 partial (O, m, l)
   const int hh = t >> 4;
-  __nv_bfloat16* dst = p.attn + ((int64_t)(a.s * kGamma + r) * p.nh + a.g * group + hh) * 128;
-  if (a.nsplit == 1) {
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+  __nv_bfloat16* dst = p.attn + ((int64_t)(a.s * kGamma + (t & 15)) * p.nh + a.g * group + hh) * 128;
+  const int64_t slot = (int64_t)unit * a.splits + split;
+  float* op = p.o_part + (slot * 128 + t) * 128;
+  const float inv = a.nsplit == 1 ? (l_run > 0.f ? 1.f / l_run : 0.f) : 1.f;
+#pragma unroll 1
+  for (int q4 = 0; q4 < 4; ++q4) {
+    float v[32];
+    tmem_ld32(tO + q4 * 32, v);
+    if (a.nsplit == 1) {
 #pragma unroll
-    for (int d8 = 0; d8 < 16; ++d8) {
-      uint32_t pk[4];
+      for (int d8 = 0; d8 < 4; ++d8) {
+        uint32_t pk[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[d8 * 8 + 2 * e] * inv, o[d8 * 8 + 2 * e + 1] * inv);
-        pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[d8 * 8 + 2 * e] * inv, v[d8 * 8 + 2 * e + 1] * inv);
+          pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        reinterpret_cast<uint4*>(dst + q4 * 32)[d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      reinterpret_cast<uint4*>(dst)[d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
-  } else {
-    const int64_t slot = (int64_t)unit * a.splits + split;
-    float* op = p.o_part + (slot * 128 + t) * 128;
+    } else {
 #pragma unroll
-    for (int i = 0; i < 128; i += 4)
-      __stcg(reinterpret_cast<float4*>(op + i), make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
-    __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
+      for (int i = 0; i < 32; i += 4)
+        __stcg(reinterpret_cast<float4*>(op + q4 * 32 + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+    }
   }
+  if (a.nsplit > 1) __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
+  tc_fence_before();  // TMEM reads done before the next item's MMAs overwrite S and O
 }
 
 // Merge the split partials of rows 4 rb .. 4 rb + 3 of one unit (a warp per row, loads of 8
@@ -570,7 +611,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const Persist
   uint8_t* sRed = sA + kAP;  // split-K partial landing buffer (the attention Q + K/V area)
   Bars& B = *reinterpret_cast<Bars*>(smem + kBarOff);
   float* rsc = reinterpret_cast<float*>(smem + kBarOff + 512);
-  EpiSmem& es = *reinterpret_cast<EpiSmem*>(sA);  // aliases the attention P area
+  EpiSmem& es = *reinterpret_cast<EpiSmem*>(sA);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int G = p.G, c = blockIdx.x;
   const int P = 2 + 6 * p.L;
@@ -592,7 +633,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const Persist
     B.flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(&B.tmem, 256);
+  if (warp == 0) tmem_alloc(&B.tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -863,7 +904,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const Persist
   if (*ab) {  // copies issued before a wait gave up: give them time to land
     for (int i = 0; i < 2000; ++i) __nanosleep(1000);
   }
-  if (warp == 0) tmem_dealloc(B.tmem, 256);
+  if (warp == 0) tmem_dealloc(B.tmem, kTmemCols);
 }
 
 }  // namespace
