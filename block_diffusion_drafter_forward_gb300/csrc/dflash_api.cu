@@ -220,7 +220,14 @@ int propose_persist(dflash_handle* h, const int32_t* bonus_tokens, const int32_t
   p.embed = static_cast<const __nv_bfloat16*>(h->embed);
   p.norm = static_cast<const __nv_bfloat16*>(h->norm);
   p.inv_pi = h->rope_inv_pi;
-  p.layers = static_cast<const PersistLayer*>(h->p_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& d = h->layer[l];
+    p.layers[l].q_norm = static_cast<const __nv_bfloat16*>(d.q_norm);
+    p.layers[l].k_norm = static_cast<const __nv_bfloat16*>(d.k_norm);
+    p.layers[l].ln_in = static_cast<const __nv_bfloat16*>(d.ln_in);
+    p.layers[l].ln_post = static_cast<const __nv_bfloat16*>(d.ln_post);
+    p.layers[l].window = c.layer_sliding[l] ? c.sliding_window : 0;
+  }
   p.maps = static_cast<const CUtensorMap*>(h->p_maps);
   p.x = h->x;
   p.xb = static_cast<__nv_bfloat16*>(h->xb);
@@ -564,7 +571,8 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     h->tc_attn = (nh / nkv) == 8;
     // single-launch persistent forward for batch 1: needs the tensor-core attention, a bf16
     // lm_head and one resident CTA per SM
-    if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && H <= persist_max_hidden()) {
+    if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && H <= persist_max_hidden() &&
+        L <= kPersistMaxL) {
       int per_sm = 0;
       if (persist_occupancy(&per_sm) == cudaSuccess && per_sm >= 1) h->persist_ok = true;
       cudaGetLastError();
@@ -589,21 +597,9 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
         return bail(DFLASH_ECUDA);
       }
       ALLOC(h->p_maps, maps.size() * sizeof(CUtensorMap));
-      std::vector<PersistLayer> pl(L);
-      for (int l = 0; l < L; ++l) {
-        const LayerW& d = h->layer[l];
-        pl[l].q_norm = static_cast<const __nv_bfloat16*>(d.q_norm);
-        pl[l].k_norm = static_cast<const __nv_bfloat16*>(d.k_norm);
-        pl[l].ln_in = static_cast<const __nv_bfloat16*>(d.ln_in);
-        pl[l].ln_post = static_cast<const __nv_bfloat16*>(d.ln_post);
-        pl[l].window = c.layer_sliding[l] ? c.sliding_window : 0;
-      }
-      ALLOC(h->p_layers, pl.size() * sizeof(PersistLayer));
       h->p_ctl_words = persist_ctl_words((int)L, (int)H, (int)F, (int)nh, (int)nkv, (int)V);
       ALLOC(h->p_ctl, h->p_ctl_words * sizeof(unsigned));
       cudaError_t e1 = cudaMemcpy(h->p_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
-      if (e1 == cudaSuccess)
-        e1 = cudaMemcpy(h->p_layers, pl.data(), pl.size() * sizeof(PersistLayer), cudaMemcpyHostToDevice);
       if (e1 != cudaSuccess) {
         cuda_fail(h, e1, "persistent forward tables");
         return bail(DFLASH_ECUDA);

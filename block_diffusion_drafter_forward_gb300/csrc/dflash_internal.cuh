@@ -157,7 +157,6 @@ struct dflash_handle {
   bool persist_ok = false;             // available for this configuration and device
   bool persist_on = false;             // used by dflash_propose (dflash_set_persistent)
   void* p_maps = nullptr;              // device CUtensorMap table
-  void* p_layers = nullptr;            // device per-layer table
   unsigned* p_ctl = nullptr;           // control words, zeroed before each launch
   size_t p_ctl_words = 0;
 

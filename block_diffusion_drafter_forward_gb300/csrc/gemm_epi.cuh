@@ -88,9 +88,45 @@ __device__ __forceinline__ void rowsum16(EpiSmem& es, const float (&w)[16], int 
   epi_sync();
 }
 
+// Epilogue inputs that do not depend on the accumulator, loaded by epilogue_pre so a caller
+// can fetch them while the MMAs are still running.
+struct EpiPre {
+  float x[16];   // EPI_RESID: residual of the chunk's 16 tokens at this thread's row
+  float lnw;     // EPI_RESID: next RMSNorm weight of the row
+  float nw;      // EPI_QKV: q_norm / k_norm weight of the row
+  float2 ip;     // EPI_QKV: RoPE inv_freq / pi of this thread's pair
+  int ctx;       // EPI_QKV: first position of the chunk's gamma block
+  int pg0, pg1;  // EPI_QKV: page ids of the block's rows (ctx / 16 and the next page)
+};
+
+// ctx_known >= 0: the block's start position is already known (saves a dependent load).
+template <int EPI>
+__device__ __forceinline__ void epilogue_pre(const GemmParams& p, EpiPre& q, int t, int n, int m0, int c0, int tile_n,
+                                             int ctx_known = -1) {
+  if constexpr (EPI == EPI_RESID) {
+    q.lnw = p.ln_next ? __bfloat162float(p.ln_next[n]) : 1.f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) q.x[c] = m0 + c0 + c < p.M ? __ldcg(p.x + (int64_t)(m0 + c0 + c) * p.H + n) : 0.f;
+  } else if constexpr (EPI == EPI_QKV) {
+    const int hh = tile_n;
+    const bool is_q = hh < p.nh, is_k = !is_q && hh < p.nh + p.nkv;
+    const int mb = m0 + c0;
+    const int s = mb / kGamma;
+    q.ctx = ctx_known >= 0 ? ctx_known : (mb < p.M ? __ldg(p.ctx_lens + s) : 0);
+    q.nw = (is_q || is_k) ? __bfloat162float((is_q ? p.q_norm : p.k_norm)[t]) : 1.f;
+    q.ip = p.inv_pi[t & 63];
+    q.pg0 = q.pg1 = -1;
+    if (!is_q && mb < p.M && q.ctx >= 0 && q.ctx + kGamma <= p.mpps * kPage) {
+      const int32_t* pt = p.page_tables + (int64_t)s * p.mpps + q.ctx / kPage;
+      q.pg0 = __ldg(pt);
+      q.pg1 = (q.ctx % kPage) ? __ldg(pt + 1) : q.pg0;
+    }
+  }
+}
+
 template <int EPI>
 __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rsc, float (&v)[16], int t, int n,
-                               int m0, int c0, int tile_n) {
+                               int m0, int c0, int tile_n, const EpiPre& q) {
   if constexpr (EPI == EPI_STORE) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
@@ -99,19 +135,15 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
     }
   } else if constexpr (EPI == EPI_RESID) {
     float sq[16];
-    const float lnw = p.ln_next ? __bfloat162float(p.ln_next[n]) : 1.f;
-    float xo[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) xo[c] = m0 + c0 + c < p.M ? __ldcg(p.x + (int64_t)(m0 + c0 + c) * p.H + n) : 0.f;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int m = m0 + c0 + c;
       float xv = 0.f;
       if (m < p.M) {
         const int64_t o = (int64_t)m * p.H + n;
-        xv = xo[c] + v[c];
+        xv = q.x[c] + v[c];
         p.x[o] = xv;
-        p.xb[o] = __float2bfloat16_rn(xv * lnw);
+        p.xb[o] = __float2bfloat16_rn(xv * q.lnw);
       }
       sq[c] = xv * xv;
     }
@@ -138,10 +170,9 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
   } else if constexpr (EPI == EPI_QKV) {
     const int hh = tile_n;
     const bool is_q = hh < p.nh, is_k = !is_q && hh < p.nh + p.nkv;
-    // the chunk's 16 tokens are one gamma block: sequence s at positions ctx .. ctx + 15
+    // the chunk's 16 tokens are one gamma block at positions ctx .. ctx + 15
     const int mb = m0 + c0;
-    const int s = mb / kGamma;
-    const int ctx = mb < p.M ? __ldg(p.ctx_lens + s) : 0;
+    const int ctx = q.ctx;
 #pragma unroll
     for (int c = 0; c < 16; ++c) v[c] *= rsc[c0 + c];
     if (is_q || is_k) {
@@ -150,18 +181,16 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
 #pragma unroll
       for (int c = 0; c < 16; ++c) sq[c] = v[c] * v[c];
       rowsum16(es, sq, t);
-      const float w = __bfloat162float((is_q ? p.q_norm : p.k_norm)[t]);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * (1.f / sqrtf(es.tot[c] * (1.f / 128.f) + p.eps)) * w;
+      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * (1.f / sqrtf(es.tot[c] * (1.f / 128.f) + p.eps)) * q.nw;
       epi_sync();
       // RoPE: pair (j, j + 64), NeoX rotate-half.  The block's positions are consecutive, so
       // the angle at ctx + c comes from the one at ctx by c rotations through one position's
       // angle (fp32 error ~c * 6e-8, far below the bf16 rounding of the result).
       const int j = t & 63;
-      const float2 ipj = p.inv_pi[j];
       float cs, sn, c1, s1;
-      rope_cs(ipj, ctx, &cs, &sn);
-      rope_cs(ipj, 1, &c1, &s1);
+      rope_cs(q.ip, ctx, &cs, &sn);
+      rope_cs(q.ip, 1, &c1, &s1);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const float a = es.xch[j][c], b = es.xch[j + 64][c];
@@ -179,10 +208,8 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
       } else if (ctx < 0 || ctx + kGamma > p.mpps * kPage) {
         if (t == 0) set_status(p.status, DFLASH_DEV_BAD_CTX);
       } else {
-        // the block's rows fall on at most two pages: look both ids up once
-        const int32_t* pt = p.page_tables + (int64_t)s * p.mpps + ctx / kPage;
-        const int pg0 = __ldg(pt);
-        const int pg1 = (ctx % kPage) ? __ldg(pt + 1) : pg0;
+        // the block's rows fall on at most two pages (ids looked up in epilogue_pre)
+        const int pg0 = q.pg0, pg1 = q.pg1;
         const int head = is_k ? hh - p.nh : hh - p.nh - p.nkv;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {

@@ -268,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           tmem_ld16(lane_addr + c0, v);
         }
-        epilogue_chunk<EPI>(p, es, rsc, v, t, n, m0, c0, tile_n);
+        EpiPre pre;
+        epilogue_pre<EPI>(p, pre, t, n, m0, c0, tile_n);
+        epilogue_chunk<EPI>(p, es, rsc, v, t, n, m0, c0, tile_n, pre);
       }
       if (p.nsplit > 1 && t == 0) p.counters[tile_lin] = 0;
       if constexpr (EPI == EPI_LMHEAD) {

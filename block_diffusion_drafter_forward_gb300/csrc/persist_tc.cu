@@ -17,8 +17,10 @@
 //   warp 6 lane 0: activation TMA producer (waits for the phase the activation comes from)
 //   warps 0-3:     epilogues (gemm_epi.cuh), block attention, split combine, embedding
 // Every projection is split evenly over the CTAs by k-blocks (stream-K): CTA c owns k-blocks
-// [c T/G, (c+1) T/G) of the T = tiles x k-blocks of the projection; a tile covered by several
-// CTAs is summed from fp32 partials in CTA order by the last one to arrive (deterministic).
+// [c T/G, (c+1) T/G) of the T = tiles x k-blocks of the projection.  A tile covered by several
+// CTAs is finished by the one holding its first k-blocks (for that CTA it is always its last
+// segment, so every CTA writes its partials before it reduces anything): the others store
+// fp32 partials and count them in; it adds them to its own in CTA order (deterministic).
 // The arithmetic of every phase is the same as the per-projection kernels'.
 #include <cudaTypedefs.h>
 #include <float.h>
@@ -68,6 +70,7 @@ struct Bars {
   uint32_t tmem;
   volatile int abort;
   int flag;
+  int ctx0;  // context length of the (single) sequence
 };
 static_assert(sizeof(Bars) <= 512, "barrier block overflows its slot");
 
@@ -275,12 +278,12 @@ __device__ __forceinline__ int chunk_range_p(int window, int ctx, int* first_key
   return (nkeys - k0 + kAKC - 1) / kAKC;
 }
 
-__device__ AItem attn_geom(const PersistParams& p, int layer, int unit, int split) {
+__device__ AItem attn_geom(const PersistParams& p, int layer, int unit, int split, int ctx0) {
   AItem a;
   a.window = p.layers[layer].window;
   a.s = unit / p.nkv;
   a.g = unit % p.nkv;
-  a.ctx = __ldg(p.ctx_lens + a.s);
+  a.ctx = ctx0;
   const int wi = a.window > 0;
   const int cps = p.attn_cps[wi];
   a.splits = p.attn_splits[wi];
@@ -337,7 +340,7 @@ __device__ __forceinline__ bool chunk_is_context(const AItem& a, int c) {
 // Before the QKV phase completes: copy the first two chunks of this CTA's first item if they
 // hold context keys only.  Returns the stages loaded (bit st).  One thread.
 __device__ int attn_prefetch(const PersistParams& p, int layer, int unit, int split, uint8_t* sKV, Bars& B) {
-  const AItem a = attn_geom(p, layer, unit, split);
+  const AItem a = attn_geom(p, layer, unit, split, B.ctx0);
   if (!a.run) return 0;
   fence_proxy_async_smem();
   int pre = 0;
@@ -367,7 +370,7 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ void attn_item(const PersistParams& p, int layer, int unit, int split, int pre, uint8_t* sA, Bars& B,
                           AttnUse& use, int t) {
   const int warp = t >> 5, lane = t & 31;
-  const AItem a = attn_geom(p, layer, unit, split);
+  const AItem a = attn_geom(p, layer, unit, split, B.ctx0);
   if (!a.run) {
     if (a.bad && split == 0 && t == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
     return;
@@ -565,8 +568,8 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
 
 // Merge the split partials of rows 4 rb .. 4 rb + 3 of one unit (a warp per row, loads of 8
 // splits in flight at a time).
-__device__ void combine_item(const PersistParams& p, int layer, int unit, int rb, int t) {
-  const AItem a = attn_geom(p, layer, unit, 0);
+__device__ void combine_item(const PersistParams& p, int layer, int unit, int rb, int t, int ctx0) {
+  const AItem a = attn_geom(p, layer, unit, 0, ctx0);
   if (!a.run || a.nsplit <= 1) return;
   const int row = rb * 4 + (t >> 5), d0 = (t & 31) * 4;
   const int64_t base = (int64_t)unit * a.splits;
@@ -603,7 +606,7 @@ __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb
 }
 
 // ---------------------------------------------------------------- the kernel
-__global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const PersistParams p) {
+__global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_constant__ PersistParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -631,6 +634,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const Persist
     mbar_init(&B.red_full, 1);
     B.abort = 0;
     B.flag = 0;
+    B.ctx0 = __ldg(p.ctx_lens);
     fence_barrier_init();
   }
   if (warp == 0) tmem_alloc(&B.tmem, kTmemCols);
@@ -749,7 +753,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const Persist
               attn_item(p, l, i / splits, i % splits, i == c ? pre : 0, sA, B, use, t);
               epi_sync();
             } else {
-              combine_item(p, l, i / 32, i % 32, t);
+              combine_item(p, l, i / 32, i % 32, t, B.ctx0);
             }
           }
         }
@@ -798,21 +802,27 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const Persist
             epi_sync();
             first = false;
           }
+          // rank 0 holds the tile's first k-blocks and finishes the tile
+          const bool finisher = sg.rank == 0;
+          const int n = sg.tile * 128 + t;
+          EpiPre pre;
+          if (finisher) {  // inputs of the epilogue, fetched while the MMAs run
+            if (gp.epi == EPI_QKV) epilogue_pre<EPI_QKV>(e, pre, t, n, 0, 0, sg.tile, B.ctx0);
+            else if (gp.epi == EPI_RESID) epilogue_pre<EPI_RESID>(e, pre, t, n, 0, 0, sg.tile);
+          }
           const int buf = segc & 1;
           wait_ab(&B.acc_full[buf], (segc >> 1) & 1, ab, p.gabort);
           tc_fence_after();
           const uint32_t acc = B.tmem + buf * kAccCols + lane_off;
-          const int n = sg.tile * 128 + t;
           float v[16];
           tmem_ld16(acc, v);
           tc_fence_before();
           epi_sync();
           if (t == 0) mbar_arrive(&B.acc_empty[buf]);  // accumulator copied: MMA may reuse it
           ++segc;
-          bool last = true;
-          if (sg.ncontrib > 1) {
-            // fp32 partial of this CTA's k-range; the last contributor sums all in CTA order
-            float* tile_ws = p.ws + (int64_t)sg.tile * maxc * (kEThreads * TN);
+          float* tile_ws = p.ws + (int64_t)sg.tile * maxc * (kEThreads * TN);
+          if (!finisher) {
+            // fp32 partial of this CTA's k-range into slot `rank`, then count it in
             float* mine = tile_ws + ((int64_t)sg.rank * kEThreads + t) * TN;
 #pragma unroll
             for (int q = 0; q < 16; q += 4)
@@ -820,74 +830,85 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const Persist
             fence_proxy_async_global();
             __threadfence();
             epi_sync();
-            if (t == 0) B.flag = atomicAdd(&p.counters[sg.tile], 1u) == (unsigned)(sg.ncontrib - 1);
-            epi_sync();
-            last = B.flag != 0;
-            if (last) {
-              __threadfence();
-#pragma unroll
-              for (int q = 0; q < 16; ++q) v[q] = 0.f;
-              if (sg.ncontrib <= kRedMax) {
-                // every partial of the tile in one bulk copy, then summed from shared memory
-                if (t == 0) {
-                  fence_proxy_async_global();
-                  fence_proxy_async_smem();
-                  mbar_arrive_expect_tx(&B.red_full, sg.ncontrib * kPartBytes);
-                  bulk_load(sRed, tile_ws, sg.ncontrib * kPartBytes, &B.red_full);
+            if (t == 0) atomicAdd(&p.counters[sg.tile], 1u);
+            continue;
+          }
+          if (sg.ncontrib > 1) {
+            // the other ncontrib - 1 partials: wait for their count, then add them in CTA order
+            const int nother = sg.ncontrib - 1;
+            if (warp == 0) {
+              // the whole warp polls (one coalesced load), so no lane sleeps in an mbarrier
+              // wait while lane 0 still has work to issue
+              for (long long sp = 0; ld_acquire(&p.counters[sg.tile]) < (unsigned)nother; ++sp) {
+                if (*ab || sp > kGridSpin) {
+                  if (lane == 0) { *ab = 1; atomicExch(p.gabort, 1); }
+                  break;
                 }
-                wait_ab(&B.red_full, red_use & 1, ab, p.gabort);
-                ++red_use;
-                for (int rk = 0; rk < sg.ncontrib; ++rk) {
-                  const float4* src = reinterpret_cast<const float4*>(sRed + (size_t)(rk * kEThreads + t) * TN * 4);
+                __nanosleep(20);
+              }
+              __syncwarp();
+            }
+            if (t == 0) {
+              p.counters[sg.tile] = 0;  // re-armed for the next phase (ordered by its barrier)
+              if (nother <= kRedMax && !*ab) {
+                fence_proxy_async_global();
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&B.red_full, nother * kPartBytes);
+                bulk_load(sRed, tile_ws + kEThreads * TN, nother * kPartBytes, &B.red_full);
+              }
+            }
+            if (nother <= kRedMax) {
+              wait_ab(&B.red_full, red_use & 1, ab, p.gabort);
+              ++red_use;
+              for (int rk = 0; rk < nother; ++rk) {
+                const float4* src = reinterpret_cast<const float4*>(sRed + (size_t)(rk * kEThreads + t) * TN * 4);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float4 f = src[q];
+                  v[4 * q] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
+                }
+              }
+            } else {
+              epi_sync();  // thread 0 saw every partial counted
+              __threadfence();
+              for (int rk0 = 1; rk0 < sg.ncontrib; rk0 += 4) {
+                float4 q4[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int rk = rk0 + u < sg.ncontrib ? rk0 + u : rk0;
+                  const float4* src = reinterpret_cast<const float4*>(tile_ws + ((int64_t)rk * kEThreads + t) * TN);
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) q4[u][q] = __ldcg(src + q);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  if (rk0 + u >= sg.ncontrib) break;
 #pragma unroll
                   for (int q = 0; q < 4; ++q) {
-                    const float4 f = src[q];
-                    v[4 * q] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
-                  }
-                }
-              } else {
-                for (int rk0 = 0; rk0 < sg.ncontrib; rk0 += 4) {
-                  float4 q4[4][4];
-#pragma unroll
-                  for (int u = 0; u < 4; ++u) {
-                    const int rk = rk0 + u < sg.ncontrib ? rk0 + u : rk0;
-                    const float4* src = reinterpret_cast<const float4*>(tile_ws + ((int64_t)rk * kEThreads + t) * TN);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) q4[u][q] = __ldcg(src + q);
-                  }
-#pragma unroll
-                  for (int u = 0; u < 4; ++u) {
-                    if (rk0 + u >= sg.ncontrib) break;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                      v[4 * q] += q4[u][q].x; v[4 * q + 1] += q4[u][q].y;
-                      v[4 * q + 2] += q4[u][q].z; v[4 * q + 3] += q4[u][q].w;
-                    }
+                    v[4 * q] += q4[u][q].x; v[4 * q + 1] += q4[u][q].y;
+                    v[4 * q + 2] += q4[u][q].z; v[4 * q + 3] += q4[u][q].w;
                   }
                 }
               }
-              if (t == 0) p.counters[sg.tile] = 0;
             }
           }
-          if (last) {
-            switch (gp.epi) {
-              case EPI_QKV: epilogue_chunk<EPI_QKV>(e, es, rsc, v, t, n, 0, 0, sg.tile); break;
-              case EPI_RESID: epilogue_chunk<EPI_RESID>(e, es, rsc, v, t, n, 0, 0, sg.tile); break;
-              case EPI_GATEUP: epilogue_chunk<EPI_GATEUP>(e, es, rsc, v, t, n, 0, 0, sg.tile); break;
-              default: epilogue_chunk<EPI_LMHEAD>(e, es, rsc, v, t, n, 0, 0, sg.tile); break;
-            }
-            if (gp.epi == EPI_LMHEAD) {
-              // the last vocabulary tile to finish turns the running argmaxes into drafts
+          switch (gp.epi) {
+            case EPI_QKV: epilogue_chunk<EPI_QKV>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
+            case EPI_RESID: epilogue_chunk<EPI_RESID>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
+            case EPI_GATEUP: epilogue_chunk<EPI_GATEUP>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
+            default: epilogue_chunk<EPI_LMHEAD>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
+          }
+          if (gp.epi == EPI_LMHEAD) {
+            // the last vocabulary tile to finish turns the running argmaxes into drafts
+            __threadfence();
+            epi_sync();
+            if (t == 0) B.flag = atomicAdd(p.amax_counter, 1u) == (unsigned)(tiles - 1);
+            epi_sync();
+            if (B.flag) {
               __threadfence();
-              epi_sync();
-              if (t == 0) B.flag = atomicAdd(p.amax_counter, 1u) == (unsigned)(tiles - 1);
-              epi_sync();
-              if (B.flag) {
-                __threadfence();
-                if (t < p.M && (t % kGamma) > 0) {
-                  const unsigned long long k = __ldcg(p.amax_best + t);
-                  p.drafts[(t / kGamma) * (kGamma - 1) + (t % kGamma) - 1] = argmax_key_index(k);
-                }
+              if (t < p.M && (t % kGamma) > 0) {
+                const unsigned long long k = __ldcg(p.amax_best + t);
+                p.drafts[(t / kGamma) * (kGamma - 1) + (t % kGamma) - 1] = argmax_key_index(k);
               }
             }
           }

@@ -10,6 +10,9 @@
 
 namespace dflash {
 
+// Layers the persistent kernel takes (its per-layer table travels in the kernel parameters).
+constexpr int kPersistMaxL = 32;
+
 struct PersistLayer {
   const __nv_bfloat16* q_norm;
   const __nv_bfloat16* k_norm;
@@ -29,7 +32,7 @@ struct PersistParams {
   const __nv_bfloat16* embed;
   const __nv_bfloat16* norm;
   const float2* inv_pi;
-  const PersistLayer* layers;       // [L], device
+  PersistLayer layers[kPersistMaxL]; // per layer (in the kernel's parameter space)
   const CUtensorMap* maps;          // [4L + 1] weights (qkv, o, gate/up, down per layer; lm_head),
                                     // then [3] activations (xb, attn, act), device, 64-B aligned
   float* x;
@@ -56,8 +59,8 @@ struct PersistParams {
   unsigned* status;
 };
 
-// Tokens (M = 16 * nb) the persistent kernel handles (bf16 lm_head only); larger batches and
-// the FP8 lm_head use the per-projection kernels.
+// Tokens (M = 16 * nb) the persistent kernel handles: one sequence (bf16 lm_head only); larger
+// batches and the FP8 lm_head use the per-projection kernels.
 constexpr int kPersistMaxM = 16;
 
 // Shared memory and split-K workspace the persistent kernel needs; the largest hidden size.
