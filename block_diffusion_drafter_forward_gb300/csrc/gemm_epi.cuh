@@ -208,20 +208,58 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
       } else if (ctx < 0 || ctx + kGamma > p.mpps * kPage) {
         if (t == 0) set_status(p.status, DFLASH_DEV_BAD_CTX);
       } else {
-        // the block's rows fall on at most two pages (ids looked up in epilogue_pre)
-        const int pg0 = q.pg0, pg1 = q.pg1;
+        // the block's rows fall on at most two pages (ids looked up in epilogue_pre); each
+        // thread writes whole 16-byte runs of the page tile layout
         const int head = is_k ? hh - p.nh : hh - p.nh - p.nkv;
+        const bool ok0 = q.pg0 >= 0 && q.pg0 < p.g.num_pages, ok1 = q.pg1 >= 0 && q.pg1 < p.g.num_pages;
+        if (t == 0 && (!ok0 || ((ctx % kPage) && !ok1))) set_status(p.status, DFLASH_DEV_BAD_PAGE);
+        const int64_t base0 = ok0 ? tile_base(p.g, p.layer, q.pg0, is_k ? 0 : 1, head) : -1;
+        const int64_t base1 = ok1 ? tile_base(p.g, p.layer, q.pg1, is_k ? 0 : 1, head) : -1;
+        if (is_k) {
+          // K rows hold 8 consecutive dims per run: gather dims through shared memory
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int li = ctx + c;
-          const int page = (li / kPage == ctx / kPage) ? pg0 : pg1;
-          if (page < 0 || page >= p.g.num_pages) {
-            if (t == 0) set_status(p.status, DFLASH_DEV_BAD_PAGE);
-            continue;
+          for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c];
+          epi_sync();
+          const int c = t >> 3, li = ctx + c;
+          const int64_t base = (li / kPage == ctx / kPage) ? base0 : base1;
+          if (base >= 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int d0 = (2 * (t & 7) + h) * 8;
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(es.xch[d0 + 2 * e][c], es.xch[d0 + 2 * e + 1][c]);
+                pk[e] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              *reinterpret_cast<uint4*>(p.pool + base + k_in_tile(li % kPage, d0, 128)) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
           }
-          const int64_t base = tile_base(p.g, p.layer, page, is_k ? 0 : 1, head);
-          p.pool[base + (is_k ? k_in_tile(li % kPage, t, 128) : v_in_tile(li % kPage, t, 128))] =
-              __float2bfloat16_rn(v[c]);
+          epi_sync();
+        } else if ((ctx & 7) == 0) {
+          // V rows hold 8 consecutive keys per run: this thread's dim, keys 8h .. 8h + 7
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int li = ctx + 8 * h;
+            const int64_t base = (li / kPage == ctx / kPage) ? base0 : base1;
+            if (base < 0) continue;
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * h + 2 * e], v[8 * h + 2 * e + 1]);
+              pk[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(p.pool + base + v_in_tile(li % kPage, t, 128)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int li = ctx + c;
+            const int64_t base = (li / kPage == ctx / kPage) ? base0 : base1;
+            if (base >= 0) p.pool[base + v_in_tile(li % kPage, t, 128)] = __float2bfloat16_rn(v[c]);
+          }
         }
       }
     }
