@@ -52,6 +52,7 @@ constexpr int kAttn = kAP + kAQ + 2 * kAKVStage;
 constexpr int kPartBytes = 128 * TN * 4;                     // one contributor's partial tile
 constexpr int kRedMax = (kAQ + 2 * kAKVStage) / kPartBytes;  // partials that fit at once
 constexpr int kBarOff = kRing + kAttn;
+
 constexpr int kSmemP = kBarOff + 512 + 256 + 1024;
 constexpr uint32_t kAccCols = 32;             // per accumulator buffer (16 used)
 constexpr uint32_t kTS = 128, kTO = 256;      // attention S/P and O columns (128 each)
@@ -566,34 +567,65 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
   tc_fence_before();  // TMEM reads done before the next item's MMAs overwrite S and O
 }
 
-// Merge the split partials of rows 4 rb .. 4 rb + 3 of one unit (a warp per row, loads of 8
-// splits in flight at a time).
-__device__ void combine_item(const PersistParams& p, int layer, int unit, int rb, int t, int ctx0) {
+// Merge the split partials of rows 4 rb .. 4 rb + 3 of one unit (a warp per row, a lane per
+// 4 dims).  Every split's 4 rows of O (2 KB) and (m, l) (32 B) arrive by bulk copy into
+// shared memory in one round trip; the merge then takes the rows' global max first and sums
+// the splits in order.
+constexpr int kCmbBytes = kAQ + 2 * kAKVStage;  // landing buffer: the attention Q + K/V area
+
+__device__ void combine_item(const PersistParams& p, int layer, int unit, int rb, int t, int ctx0, uint8_t* sBuf,
+                             Bars& B, int& red_use) {
   const AItem a = attn_geom(p, layer, unit, 0, ctx0);
   if (!a.run || a.nsplit <= 1) return;
-  const int row = rb * 4 + (t >> 5), d0 = (t & 31) * 4;
+  const int warp = t >> 5, lane = t & 31;
+  const int r0 = rb * 4, row = r0 + warp, d0 = lane * 4;
   const int64_t base = (int64_t)unit * a.splits;
+  const int ns = a.nsplit;
   float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-  for (int q0 = 0; q0 < a.nsplit; q0 += 8) {
-    float2 ml[8];
-    float4 ov[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int q = q0 + u < a.nsplit ? q0 + u : q0;
-      ml[u] = __ldcg(reinterpret_cast<const float2*>(p.ml_part + ((base + q) * 128 + row) * 2));
-      ov[u] = __ldcg(reinterpret_cast<const float4*>(p.o_part + ((base + q) * 128 + row) * 128 + d0));
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (q0 + u >= a.nsplit) break;
-      if (ml[u].x > M) {
-        const float sc = M == -FLT_MAX ? 0.f : exp2f(M - ml[u].x);
-        a0 *= sc; a1 *= sc; a2 *= sc; a3 *= sc; L *= sc;
-        M = ml[u].x;
+  if (ns * (2048 + 32) <= kCmbBytes) {
+    volatile int* ab = &B.abort;
+    if (t == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&B.red_full, ns * (2048 + 32));
+      for (int q = 0; q < ns; ++q) {
+        bulk_load(sBuf + q * 2048, p.o_part + ((base + q) * 128 + r0) * 128, 2048, &B.red_full);
+        bulk_load(sBuf + ns * 2048 + q * 32, p.ml_part + ((base + q) * 128 + r0) * 2, 32, &B.red_full);
       }
-      const float w = ml[u].x == -FLT_MAX ? 0.f : exp2f(ml[u].x - M);
-      a0 += ov[u].x * w; a1 += ov[u].y * w; a2 += ov[u].z * w; a3 += ov[u].w * w;
-      L += ml[u].y * w;
+    }
+    wait_ab(&B.red_full, red_use & 1, ab, p.gabort);
+    ++red_use;
+    const float* so = reinterpret_cast<const float*>(sBuf);
+    const float2* sml = reinterpret_cast<const float2*>(sBuf + ns * 2048);
+    for (int q = 0; q < ns; ++q) M = fmaxf(M, sml[q * 4 + warp].x);
+    for (int q = 0; q < ns; ++q) {
+      const float2 ml = sml[q * 4 + warp];
+      const float w = ml.x == -FLT_MAX ? 0.f : exp2f(ml.x - M);
+      const float4 ov = *reinterpret_cast<const float4*>(so + (q * 4 + warp) * 128 + d0);
+      a0 += ov.x * w; a1 += ov.y * w; a2 += ov.z * w; a3 += ov.w * w;
+      L += ml.y * w;
+    }
+  } else {
+    for (int q0 = 0; q0 < ns; q0 += 8) {
+      float2 ml[8];
+      float4 ov[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int q = q0 + u < ns ? q0 + u : q0;
+        ml[u] = __ldcg(reinterpret_cast<const float2*>(p.ml_part + ((base + q) * 128 + row) * 2));
+        ov[u] = __ldcg(reinterpret_cast<const float4*>(p.o_part + ((base + q) * 128 + row) * 128 + d0));
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (q0 + u >= ns) break;
+        if (ml[u].x > M) {
+          const float sc = M == -FLT_MAX ? 0.f : exp2f(M - ml[u].x);
+          a0 *= sc; a1 *= sc; a2 *= sc; a3 *= sc; L *= sc;
+          M = ml[u].x;
+        }
+        const float w = ml[u].x == -FLT_MAX ? 0.f : exp2f(ml[u].x - M);
+        a0 += ov[u].x * w; a1 += ov[u].y * w; a2 += ov[u].z * w; a3 += ov[u].w * w;
+        L += ml[u].y * w;
+      }
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -611,6 +643,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
   uint8_t* sA = smem + kRing;
+  auto stage = [&](int s) { return ring + s * kStage; };
   uint8_t* sRed = sA + kAP;  // split-K partial landing buffer (the attention Q + K/V area)
   Bars& B = *reinterpret_cast<Bars*>(smem + kBarOff);
   float* rsc = reinterpret_cast<float*>(smem + kBarOff + 512);
@@ -656,12 +689,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         Seg sg;
         while (it.next(sg) && !*ab) {
           for (int kk = 0; kk < sg.nkb; ++kk, ++j) {
-            const int s = j % kS;
-            if (j >= kS && !wait_ab(&B.empty[s], ((j / kS) - 1) & 1, ab, p.gabort)) break;
+            const int s = j % kS, u = j / kS;
+            if (u > 0 && !wait_ab(&B.empty[s], (u - 1) & 1, ab, p.gabort)) break;
             // arm the stage for the weight and the activation tile (the activation producer
             // adds its copy to the same phase, before or after this arrive)
             mbar_arrive_expect_tx(&B.full[s], kStage);
-            tma_load_2d(ring + s * kStage, wm, &B.full[s], (sg.kb0 + kk) * 64, sg.tile * 128, pol);
+            tma_load_2d(stage(s), wm, &B.full[s], (sg.kb0 + kk) * 64, sg.tile * 128, pol);
           }
         }
       }
@@ -685,11 +718,11 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             waited = true;
           }
           for (int kk = 0; kk < sg.nkb && !*ab; ++kk, ++j) {
-            const int s = j % kS;
-            // use j of stage s starts once the MMA released use j - kS; the release of use j
+            const int s = j % kS, u = j / kS;
+            // use u of stage s starts once the MMA released use u - 1; the release of use u
             // needs this copy, so the stage cannot run a phase ahead of it
-            if (j >= kS && !wait_ab(&B.empty[s], ((j / kS) - 1) & 1, ab, p.gabort)) break;
-            tma_load_2d(ring + s * kStage + kAB, xm, &B.full[s], (sg.kb0 + kk) * 64, 0, pol);
+            if (u > 0 && !wait_ab(&B.empty[s], (u - 1) & 1, ab, p.gabort)) break;
+            tma_load_2d(stage(s) + kAB, xm, &B.full[s], (sg.kb0 + kk) * 64, 0, pol);
           }
         }
       }
@@ -711,12 +744,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
           tc_fence_after();
           const uint32_t d = B.tmem + buf * kAccCols;
           for (int kk = 0; kk < sg.nkb; ++kk, ++j) {
-            const int s = j % kS;
-            wait_ab(&B.full[s], (j / kS) & 1, ab, p.gabort);
+            const int s = j % kS, u = j / kS;
+            wait_ab(&B.full[s], u & 1, ab, p.gabort);
             tc_fence_after();
             if (!*ab) {
-              const uint64_t ad = desc_sw128(ring + s * kStage);
-              const uint64_t bd = desc_sw128(ring + s * kStage + kAB);
+              const uint64_t ad = desc_sw128(stage(s));
+              const uint64_t bd = desc_sw128(stage(s) + kAB);
 #pragma unroll
               for (int k = 0; k < 4; ++k) mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || k > 0) ? 1u : 0u);
             }
@@ -753,7 +786,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
               attn_item(p, l, i / splits, i % splits, i == c ? pre : 0, sA, B, use, t);
               epi_sync();
             } else {
-              combine_item(p, l, i / 32, i % 32, t, B.ctx0);
+              combine_item(p, l, i / 32, i % 32, t, B.ctx0, sRed, B, red_use);
+              epi_sync();  // the landing buffer is reused by the next item
             }
           }
         }
