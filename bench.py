@@ -85,8 +85,35 @@ def work_model(cfg, wl, logits: bool):
         "lm_head": (lm_w + M * H * es + (M * V * es if logits else 0), 2 * M * V * H),
         "attention": (kv_read / L + M * nh * hd * es * 2, sum(sum(4 * cfg.gamma * nh * hd * k for k in ks)
                                                                for ks in keys) / L),
+        # the single-launch forward does the whole step's work in one kernel
+        "persistent_forward": (nbytes, flops),
     }
     return nbytes, flops, per_kernel
+
+
+def kernel_sources_sha() -> str:
+    """Hash of the CUDA sources, to tell whether a stored ncu traffic figure still applies."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "block_diffusion_drafter_forward_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on these sources."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh).get(f"{kernel}@{workload}")
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("sources_sha") != kernel_sources_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -396,7 +423,7 @@ def main():
             roof = {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf}
         else:
             roof = {"bound": "hbm", "achieved": bw, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": bw / pk["hbm_gbs"]}
-        roof.update({"kernel": dom, "traffic": None, "peak_source": src,
+        roof.update({"kernel": dom, "traffic": measured_traffic(dom, wl.name), "peak_source": src,
                      "algorithmic_bytes_per_launch": b_per, "launch_us": 1e6 * t_launch})
     t_roof = max(nbytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
 
