@@ -298,27 +298,41 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Pipelined variant for long key ranges (many chunks per CTA).  Warp 4 only streams K/V
-// pages into a 2-stage ring; warps 0-3 run the softmax while the tensor cores work ahead:
-// S of chunk c+1 (second TMEM buffer) is computed during the softmax of chunk c, P is
-// written as bf16 over its own S columns in TMEM and read from there by the P V MMA, and O
-// accumulates in TMEM across chunks.  ~96 KB of shared memory: two CTAs share an SM.  O is rescaled
-// only when a row's running maximum grows by more than 2^8 (probabilities stay <= 256, so
-// fp32 sums are safe), which after the first chunks is rare; the normaliser l uses the
-// same stale maximum, so the result is unchanged.
-constexpr int kPipeStages = 2;
-constexpr int kPipeSmem = kQBytes + kPipeStages * kKVStage + 256 + 1024;
+// Kernel for long key ranges (many chunks per CTA).  Keys go in super-chunks of two 64-key
+// chunks (128 keys): warp 4 streams their K/V pages into three 64 KB buffers (two
+// super-chunks of look-ahead: at full HBM load a page copy takes longer than one softmax
+// pass), warp 5 issues
+// the MMAs, warps 0-3 run the softmax.  While the softmax works on super-chunk i, the tensor
+// cores already compute S of super-chunk i + 1 into the second TMEM buffer.  Per super-chunk:
+// one max pass and one exp pass (ex2.approx) over the 128 scores of a row, P written back as
+// bf16 pairs over its own S columns and read from TMEM by the P V MMA, O accumulated in TMEM
+// and rescaled there only when a row's running max grows.  Loops stay rolled.  225 KB of
+// shared memory and 512 TMEM columns: one CTA per SM.
+constexpr int kScChunks = 2;                                 // chunks per super-chunk
+constexpr int kScBuf = kScChunks * kKVStage;                 // 64 KB of K/V per buffer
+constexpr int kScBufs = 3;                                   // K/V buffers (super-chunks in flight)
+constexpr int kScSmem = kQBytes + kScBufs * kScBuf + 512 + 1024;
+constexpr int kScThreads = 192;
+constexpr int kScWaves = 4;  // work items per SM the split size aims at
 
-__global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p) {
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + kQBytes;
-  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + kPipeStages * kKVStage);
-  uint64_t* kv_empty = kv_full + kPipeStages;
-  uint64_t* s_done = kv_empty + kPipeStages;       // [2]
-  uint64_t* o_done = s_done + 2;                   // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
+  uint8_t* sKV = sQ + kQBytes;  // buffer b at sKV + b * kScBuf: chunk i's K pages, then its V pages
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + kScBufs * kScBuf);
+  uint64_t* kv_empty = kv_full + kScBufs;
+  uint64_t* s_full = kv_empty + kScBufs;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* q_full = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -339,220 +353,258 @@ __global__ void __launch_bounds__(160, 1) attn_tc_pipe_kernel(const AttnParams p
   }
   if (split >= nsplit) return;
   const int c_begin = split * p.chunks_per_split;
-  const int n = min(nch, c_begin + p.chunks_per_split) - c_begin;
+  const int n = min(nch, c_begin + p.chunks_per_split) - c_begin;  // chunks of this CTA
+  const int nsc = (n + kScChunks - 1) / kScChunks;                  // super-chunks
   const int nkeys = ctx + kGamma;
   const int32_t* pt = p.page_tables + (int64_t)s * p.mpps;
   const int npages_seq = (nkeys + kPage - 1) / kPage;
   const int safe_keys = ctx & ~(kPage - 1);
 
   if (t == 0) {
-    for (int i = 0; i < kPipeStages; ++i) {
+    for (int i = 0; i < kScBufs; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_done[i], 1);
-      mbar_init(&o_done[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
     }
+    mbar_init(o_done, 1);
+    mbar_init(q_full, 128);
     flags[0] = 0;
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 256);
+  if (warp == 0) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS[2] = {tmem, tmem + 64}, tO = tmem + 128;
+  const uint32_t tS[2] = {tmem, tmem + 128}, tO = tmem + 256;
+  constexpr uint32_t idesc_s = idesc_bf16(128, kKC);
+  constexpr uint32_t idesc_o = idesc_bf16(128, 128);
   pdl_trigger();
 
   if (warp == 4) {
-    // ---------------- K/V page producer
-    if (lane == 0) {
-      bool waited = false;
-      for (int i = 0; i < n; ++i) {
-        const int st = i % kPipeStages, c = c_begin + i;
-        if (i >= kPipeStages && !mbar_wait_ab(&kv_empty[st], ((i / kPipeStages) - 1) & 1, flags)) {
-          flags[0] = 1;
-          break;
-        }
-        if (!waited && k0 + (c + 1) * kKC > safe_keys) {  // chunk holds block rows
-          pdl_wait();
-          waited = true;
-        }
-        uint8_t* dK = sKV + st * kKVStage;
-        uint8_t* dV = dK + kPagesPerChunk * kTileBytes;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * kPagesPerChunk * kTileBytes);
-        const int pg0 = (k0 + c * kKC) / kPage;
-        int pages[kPagesPerChunk];
-#pragma unroll
-        for (int q = 0; q < kPagesPerChunk; ++q) pages[q] = __ldg(pt + (pg0 + q < npages_seq ? pg0 + q : 0));
-#pragma unroll
-        for (int q = 0; q < kPagesPerChunk; ++q) {
-          int page = pages[q];
-          if (page < 0 || page >= p.g.num_pages) {
-            atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
-            page = 0;
-          }
-          bulk_load(dK + q * kTileBytes, p.pool + tile_base(p.g, p.layer, page, 0, g), kTileBytes, &kv_full[st]);
-          bulk_load(dV + q * kTileBytes, p.pool + tile_base(p.g, p.layer, page, 1, g), kTileBytes, &kv_full[st]);
-        }
+    // ---------------- K/V page producer: lane l < 8 copies page l % 4 of chunk l / 4 of a
+    // super-chunk (its K and V tiles); the page ids of the next super-chunk are fetched while
+    // the warp waits for a free buffer
+    bool waited = false;
+    auto page_of = [&](int i) {
+      const int ci = lane >> 2, q = lane & 3;
+      const int c = c_begin + i * kScChunks + ci;
+      if (lane >= kScChunks * kPagesPerChunk || i >= nsc || c >= c_begin + n) return 0;
+      const int pg = (k0 + c * kKC) / kPage + q;
+      return __ldg(pt + (pg < npages_seq ? pg : 0));
+    };
+    int page = page_of(0);
+    for (int i = 0; i < nsc; ++i) {
+      const int b = i % kScBufs;
+      if (i >= kScBufs && !mbar_wait_ab(&kv_empty[b], ((i / kScBufs) - 1) & 1, flags)) {
+        flags[0] = 1;
+        break;
       }
-      if (!waited) pdl_wait();
+      const int nchk = min(kScChunks, n - i * kScChunks);
+      if (!waited && k0 + (c_begin + i * kScChunks + nchk) * kKC > safe_keys) {  // holds block rows
+        pdl_wait();
+        waited = true;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[b], nchk * kKVStage);
+      __syncwarp();
+      if (lane < nchk * kPagesPerChunk) {
+        int pg = page;
+        if (pg < 0 || pg >= p.g.num_pages) {
+          atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
+          pg = 0;
+        }
+        uint8_t* dK = sKV + b * kScBuf + (lane >> 2) * kKVStage + (lane & 3) * kTileBytes;
+        uint8_t* dV = dK + kPagesPerChunk * kTileBytes;
+        bulk_load(dK, p.pool + tile_base(p.g, p.layer, pg, 0, g), kTileBytes, &kv_full[b]);
+        bulk_load(dV, p.pool + tile_base(p.g, p.layer, pg, 1, g), kTileBytes, &kv_full[b]);
+      }
+      page = page_of(i + 1);
+    }
+    if (!waited) pdl_wait();
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------- MMA issuer (lane 0): S of super-chunk i + 1 goes out before P V of i
+    if (lane == 0) {
+      auto issue_s = [&](int i) {
+        const int b = i & 1, kb = i % kScBufs;
+        const int nchk = min(kScChunks, n - i * kScChunks);
+        if (!mbar_wait_ab(&kv_full[kb], (i / kScBufs) & 1, flags)) flags[0] = 1;
+        tc_fence_after();
+        if (!flags[0]) {
+          for (int ci = 0; ci < nchk; ++ci) {
+            const uint8_t* sK = sKV + kb * kScBuf + ci * kKVStage;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_bf16(tS[b] + ci * kKC, desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048),
+                       idesc_s, k > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&s_full[b]);
+      };
+      if (!mbar_wait_ab(q_full, 0, flags)) flags[0] = 1;
+      tc_fence_after();
+      if (nsc > 0) issue_s(0);
+      for (int i = 0; i < nsc; ++i) {
+        const int b = i & 1, kb = i % kScBufs;
+        const int nchk = min(kScChunks, n - i * kScChunks);
+        if (i + 1 < nsc) issue_s(i + 1);
+        if (!mbar_wait_ab(&p_full[b], (i >> 1) & 1, flags)) flags[0] = 1;
+        tc_fence_after();
+        if (!flags[0]) {
+          for (int kk = 0; kk < nchk * kPagesPerChunk; ++kk) {  // 16 keys = 8 TMEM columns of P each
+            const uint8_t* sV = sKV + kb * kScBuf + (kk / kPagesPerChunk) * kKVStage + kPagesPerChunk * kTileBytes +
+                                (kk % kPagesPerChunk) * kTileBytes;
+            mma_bf16_tmem_a(tO, tS[b] + kk * 8, desc_noswz(sV, 128, 256), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&kv_empty[kb]);
+        mma_commit(o_done);
+      }
     }
     __syncwarp();
   } else {
-    // ---------------- warps 0-3: queries, softmax, MMA issue (thread 0)
+    // ---------------- warps 0-3: queries, softmax, output
     pdl_wait();
     {
       const int hh = t >> 4, r = t & 15;
       const uint4* src =
           reinterpret_cast<const uint4*>(p.q + ((int64_t)(s * kGamma + r) * p.nh + g * group + hh) * 128);
+      uint4 qv[16];
 #pragma unroll
-      for (int d8 = 0; d8 < 16; ++d8)
-        *reinterpret_cast<uint4*>(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16) = src[d8];
+      for (int d8 = 0; d8 < 16; ++d8) qv[d8] = src[d8];
+#pragma unroll
+      for (int d8 = 0; d8 < 16; ++d8) *reinterpret_cast<uint4*>(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16) = qv[d8];
     }
     fence_proxy_async_smem();
-    named_barrier(1, 128);
-    constexpr uint32_t idesc_s = idesc_bf16(128, kKC);
-    constexpr uint32_t idesc_o = idesc_bf16(128, 128);
-    auto issue_s = [&](int i) {  // thread 0: S(i) = Q K(i)^T into tS[i & 1]
-      const int st = i % kPipeStages;
-      if (!mbar_wait_ab(&kv_full[st], (i / kPipeStages) & 1, flags)) flags[0] = 1;
-      tc_fence_after();
-      if (!flags[0]) {
-        const uint8_t* sK = sKV + st * kKVStage;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_bf16(tS[i & 1], desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048), idesc_s,
-                   k > 0 ? 1u : 0u);
-      }
-      mma_commit(&s_done[i & 1]);
-    };
-    if (t == 0) issue_s(0);
+    mbar_arrive(q_full);
     const int r = t & 15;
     const int pos_q = ctx + r;
-    const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    float m_used = -FLT_MAX, l_run = 0.f;
-    for (int i = 0; i < n; ++i) {
-      const int b = i & 1, st = i % kPipeStages;
-      if (!mbar_wait_ab(&s_done[b], (i >> 1) & 1, flags)) flags[0] = 1;
+    const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+    float m_run = -FLT_MAX, l_run = 0.f;
+#pragma unroll 1
+    for (int i = 0; i < nsc; ++i) {
+      const int b = i & 1;
+      const int nchk = min(kScChunks, n - i * kScChunks);
+      if (!mbar_wait_ab(&s_full[b], (i >> 1) & 1, flags)) flags[0] = 1;
       tc_fence_after();
-      const int kbase = k0 + (c_begin + i) * kKC;
+      // every key of the super-chunk visible to every row: no masking
+      const int kb = k0 + (c_begin + i * kScChunks) * kKC;
+      const bool full = kb + nchk * kKC <= nkeys && (p.window <= 0 || ctx + kGamma - 1 - kb < p.window);
       float mc = -FLT_MAX;
-#pragma unroll
-      for (int q4 = 0; q4 < kKC / 32; ++q4) {
+#pragma unroll 1
+      for (int q4 = 0; q4 < 2 * nchk; ++q4) {
         float v[32];
         tmem_ld32(tS[b] + lane_off + q4 * 32, v);
+        if (full) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int key = kbase + q4 * 32 + j;
-          if (key < nkeys && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[j] * scale_log2);
+          for (int j = 0; j < 32; ++j) mc = fmaxf(mc, v[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int key = kb + q4 * 32 + j;
+            if (key < nkeys && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[j]);
+          }
         }
       }
-      // lazy rescale: move the reference maximum only when it grew by more than 2^8
-      float m_new = m_used;
-      if (mc > m_used + 8.f || (m_used == -FLT_MAX && mc > -FLT_MAX)) m_new = mc;
-      // (P of chunk i goes over S[b]; S(i) already overwrote P(i-2) after PV(i-2) in order)
-      // TMEM loads/stores are warp-collective: rescale a warp's rows together (factor 1 for
-      // rows whose reference maximum did not move)
-      const bool rescale = m_new != m_used && m_used != -FLT_MAX && i > 0;
-      if (__any_sync(0xffffffffu, rescale)) {
-        if (!mbar_wait_ab(&o_done[b ^ 1], ((i - 1) >> 1) & 1, flags)) flags[0] = 1;
+      // max(s) * c == max(s * c) for c > 0 (rounding is monotonic)
+      const float m_new = fmaxf(m_run, mc == -FLT_MAX ? -FLT_MAX : mc * scale_log2);
+      const float alpha = m_run == -FLT_MAX ? 1.f : ex2_approx(m_run - m_new);
+      if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O holds super-chunks 0 .. i-1 once the P V of i-1 is done: scale it in TMEM
+        if (!mbar_wait_ab(o_done, (i - 1) & 1, flags)) flags[0] = 1;
         tc_fence_after();
-        const float a = rescale ? exp2f(m_used - m_new) : 1.f;
-#pragma unroll
+#pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           float v[32];
           tmem_ld32(tO + lane_off + q4 * 32, v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= a;
+          for (int j = 0; j < 32; ++j) v[j] *= alpha;
           tmem_st32(tO + lane_off + q4 * 32, v);
         }
-        l_run *= a;
       }
-      m_used = m_new;
+      // P = 2^(s c - m) as bf16 pairs: keys 64 h .. 64 h + 63 into columns 32 h .. 32 h + 31
+      // (over scores already read)
       float lsum = 0.f;
-      uint32_t pw[kKC / 2];
+#pragma unroll 1
+      for (int h = 0; h < nchk; ++h) {
+        uint32_t pk[32];
 #pragma unroll
-      for (int q4 = 0; q4 < kKC / 32; ++q4) {
-        float v[32];
-        tmem_ld32(tS[b] + lane_off + q4 * 32, v);
+        for (int q = 0; q < 2; ++q) {
+          float v[32];
+          tmem_ld32(tS[b] + lane_off + (2 * h + q) * 32, v);
+          if (full) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pr[2];
+            for (int e = 0; e < 16; ++e) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2_approx(fmaf(v[2 * e], scale_log2, -m_new)),
+                                                              ex2_approx(fmaf(v[2 * e + 1], scale_log2, -m_new)));
+              lsum += __low2float(h2) + __high2float(h2);
+              pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+          } else {
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int jj = 2 * e + u;
-            const int key = kbase + q4 * 32 + jj;
-            const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
-            pr[u] = vis ? exp2f(v[jj] * scale_log2 - m_used) : 0.f;
+            for (int e = 0; e < 16; ++e) {
+              float pr[2];
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int key = kb + (2 * h + q) * 32 + 2 * e + u;
+                const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
+                pr[u] = vis ? ex2_approx(fmaf(v[2 * e + u], scale_log2, -m_new)) : 0.f;
+              }
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
+              lsum += __low2float(h2) + __high2float(h2);
+              pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
           }
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
-          lsum += __low2float(h2) + __high2float(h2);
-          pw[q4 * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
+        tmem_st32u(tS[b] + lane_off + h * 32, pk);
       }
-      tmem_st32u(tS[b] + lane_off, pw);  // P(i): 64 bf16 per row in S[b] columns 0..31
-      l_run += lsum;
+      l_run = l_run * alpha + lsum;
+      m_run = m_new;
       tc_fence_before();
-      named_barrier(1, 128);
-      if (t == 0) {
-        tc_fence_after();
-        if (!flags[0]) {
-          const uint8_t* sV = sKV + st * kKVStage + kPagesPerChunk * kTileBytes;
-#pragma unroll
-          for (int k = 0; k < kPagesPerChunk; ++k)  // K = 16 keys = 8 TMEM columns of P each
-            mma_bf16_tmem_a(tO, tS[b] + k * 8, desc_noswz(sV + k * kTileBytes, 128, 256), idesc_o,
-                            (i > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(&o_done[b]);
-        mma_commit(&kv_empty[st]);
-        if (i + 1 < n) issue_s(i + 1);
-      }
+      mbar_arrive(&p_full[b]);
     }
-    if (n > 0 && !mbar_wait_ab(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, flags)) flags[0] = 1;
+    if (nsc > 0 && !mbar_wait_ab(o_done, (nsc - 1) & 1, flags)) flags[0] = 1;
     tc_fence_after();
-    named_barrier(1, 128);
     const int hh = t >> 4;
     __nv_bfloat16* dst = p.out + ((int64_t)(s * kGamma + r) * p.nh + g * group + hh) * 128;
     if (flags[0]) {
       if (t == 0) atomicOr(p.status, DFLASH_DEV_TIMEOUT);
       for (int i = 0; i < 2000; ++i) __nanosleep(1000);
-    } else if (nsplit == 1) {
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float v[32];
-        tmem_ld32(tO + lane_off + q4 * 32, v);
-#pragma unroll
-        for (int d8 = 0; d8 < 4; ++d8) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[d8 * 8 + 2 * e] * inv, v[d8 * 8 + 2 * e + 1] * inv);
-            pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          reinterpret_cast<uint4*>(dst)[q4 * 4 + d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-      }
     } else {
       const int64_t slot = (int64_t)unit * gridDim.y + split;
       float* op = p.o_part + (slot * 128 + t) * 128;
-#pragma unroll
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
         float v[32];
         tmem_ld32(tO + lane_off + q4 * 32, v);
+        if (nsplit == 1) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          __stcg(reinterpret_cast<float4*>(op + q4 * 32 + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+          for (int d8 = 0; d8 < 4; ++d8) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[d8 * 8 + 2 * e] * inv, v[d8 * 8 + 2 * e + 1] * inv);
+              pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            reinterpret_cast<uint4*>(dst)[q4 * 4 + d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            __stcg(reinterpret_cast<float4*>(op + q4 * 32 + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+        }
       }
-      __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_used, l_run));
+      if (nsplit > 1) __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // Merge the split partials of every (sequence, kv head) unit with more than one split, in
@@ -606,9 +658,10 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
 
 }  // namespace
 
-// Partial slots any launch needs: units * splits <= 2 * num_sms + units (splits =
-// ceil(nch / cps) with cps >= units * nch / (2 * num_sms)).
-int64_t attn_tc_partial_slots(int num_sms, int max_units) { return 2 * (int64_t)num_sms + max_units; }
+// Partial slots any launch needs: units * splits <= kScWaves * num_sms + units (splits =
+// ceil(nch / cps) with cps >= units * nch / (kScWaves * num_sms), and fewer for the compact
+// kernel).
+int64_t attn_tc_partial_slots(int num_sms, int max_units) { return kScWaves * (int64_t)num_sms + max_units; }
 
 cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, cudaStream_t st) {
   static bool attr = false;
@@ -627,29 +680,32 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   p.max_ctx = max_ctx_len;
   static bool attr2 = false;
   if (!attr2) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmem);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_sc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScSmem);
     if (e != cudaSuccess) return e;
     attr2 = true;
   }
-  // many chunks per CTA: the pipelined kernel; a few: the compact one (it fits beside a
-  // projection CTA on one SM, so it overlaps the QKV kernel under programmatic launch)
+  // many chunks per CTA: the super-chunk kernel (one CTA per SM); a few: the compact one (it
+  // fits beside a projection CTA on one SM, so it overlaps the QKV kernel under programmatic
+  // launch)
   const bool pipe = cps >= 4;
-  if (pipe) {  // two pipelined CTAs fit on an SM: size the split for 2 x num_sms CTAs
-    cps = std::max(4, (units * nch + 2 * num_sms - 1) / (2 * num_sms));
+  if (pipe) {
+    // one CTA per SM and serial chunks inside a CTA: ~4 waves of short items let the block
+    // scheduler even out ragged context lengths
+    cps = std::max(4, (units * nch + kScWaves * num_sms - 1) / (kScWaves * num_sms));
   }
   const int splits_l = (nch + cps - 1) / cps;
   p.chunks_per_split = cps;
   cudaLaunchConfig_t ac = {};
   ac.gridDim = dim3(units, splits_l);
-  ac.blockDim = dim3(pipe ? 160 : 128);
-  ac.dynamicSmemBytes = pipe ? kPipeSmem : kSmem;
+  ac.blockDim = dim3(pipe ? kScThreads : 128);
+  ac.dynamicSmemBytes = pipe ? kScSmem : kSmem;
   ac.stream = st;
   cudaLaunchAttribute aa[1];
   aa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   aa[0].val.programmaticStreamSerializationAllowed = 1;
   ac.attrs = aa;
   ac.numAttrs = 1;
-  cudaError_t e = pipe ? cudaLaunchKernelEx(&ac, attn_tc_pipe_kernel, p) : cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
+  cudaError_t e = pipe ? cudaLaunchKernelEx(&ac, attn_tc_sc_kernel, p) : cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
   if (e != cudaSuccess || splits_l == 1) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units, 32);
