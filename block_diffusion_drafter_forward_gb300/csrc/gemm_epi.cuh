@@ -15,9 +15,12 @@ namespace {
 
 constexpr int kThreads = 128;
 
-// Barrier over the 128 epilogue threads (warps 0-3) only, so the epilogue also runs inside
-// kernels whose other warps are busy elsewhere (non-aligned named barrier 2).
-__device__ __forceinline__ void epi_sync() { asm volatile("barrier.sync 2, 128;" ::: "memory"); }
+// Barrier over the 128 threads of one epilogue warpgroup (threads 128 g .. 128 g + 127 use
+// named barrier 2 + g), so the epilogue also runs inside kernels whose other warps are busy
+// elsewhere, and several groups can run epilogues side by side (non-aligned form).
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("barrier.sync %0, 128;" ::"r"(2 + (int)(threadIdx.x >> 7)) : "memory");
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -44,8 +44,13 @@ using namespace tc;
 // FP8A: the weight arrives as e4m3 codes (TMA, 64-byte rows) and warps 2-3 widen each
 // stage to the bf16 128-byte-swizzled A tile before the MMA reads it (the per-row scale is
 // applied in the epilogue), so the activations stay bf16 (weight-only FP8).
+// Epilogue warpgroups: wide token tiles hand their 16-token chunks round-robin to 2 or 4
+// groups of 4 warps, so the latency-bound per-chunk epilogues run side by side (warps 4k..4k+3
+// read the same TMEM lanes as warps 0-3).
+__host__ __device__ constexpr int epi_groups(int TN) { return TN >= 128 ? 4 : (TN >= 64 ? 2 : 1); }
+
 template <int EPI, int TN, int STAGES, bool FP8A>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads * epi_groups(TN), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmParams p) {
   constexpr int A_BYTES = 128 * 64 * 2;
@@ -55,7 +60,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t LOAD_BYTES = (FP8A ? A8_BYTES : A_BYTES) + B_BYTES;
   constexpr int W_OFF = FP8A ? A_BYTES + B_BYTES : 0;  // where the TMA puts the weight tile
   constexpr uint32_t TMEM_COLS = TN < 32 ? 32 : TN;
-  static_assert(sizeof(EpiSmem) <= STAGES * STAGE_BYTES, "epilogue scratch must fit in the stages");
+  constexpr int WG = epi_groups(TN);
+  static_assert(WG * sizeof(EpiSmem) <= STAGES * STAGE_BYTES, "epilogue scratch must fit in the stages");
+  static_assert(sizeof(EpiSmem) % 16 == 0, "epilogue scratch alignment");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);  // barriers: 1 KB, then EpiSmem
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(accf);
     }
     __syncwarp();
-  } else if (FP8A) {
+  } else if (FP8A && warp < 4) {
     // ---------------- e4m3 -> bf16 widening (warps 2-3): thread ct owns rows ct, ct + 64
     const int ct = t - 64;
     for (int i = 0; i < nloc; ++i) {
@@ -181,13 +188,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
-  // ---------------- epilogue: all four warps
+  // ---------------- epilogue: every warpgroup (et = row of the tile, wg = its group)
   pdl_wait();
+  const int et = t & (kThreads - 1), wg = t / kThreads;
   // the exchange scratch aliases the drained stages; the row scales (needed while the
   // stages are still filling) sit after the barriers
-  EpiSmem& es = *reinterpret_cast<EpiSmem*>(smem);
+  EpiSmem& es = *reinterpret_cast<EpiSmem*>(smem + wg * sizeof(EpiSmem));
   float* const rsc = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);
-  if (p.ss_in && warp >= 2) {
+  if (p.ss_in && warp >= 2 && warp < 4) {
     // input row scales 1/RMS(x_m) from the producer's per-128-column partials, computed by
     // the warps that are idle during the mainloop
     for (int c = t - 64; c < TN; c += 64) {
@@ -216,14 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2000; ++i) __nanosleep(1000);
   } else {
     const int m0 = tile_m * TN;
-    const int n = tile_n * 128 + t;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const int n = tile_n * 128 + et;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const int64_t tile_lin = (int64_t)tile_n * gridDim.x + tile_m;
     bool last = true;
     if (p.nsplit > 1) {
-      float* mine = p.ws + ((tile_lin * p.nsplit + split) * kThreads + t) * TN;
+      float* mine = p.ws + ((tile_lin * p.nsplit + split) * kThreads + et) * TN;
 #pragma unroll 1
-      for (int c0 = 0; c0 < TN; c0 += 16) {
+      for (int c0 = wg * 16; c0 < TN; c0 += 16 * WG) {
         float v[16];
         tmem_ld16(lane_addr + c0, v);
 #pragma unroll
@@ -239,7 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (last) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < TN; c0 += 16) {
+      for (int c0 = wg * 16; c0 < TN; c0 += 16 * WG) {
+        EpiPre pre;  // inputs first, so their loads overlap the partials' loads
+        epilogue_pre<EPI>(p, pre, et, n, m0, c0, tile_n);
         float v[16];
         if (p.nsplit > 1) {
 #pragma unroll
@@ -248,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float4 q4[4][4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const float* src = p.ws + ((tile_lin * p.nsplit + (s0 + u)) * kThreads + t) * TN + c0;
+              const float* src = p.ws + ((tile_lin * p.nsplit + (s0 + u)) * kThreads + et) * TN + c0;
 #pragma unroll
               for (int c = 0; c < 4; ++c)
                 q4[u][c] = s0 + u < p.nsplit ? __ldcg(reinterpret_cast<const float4*>(src) + c)
@@ -268,9 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           tmem_ld16(lane_addr + c0, v);
         }
-        EpiPre pre;
-        epilogue_pre<EPI>(p, pre, t, n, m0, c0, tile_n);
-        epilogue_chunk<EPI>(p, es, rsc, v, t, n, m0, c0, tile_n, pre);
+        epilogue_chunk<EPI>(p, es, rsc, v, et, n, m0, c0, tile_n, pre);
       }
       if (p.nsplit > 1 && t == 0) p.counters[tile_lin] = 0;
       if constexpr (EPI == EPI_LMHEAD) {
@@ -282,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (flags[1]) {
           // every vocabulary tile of these tokens has folded its best into amax_best
           __threadfence();
-          for (int c = t; c < TN; c += kThreads) {
+          for (int c = t; c < TN; c += kThreads * WG) {
             const int m = m0 + c;
             if (m < p.M) {
               const unsigned long long k = atomicExch(p.amax_best + m, 0ull);  // read and re-arm
@@ -329,7 +337,7 @@ cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPar
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kThreads * epi_groups(TN));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[1];
