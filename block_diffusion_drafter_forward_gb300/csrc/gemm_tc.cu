@@ -44,13 +44,11 @@ using namespace tc;
 // FP8A: the weight arrives as e4m3 codes (TMA, 64-byte rows) and warps 2-3 widen each
 // stage to the bf16 128-byte-swizzled A tile before the MMA reads it (the per-row scale is
 // applied in the epilogue), so the activations stay bf16 (weight-only FP8).
-// Epilogue warpgroups: wide token tiles hand their 16-token chunks round-robin to 2 or 4
-// groups of 4 warps, so the latency-bound per-chunk epilogues run side by side (warps 4k..4k+3
-// read the same TMEM lanes as warps 0-3).
-__host__ __device__ constexpr int epi_groups(int TN) { return TN >= 128 ? 4 : (TN >= 64 ? 2 : 1); }
-
-template <int EPI, int TN, int STAGES, bool FP8A>
-__global__ void __launch_bounds__(kThreads * epi_groups(TN), 1)
+// WG epilogue warpgroups: wide token tiles hand their 16-token chunks round-robin to WG
+// groups of 4 warps, so the latency-bound per-chunk epilogues run side by side (warps
+// 4k..4k+3 read the same TMEM lanes as warps 0-3).  With WG <= 2 two CTAs fit on an SM.
+template <int EPI, int TN, int STAGES, bool FP8A, int WG>
+__global__ void __launch_bounds__(kThreads * WG, WG <= 2 ? 2 : 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmParams p) {
   constexpr int A_BYTES = 128 * 64 * 2;
@@ -60,7 +58,6 @@ __global__ void __launch_bounds__(kThreads * epi_groups(TN), 1)
   constexpr uint32_t LOAD_BYTES = (FP8A ? A8_BYTES : A_BYTES) + B_BYTES;
   constexpr int W_OFF = FP8A ? A_BYTES + B_BYTES : 0;  // where the TMA puts the weight tile
   constexpr uint32_t TMEM_COLS = TN < 32 ? 32 : TN;
-  constexpr int WG = epi_groups(TN);
   static_assert(WG * sizeof(EpiSmem) <= STAGES * STAGE_BYTES, "epilogue scratch must fit in the stages");
   static_assert(sizeof(EpiSmem) % 16 == 0, "epilogue scratch alignment");
   extern __shared__ uint8_t smem_raw[];
@@ -324,11 +321,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int EPI, int TN, int STAGES, bool FP8A>
+template <int EPI, int TN, int STAGES, bool FP8A, int WG>
 cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
                      cudaStream_t st, bool pdl) {
   constexpr int smem = STAGES * (128 * 64 * 2 + TN * 64 * 2 + (FP8A ? 128 * 64 : 0)) + 1024 + 256 + 1024;
-  auto kern = gemm_tc_kernel<EPI, TN, STAGES, FP8A>;
+  auto kern = gemm_tc_kernel<EPI, TN, STAGES, FP8A, WG>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -337,7 +334,7 @@ cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPar
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads * epi_groups(TN));
+  cfg.blockDim = dim3(kThreads * WG);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[1];
@@ -351,12 +348,18 @@ cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPar
 template <int EPI, int TN>
 cudaError_t launch_tn(const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
                       cudaStream_t st, bool pdl, bool fp8a) {
-  // stages: keep two CTAs per SM possible for the skinny shapes
-  constexpr int STAGES = TN <= 32 ? 6 : (TN <= 64 ? 5 : (TN <= 128 ? 4 : 3));
+  // stages: keep two CTAs per SM possible (grids of a little more than one CTA per SM then
+  // overlap instead of running a second, nearly empty wave).  128-token tiles with split-K
+  // partials to reduce take one SM each with 4 epilogue warpgroups instead.
+  constexpr int STAGES = TN <= 32 ? 6 : (TN <= 64 ? 4 : 3);
+  constexpr int WG = TN >= 64 ? 2 : 1;
   if constexpr (EPI == EPI_LMHEAD) {
-    if (fp8a) return launch_t<EPI, TN, STAGES - 1, true>(tw, tx, p, grid, st, pdl);
+    if (fp8a) return launch_t<EPI, TN, STAGES - 1, true, WG>(tw, tx, p, grid, st, pdl);
   }
-  return launch_t<EPI, TN, STAGES, false>(tw, tx, p, grid, st, pdl);
+  if constexpr (TN >= 128) {
+    if (p.nsplit > 1) return launch_t<EPI, TN, 4, false, 4>(tw, tx, p, grid, st, pdl);
+  }
+  return launch_t<EPI, TN, STAGES, false, WG>(tw, tx, p, grid, st, pdl);
 }
 
 template <int EPI>
