@@ -268,7 +268,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
   const int tn = pick_tn(M);
   auto splits = [&](int N, int K) {
     const int tiles = ((N + 127) / 128) * ((M + tn - 1) / tn);
-    return pick_splits(tiles, K / 64, h->num_sms);
+    return pick_splits(tiles, K / 64, h->num_sms, tn);
   };
   GemmParams base;
   base.ws = h->ws;
@@ -548,7 +548,7 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     auto account = [&](int64_t N, int64_t K, int64_t m) {
       const int tn = pick_tn((int)m);
       const int64_t tiles = ((N + 127) / 128) * ((m + tn - 1) / tn);
-      const int ns = pick_splits((int)tiles, (int)(K / 64), h->num_sms);
+      const int ns = pick_splits((int)tiles, (int)(K / 64), h->num_sms, tn);
       if (ns > 1) need = std::max(need, (size_t)(tiles * ns * 128 * tn));
       return tiles <= kCounters - 64;
     };
@@ -675,7 +675,7 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
       const void* tp = static_cast<const char*>(taps) + (int64_t)done * tapd * h->esz;
       auto splits = [&](int64_t N, int64_t K) {
         const int tn = pick_tn(m);
-        return pick_splits((int)(((N + 127) / 128) * ((m + tn - 1) / tn)), (int)(K / 64), h->num_sms);
+        return pick_splits((int)(((N + 127) / 128) * ((m + tn - 1) / tn)), (int)(K / 64), h->num_sms, tn);
       };
       GemmParams pf;
       pf.ws = h->ws;

@@ -398,8 +398,10 @@ int pick_tn(int M) {
   return 128;  // larger batches: several 128-token tiles, consecutive in the grid (weight tile reuse in L2)
 }
 
-int pick_splits(int tiles, int nkb, int num_sms) {
-  int s = (num_sms + tiles - 1) / tiles;  // about one CTA per SM
+int pick_splits(int tiles, int nkb, int num_sms, int tn) {
+  // about one CTA per SM; 128-token tiles that split run one CTA per SM (4 epilogue
+  // warpgroups), so they round down rather than start a second, mostly empty wave
+  int s = tn >= 128 ? num_sms / tiles : (num_sms + tiles - 1) / tiles;
   if (s > nkb) s = nkb;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : s;

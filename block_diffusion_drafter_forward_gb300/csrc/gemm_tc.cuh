@@ -60,7 +60,8 @@ struct GemmParams {
 };
 
 int pick_tn(int M);
-int pick_splits(int tiles, int nkb, int num_sms);
+// Split-K ways for `tiles` output tiles of `nkb` k-blocks with tn-token tiles.
+int pick_splits(int tiles, int nkb, int num_sms, int tn);
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld_elems, int box_rows);
 // D = W [N, K] x X [M, K]^T with the epilogue `epi`; nsplit K-splits (1 for EPI_LMHEAD).
 // w_fp8: W holds e4m3 codes (EPI_LMHEAD only; p.row_scale carries the per-row scales).
