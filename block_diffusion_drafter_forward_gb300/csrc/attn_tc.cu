@@ -386,8 +386,8 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnPar
 
   if (warp == 4) {
     // ---------------- K/V page producer: lane l < 8 copies page l % 4 of chunk l / 4 of a
-    // super-chunk (its K and V tiles); the page ids of the next super-chunk are fetched while
-    // the warp waits for a free buffer
+    // super-chunk (its K and V tiles, into the chunk's K and V regions); the page ids of the
+    // next super-chunk are fetched while the warp waits for a free buffer
     bool waited = false;
     auto page_of = [&](int i) {
       const int ci = lane >> 2, q = lane & 3;

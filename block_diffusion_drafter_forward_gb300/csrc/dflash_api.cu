@@ -501,8 +501,9 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
   // ---- paged pool
   PoolGeom& g = h->geom;
   g.tile = kPage * hd;
-  g.head_stride = g.tile;
-  g.kv_stride = nkv * g.tile;
+  // a head's V tile right after its K tile: one 8 KB run per (layer, page, head)
+  g.kv_stride = g.tile;
+  g.head_stride = 2 * g.tile;
   g.page_stride = 2 * nkv * g.tile;
   g.layer_stride = (int64_t)c.num_pages * g.page_stride;
   g.num_pages = c.num_pages;

@@ -174,7 +174,9 @@ int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t*
 /* Layout of the library-owned K/V pool (for tests and inspection).  *pool = device base,
  * *bytes = size, strides (in ELEMENTS of cfg.dtype) for the tile index
  * [layer][page][kv (0 = K, 1 = V)][kv_head] in strides[0..3]; strides[4] = elements per
- * tile (16 * head_dim); strides[5] = element size in bytes.  Inside a tile of page rows
+ * tile (16 * head_dim); strides[5] = element size in bytes.  A head's V tile directly follows
+ * its K tile (strides[2] == strides[4]), so one page of one head is one contiguous run of
+ * K then V.  Inside a tile of page rows
  * j (0..15) and head dims d (0..hd-1), the element offset is
  *   K tile:  ((j/8) * (hd/8) + d/8) * 64 + (j%8) * 8 + d%8
  *   V tile:  ((d/8) * 2     + j/8) * 64 + (d%8) * 8 + j%8
