@@ -557,18 +557,13 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     for (int64_t m = kGamma; m <= R; m += kGamma)
       fits = account(qkvd, H, m) && account(H, qd, m) && account(2 * F, H, m) && account(H, F, m) && fits;
     for (int64_t m = 1; m <= Rw; m = m < 256 ? m + 1 : m + 256)
-      fits = account(H, tapd, m) && account(L * 2 * kvd, 2 * H, m) && fits;
-    fits = account(H, tapd, Rw) && account(L * 2 * kvd, 2 * H, Rw) && fits;
+      fits = account(H, tapd, m) && account(L * 2 * kvd, H, m) && fits;
+    fits = account(H, tapd, Rw) && account(L * 2 * kvd, H, Rw) && fits;
     if (!fits || tapd % 64) {
       fail(h, DFLASH_EUNSUPPORTED, "GEMM tiling out of range (too many tiles or n_taps*target_hidden % 64 != 0)");
       return bail(DFLASH_EUNSUPPORTED);
     }
     ALLOC(h->wf2, Rw * 2 * H * es);
-    ALLOC(h->w_ctxkv2, L * 2 * kvd * 2 * H * es);
-    if (launch_repeat_cols(h->w_ctxkv, (int)(L * 2 * kvd), (int)H, h->w_ctxkv2, st) != cudaSuccess) {
-      fail(h, DFLASH_ECUDA, "repeat context-K/V weight");
-      return bail(DFLASH_ECUDA);
-    }
     h->tc_attn = (nh / nkv) == 8;
     // single-launch persistent forward for batch 1: needs the tensor-core attention, a bf16
     // lm_head and one resident CTA per SM
@@ -669,8 +664,9 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
   const int64_t H = c.hidden, tapd = (int64_t)c.n_taps * c.target_hidden;
   const int kvall = c.n_layers * 2 * c.n_kv_heads * c.head_dim;
   if (h->tc) {
-    // tensor-core writer: fc GEMM -> hidden_norm (fp32) -> [hi | lo] bf16 -> one GEMM over
-    // [W | W] for every layer's K and V with the k_norm / RoPE / scatter epilogue
+    // tensor-core writer: fc GEMM -> hidden_norm (fp32) -> [hi | lo] bf16 -> one GEMM for every
+    // layer's K and V (each weight tile times both halves) with the k_norm / RoPE / scatter
+    // epilogue
     for (int32_t done = 0; done < n; done += c.max_write_rows) {
       const int m = std::min<int32_t>(c.max_write_rows, n - done);
       const void* tp = static_cast<const char*>(taps) + (int64_t)done * tapd * h->esz;
@@ -702,8 +698,8 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
       pk.first = first + done;
       pk.g = h->geom;
       pk.pool = static_cast<__nv_bfloat16*>(h->pool);
-      KL(K_W_KV, launch_gemm_tc(EPI_CTXKV, h->w_ctxkv2, kvall, (int)(2 * H), h->wf2, (int)(2 * H), m, pk,
-                                splits(kvall, 2 * H), st, false),
+      KL(K_W_KV, launch_gemm_tc(EPI_CTXKV, h->w_ctxkv, kvall, (int)H, h->wf2, (int)(2 * H), m, pk,
+                                splits(kvall, H), st, false),
          "writer kv");
     }
     return DFLASH_OK;

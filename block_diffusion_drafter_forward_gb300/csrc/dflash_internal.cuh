@@ -138,7 +138,6 @@ struct dflash_handle {
   float* wy = nullptr;                 // [Rw, max(H, L*2*kv)] fp32
   float* wf = nullptr;                 // [Rw, H] ctx features (fp32)
   void* wf2 = nullptr;                 // [Rw, 2H] ctx features as bf16 [hi | lo] (tensor-core writer)
-  void* w_ctxkv2 = nullptr;            // [L * 2 * kv, 2H] fused context-K/V weight repeated [W | W]
 
   // tensor-core (bf16) path scratch
   void* xb = nullptr;                  // [rows, H] bf16 copy of the residual stream
@@ -200,7 +199,6 @@ cudaError_t launch_ctxkv_post(const dflash_handle* h, const float* ykv, int n, c
                               const int32_t* page_table, int first, cudaStream_t st);
 cudaError_t launch_embed_tc(const dflash_handle* h, const int32_t* bonus, int nb, cudaStream_t st);
 cudaError_t launch_split_hi_lo(const float* x, int rows, int n, void* out, cudaStream_t st);
-cudaError_t launch_repeat_cols(const void* w, int rows, int cols, void* out, cudaStream_t st);
 cudaError_t launch_fold_norm(const void* A, const void* B, int mode, int rows, int cols, const void* ln, void* out,
                              cudaStream_t st);
 cudaError_t launch_quantize_fp8(const void* w, int rows, int cols, int dtype, uint8_t* codes,

@@ -41,6 +41,9 @@ namespace {
 
 using namespace tc;
 
+// EPI_CTXKV (the context-K/V writer) takes its fp32 activations as a bf16 pair: X holds
+// [hi | lo] along K (ldx = 2K) and every weight tile is multiplied by both halves into the
+// same accumulator, so the weight is read once while the product keeps the fp32 operand.
 // FP8A: the weight arrives as e4m3 codes (TMA, 64-byte rows) and warps 2-3 widen each
 // stage to the bf16 128-byte-swizzled A tile before the MMA reads it (the per-row scale is
 // applied in the epilogue), so the activations stay bf16 (weight-only FP8).
@@ -54,8 +57,10 @@ __global__ void __launch_bounds__(kThreads * WG, WG <= 2 ? 2 : 1)
   constexpr int A_BYTES = 128 * 64 * 2;
   constexpr int B_BYTES = TN * 64 * 2;
   constexpr int A8_BYTES = FP8A ? 128 * 64 : 0;
-  constexpr int STAGE_BYTES = A_BYTES + B_BYTES + A8_BYTES;
-  constexpr uint32_t LOAD_BYTES = (FP8A ? A8_BYTES : A_BYTES) + B_BYTES;
+  constexpr bool HILO = EPI == EPI_CTXKV;
+  constexpr int NB = HILO ? 2 : 1;  // activation tiles per stage
+  constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES + A8_BYTES;
+  constexpr uint32_t LOAD_BYTES = (FP8A ? A8_BYTES : A_BYTES) + NB * B_BYTES;
   constexpr int W_OFF = FP8A ? A_BYTES + B_BYTES : 0;  // where the TMA puts the weight tile
   constexpr uint32_t TMEM_COLS = TN < 32 ? 32 : TN;
   static_assert(WG * sizeof(EpiSmem) <= STAGES * STAGE_BYTES, "epilogue scratch must fit in the stages");
@@ -105,8 +110,12 @@ __global__ void __launch_bounds__(kThreads * WG, WG <= 2 ? 2 : 1)
         tma_load_2d(smem + i * STAGE_BYTES + W_OFF, &tmW, &full[i], (kb0 + i) * 64, tile_n * 128, pol_w);
       }
       pdl_wait();  // everything the previous kernel wrote is visible from here on
-      for (int i = 0; i < pre; ++i)
+      for (int i = 0; i < pre; ++i) {
         tma_load_2d(smem + i * STAGE_BYTES + A_BYTES, &tmX, &full[i], (kb0 + i) * 64, tile_m * TN, pol_x);
+        if constexpr (HILO)
+          tma_load_2d(smem + i * STAGE_BYTES + A_BYTES + B_BYTES, &tmX, &full[i], p.K + (kb0 + i) * 64, tile_m * TN,
+                      pol_x);
+      }
       for (int i = pre; i < nloc; ++i) {
         const int s = i % STAGES;
         if (!mbar_wait(&empty[s], ((i / STAGES) - 1) & 1)) {
@@ -116,6 +125,9 @@ __global__ void __launch_bounds__(kThreads * WG, WG <= 2 ? 2 : 1)
         mbar_arrive_expect_tx(&full[s], LOAD_BYTES);
         tma_load_2d(smem + s * STAGE_BYTES + W_OFF, &tmW, &full[s], (kb0 + i) * 64, tile_n * 128, pol_w);
         tma_load_2d(smem + s * STAGE_BYTES + A_BYTES, &tmX, &full[s], (kb0 + i) * 64, tile_m * TN, pol_x);
+        if constexpr (HILO)
+          tma_load_2d(smem + s * STAGE_BYTES + A_BYTES + B_BYTES, &tmX, &full[s], p.K + (kb0 + i) * 64, tile_m * TN,
+                      pol_x);
       }
     }
     __syncwarp();
@@ -134,6 +146,11 @@ __global__ void __launch_bounds__(kThreads * WG, WG <= 2 ? 2 : 1)
         const uint64_t bd = desc_sw128(smem + s * STAGE_BYTES + A_BYTES);
 #pragma unroll
         for (int k = 0; k < 4; ++k) mma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (i > 0 || k > 0) ? 1u : 0u);
+        if constexpr (HILO) {
+          const uint64_t bl = desc_sw128(smem + s * STAGE_BYTES + A_BYTES + B_BYTES);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_bf16(tmem, ad + 2 * k, bl + 2 * k, idesc, 1u);
+        }
         mma_commit(&empty[s]);
       }
       mma_commit(accf);
@@ -324,7 +341,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 template <int EPI, int TN, int STAGES, bool FP8A, int WG>
 cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
                      cudaStream_t st, bool pdl) {
-  constexpr int smem = STAGES * (128 * 64 * 2 + TN * 64 * 2 + (FP8A ? 128 * 64 : 0)) + 1024 + 256 + 1024;
+  constexpr int smem =
+      STAGES * (128 * 64 * 2 + (EPI == EPI_CTXKV ? 2 : 1) * TN * 64 * 2 + (FP8A ? 128 * 64 : 0)) + 1024 + 256 + 1024;
   auto kern = gemm_tc_kernel<EPI, TN, STAGES, FP8A, WG>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -355,6 +373,14 @@ cudaError_t launch_tn(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPa
   constexpr int WG = TN >= 64 ? 2 : 1;
   if constexpr (EPI == EPI_LMHEAD) {
     if (fp8a) return launch_t<EPI, TN, STAGES - 1, true, WG>(tw, tx, p, grid, st, pdl);
+  }
+  if constexpr (EPI == EPI_CTXKV) {  // two activation tiles per stage
+    if constexpr (TN >= 128) {  // compute-heavy: two CTAs per SM rather than a deep ring
+      if (p.nsplit > 1) return launch_t<EPI, TN, 4, false, 4>(tw, tx, p, grid, st, pdl);
+      return launch_t<EPI, TN, 2, false, 2>(tw, tx, p, grid, st, pdl);
+    }
+    if constexpr (TN == 64) return launch_t<EPI, TN, 3, false, 2>(tw, tx, p, grid, st, pdl);
+    return launch_t<EPI, TN, 5, false, 1>(tw, tx, p, grid, st, pdl);
   }
   if constexpr (TN >= 128) {
     if (p.nsplit > 1) return launch_t<EPI, TN, 4, false, 4>(tw, tx, p, grid, st, pdl);
@@ -426,7 +452,7 @@ cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, 
   CUtensorMap tw, tx;
   if (w_fp8 && epi != EPI_LMHEAD) return cudaErrorInvalidValue;
   if (w_fp8 ? !make_tmap_u8(&tw, W, N, K) : !make_tmap_bf16(&tw, W, N, K, K, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tx, X, M, K, ldx, TN)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tx, X, M, epi == EPI_CTXKV ? 2 * (int64_t)K : K, ldx, TN)) return cudaErrorInvalidValue;
   p.N = N;
   p.K = K;
   p.M = M;

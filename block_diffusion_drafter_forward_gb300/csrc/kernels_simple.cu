@@ -403,8 +403,8 @@ __global__ void fold_norm_kernel(const __nv_bfloat16* __restrict__ A, const __nv
     out[(int64_t)p * cols + k] = ln ? __float2bfloat16_rn(__bfloat162float(src[k]) * __bfloat162float(ln[k])) : src[k];
 }
 
-// x (fp32) -> [hi | lo] bf16 with hi = bf16(x), lo = bf16(x - hi): a GEMM over the doubled
-// K with the weight repeated ([W | W]) then sees x to ~16 mantissa bits.
+// x (fp32) -> [hi | lo] bf16 with hi = bf16(x), lo = bf16(x - hi): a GEMM that multiplies
+// every weight tile by both halves into one accumulator then sees x to ~16 mantissa bits.
 __global__ void split_hi_lo_kernel(const float* __restrict__ x, int n, __nv_bfloat16* __restrict__ out) {
   const float* xr = x + (int64_t)blockIdx.x * n;
   __nv_bfloat16* o = out + (int64_t)blockIdx.x * 2 * n;
@@ -416,26 +416,11 @@ __global__ void split_hi_lo_kernel(const float* __restrict__ x, int n, __nv_bflo
   }
 }
 
-// out[r] = [w[r] | w[r]] (rows x 2 cols), bf16
-__global__ void repeat_cols_kernel(const __nv_bfloat16* __restrict__ w, int cols, __nv_bfloat16* __restrict__ out) {
-  const __nv_bfloat16* src = w + (int64_t)blockIdx.x * cols;
-  __nv_bfloat16* dst = out + (int64_t)blockIdx.x * 2 * cols;
-  for (int k = threadIdx.x; k < cols; k += blockDim.x) {
-    dst[k] = src[k];
-    dst[cols + k] = src[k];
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_split_hi_lo(const float* x, int rows, int n, void* out, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   split_hi_lo_kernel<<<rows, 256, 0, st>>>(x, n, static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_repeat_cols(const void* w, int rows, int cols, void* out, cudaStream_t st) {
-  repeat_cols_kernel<<<rows, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w), cols, static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }
 
