@@ -367,7 +367,7 @@ template <int EPI, int TN>
 cudaError_t launch_tn(const CUtensorMap& tw, const CUtensorMap& tx, const GemmParams& p, dim3 grid,
                       cudaStream_t st, bool pdl, bool fp8a) {
   // stages: keep two CTAs per SM possible (grids of a little more than one CTA per SM then
-  // overlap instead of running a second, nearly empty wave).  128-token tiles with split-K
+  // overlap instead of running a second, nearly empty wave).  Wide tiles with split-K
   // partials to reduce take one SM each with 4 epilogue warpgroups instead.
   constexpr int STAGES = TN <= 32 ? 6 : (TN <= 64 ? 4 : 3);
   constexpr int WG = TN >= 64 ? 2 : 1;
@@ -382,8 +382,8 @@ cudaError_t launch_tn(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPa
     if constexpr (TN == 64) return launch_t<EPI, TN, 3, false, 2>(tw, tx, p, grid, st, pdl);
     return launch_t<EPI, TN, 5, false, 1>(tw, tx, p, grid, st, pdl);
   }
-  if constexpr (TN >= 128) {
-    if (p.nsplit > 1) return launch_t<EPI, TN, 4, false, 4>(tw, tx, p, grid, st, pdl);
+  if constexpr (TN >= 64) {  // split tiles: one CTA per SM, 4 warpgroups, a deep ring
+    if (p.nsplit > 1) return launch_t<EPI, TN, TN >= 128 ? 4 : 8, false, 4>(tw, tx, p, grid, st, pdl);
   }
   return launch_t<EPI, TN, STAGES, false, WG>(tw, tx, p, grid, st, pdl);
 }
@@ -425,9 +425,9 @@ int pick_tn(int M) {
 }
 
 int pick_splits(int tiles, int nkb, int num_sms, int tn) {
-  // about one CTA per SM; 128-token tiles that split run one CTA per SM (4 epilogue
-  // warpgroups), so they round down rather than start a second, mostly empty wave
-  int s = tn >= 128 ? num_sms / tiles : (num_sms + tiles - 1) / tiles;
+  // about one CTA per SM; wide tiles that split run one CTA per SM (4 epilogue warpgroups),
+  // so they round down rather than start a second, mostly empty wave
+  int s = tn >= 64 ? num_sms / tiles : (num_sms + tiles - 1) / tiles;
   if (s > nkb) s = nkb;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : s;
