@@ -91,15 +91,25 @@ def work_model(cfg, wl, logits: bool):
     return nbytes, flops, per_kernel
 
 
-def kernel_sources_sha() -> str:
-    """Hash of the CUDA sources, to tell whether a stored ncu traffic figure still applies."""
+# The sources that define each measured kernel (its own file and every header it includes).
+KERNEL_SOURCES = {
+    "persistent_forward": ("persist_tc.cu", "persist_tc.cuh", "gemm_epi.cuh", "gemm_tc.cuh", "tc_common.cuh",
+                           "dflash_internal.cuh"),
+}
+
+
+def kernel_sources_sha(kernel: str = "persistent_forward", read=None) -> str:
+    """Hash of the sources of `kernel`, to tell whether a stored ncu traffic figure still
+    applies.  `read(name) -> bytes` overrides how a file under csrc/ is read."""
     import hashlib
-    h = hashlib.sha256()
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "block_diffusion_drafter_forward_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                return fh.read()
+    h = hashlib.sha256()
+    for f in sorted(KERNEL_SOURCES.get(kernel, ())):
+        h.update(f.encode() + read(f))
     return h.hexdigest()[:16]
 
 
@@ -111,7 +121,7 @@ def measured_traffic(kernel: str, workload: str):
             rec = json.load(fh).get(f"{kernel}@{workload}")
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("sources_sha") != kernel_sources_sha():
+    if not rec or kernel not in KERNEL_SOURCES or rec.get("sources_sha") != kernel_sources_sha(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 

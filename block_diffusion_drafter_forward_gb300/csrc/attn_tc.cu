@@ -687,8 +687,8 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   // many chunks per CTA: the super-chunk kernel (one CTA per SM); a few: the compact one (it
   // fits beside a projection CTA on one SM, so it overlaps the QKV kernel under programmatic
   // launch)
-  const bool pipe = cps >= 4;
-  if (pipe) {
+  const bool sc = cps >= 4;
+  if (sc) {
     // one CTA per SM and serial chunks inside a CTA: ~4 waves of short items let the block
     // scheduler even out ragged context lengths
     cps = std::max(4, (units * nch + kScWaves * num_sms - 1) / (kScWaves * num_sms));
@@ -697,15 +697,15 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   p.chunks_per_split = cps;
   cudaLaunchConfig_t ac = {};
   ac.gridDim = dim3(units, splits_l);
-  ac.blockDim = dim3(pipe ? kScThreads : 128);
-  ac.dynamicSmemBytes = pipe ? kScSmem : kSmem;
+  ac.blockDim = dim3(sc ? kScThreads : 128);
+  ac.dynamicSmemBytes = sc ? kScSmem : kSmem;
   ac.stream = st;
   cudaLaunchAttribute aa[1];
   aa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   aa[0].val.programmaticStreamSerializationAllowed = 1;
   ac.attrs = aa;
   ac.numAttrs = 1;
-  cudaError_t e = pipe ? cudaLaunchKernelEx(&ac, attn_tc_sc_kernel, p) : cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
+  cudaError_t e = sc ? cudaLaunchKernelEx(&ac, attn_tc_sc_kernel, p) : cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
   if (e != cudaSuccess || splits_l == 1) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units, 32);

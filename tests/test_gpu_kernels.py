@@ -40,7 +40,7 @@ def test_gemm_bf16_matches_exact_product(N, K, M):
 
 @pytest.mark.parametrize("cfgname,ctx", [("qwen3_8l_bf16", [4096]), ("qwen3_8l_bf16", [0, 17, 300, 129]),
                                          ("wide_5l_yarn_bf16", [3000]),
-                                         # long ranges: the pipelined kernel (>= 4 chunks per CTA)
+                                         # long ranges: the super-chunk kernel (>= 4 chunks per CTA)
                                          ("qwen3_8l_bf16", [8000, 7000, 6100, 5000, 3000, 8100, 100, 7777]),
                                          ("wide_5l_yarn_bf16", [6000, 5000, 9000, 4000])])
 def test_tensor_core_attention_matches_cuda_core(cfgname, ctx):
