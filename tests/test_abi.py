@@ -86,3 +86,6 @@ def test_calls_on_null_handle(lib):
     assert lib.dflash_write_ctx_kv(None, None, None, None, 0, 0, None) == -1
     assert lib.dflash_destroy(None) == 0
     assert lib.dflash_kv_layout(None, None, None, None) == -1
+    assert lib.dflash_set_persistent(None, 1) == -1
+    assert lib.dflash_set_persistent(None, 0) == -1
+    assert lib.dflash_persistent(None) == 0

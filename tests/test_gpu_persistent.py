@@ -122,3 +122,25 @@ def test_persistent_hidden_only_outputs():
     d_only, _, _ = rig.propose(logits=False, hidden=False)
     assert torch.equal(d_full, d_only)
     assert np.all(d_only.cpu().numpy() >= 0)
+
+
+def test_graph_replay_reads_new_inputs():
+    # dflash_propose replays a captured graph for the same buffers: new values written into the
+    # same bonus-token buffer must be used (on both launch shapes)
+    wl = make_workload(CONFIGS["qwen3_8l_bf16"], 70, [500])
+    rig = Rig(wl)
+    g, V = rig.cfg.gamma, rig.cfg.vocab
+    drafts = torch.empty((1, g - 1), dtype=torch.int32, device="cuda")
+    z = torch.empty((g, V), dtype=torch.bfloat16, device="cuda")
+    h = torch.empty((g, rig.cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    first = int(wl.bonus[0])
+    for persistent in (True, False):
+        rig.drafter.set_persistent(persistent)
+        for bonus in (first, (first + 12345) % V, first):
+            wl.bonus[0] = bonus
+            rig.bonus.fill_(bonus)
+            rig.drafter.propose(rig.bonus, rig.ctx_lens, rig.page_tables, wl.max_ctx_len, drafts=drafts, logits=z,
+                                hidden=h)
+            torch.cuda.synchronize()
+            assert rig.drafter.device_status() == 0
+            _check_vs_oracle(rig, drafts, z, h)
