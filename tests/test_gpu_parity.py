@@ -63,31 +63,43 @@ def test_tiny_fp32_ragged_batch_with_empty_context():
     run_and_check(wl)
 
 
-def test_tiny_fp32_slot_writeback_exact():
+@pytest.mark.parametrize("cfg_name,ctxs,sentinel", [
+    ("tiny_fp32", [37, 50], -12345.0),
+    ("qwen3_8l_bf16", [37, 50], -12288.0),   # per-projection kernels, 4 kv heads
+    ("qwen3_8l_bf16", [93], -12288.0),       # single-launch forward
+])
+def test_slot_writeback_exact(cfg_name, ctxs, sentinel):
     """A sentinel-filled pool: the writer changes exactly the slots of rows 0..c-1 and
-    propose exactly the slots c..c+15, layer by layer (integer placement, bit-exact)."""
-    wl = make_workload(CONFIGS["tiny_fp32"], 12, [37, 50])
+    propose exactly the slots c..c+15, layer by layer (integer placement, bit-exact).
+    The sentinel is exact in the pool's dtype."""
+    wl = make_workload(CONFIGS[cfg_name], 12, ctxs)
     rig = Rig(wl, write=False)
     pool = pool_view(rig.drafter)
-    pool.fill_(-12345.0)
+    pool.fill_(sentinel)
     rig.write_all(chunk=20)
     _, _, st = rig.drafter.kv_layout()
-    tile = st[4]
-    hd = wl.cfg.head_dim
-    changed = (pool != -12345.0).view(wl.cfg.n_layers, wl.num_pages, 2, wl.cfg.n_kv_heads, 16, hd)
-    # K tile element (j, d) -> row j; V tile (j, d) -> row j via the documented layouts
-    expect = torch.zeros((wl.num_pages, 16), dtype=torch.bool)
+    hd, L, P, nkv = wl.cfg.head_dim, wl.cfg.n_layers, wl.num_pages, wl.cfg.n_kv_heads
+    # every tile's base through the published strides (any tile order), then the documented
+    # in-tile layouts: K tile element (j, d) -> row j; V tile (j, d) -> row j
+    idx = torch.arange
+    base = (idx(L)[:, None, None, None] * st[0] + idx(P)[None, :, None, None] * st[1]
+            + idx(2)[None, None, :, None] * st[2] + idx(nkv)[None, None, None, :] * st[3]).cuda()
+    j = torch.arange(16)[:, None]
+    d = torch.arange(hd)[None, :]
+    kinner = (((j // 8) * (hd // 8) + d // 8) * 64 + (j % 8) * 8 + d % 8).cuda()
+    vinner = (((d // 8) * 2 + j // 8) * 64 + (d % 8) * 8 + j % 8).cuda()
+
+    def changed_rows():
+        # [L, P, nkv, 16, hd] booleans for the K tiles and the V tiles
+        ch = (pool != sentinel)
+        return (ch[base[:, :, 0, :, None, None] + kinner[None, None, None]],
+                ch[base[:, :, 1, :, None, None] + vinner[None, None, None]])
+
+    expect = torch.zeros((P, 16), dtype=torch.bool)
     for s in range(wl.nb):
         sl = page_slots(wl.page_tables[s], 0, int(wl.ctx_lens[s]))
         expect[sl // 16, sl % 16] = True
-    del tile
-    flat = changed.view(wl.cfg.n_layers, wl.num_pages, 2, wl.cfg.n_kv_heads, 16 * hd)
-    j = torch.arange(16)[:, None]
-    d = torch.arange(hd)[None, :]
-    kinner = (((j // 8) * (hd // 8) + d // 8) * 64 + (j % 8) * 8 + d % 8).reshape(-1)
-    vinner = (((d // 8) * 2 + j // 8) * 64 + (d % 8) * 8 + j % 8).reshape(-1)
-    kk = flat[:, :, 0][..., kinner.cuda()].view(wl.cfg.n_layers, wl.num_pages, wl.cfg.n_kv_heads, 16, hd)
-    vv = flat[:, :, 1][..., vinner.cuda()].view(wl.cfg.n_layers, wl.num_pages, wl.cfg.n_kv_heads, 16, hd)
+    kk, vv = changed_rows()
     e = expect.cuda()[None, :, None, :, None].expand_as(kk)
     assert torch.equal(kk, e) and torch.equal(vv, e)
     # propose adds the transient block rows c..c+15
@@ -96,9 +108,9 @@ def test_tiny_fp32_slot_writeback_exact():
         c = int(wl.ctx_lens[s])
         sl = page_slots(wl.page_tables[s], c, 16)
         expect[sl // 16, sl % 16] = True
-    changed = (pool != -12345.0).view(wl.cfg.n_layers, wl.num_pages, 2, wl.cfg.n_kv_heads, 16 * hd)
-    kk = changed[:, :, 0][..., kinner.cuda()].view(wl.cfg.n_layers, wl.num_pages, wl.cfg.n_kv_heads, 16, hd)
-    assert torch.equal(kk, expect.cuda()[None, :, None, :, None].expand_as(kk))
+    kk, vv = changed_rows()
+    e = expect.cuda()[None, :, None, :, None].expand_as(kk)
+    assert torch.equal(kk, e) and torch.equal(vv, e)
 
 
 def test_tiny_fp32_writer_chunking_is_bit_exact():
