@@ -191,7 +191,10 @@ int check_cfg(const dflash_cfg& c) {
 }
 
 // The bf16 gamma-block forward of one sequence as ONE persistent kernel (persist_tc.cu):
-// same arithmetic as propose_tc's per-projection kernels, no launch or grid-drain gaps
+// memra-engine dflash.rs forward_round (every layer: QKV with q/k RMSNorm and RoPE, the
+// block's K/V into its pool slots, non-causal GQA attention over context + block, o_proj,
+// SiLU-gated MLP) + final norm + lm_head + the draft step's argmax over rows 1..15; the same
+// arithmetic as propose_tc's per-projection kernels, without launch or grid-drain gaps
 // between the projections.
 int propose_persist(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens,
                     const int32_t* page_tables, int nb, int max_ctx_len, int32_t* draft_tokens, void* logits,
