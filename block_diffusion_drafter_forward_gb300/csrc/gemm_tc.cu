@@ -2,13 +2,14 @@
 // with the drafter's per-projection epilogues fused in.
 //
 // Orientation ("swap AB"): the weight W [N, K] is the A operand, so 128 weight rows fill
-// the UMMA M = 128 dimension, and the TN (16..256) token rows of the activation X [M, K]
+// the UMMA M = 128 dimension, and the TN (16..128) token rows of the activation X [M, K]
 // are the N dimension.  The accumulator tile D[n, m] sits in TMEM, one weight row per
 // TMEM lane.  Tiles are staged by TMA (128-byte swizzle) through an mbarrier ring;
 // weights are requested before the programmatic-dependent-launch wait, so a kernel
 // streams its weights while its predecessor in the stream is still finishing.
 // Split-K: each split writes fp32 partials, the last split of a tile (atomic counter)
-// sums them in split order (deterministic) and runs the epilogue.
+// sums them in split order (deterministic) and runs the epilogue.  Wide token tiles run the
+// epilogue's 16-token chunks on 2 or 4 warpgroups side by side.
 //
 // Epilogues (memra-engine `dflash.rs` forward_round; spark_model `dflash_head` pages):
 //   EPI_STORE : out[m, n] = r_m * D                       (plain projection, fp32 out)
@@ -19,11 +20,13 @@
 //   EPI_RESID : x[m, n] += D (o_proj / down_proj residual), bf16(x * ln_next) as the next
 //               projection's operand, per-tile partial sums of x^2 for the next RMSNorm.
 //   EPI_GATEUP: tile = 64 gate rows + 64 up rows; act = silu(r_m g) * (r_m u).
-//   EPI_LMHEAD: logits (optional, bf16), per-row fp32 scale for the FP8 head, per-tile
-//               argmax partials and, in the last tile, the per-row argmax -> drafts.
+//   EPI_LMHEAD: logits (optional, bf16), per-row fp32 scale for the FP8 head, each tile's
+//               per-token best (logit, index) folded in with a 64-bit atomicMax; the last
+//               tile turns them into drafts.
 //   EPI_CTXKV : context-K/V writer (dflash.rs ingest_ctx): tile = one head of one layer's
 //               K or V; K gets k_norm, RoPE at the row's position and mscale; both are
-//               scattered to the row's paged slot.
+//               scattered to the row's paged slot.  The fp32 operand comes as bf16 hi + lo
+//               (see below).
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -396,7 +399,6 @@ cudaError_t launch_epi(int TN, const CUtensorMap& tw, const CUtensorMap& tx, con
     case 32: return launch_tn<EPI, 32>(tw, tx, p, grid, st, pdl, fp8a);
     case 64: return launch_tn<EPI, 64>(tw, tx, p, grid, st, pdl, fp8a);
     case 128: return launch_tn<EPI, 128>(tw, tx, p, grid, st, pdl, fp8a);
-    case 256: return launch_tn<EPI, 256>(tw, tx, p, grid, st, pdl, fp8a);
   }
   return cudaErrorInvalidValue;
 }
