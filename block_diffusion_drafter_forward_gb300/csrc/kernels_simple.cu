@@ -202,8 +202,8 @@ __global__ void qkv_post_kernel(const float* __restrict__ y, int ldy, const T* _
 template <typename T>
 __global__ void attention_kernel(const T* __restrict__ q, const T* __restrict__ pool, PoolGeom g, int layer,
                                  const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ page_tables,
-                                 int mpps, int rows, int nh, int nkv, int hd, int window, T* __restrict__ out,
-                                 unsigned* status) {
+                                 int mpps, int max_ctx, int rows, int nh, int nkv, int hd, int window,
+                                 T* __restrict__ out, unsigned* status) {
   const int lane = threadIdx.x & 31;
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (wid >= rows * nh) return;
@@ -212,6 +212,10 @@ __global__ void attention_kernel(const T* __restrict__ q, const T* __restrict__ 
   const int kvh = h / (nh / nkv);
   const int ctx = ctx_lens[s];
   if (ctx < 0 || ctx + kGamma > mpps * kPage) return;  // flagged by qkv_post
+  if (ctx > max_ctx) {  // the caller's bound on every ctx_len of this call
+    if (lane == 0 && r == 0 && h == 0) flag(status, DFLASH_DEV_BAD_CTX);
+    return;
+  }
   const int nkeys = ctx + kGamma, pq = ctx + r;
   const int per = hd >> 5;  // dims per lane (2 or 4)
   float qv[4], o[4];
@@ -519,15 +523,15 @@ cudaError_t launch_qkv_post(const dflash_handle* h, int layer, const float* y, c
 }
 
 cudaError_t launch_attention(const dflash_handle* h, int layer, const void* q, const int32_t* ctx_lens,
-                             const int32_t* page_tables, int nb, int /*max_ctx_len*/, void* out, cudaStream_t st) {
+                             const int32_t* page_tables, int nb, int max_ctx_len, void* out, cudaStream_t st) {
   const dflash_cfg& c = h->cfg;
   const int rows = nb * kGamma;
   const int warps = rows * c.n_q_heads;
   const int window = c.layer_sliding[layer] ? c.sliding_window : 0;
   DISPATCH_T(c.dtype, attention_kernel<T><<<(warps + 3) / 4, 128, 0, st>>>(
                           static_cast<const T*>(q), static_cast<const T*>(h->pool), h->geom, layer, ctx_lens,
-                          page_tables, c.max_pages_per_seq, rows, c.n_q_heads, c.n_kv_heads, c.head_dim, window,
-                          static_cast<T*>(out), h->d_status));
+                          page_tables, c.max_pages_per_seq, max_ctx_len, rows, c.n_q_heads, c.n_kv_heads,
+                          c.head_dim, window, static_cast<T*>(out), h->d_status));
   return cudaGetLastError();
 }
 
