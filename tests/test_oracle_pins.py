@@ -358,3 +358,91 @@ def test_drafts_drop_anchor_row():
     lm = W.get("lm_head").astype(np.float64)
     np.testing.assert_allclose(z, h @ lm.T, rtol=1e-12)
     assert tok.tolist() == np.argmax(h[1:] @ lm.T, axis=1).tolist() and tok.shape == (15,)
+
+
+# ----------------------------------------------------------------------------- layer wiring
+# Probes with elementary weight matrices: E[i, j] = 1 sends input feature j to output feature i
+# under the [out, in] row-major layout of every projection.  The tiny drafter's q and o
+# projections are square (q_dim == hidden), so a transposed operand there changes no shape; the
+# probes make it land on the wrong feature instead.
+
+
+def _elem(rows, cols, i, j, val=1.0):
+    m = np.zeros((rows, cols), np.float32)
+    m[i, j] = val
+    return m
+
+
+def _layer0(cfg, W, over, bonus=9, ctx=64):
+    wl = make_workload(cfg, 1, [ctx])
+    o = O.Oracle(cfg, DictWeights(W, over))
+    f = o.ctx_features(workload_taps(wl, 0, 0, ctx))
+    ks, vs = o.ctx_kv(f, np.arange(ctx))
+    seen = {}
+    o.forward_block(ks, vs, np.arange(ctx), bonus, ctx, layer_hook=lambda l, d: seen.setdefault(l, d))
+    x0 = W.get("embed")[[bonus] + [cfg.mask_token_id] * (cfg.gamma - 1)].astype(np.float64)
+    return seen[0], x0
+
+
+def _torch_rms(x, w, eps):
+    t = torch.nn.functional.rms_norm(torch.from_numpy(x), (x.shape[-1],), torch.from_numpy(w), eps=eps)
+    return t.numpy()
+
+
+def test_o_proj_and_mlp_wiring():
+    cfg, _, W = tiny()
+    H, F, qd = cfg.hidden, cfg.n_ff, cfg.q_dim
+    over = {"L0.wo": _elem(H, qd, 5, 200),             # attention feature 200 -> residual feature 5
+            "L0.w_gate": _elem(F, H, 7, 11, 2.0),       # act 7 gated by 2 * n[11]
+            "L0.w_up": _elem(F, H, 7, 13),              # ... times n[13]
+            "L0.w_down": _elem(H, F, 9, 7)}             # act 7 -> residual feature 9
+    d, x0 = _layer0(cfg, W, over)
+    # attention residual: x1 = x + o_proj(attn) touches feature 5 only, by attn[:, 200]
+    dx1 = d["x1"] - x0
+    np.testing.assert_array_equal(np.delete(dx1, 5, axis=1), 0.0)
+    np.testing.assert_allclose(dx1[:, 5], d["attn"][:, 200], rtol=1e-12, atol=1e-15)
+    assert np.abs(d["attn"][:, 200]).min() > 1e-6
+    # MLP residual on x1 (not on x): feature 9 only, by silu(gate) * up of the post-normed x1
+    n = _torch_rms(d["x1"], W.get("L0.ln_post").astype(np.float64), cfg.rms_eps)
+    act = torch.nn.functional.silu(torch.from_numpy(2.0 * n[:, 11])).numpy() * n[:, 13]
+    dx = d["x"] - d["x1"]
+    np.testing.assert_array_equal(np.delete(dx, 9, axis=1), 0.0)
+    np.testing.assert_allclose(dx[:, 9], act, rtol=1e-12, atol=1e-15)
+    # silu takes the gate: with the roles swapped the values differ
+    swapped = torch.nn.functional.silu(torch.from_numpy(n[:, 13])).numpy() * 2.0 * n[:, 11]
+    assert np.abs(swapped - act).max() > 1e-3
+
+
+def test_q_proj_orientation_and_head_split():
+    cfg, _, W = tiny()
+    H, qd, hd = cfg.hidden, cfg.q_dim, cfg.head_dim
+    i, j = 2 * hd + 3, 17                              # input feature 17 -> head 2, dim 3
+    d, _ = _layer0(cfg, W, {"L0.wq": _elem(qd, H, i, j)})
+    q = d["q"]                                          # [gamma, nh, hd] after q_norm and RoPE
+    raw = d["xn"][:, j]
+    for h in range(cfg.n_q_heads):
+        nz = np.flatnonzero(np.abs(q[:, h]).max(axis=0))
+        # one nonzero raw dim: q_norm keeps it alone, RoPE pairs it with its rotate-half partner
+        assert nz.tolist() == ([3, 3 + hd // 2] if h == 2 else []), (h, nz)
+    # q_norm of a one-hot head vector: |v| / sqrt(v^2 / hd + eps) * w; RoPE keeps the pair norm
+    w3 = float(W.get("L0.q_norm")[3])
+    expect = np.abs(raw) / np.sqrt(raw ** 2 / hd + cfg.rms_eps) * abs(w3)
+    np.testing.assert_allclose(np.hypot(q[:, 2, 3], q[:, 2, 3 + hd // 2]), expect, rtol=1e-12)
+
+
+def test_uniform_values_give_identical_rows():
+    # no context and bonus == mask: the gamma block rows carry the same token, so every
+    # layer's V rows are equal (V takes no RoPE) and each softmax-weighted sum returns that
+    # row, whatever the position-dependent scores; every final hidden row is then equal
+    cfg, _, W = tiny()
+    o = O.Oracle(cfg, W)
+    empty = [np.zeros((0, cfg.n_kv_heads, cfg.head_dim))] * cfg.n_layers
+    seen = {}
+    h = o.forward_block(empty, empty, np.zeros(0), cfg.mask_token_id, 0,
+                        layer_hook=lambda l, d: seen.setdefault(l, d))
+    np.testing.assert_allclose(h, np.broadcast_to(h[0], h.shape), rtol=1e-12, atol=1e-14)
+    q = seen[0]["q"]
+    assert np.abs(q - q[0]).max() > 1e-3              # the queries do differ by position
+    # a distinct bonus token breaks it
+    h2 = o.forward_block(empty, empty, np.zeros(0), 9, 0)
+    assert np.abs(h2[1:] - h2[0]).max() > 1e-3
