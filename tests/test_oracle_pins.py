@@ -446,3 +446,27 @@ def test_uniform_values_give_identical_rows():
     # a distinct bonus token breaks it
     h2 = o.forward_block(empty, empty, np.zeros(0), 9, 0)
     assert np.abs(h2[1:] - h2[0]).max() > 1e-3
+
+
+def test_ctx_features_are_hidden_normed_projections():
+    # f = hidden_norm(fc taps): dividing out the norm weight leaves rows of unit RMS, and a
+    # scaled tap row gives the same feature row up to the eps term (eps / mean(y^2) ~ 3e-6
+    # here: the norm follows the linear map)
+    cfg, wl, W = tiny()
+    o = O.Oracle(cfg, W)
+    taps = workload_taps(wl, 0, 0, 8).astype(np.float64)
+    f = o.ctx_features(taps)
+    w = W.get("hidden_norm").astype(np.float64)
+    rms = np.sqrt(np.mean((f / w) ** 2, axis=1))
+    y = taps @ W.get("fc").astype(np.float64).T
+    np.testing.assert_allclose(rms, np.sqrt(np.mean(y ** 2, axis=1) / (np.mean(y ** 2, axis=1) + cfg.rms_eps)),
+                               rtol=1e-12)
+    np.testing.assert_allclose(o.ctx_features(7.0 * taps), f, rtol=1e-5, atol=1e-6)  # taps enter as fp32
+    # fc rows index output features: a one-hot fc row picks one tap column
+    over = {"fc": _elem(cfg.hidden, cfg.n_taps * cfg.target_hidden, 3, 100)}
+    g = O.Oracle(cfg, DictWeights(W, over)).ctx_features(taps)
+    np.testing.assert_array_equal(np.delete(g, 3, axis=1), 0.0)
+    # one nonzero feature t of H: t / sqrt(t^2 / H + eps) = sign(t) sqrt(H) / sqrt(1 + eps H / t^2)
+    t = taps[:, 100].astype(np.float32).astype(np.float64)
+    np.testing.assert_allclose(g[:, 3], np.sign(t) * np.sqrt(cfg.hidden) * w[3]
+                               / np.sqrt(1 + cfg.rms_eps * cfg.hidden / t ** 2), rtol=1e-12)
