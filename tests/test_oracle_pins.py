@@ -249,10 +249,29 @@ def test_e4m3_roundtrip_and_spec_points():
 
 
 def test_e4m3_encode_matches_torch_cast():
-    x = np.concatenate([RNG.standard_normal(200_000) * s for s in (0.003, 0.1, 1, 30, 200)])
+    # 10^7 values over every binade in range
+    x = np.concatenate([RNG.standard_normal(2_000_000) * s for s in (0.003, 0.1, 1, 30, 200)])
     x = np.clip(x, -448, 448).astype(np.float32)
     ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     np.testing.assert_array_equal(O.e4m3_encode(x), ref)
+
+
+def test_e4m3_encode_ties_to_even_at_every_midpoint():
+    # the exact midpoint between each pair of neighbouring finite codes (subnormal and normal,
+    # both signs) rounds to the code with the even mantissa; a hair either side rounds to the
+    # nearer code
+    pos = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))    # 0 .. 448, increasing
+    lo, hi = pos[:-1], pos[1:]
+    mid = (lo + hi) / 2
+    codes = np.arange(0x7E, dtype=np.uint8)
+    even = np.where(codes % 2 == 0, codes, codes + 1).astype(np.uint8)
+    np.testing.assert_array_equal(O.e4m3_encode(mid), even)
+    np.testing.assert_array_equal(O.e4m3_encode(-mid), even | 0x80)
+    step = (hi - lo) / 64
+    np.testing.assert_array_equal(O.e4m3_encode(mid - step), codes)
+    np.testing.assert_array_equal(O.e4m3_encode(mid + step), codes + 1)
+    ref = torch.from_numpy(mid.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(ref, even)
 
 
 def test_fp8_quantize_rows():
