@@ -118,6 +118,19 @@ def test_yarn_wide_drafter_divisors():
     assert abs(ms - (1 + 0.1 * math.log(32))) < 1e-15 and abs(ms - 1.346574) < 1e-6
 
 
+def test_yarn_ramp_guard_when_low_equals_high():
+    # original 8192, beta_slow 1400: corr = 128 ln(8192 / (2 pi 1400)) / (2 ln 1e6) = -0.33,
+    # so high = ceil = 0; beta_fast 3000 gives corr < 0 and low = max(floor, 0) = 0.  With
+    # low == high the ramp's denominator is the 0.001 guard: dim 0 keeps its frequency and
+    # every other dim is divided by the full factor
+    d, theta, orig = 128, 1e6, 8192.0
+    corr = lambda r: d * math.log(orig / (2 * math.pi * r)) / (2 * math.log(theta))  # noqa: E731
+    assert -1 < corr(1400.0) <= 0 and corr(3000.0) < 0
+    ff = O.yarn_divisors(d, theta, (8.0, orig, 3000.0, 1400.0))
+    assert ff[0] == 1.0
+    np.testing.assert_allclose(ff[1:], 8.0, rtol=1e-12)
+
+
 def test_yarn_factor_one_is_plain():
     a, _ = O.rope_inv_freq(128, 1e6)
     b, ms = O.rope_inv_freq(128, 1e6, (1.0, 8192.0, 32.0, 1.0))
