@@ -191,6 +191,16 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- oracle timing
 
 
+def oracle_threads() -> int:
+    """Threads the oracle's numpy BLAS runs on: the usual thread-count variables when set, else
+    every core (the OpenBLAS default)."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return min(int(v), os.cpu_count() or 1)
+    return os.cpu_count() or 1
+
+
 def oracle_timing(wl, budget_s: float = 20.0):
     """The CPU oracle (float64 numpy, as it stands) on a bounded sample of the workload:
     context K/V of one band precomputed, then its gamma-block forward + lm_head + argmax
@@ -215,7 +225,7 @@ def oracle_timing(wl, budget_s: float = 20.0):
         if time.time() - t_all + times[-1] > budget_s or len(times) >= 5:
             break
     t = statistics.mean(times)
-    return {"value": (cfg.gamma - 1) / t, "unit": "draft tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": (cfg.gamma - 1) / t, "unit": "draft tokens/s", "cores": oracle_threads(), "kind": "oracle",
             "sample": f"band 0 of {wl.name} (ctx {c}): float64 numpy gamma-block forward + lm_head + argmax, "
                       f"{len(times)} run(s), context K/V precomputed outside the timing"}
 
@@ -270,7 +280,7 @@ def run_reference(args, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
             "config": {"workload": wl.name, "nb_timed": 1, "ctx": c},
-            "cpu_baseline": {"value": value, "unit": "draft tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "draft tokens/s", "cores": oracle_threads(), "kind": "oracle",
                              "sample": f"band 0 of {wl.name}: one gamma-block forward + lm_head + argmax per step "
                                        "(float64 numpy oracle); context K/V precomputed before the timing"},
             "e2e": {"value": value, "unit": "draft tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

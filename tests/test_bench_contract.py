@@ -42,3 +42,14 @@ def test_reference_arm_other_ranks_exit_without_work():
     r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_oracle_threads_follow_the_environment(monkeypatch):
+    import bench
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        monkeypatch.delenv(var, raising=False)
+    assert bench.oracle_threads() == (os.cpu_count() or 1)
+    monkeypatch.setenv("OMP_NUM_THREADS", "1")
+    assert bench.oracle_threads() == 1
+    monkeypatch.setenv("OPENBLAS_NUM_THREADS", "2")
+    assert bench.oracle_threads() == min(2, os.cpu_count() or 1)
