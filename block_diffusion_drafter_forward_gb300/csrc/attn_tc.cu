@@ -24,6 +24,7 @@
 
 #include "attn_tc.cuh"
 #include "dflash_internal.cuh"
+#include "launch_util.cuh"
 #include "tc_common.cuh"
 
 namespace dflash {
@@ -664,12 +665,9 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
 int64_t attn_tc_partial_slots(int num_sms, int max_units) { return kScWaves * (int64_t)num_sms + max_units; }
 
 cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0}, attr2{0};
+  if (cudaError_t e = smem_attr_once(attn_tc_kernel, kSmem, attr); e != cudaSuccess) return e;
+  if (cudaError_t e = smem_attr_once(attn_tc_sc_kernel, kScSmem, attr2); e != cudaSuccess) return e;
   const int units = nb * p.nkv;
   // the most chunks any sequence with ctx <= max_ctx_len visits
   int k0;
@@ -678,12 +676,6 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
   int cps = (units * nch + num_sms - 1) / num_sms;
   if (cps < 1) cps = 1;
   p.max_ctx = max_ctx_len;
-  static bool attr2 = false;
-  if (!attr2) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_sc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScSmem);
-    if (e != cudaSuccess) return e;
-    attr2 = true;
-  }
   // many chunks per CTA: the super-chunk kernel (one CTA per SM); a few: the compact one (it
   // fits beside a projection CTA on one SM, so it overlaps the QKV kernel under programmatic
   // launch)

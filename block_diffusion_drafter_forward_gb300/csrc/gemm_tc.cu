@@ -37,6 +37,7 @@
 #include "dflash_internal.cuh"
 #include "gemm_epi.cuh"
 #include "gemm_tc.cuh"
+#include "launch_util.cuh"
 #include "tc_common.cuh"
 
 namespace dflash {
@@ -347,12 +348,9 @@ cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPar
   constexpr int smem =
       STAGES * (128 * 64 * 2 + (EPI == EPI_CTXKV ? 2 : 1) * TN * 64 * 2 + (FP8A ? 128 * 64 : 0)) + 1024 + 256 + 1024;
   auto kern = gemm_tc_kernel<EPI, TN, STAGES, FP8A, WG>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};
+  cudaError_t ea = smem_attr_once(kern, smem, attr_set);
+  if (ea != cudaSuccess) return ea;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads * WG);
