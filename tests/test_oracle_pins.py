@@ -502,3 +502,51 @@ def test_ctx_features_are_hidden_normed_projections():
     t = taps[:, 100].astype(np.float32).astype(np.float64)
     np.testing.assert_allclose(g[:, 3], np.sign(t) * np.sqrt(cfg.hidden) * w[3]
                                / np.sqrt(1 + cfg.rms_eps * cfg.hidden / t ** 2), rtol=1e-12)
+
+
+def test_forward_window_rule_at_the_layer_level():
+    # a window covering every key (p - j <= 64 + 15 < 80) is exactly full attention; a window one
+    # shorter masks key 0 for the last block row (p - j = 79 >= 79) and changes the output; the
+    # window applies only on the layers marked sliding
+    import dataclasses
+    base = dataclasses.replace(CONFIGS["tiny_fp32"], n_layers=2)
+    W = make_weights(base, 1)
+    wl = make_workload(base, 1, [64])
+    taps, pos = workload_taps(wl, 0, 0, 64), np.arange(64)
+
+    def run(**kw):
+        o = O.Oracle(dataclasses.replace(base, **kw), W)
+        ks, vs = o.ctx_kv(o.ctx_features(taps), pos)
+        return o.forward_block(ks, vs, pos, 5, 64)
+
+    full = run()
+    np.testing.assert_array_equal(run(sliding_window=80, layer_sliding=(True, True)), full)
+    # W = 79 takes key 0 from row 15 in layer 0 only; the other rows change through that row's
+    # block key in layer 1
+    short = run(sliding_window=79, layer_sliding=(True, False))
+    assert np.abs(short - full).max() > 1e-9
+    a = run(sliding_window=20, layer_sliding=(True, False))
+    b = run(sliding_window=20, layer_sliding=(False, True))
+    assert np.abs(a - b).max() > 1e-3 and np.abs(a - full).max() > 1e-3
+
+
+def test_fp8_lm_head_is_exact_on_the_e4m3_grid():
+    # lm_head rows that are e4m3 values times 2^-k (with a +-448 entry, so the row scale is
+    # exactly 2^-k) quantise without loss: the FP8 logits equal the full-precision ones
+    import dataclasses
+    cfg = dataclasses.replace(CONFIGS["tiny_fp32"], lm_head_dtype="fp8")
+    W = make_weights(cfg, 1)
+    rng = np.random.default_rng(7)
+    V, H = cfg.vocab, cfg.hidden
+    codes = rng.integers(0, 256, size=(V, H)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38                      # no NaN codes
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    vals[:, 0] = np.where(rng.random(V) < 0.5, 448.0, -448.0)
+    k = rng.integers(4, 14, size=V)
+    lm = (vals * np.ldexp(1.0, -k)[:, None]).astype(np.float32)
+    assert np.array_equal(lm.astype(np.float64), vals * np.ldexp(1.0, -k)[:, None])
+    o = O.Oracle(cfg, DictWeights(W, {"lm_head": lm}))
+    q, scale = o.fp8_lm_head()
+    np.testing.assert_array_equal(scale, np.ldexp(1.0, -k).astype(np.float32))
+    h = RNG.standard_normal((cfg.gamma, H))
+    np.testing.assert_allclose(o.logits(h), h @ lm.astype(np.float64).T, rtol=1e-13, atol=1e-13)
