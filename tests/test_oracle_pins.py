@@ -237,6 +237,21 @@ def test_page_slots_and_paged_equals_contiguous():
     assert np.isnan(pool.k[0]).all()
 
 
+# ----------------------------------------------------------------------------- bf16 inputs
+
+
+def test_bf16_decode_all_patterns_vs_torch():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    with np.errstate(invalid="ignore"):  # signalling-NaN patterns warn when widened
+        got = O.bf16_to_f64(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    # sign of zero and the infinities survive
+    assert np.signbit(got[0x8000]) and not np.signbit(got[0]) and got[0x7F80] == np.inf and got[0xFF80] == -np.inf
+
+
 # ----------------------------------------------------------------------------- FP8 e4m3
 
 
