@@ -565,3 +565,14 @@ def test_fp8_lm_head_is_exact_on_the_e4m3_grid():
     np.testing.assert_array_equal(scale, np.ldexp(1.0, -k).astype(np.float32))
     h = RNG.standard_normal((cfg.gamma, H))
     np.testing.assert_allclose(o.logits(h), h @ lm.astype(np.float64).T, rtol=1e-13, atol=1e-13)
+
+
+def test_logits_do_not_depend_on_the_vocabulary_chunking():
+    import dataclasses
+    for head in ("f32", "fp8"):
+        cfg = dataclasses.replace(CONFIGS["tiny_fp32"], lm_head_dtype=head)
+        o = O.Oracle(cfg, make_weights(cfg, 1))
+        h = RNG.standard_normal((cfg.gamma, cfg.hidden))
+        np.testing.assert_allclose(o.logits(h, chunk=300), o.logits(h), rtol=1e-13, atol=1e-15)
+        # rows are independent: a subset of rows gives the same rows
+        np.testing.assert_allclose(o.logits(h[3:5], chunk=7), o.logits(h)[3:5], rtol=1e-13, atol=1e-15)
