@@ -374,6 +374,16 @@ int propose_graph(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* 
 
 }  // namespace
 
+// The single launch cuts each projection's (128-row tile, 64-wide k-block) units into G equal
+// ranges, one per CTA.  With fewer units than CTAs some ranges are empty, and a tile's finisher
+// would wait for partials from the empty ranges between its first and last owner.
+static bool persist_every_cta_has_work(int64_t H, int64_t F, int64_t nh, int64_t nkv, int64_t V, int G) {
+  const int64_t shapes[5][2] = {{(nh + 2 * nkv) * 128, H}, {H, nh * 128}, {2 * F, H}, {H, F}, {V, H}};
+  for (const auto& sh : shapes)
+    if (((sh[0] + 127) / 128) * (sh[1] / 64) < (int64_t)G) return false;
+  return true;
+}
+
 extern "C" {
 
 const char* dflash_last_error(const dflash_handle* h) { return h ? h->err.c_str() : g_create_error.c_str(); }
@@ -569,9 +579,10 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     ALLOC(h->wf2, Rw * 2 * H * es);
     h->tc_attn = (nh / nkv) == 8;
     // single-launch persistent forward for batch 1: needs the tensor-core attention, a bf16
-    // lm_head and one resident CTA per SM
+    // lm_head, one resident CTA per SM, and at least one (tile, k-block) unit of every projection
+    // per CTA (its split-K finisher counts every CTA between a tile's first and last owner)
     if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && H <= persist_max_hidden() &&
-        L <= kPersistMaxL) {
+        L <= kPersistMaxL && persist_every_cta_has_work(H, F, nh, nkv, V, h->num_sms)) {
       int per_sm = 0;
       if (persist_occupancy(&per_sm) == cudaSuccess && per_sm >= 1) h->persist_ok = true;
       cudaGetLastError();
