@@ -964,6 +964,15 @@ int dflash_device_status(dflash_handle* h, dflash_stream stream, uint32_t* flags
   CK(cudaMemcpyAsync(&v, h->d_status, sizeof(unsigned), cudaMemcpyDeviceToHost, st), "status read");
   CK(cudaMemsetAsync(h->d_status, 0, sizeof(unsigned), st), "status clear");
   CK(cudaStreamSynchronize(st), "status sync");
+  if ((v & DFLASH_DEV_TIMEOUT) && h->counters) {
+    // a kernel that gave up a wait may have left split-K and argmax tile counters part-counted:
+    // re-arm them so the next call starts from zero
+    CK(cudaMemsetAsync(h->counters, 0, kCounters * sizeof(unsigned), st), "counter reset");
+    if (h->attn_counters)
+      CK(cudaMemsetAsync(h->attn_counters, 0, (size_t)h->cfg.max_batch * h->cfg.n_kv_heads * sizeof(unsigned), st),
+         "counter reset");
+    CK(cudaStreamSynchronize(st), "counter reset sync");
+  }
   if (flags) *flags = v;
   if (v) return fail(h, DFLASH_EDEVICE, "device-side check fired (see flags)");
   return DFLASH_OK;

@@ -241,7 +241,9 @@ int dflash_attention_check(dflash_handle* h, int32_t layer, const int32_t* ctx_l
                            void* out_cuda_core, void* out_tensor_core, dflash_stream stream);
 
 /* Synchronise `stream`, read the device status word into *flags (may be NULL) and clear
- * it.  Returns DFLASH_EDEVICE when any bit was set, else DFLASH_OK. */
+ * it.  When DFLASH_DEV_TIMEOUT was set it also re-arms the handle's internal tile counters
+ * (a kernel that gave up a wait may have left them part-counted), so the next call starts
+ * clean.  Returns DFLASH_EDEVICE when any bit was set, else DFLASH_OK. */
 int dflash_device_status(dflash_handle* h, dflash_stream stream, uint32_t* flags);
 
 /* Last error message of the handle ("" if none); with h == NULL the message of the last
