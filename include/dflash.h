@@ -20,9 +20,11 @@
  *   - The return value is a dflash_status.  A non-zero status means nothing was
  *     launched by that call (argument and capacity checks run on the host first);
  *     dflash_last_error() then gives a message.
- *   - Device-side checks (a page id outside [0, num_pages), a context length beyond the
- *     host bound) never trap: the offending row is skipped and a bit is set in the
- *     handle's device status word, read (and cleared) by dflash_device_status().
+ *   - Device-side checks (a page id outside [0, num_pages), a context length outside
+ *     [0, max_ctx_len] or past the page table, a bonus token outside [0, vocab), a bounded
+ *     wait that gave up) never trap: the offending row is skipped (a bad token's row is
+ *     embedded as zeros) and a bit is set in the handle's device status word, read (and
+ *     cleared) by dflash_device_status().
  *   - A handle is not thread-safe: one caller at a time (one draft step at a time, as in
  *     the pages' proposer contract).
  */
