@@ -167,7 +167,11 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
  * ctx_lens, used for grid sizing; it must satisfy max_ctx_len + gamma <=
  * 16 * max_pages_per_seq (ECAPACITY).  The block K/V are written transiently into rows
  * ctx_lens[s]..ctx_lens[s]+gamma-1 of each sequence's pages (never committed: the next
- * dflash_write_ctx_kv at first = ctx_len overwrites them).  1 <= nb <= max_batch. */
+ * dflash_write_ctx_kv at first = ctx_len overwrites them).  1 <= nb <= max_batch.
+ * The launch sequence is captured as a CUDA graph the first time a given set of pointers,
+ * nb and max_ctx_len is seen (a small per-handle cache) and replayed after that; the values
+ * in the input buffers may change freely between calls.  A caller that passes new buffer
+ * addresses every call pays a graph capture each time: reuse the buffers. */
 int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens,
                    const int32_t* page_tables, int32_t nb, int32_t max_ctx_len,
                    int32_t* draft_tokens, void* logits, void* final_hidden,
