@@ -422,7 +422,7 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
   }
   h->tc = c.dtype == DFLASH_BF16;
   if (h->tc && (c.head_dim != 128 || c.hidden % 128 || c.n_ff % 64 || c.target_hidden % 8)) {
-    fail(h, DFLASH_EUNSUPPORTED, "bf16 path needs head_dim 128, hidden % 128 == 0 and n_ff % 64 == 0");
+    fail(h, DFLASH_EUNSUPPORTED, "bf16 path needs head_dim 128, hidden % 128 == 0, n_ff % 64 == 0 and target_hidden % 8 == 0");
     return bail(DFLASH_EUNSUPPORTED);
   }
   const size_t es = h->esz;
