@@ -42,6 +42,30 @@ def _stream(stream: Optional[torch.cuda.Stream]) -> int:
     return (stream or torch.cuda.current_stream()).cuda_stream
 
 
+def check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, shape: Tuple[int, ...], min_rows: bool = False,
+                 device_type: str = "cuda") -> None:
+    """The C ABI takes raw pointers and cannot see sizes or types, so every tensor is checked here
+    before its address is passed: a contiguous `dtype` tensor of exactly `shape` (or, with
+    `min_rows`, at least shape[0] rows) on a `device_type` device; ValueError otherwise."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.device.type != device_type:
+        raise ValueError(f"{name}: expected a {device_type} tensor, got one on {t.device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    got, want = tuple(t.shape), tuple(shape)
+    if len(got) == len(want) and want:
+        rows_ok = got[0] >= want[0] if min_rows else got[0] == want[0]
+        ok = rows_ok and got[1:] == want[1:]
+    else:
+        ok = got == want
+    if not ok:
+        rows = f">={want[0]}" if min_rows and want else ""
+        raise ValueError(f"{name}: expected shape {want if not rows else (rows,) + want[1:]}, got {got}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
 class Drafter:
     """One drafter handle.  `tensors` maps fc, hidden_norm, norm, embed, lm_head and
     L{l}.{ln_in, wq, ...} to contiguous device tensors of the config's dtype."""
@@ -74,19 +98,35 @@ class Drafter:
         except Exception:
             pass
 
+    @property
+    def act_dtype(self) -> torch.dtype:
+        """dtype of the taps, logits and hidden outputs (fp32 drafter: float32, else bfloat16)."""
+        return torch.float32 if self.cfg.dtype == "f32" else torch.bfloat16
+
     def write_ctx_kv(self, taps: torch.Tensor, positions: torch.Tensor, page_table: torch.Tensor, first: int,
                      stream=None) -> None:
-        n = int(taps.shape[0])
+        n = int(taps.shape[0]) if taps.dim() >= 1 else -1
+        check_tensor(taps, "taps", self.act_dtype, (n, self.cfg.n_taps * self.cfg.target_hidden))
+        check_tensor(positions, "positions", torch.int32, (n,))
+        check_tensor(page_table, "page_table", torch.int32, (self.ccfg.max_pages_per_seq,))
         L.dflash_write_ctx_kv(self.handle, taps.data_ptr(), positions.data_ptr(), page_table.data_ptr(), first, n,
                               _stream(stream))
 
     def propose(self, bonus: torch.Tensor, ctx_lens: torch.Tensor, page_tables: torch.Tensor, max_ctx_len: int,
                 drafts: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
                 hidden: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        nb = int(bonus.shape[0])
-        dev = bonus.device
+        nb = int(bonus.shape[0]) if bonus.dim() == 1 else -1
+        g = self.cfg.gamma
+        check_tensor(bonus, "bonus", torch.int32, (nb,))
+        check_tensor(ctx_lens, "ctx_lens", torch.int32, (nb,))
+        check_tensor(page_tables, "page_tables", torch.int32, (nb, self.ccfg.max_pages_per_seq), min_rows=True)
         if drafts is None:
-            drafts = torch.empty((nb, self.cfg.gamma - 1), dtype=torch.int32, device=dev)
+            drafts = torch.empty((nb, g - 1), dtype=torch.int32, device=bonus.device)
+        check_tensor(drafts, "drafts", torch.int32, (nb, g - 1))
+        if logits is not None:
+            check_tensor(logits, "logits", self.act_dtype, (nb * g, self.cfg.vocab))
+        if hidden is not None:
+            check_tensor(hidden, "hidden", self.act_dtype, (nb * g, self.cfg.hidden))
         L.dflash_propose(self.handle, bonus.data_ptr(), ctx_lens.data_ptr(), page_tables.data_ptr(), nb,
                          int(max_ctx_len), drafts.data_ptr(), logits.data_ptr() if logits is not None else 0,
                          hidden.data_ptr() if hidden is not None else 0, _stream(stream))
