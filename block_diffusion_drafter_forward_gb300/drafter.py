@@ -66,6 +66,19 @@ def check_tensor(t: torch.Tensor, name: str, dtype: torch.dtype, shape: Tuple[in
         raise ValueError(f"{name}: must be contiguous")
 
 
+def weight_shapes(cfg) -> Dict[str, Tuple[int, ...]]:
+    """Shape of every weight dflash_create reads, HF layout (Linear weights [out, in])."""
+    H, F, V, hd = cfg.hidden, cfg.n_ff, cfg.vocab, cfg.head_dim
+    qd, kvd = cfg.n_q_heads * hd, cfg.n_kv_heads * hd
+    out = {"fc": (H, cfg.n_taps * cfg.target_hidden), "hidden_norm": (H,), "norm": (H,), "embed": (V, H),
+           "lm_head": (V, H)}
+    layer = {"ln_in": (H,), "wq": (qd, H), "wk": (kvd, H), "wv": (kvd, H), "q_norm": (hd,), "k_norm": (hd,),
+             "wo": (H, qd), "ln_post": (H,), "w_gate": (F, H), "w_up": (F, H), "w_down": (H, F)}
+    for l in range(cfg.n_layers):
+        out.update({f"L{l}.{t}": sh for t, sh in layer.items()})
+    return out
+
+
 class Drafter:
     """One drafter handle.  `tensors` maps fc, hidden_norm, norm, embed, lm_head and
     L{l}.{ln_in, wq, ...} to contiguous device tensors of the config's dtype."""
@@ -74,6 +87,12 @@ class Drafter:
                  max_pages_per_seq: int, max_write_rows: int = 4096, stream=None):
         self.cfg = cfg
         self.tensors = tensors
+        shapes = weight_shapes(cfg)
+        missing = [n for n in shapes if n not in tensors]
+        if missing:
+            raise ValueError(f"missing weight {missing[0]}" + (f" (+{len(missing) - 1} more)" if len(missing) > 1 else ""))
+        for name, shape in shapes.items():
+            check_tensor(tensors[name], name, self.act_dtype, shape)
         self.ccfg = make_cfg(cfg, num_pages, max_batch, max_pages_per_seq, max_write_rows)
         layers = (L.dflash_layer_weights * cfg.n_layers)()
         for l in range(cfg.n_layers):

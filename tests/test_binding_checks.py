@@ -54,3 +54,27 @@ def test_propose_and_write_check_before_calling_the_library():
     with pytest.raises(ValueError, match="taps"):
         d.write_ctx_kv(torch.zeros(4, 768), torch.zeros(4, **i32), torch.zeros(8, **i32), 0)
     assert d.act_dtype == torch.float32
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8l_bf16", "wide_5l_yarn_bf16"])
+def test_weight_shapes_match_the_generator(name):
+    # the binding's expected shapes against the seeded generator's own table (HF layout)
+    from block_diffusion_drafter_forward_gb300.drafter import weight_shapes
+    from synth import make_weights
+    cfg = CONFIGS[name]
+    W = make_weights(cfg, 1)
+    shapes = weight_shapes(cfg)
+    assert set(shapes) == set(W.names())
+    for n, sh in shapes.items():
+        assert tuple(W.spec(n)[0]) == sh, n
+
+
+def test_create_checks_every_weight_first():
+    cfg = CONFIGS["tiny_fp32"]
+    from block_diffusion_drafter_forward_gb300.drafter import weight_shapes
+    tensors = {n: torch.zeros(sh) for n, sh in weight_shapes(cfg).items()}
+    with pytest.raises(ValueError, match="expected a cuda tensor"):
+        Drafter(cfg, tensors, num_pages=8, max_batch=1, max_pages_per_seq=8)
+    del tensors["L0.wq"]
+    with pytest.raises(ValueError, match="missing weight L0.wq"):
+        Drafter(cfg, tensors, num_pages=8, max_batch=1, max_pages_per_seq=8)
