@@ -11,6 +11,9 @@
 // __device__ array of fixed size.  Every GPU that loads the library holds it until the
 // process exits.  All calls share it, so two calls that overlap on the GPU (different
 // streams, or different host threads) race on it and produce garbage: serialise them.
+// A bounded wait inside the kernel that gives up (only on a GPU starved for many seconds)
+// leaves its tile unwritten; this entry point has no status word to report that.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -33,11 +36,44 @@ struct NoAllocScratch {
   unsigned* counters = nullptr;
 };
 
-// Device addresses of the arrays, looked up once per device with that device current.
-// (In host code the array names are host-side stand-ins, not device addresses.)
+// Device addresses of the arrays, looked up with the device current.  (In host code the array
+// names are host-side stand-ins, not device addresses.)  An address belongs to the context the
+// library's module was loaded into: after cudaDeviceReset, or after the primary context was
+// released and created again, the module is loaded anew and the arrays may move.  So the cache
+// is keyed on the current context's unique id, and a new context means a new lookup.
 std::mutex g_mu;
 NoAllocScratch g_scratch[64];
-bool g_ready[64] = {};
+unsigned long long g_ctx_id[64] = {};  // 0: not looked up yet
+
+// Driver entry points through the runtime (the library does not link libcuda itself).
+typedef CUresult (*PFN_ctx_get_current)(CUcontext*);
+typedef CUresult (*PFN_ctx_get_id)(CUcontext, unsigned long long*);
+
+template <typename F>
+F driver_fn(const char* name, int version) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(ptr);
+}
+
+// Unique id of the calling thread's current context (0 if none or not available).
+unsigned long long current_ctx_id() {
+  static PFN_ctx_get_current get_current = nullptr;
+  static PFN_ctx_get_id get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<PFN_ctx_get_current>("cuCtxGetCurrent", 4000);
+    get_id = driver_fn<PFN_ctx_get_id>("cuCtxGetId", 12000);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 cudaError_t scratch_for_current_device(NoAllocScratch* out) {
   int dev = 0;
@@ -45,14 +81,16 @@ cudaError_t scratch_for_current_device(NoAllocScratch* out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ready[dev]) {
+  const unsigned long long id = current_ctx_id();
+  if (id == 0 || id != g_ctx_id[dev]) {
     NoAllocScratch s;
+    // the first lookup also makes the device's primary context current
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.partials), g_noalloc_partials);
     if (e != cudaSuccess) return e;
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.counters), g_noalloc_counters);
     if (e != cudaSuccess) return e;
     g_scratch[dev] = s;
-    g_ready[dev] = true;
+    g_ctx_id[dev] = current_ctx_id();
   }
   *out = g_scratch[dev];
   return cudaSuccess;

@@ -26,10 +26,12 @@
 #include <float.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "dflash_internal.cuh"
 #include "gemm_epi.cuh"
 #include "gemm_tc.cuh"
+#include "launch_util.cuh"
 #include "persist_tc.cuh"
 #include "tc_common.cuh"
 
@@ -1007,15 +1009,10 @@ void persist_attn_split(int units, int max_ctx, int window, int G, int* cps, int
   *splits = (nch + c - 1) / c;
 }
 
-static cudaError_t persist_attr() {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemP);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  return cudaSuccess;
-}
+// The shared-memory limit is a property of the device's context: raise it once per device.
+static std::atomic<unsigned long long> g_persist_attr{0};
+
+static cudaError_t persist_attr() { return smem_attr_once(persist_kernel, kSmemP, g_persist_attr); }
 
 cudaError_t persist_occupancy(int* per_sm) {
   cudaError_t e = persist_attr();

@@ -229,12 +229,16 @@ int dflash_gemm_bf16(const void* W, int32_t N, int32_t K, const void* X, int32_t
  * device memory at start-up, a memory pool that owns the device, a runtime that forbids
  * allocation after initialisation.  Its scratch (split-K partials, tile counters) is a
  * fixed array in the library's device image: 8 MiB of partials and 4096 tiles, held on
- * every GPU that loads the library until the process exits.  Shapes that need more
- * (tiles * nsplit * 128 * TN floats, TN = 16/32/64/128/256 by M) return ECAPACITY.  All
- * calls share that array: calls that overlap on the GPU (two streams, two threads) race
- * and give wrong results, so serialise them.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  Each call zeroes the counters it uses on `stream`. */
+ * every GPU that loads the library until the process exits.  With TN = 16, 32, 64 or 128
+ * token columns per tile (M <= 16, <= 32, <= 64, else 128) and tiles = ceil(N/128) *
+ * ceil(M/TN), shapes need tiles <= 4096 and tiles * nsplit * 128 * TN <= 2^21 floats;
+ * larger ones return ECAPACITY.  All calls share that array: calls that overlap on the GPU
+ * (two streams, two threads) race and give wrong results, so serialise them.  The first
+ * call in a CUDA context (per device, and again after cudaDeviceReset or a new primary
+ * context) looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Each call zeroes the counters
+ * it uses on `stream`.  A bounded device-side wait that gives up is not reported by this
+ * call (it leaves the affected output tiles unwritten). */
 int dflash_gemm_bf16_noalloc(const void* W, int32_t N, int32_t K, const void* X, int32_t M,
                              float* out, int32_t nsplit, dflash_stream stream);
 

@@ -88,6 +88,19 @@ CONFIGS: Dict[str, DrafterConfig] = {
         yarn=(32.0, 8192.0, 32.0, 1.0), sliding_window=2048,
         layer_sliding=(True, True, True, True, False)),
     "qwen3_8l_fp8head": DrafterConfig(name="qwen3_8l_fp8head", lm_head_dtype="fp8", **_C2_ARCH),
+    # shapes the C ABI accepts beside the five above, each on a different kernel route:
+    # the tiny fp32 drafter with an e4m3 lm_head (CUDA-core FP8 GEMV), a bf16 drafter with
+    # 4 query heads per kv head (CUDA-core attention between tensor-core projections), and a
+    # bf16 drafter with 8 query heads per kv head too small for the single-launch forward
+    "tiny_fp32_fp8head": DrafterConfig(
+        name="tiny_fp32_fp8head", hidden=256, n_q_heads=4, n_kv_heads=1, head_dim=64, n_ff=512,
+        n_layers=1, vocab=2048, n_taps=3, target_hidden=256, dtype="f32", lm_head_dtype="fp8"),
+    "small_gqa4_bf16": DrafterConfig(
+        name="small_gqa4_bf16", hidden=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, n_ff=2048,
+        n_layers=2, vocab=8192, n_taps=2, target_hidden=1024),
+    "small_gqa8_bf16": DrafterConfig(
+        name="small_gqa8_bf16", hidden=1024, n_q_heads=8, n_kv_heads=1, head_dim=128, n_ff=2048,
+        n_layers=2, vocab=8192, n_taps=2, target_hidden=1024),
 }
 
 

@@ -53,3 +53,14 @@ def test_oracle_threads_follow_the_environment(monkeypatch):
     assert bench.oracle_threads() == 1
     monkeypatch.setenv("OPENBLAS_NUM_THREADS", "2")
     assert bench.oracle_threads() == min(2, os.cpu_count() or 1)
+
+
+def test_oracle_legs_set_their_thread_count():
+    """The CPU baseline's two legs run the oracle in child interpreters whose BLAS thread count is
+    set before numpy loads: one leg on every core, one single-threaded."""
+    import bench
+    one = bench.run_oracle_leg("tiny_fp32_nb1_ctx64", 1, 1.0, 1)
+    assert one["threads"] == 1 and one["runs"] == 1 and one["s_per_forward"] > 0 and one["ctx"] == 64
+    allc = bench.run_oracle_leg("tiny_fp32_nb1_ctx64", os.cpu_count() or 1, 1.0, 2)
+    assert allc["threads"] == (os.cpu_count() or 1) and 1 <= allc["runs"] <= 2
+    assert bench.cpu_model()

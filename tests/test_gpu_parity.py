@@ -161,9 +161,11 @@ def test_qwen3_8l_full_size_nb1_ctx4096():
     run_and_check(WORKLOADS["qwen3_8l_nb1_ctx4096"]())
 
 
-def test_qwen3_8l_nb32_ragged_full_size_sampled():
+def test_qwen3_8l_nb32_ragged_full_size_every_band():
+    """The 32-sequence ragged batch at full size: every band against the oracle, and the
+    context K/V pool rows of layers 0 and 7 of every sequence."""
     wl = WORKLOADS["qwen3_8l_nb32_ragged"]()
-    run_and_check(wl, bands=[0, 13, 31], check_kv=False)
+    run_and_check(wl)
 
 
 def test_qwen3_8l_small_batch_all_bands():
@@ -208,6 +210,36 @@ def test_fp8_head_codes_and_scales_bit_exact():
         assert np.array_equal(scale[sl].cpu().numpy(), rs)
 
 
-def test_fp8_head_full_size_nb4_sampled():
-    wl = WORKLOADS["fp8head_nb4_ctx32768"]()
-    run_and_check(wl, bands=[2], check_kv=False)
+@pytest.mark.parametrize("name,bands", [
+    ("fp8head_nb1_ctx32768", [0]),
+    ("fp8head_nb4_ctx32768", [2]),
+    ("fp8head_nb16_ctx32768", [0, 9, 15]),
+    ("fp8head_nb64_ctx32768", [0, 37, 63]),
+])
+def test_fp8_head_sweep_full_size_sampled(name, bands):
+    """The FP8-lm_head throughput sweep at full size (32 768 context rows per sequence): the
+    oracle recomputes the sampled bands one by one."""
+    run_and_check(WORKLOADS[name](), bands=bands, check_kv=False)
+
+
+# ----------------------------------------------------------------------------- other accepted shapes
+
+
+def test_tiny_fp32_with_fp8_head():
+    """The e4m3 lm_head on the fp32 drafter (CUDA-core FP8 GEMV over fp32 activations)."""
+    rig, _ = run_and_check(make_workload(CONFIGS["tiny_fp32_fp8head"], 53, [64, 9]))
+    codes_ptr, scale_ptr = dflash_fp8_lm_head(rig.drafter.handle)
+    V, H = rig.cfg.vocab, rig.cfg.hidden
+    codes = torch.as_tensor(DevView(codes_ptr, V * H, "|u1"), device="cuda").view(V, H)
+    rc, rs = fp8_quantize_rows(rig.W.get("lm_head").astype(np.float32))
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("cfg_name", ["small_gqa4_bf16", "small_gqa8_bf16"])
+def test_small_bf16_drafters_on_the_per_projection_kernels(cfg_name):
+    """bf16 drafters the single launch does not take: 4 query heads per kv head (CUDA-core
+    attention between the tensor-core projections), and 8 per kv head with an o_proj of
+    fewer (tile, k-block) units than SMs.  Both at nb = 1 and on a ragged batch."""
+    for seed, ctxs in ((54, [300]), (55, [0, 77, 1000])):
+        rig, _ = run_and_check(make_workload(CONFIGS[cfg_name], seed, ctxs))
+        assert not rig.drafter.persistent

@@ -407,6 +407,55 @@ def test_drafts_drop_anchor_row():
     assert tok.tolist() == np.argmax(h[1:] @ lm.T, axis=1).tolist() and tok.shape == (15,)
 
 
+class _ScaledNorms(O.Oracle):
+    """The oracle with some weights multiplied by exact float64 factors."""
+
+    def __init__(self, cfg, weights, scales, mscale):
+        super().__init__(cfg, weights, cache=True)
+        self.scales = scales
+        self.mscale = mscale
+
+    def W(self, name):
+        a = super().W(name)
+        return a * self.scales[name] if name in self.scales else a
+
+
+def test_yarn_mscale_multiplies_both_q_and_k():
+    """Where the YaRN mscale sits in the whole forward (context K of every layer, the block's q
+    and k).  RMSNorm is linear in its weight and RoPE is linear in its input, so multiplying q
+    and k by mscale after the rotation is the same as multiplying the q_norm and k_norm weights
+    by mscale and rotating with mscale 1 (the YaRN frequencies unchanged).  The YaRN forward must
+    equal that, and must differ from the forms that scale only q, only k, or neither."""
+    import dataclasses
+    cfg = dataclasses.replace(CONFIGS["tiny_fp32"], name="tiny_yarn", n_layers=2, yarn=(32.0, 8192.0, 32.0, 1.0))
+    W = make_weights(cfg, 1)
+    wl = make_workload(cfg, 1, [64])
+    taps = workload_taps(wl, 0, 0, 64)
+    pos = np.arange(5000, 5064)                       # angles far from zero
+    o = O.Oracle(cfg, W, cache=True)
+    m = o.mscale
+    assert abs(m - (1 + 0.1 * math.log(32))) < 1e-15
+    ref = o.run_sequence(taps, pos, 77)
+
+    def variant(q, k):
+        sc = {}
+        for l in range(cfg.n_layers):
+            if q:
+                sc[f"L{l}.q_norm"] = m
+            if k:
+                sc[f"L{l}.k_norm"] = m
+        return _ScaledNorms(cfg, W, sc, 1.0).run_sequence(taps, pos, 77)
+
+    both = variant(True, True)
+    rel = lambda a, b: np.abs(a - b).max() / np.abs(b).max()  # noqa: E731
+    for l in range(cfg.n_layers):
+        assert rel(both["k"][l], ref["k"][l]) < 1e-13
+        np.testing.assert_array_equal(both["v"][l], ref["v"][l])
+    assert rel(both["h"], ref["h"]) < 1e-12 and rel(both["logits"], ref["logits"]) < 1e-12
+    for q, k in ((True, False), (False, True), (False, False)):
+        assert rel(variant(q, k)["h"], ref["h"]) > 1e-3, (q, k)
+
+
 # ----------------------------------------------------------------------------- layer wiring
 # Probes with elementary weight matrices: E[i, j] = 1 sends input feature j to output feature i
 # under the [out, in] row-major layout of every projection.  The tiny drafter's q and o
