@@ -24,8 +24,8 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+def _compile(src: str, extra, build_dir: str) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [NVCC, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -33,21 +33,26 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(verbose: bool = False, ptxas_verbose: bool = False, defines=(), lib_path: str = LIB,
+          build_dir: str = BUILD_DIR) -> str:
+    """Compile every translation unit (in parallel) and link `lib_path`.  `defines` are extra
+    preprocessor definitions (for instance DFLASH_PHASE_TRACE=1 for the phase-timeline build,
+    which goes to its own library and build folder)."""
+    os.makedirs(build_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    extra += [f"-D{d}" for d in defines]
     srcs = sources()
     with ThreadPoolExecutor(max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
+    tmp = lib_path + ".tmp"
     cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     if verbose:
-        print(f"built {LIB}")
-    return LIB
+        print(f"built {lib_path}")
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -3,10 +3,12 @@
 // before any launch; every launch is stream-ordered on the caller's stream.
 #include <math.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
 #include <string>
+#include <vector>
 
 #include "dflash_internal.cuh"
 #include "attn_tc.cuh"
@@ -248,6 +250,7 @@ int propose_persist(dflash_handle* h, const int32_t* bonus_tokens, const int32_t
   p.logits = static_cast<__nv_bfloat16*>(logits);
   p.final_hidden = static_cast<__nv_bfloat16*>(final_hidden);
   p.status = h->d_status;
+  p.trace = h->p_trace;
   persist_bind_ctl(p, h->p_ctl);
   CK(cudaMemsetAsync(h->p_ctl, 0, h->p_ctl_words * sizeof(unsigned), st), "persistent control reset");
   KL(K_PERSIST, launch_persist(p, st), "persistent forward");
@@ -609,6 +612,11 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
       ALLOC(h->p_maps, maps.size() * sizeof(CUtensorMap));
       h->p_ctl_words = persist_ctl_words((int)L, (int)H, (int)F, (int)nh, (int)nkv, (int)V);
       ALLOC(h->p_ctl, h->p_ctl_words * sizeof(unsigned));
+#if DFLASH_PHASE_TRACE
+      h->p_trace_words = (size_t)h->num_sms * (2 + 6 * L) * kTraceSlots;
+      ALLOC(h->p_trace, h->p_trace_words * sizeof(unsigned long long));
+      cudaMemsetAsync(h->p_trace, 0, h->p_trace_words * sizeof(unsigned long long), st);
+#endif
       cudaError_t e1 = cudaMemcpy(h->p_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
       if (e1 != cudaSuccess) {
         cuda_fail(h, e1, "persistent forward tables");
@@ -973,6 +981,24 @@ int dflash_device_status(dflash_handle* h, dflash_stream stream, uint32_t* flags
          "counter reset");
     CK(cudaStreamSynchronize(st), "counter reset sync");
   }
+#if DFLASH_PHASE_TRACE
+  // phase-timeline builds: the last persistent launch's stamps to $DFLASH_TRACE_FILE
+  // (int32 CTAs, int32 phases, int32 slots, then the uint64 stamps)
+  if (h->p_trace) {
+    const char* path = getenv("DFLASH_TRACE_FILE");
+    if (path && *path) {
+      std::vector<unsigned long long> tr(h->p_trace_words);
+      CK(cudaMemcpy(tr.data(), h->p_trace, tr.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost),
+         "trace read");
+      if (FILE* f = fopen(path, "wb")) {
+        const int32_t hdr[3] = {h->num_sms, 2 + 6 * h->cfg.n_layers, kTraceSlots};
+        fwrite(hdr, sizeof(hdr), 1, f);
+        fwrite(tr.data(), sizeof(unsigned long long), tr.size(), f);
+        fclose(f);
+      }
+    }
+  }
+#endif
   if (flags) *flags = v;
   if (v) return fail(h, DFLASH_EDEVICE, "device-side check fired (see flags)");
   return DFLASH_OK;

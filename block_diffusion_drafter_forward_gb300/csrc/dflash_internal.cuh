@@ -158,6 +158,8 @@ struct dflash_handle {
   void* p_maps = nullptr;              // device CUtensorMap table
   unsigned* p_ctl = nullptr;           // control words, zeroed before each launch
   size_t p_ctl_words = 0;
+  unsigned long long* p_trace = nullptr;  // phase timeline (DFLASH_PHASE_TRACE builds only)
+  size_t p_trace_words = 0;
 
   unsigned* d_status = nullptr;        // device status word
   dflash::Prof prof;

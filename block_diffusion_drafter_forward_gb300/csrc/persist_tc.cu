@@ -156,6 +156,24 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* ptr) {
   return v;
 }
 
+// Phase timeline (DFLASH_PHASE_TRACE builds): %globaltimer into slot `slot` of (CTA, phase).
+//   0 epilogue warps past the phase barrier      1 activation producer past the barrier
+//   2 first weight copy of the phase issued        3 last MMA of the phase committed
+//   4 first accumulator (or attention Q) ready     5 split-K partials counted (finisher)
+//   6 split-K partials landed / last attention item done
+//   7 phase arrival
+__device__ __forceinline__ void trace_stamp(const PersistParams& p, int ph, int slot) {
+#if DFLASH_PHASE_TRACE
+  if (p.trace) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    p.trace[((size_t)blockIdx.x * (2 + 6 * p.L) + ph) * kTraceSlots + slot] = t;
+  }
+#else
+  (void)p; (void)ph; (void)slot;
+#endif
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -689,6 +707,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         const CUtensorMap* wm = p.maps + gp.wmap;
         SegIter it((gp.N + 127) / 128, gp.K / 64, G, c);
         Seg sg;
+        bool first_w = true;
         while (it.next(sg) && !*ab) {
           for (int kk = 0; kk < sg.nkb; ++kk, ++j) {
             const int s = j % kS, u = j / kS;
@@ -697,6 +716,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             // adds its copy to the same phase, before or after this arrive)
             mbar_arrive_expect_tx(&B.full[s], kStage);
             tma_load_2d(stage(s), wm, &B.full[s], (sg.kb0 + kk) * 64, sg.tile * 128, pol);
+            if (first_w) { trace_stamp(p, ph, 2); first_w = false; }
           }
         }
       }
@@ -717,6 +737,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         while (it.next(sg) && !*ab) {
           if (!waited) {
             grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+            trace_stamp(p, ph, 1);
             waited = true;
           }
           for (int kk = 0; kk < sg.nkb && !*ab; ++kk, ++j) {
@@ -760,6 +781,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
           mma_commit(&B.acc_full[buf]);
           ++segc;
         }
+        trace_stamp(p, ph, 3);
       }
     }
     __syncwarp();
@@ -781,6 +803,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
           int pre = 0;
           if (kind == PH_ATTN && t == 0) pre = attn_prefetch(p, l, c / splits, c % splits, sA + kAP + kAQ, B);
           if (t == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+          if (t == 0) trace_stamp(p, ph, 0);
           epi_sync();
           for (int i = c; i < items && !*ab; i += G) {
             if (kind == PH_ATTN) {
@@ -792,6 +815,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
               epi_sync();  // the landing buffer is reused by the next item
             }
           }
+          if (t == 0) trace_stamp(p, ph, 6);
         }
       } else {
         // GEMM epilogues of this CTA's segments
@@ -833,6 +857,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         while (it.next(sg)) {
           if (first) {
             if (t == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+            if (t == 0) trace_stamp(p, ph, 0);
             epi_sync();
             if (e.ss_in && t < TN) rsc[t] = t < p.M ? row_rscale(p, e.ss_in, t) : 1.f;
             epi_sync();
@@ -848,6 +873,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
           }
           const int buf = segc & 1;
           wait_ab(&B.acc_full[buf], (segc >> 1) & 1, ab, p.gabort);
+          if (t == 0) trace_stamp(p, ph, 4);
           tc_fence_after();
           const uint32_t acc = B.tmem + buf * kAccCols + lane_off;
           float v[16];
@@ -884,6 +910,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
               }
               __syncwarp();
             }
+            if (t == 0) trace_stamp(p, ph, 5);
             if (t == 0) {
               p.counters[sg.tile] = 0;  // re-armed for the next phase (ordered by its barrier)
               if (nother <= kRedMax && !*ab) {
@@ -895,6 +922,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             }
             if (nother <= kRedMax) {
               wait_ab(&B.red_full, red_use & 1, ab, p.gabort);
+              if (t == 0) trace_stamp(p, ph, 6);
               ++red_use;
               for (int rk = 0; rk < nother; ++rk) {
                 const float4* src = reinterpret_cast<const float4*>(sRed + (size_t)(rk * kEThreads + t) * TN * 4);
@@ -953,6 +981,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
       // phase done on this CTA
       epi_sync();
       if (t == 0) grid_arrive(&p.bar[ph]);
+      if (t == 0) trace_stamp(p, ph, 7);
     }
   }
   tc_fence_before();

@@ -57,7 +57,15 @@ struct PersistParams {
   unsigned* bar;                    // [3 + 6L] phase arrival counters
   int* gabort;                      // grid-wide "a wait gave up" flag
   unsigned* status;
+  // Phase timeline (builds with DFLASH_PHASE_TRACE=1 only; else unused and null):
+  // [G][phases][kTraceSlots] %globaltimer stamps, see persist_tc.cu.
+  unsigned long long* trace;
 };
+
+#ifndef DFLASH_PHASE_TRACE
+#define DFLASH_PHASE_TRACE 0
+#endif
+constexpr int kTraceSlots = 8;
 
 // Tokens (M = 16 * nb) the persistent kernel handles: one sequence (bf16 lm_head only); larger
 // batches and the FP8 lm_head use the per-projection kernels.

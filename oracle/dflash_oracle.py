@@ -22,6 +22,8 @@ What it follows (page = the source listing it is read from):
       - FP8 "Phase G" block: weight-only e4m3 with a per-output-row fp32 scale
   * spark_model `layers/dflash_head.rs` (Atlas docs): batched propose stacks
     sequences seq-major, gamma rows each; row 0 of each band is the anchor echo.
+  * DSpark Markov head (memra `dflash.rs` draft step, Markov chain block; Atlas
+    `dflash_head.rs` DSpark fields): `markov_chain` below.
 
 Readings where the pages leave a step open (each is also listed in the design notes):
   eps inside the square root; NeoX rotate-half RoPE over the full head_dim;
@@ -252,6 +254,37 @@ def fp8_quantize_rows(w: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     return e4m3_encode(ratio), scale
 
 
+# ----------------------------------------------------------------------------- DSpark Markov chain
+
+
+def markov_chain(z: np.ndarray, bonus: int, w1: np.ndarray, w2: np.ndarray):
+    """Semi-autoregressive Markov fix-up of one band's draft logits (memra-engine dflash.rs,
+    draft step of generate_spec_dflash, the SEMI-AR MARKOV CHAIN block; Atlas dflash_head.rs,
+    DSpark heads: markov_w1 [V, rank] prev-token table, markov_w2 [V, rank] = Linear(rank, V)).
+
+    z: [b-1, V] logits of block rows 1..b-1.  Left to right, starting from the bonus token:
+        chain_0 = bonus
+        for k = 0 .. b-2:
+            f      = w1[chain_k]                       (rank-vector of the previous token)
+            z_k   += w2 @ f                            (bias_v = sum_j w2[v, j] f_j)
+            chain_{k+1} = argmax_v z_k                 (ties -> lowest id)
+    Returns (adjusted logits [b-1, V], tokens chain_1..chain_{b-1} [b-1], top-1 minus top-2
+    margins of the adjusted rows [b-1])."""
+    z = np.array(z, dtype=np.float64, copy=True)
+    w1 = np.asarray(w1, dtype=np.float64)
+    w2 = np.asarray(w2, dtype=np.float64)
+    prev = int(bonus)
+    tokens = np.empty(z.shape[0], dtype=np.int64)
+    margins = np.empty(z.shape[0], dtype=np.float64)
+    for k in range(z.shape[0]):
+        z[k] += w2 @ w1[prev]
+        idx, margin = Oracle.argmax_rows(z[k:k + 1])
+        prev = int(idx[0])
+        tokens[k] = prev
+        margins[k] = margin[0]
+    return z, tokens, margins
+
+
 # ----------------------------------------------------------------------------- the drafter
 
 
@@ -416,6 +449,18 @@ class Oracle:
         z = self.logits(h)
         tok, margin = self.argmax_rows(z[1:])
         return z, tok, margin
+
+    # ---- DSpark Markov head: dflash.rs draft step, semi-AR Markov chain
+
+    def drafts_markov(self, h: np.ndarray, bonus: int):
+        """Drafts with the DSpark Markov fix-up (see markov_chain): logits of rows 1..gamma-1,
+        then the left-to-right chain from the bonus token.  Returns (row-0 logits [V],
+        adjusted logits [gamma-1, V], tokens [gamma-1], margins [gamma-1])."""
+        z = self.logits(h)
+        w1 = to_f64(self.w.get("markov_w1", keep=self.cache), self.cfg.dtype)
+        w2 = to_f64(self.w.get("markov_w2", keep=self.cache), self.cfg.dtype)
+        adj, tok, margin = markov_chain(z[1:], bonus, w1, w2)
+        return z[0], adj, tok, margin
 
     # ---- whole sequence: features -> cache -> block forward
 

@@ -21,6 +21,7 @@ fp32 normals come straight from numpy's standard_normal.
 """
 from __future__ import annotations
 
+import math
 import os
 import statistics
 import zlib
@@ -53,6 +54,7 @@ class DrafterConfig:
     yarn: Optional[Tuple[float, float, float, float]] = None
     sliding_window: int = 0
     layer_sliding: Tuple[bool, ...] = ()
+    markov_rank: int = 0          # DSpark Markov head rank (0: none)
     dtype: str = "bf16"          # 'f32' or 'bf16': weights, activations and KV cache
     lm_head_dtype: str = "bf16"  # same as dtype, or 'fp8' (e4m3 + per-row fp32 scale)
     page_size: int = 16
@@ -98,6 +100,13 @@ CONFIGS: Dict[str, DrafterConfig] = {
     "small_gqa4_bf16": DrafterConfig(
         name="small_gqa4_bf16", hidden=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, n_ff=2048,
         n_layers=2, vocab=8192, n_taps=2, target_hidden=1024),
+    # DSpark Markov head (rank 256, as in the pages' DSpark drafter) on the 8-layer drafter, and
+    # a rank-32 head on the tiny fp32 drafter
+    "qwen3_8l_markov": DrafterConfig(name="qwen3_8l_markov", markov_rank=256, **_C2_ARCH),
+    "tiny_fp32_markov": DrafterConfig(
+        name="tiny_fp32_markov", hidden=256, n_q_heads=4, n_kv_heads=1, head_dim=64, n_ff=512,
+        n_layers=1, vocab=2048, n_taps=3, target_hidden=256, dtype="f32", lm_head_dtype="f32",
+        markov_rank=32),
     "small_gqa8_bf16": DrafterConfig(
         name="small_gqa8_bf16", hidden=1024, n_q_heads=8, n_kv_heads=1, head_dim=128, n_ff=2048,
         n_layers=2, vocab=8192, n_taps=2, target_hidden=1024),
@@ -235,6 +244,12 @@ class Weights:
             return (H,), 1.0, 0.05
         if name in ("embed", "lm_head"):
             return (c.vocab, H), 0.0, 0.02
+        # DSpark Markov head: a unit-variance previous-token table and a projection scaled so
+        # the bias w2 . w1[prev] has about unit spread, the spread of the logits themselves
+        if name == "markov_w1":
+            return (c.vocab, c.markov_rank), 0.0, 1.0
+        if name == "markov_w2":
+            return (c.vocab, c.markov_rank), 0.0, 1.0 / math.sqrt(c.markov_rank)
         layer, t = name.split(".")
         assert layer[0] == "L" and 0 <= int(layer[1:]) < c.n_layers, name
         return {
@@ -253,6 +268,8 @@ class Weights:
 
     def names(self) -> List[str]:
         out = ["fc", "hidden_norm", "norm", "embed", "lm_head"]
+        if self.cfg.markov_rank > 0:
+            out += ["markov_w1", "markov_w2"]
         for l in range(self.cfg.n_layers):
             out += [f"L{l}.{t}" for t in self.LAYER_TENSORS]
         return out

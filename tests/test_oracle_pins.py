@@ -625,3 +625,91 @@ def test_logits_do_not_depend_on_the_vocabulary_chunking():
         np.testing.assert_allclose(o.logits(h, chunk=300), o.logits(h), rtol=1e-13, atol=1e-15)
         # rows are independent: a subset of rows gives the same rows
         np.testing.assert_allclose(o.logits(h[3:5], chunk=7), o.logits(h)[3:5], rtol=1e-13, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------- DSpark Markov chain
+
+
+def test_markov_zero_projection_is_the_plain_argmax():
+    z = RNG.standard_normal((15, 40))
+    w1 = RNG.standard_normal((40, 8))
+    adj, tok, margin = O.markov_chain(z, 3, w1, np.zeros((40, 8)))
+    np.testing.assert_array_equal(adj, z)
+    idx, m = O.Oracle.argmax_rows(z)
+    assert tok.tolist() == idx.tolist() and np.allclose(margin, m)
+
+
+def test_markov_shift_chain_closed_form():
+    """w1 = identity and w2 = alpha * (the permutation v -> v + 3 mod V): each step's bias is
+    alpha on the successor of the previous token, so the chain walks bonus + 3, bonus + 6, ...
+    whatever the (small) logits, and each adjusted row is z plus alpha at that token."""
+    V, alpha, bonus = 11, 100.0, 4
+    perm = np.zeros((V, V))
+    for v in range(V):
+        perm[(v + 3) % V, v] = 1.0               # w2 @ e_v = e_{v+3}
+    z = 0.1 * RNG.standard_normal((15, V))
+    adj, tok, margin = O.markov_chain(z, bonus, np.eye(V), alpha * perm)
+    expect = [(bonus + 3 * (k + 1)) % V for k in range(15)]
+    assert tok.tolist() == expect
+    for k in range(15):
+        row = z[k].copy()
+        row[expect[k]] += alpha
+        np.testing.assert_allclose(adj[k], row, rtol=0, atol=1e-12)
+    assert np.all(margin > alpha - 1)
+
+
+def test_markov_bias_uses_the_realised_previous_token():
+    """Row 0's plain argmax is token 1, but the bias of the bonus (0) moves it to 2; row 1's bias
+    must then come from 2 (giving 4), not from the plain argmax 1 (giving 3) or the bonus (2)."""
+    V = 5
+    w2 = np.zeros((V, V))
+    w2[2, 0] = 2.0       # prev 0 -> +2 on token 2
+    w2[3, 1] = 1.0       # prev 1 -> +1 on token 3
+    w2[4, 2] = 1.0       # prev 2 -> +1 on token 4
+    z = np.zeros((2, V))
+    z[0, 1] = 1.0
+    _, tok, _ = O.markov_chain(z, 0, np.eye(V), w2)
+    assert tok.tolist() == [2, 4]
+
+
+def test_markov_matches_explicit_loops():
+    """A rank smaller than the vocabulary, random tables, against plain Python loops over the
+    definition bias_v = sum_j w2[v][j] * w1[prev][j] with a first-maximum argmax."""
+    V, R, b = 13, 4, 6
+    rng = np.random.default_rng(7)
+    z = rng.standard_normal((b - 1, V))
+    w1 = rng.standard_normal((V, R))
+    w2 = rng.standard_normal((V, R))
+    prev, toks, rows = 9, [], []
+    for k in range(b - 1):
+        row = [float(z[k][v]) + sum(float(w2[v][j]) * float(w1[prev][j]) for j in range(R)) for v in range(V)]
+        best = 0
+        for v in range(1, V):
+            if row[v] > row[best]:
+                best = v
+        toks.append(best)
+        rows.append(row)
+        prev = best
+    adj, tok, _ = O.markov_chain(z, 9, w1, w2)
+    assert tok.tolist() == toks
+    np.testing.assert_allclose(adj, np.array(rows), rtol=1e-12, atol=1e-12)
+
+
+def test_markov_head_in_the_drafter():
+    """The tiny drafter with a rank-32 head: with w2 zeroed the Markov drafts are the plain
+    drafts; with the seeded head at least one draft changes (the head is not a no-op)."""
+    cfg = CONFIGS["tiny_fp32_markov"]
+    W = make_weights(cfg, 1)
+    wl = make_workload(cfg, 1, [64])
+    taps = workload_taps(wl, 0, 0, 64)
+    o = O.Oracle(cfg, W, cache=True)
+    ref = o.run_sequence(taps, wl.ctx_positions(0, 0, 64), 77)
+    zero = O.Oracle(cfg, DictWeights(W, {"markov_w2": np.zeros((cfg.vocab, cfg.markov_rank), np.float32)}))
+    z0, adj0, tok0, _ = zero.drafts_markov(ref["h"], 77)
+    assert tok0.tolist() == ref["tokens"].tolist()
+    np.testing.assert_allclose(z0, ref["logits"][0], rtol=1e-12)
+    _, adj, tok, _ = o.drafts_markov(ref["h"], 77)
+    assert tok.tolist() != ref["tokens"].tolist()
+    w1 = W.get("markov_w1").astype(np.float64)
+    w2 = W.get("markov_w2").astype(np.float64)
+    np.testing.assert_allclose(adj[0], ref["logits"][1] + w2 @ w1[77], rtol=1e-12, atol=1e-12)
