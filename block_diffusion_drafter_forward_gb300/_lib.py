@@ -50,6 +50,7 @@ class dflash_cfg(ctypes.Structure):
         ("dtype", ctypes.c_int32), ("lm_head_dtype", ctypes.c_int32),
         ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("max_batch", ctypes.c_int32),
         ("max_pages_per_seq", ctypes.c_int32), ("max_write_rows", ctypes.c_int32),
+        ("markov_rank", ctypes.c_int32),
     ]
 
 
@@ -61,7 +62,8 @@ class dflash_layer_weights(ctypes.Structure):
 class dflash_weights(ctypes.Structure):
     _fields_ = [("fc", ctypes.c_void_p), ("hidden_norm", ctypes.c_void_p), ("norm", ctypes.c_void_p),
                 ("embed", ctypes.c_void_p), ("lm_head", ctypes.c_void_p),
-                ("layers", ctypes.POINTER(dflash_layer_weights))]
+                ("layers", ctypes.POINTER(dflash_layer_weights)),
+                ("markov_w1", ctypes.c_void_p), ("markov_w2", ctypes.c_void_p)]
 
 
 EXPORTS = ("dflash_create", "dflash_destroy", "dflash_write_ctx_kv", "dflash_propose", "dflash_kv_layout",

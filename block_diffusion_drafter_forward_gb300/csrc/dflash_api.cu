@@ -13,6 +13,7 @@
 #include "dflash_internal.cuh"
 #include "attn_tc.cuh"
 #include "gemm_tc.cuh"
+#include "markov.cuh"
 #include "persist_tc.cuh"
 
 using namespace dflash;
@@ -189,6 +190,13 @@ int check_cfg(const dflash_cfg& c) {
   for (int l = 0; l < c.n_layers; ++l)
     if (c.layer_sliding[l] && c.sliding_window <= 0) return bad("sliding layer with sliding_window <= 0");
   if ((int64_t)c.max_pages_per_seq * kPage > (1ll << 30)) return bad("max_pages_per_seq too large");
+  if (c.markov_rank < 0) return bad("markov_rank must be >= 0");
+  if (c.markov_rank > 0 &&
+      (c.markov_rank % 32 || c.markov_rank > kMarkovMaxRank || c.max_batch > kMarkovMaxBatch ||
+       markov_smem_bytes(c.max_batch, c.markov_rank) > (size_t)kMarkovMaxSmem))
+    return fail(nullptr, DFLASH_EUNSUPPORTED,
+                "Markov head needs markov_rank % 32 == 0, rank <= 1024, max_batch <= 64 and "
+                "max_batch * rank <= 40960");
   return DFLASH_OK;
 }
 
@@ -365,6 +373,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
     p.amax_counter = h->counters + kCounters - 64;
     p.drafts = draft_tokens;
     p.row_scale = fp8 ? h->lm_scale : nullptr;
+    p.logits32 = c.markov_rank > 0 ? h->logits32 : nullptr;  // the Markov head reads fp32 logits
     KL(K_LMHEAD, launch_gemm_tc(EPI_LMHEAD, fp8 ? (const void*)h->lm_fp8 : h->lm_head, c.vocab, H, h->xn, H, M, p, 1,
                                 st, false, fp8),
        "lm_head");
@@ -400,6 +409,8 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
   const dflash_cfg& c = *cfg;
   if (!w->fc || !w->hidden_norm || !w->norm || !w->embed || !w->lm_head || !w->layers)
     return fail(nullptr, DFLASH_EINVAL, "null weight pointer");
+  if (c.markov_rank > 0 && (!w->markov_w1 || !w->markov_w2))
+    return fail(nullptr, DFLASH_EINVAL, "null Markov head weight pointer");
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& lw = w->layers[l];
     if (!lw.ln_in || !lw.wq || !lw.wk || !lw.wv || !lw.q_norm || !lw.k_norm || !lw.wo || !lw.ln_post ||
@@ -499,6 +510,23 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     D2D((char*)h->kn_all + l * hd * es, lw.k_norm, hd * es);
   }
 
+  // ---- DSpark Markov head: both tables copied; per-step control words
+  if (c.markov_rank > 0) {
+    const size_t mb = (size_t)V * c.markov_rank * es;
+    ALLOC(h->mk_w1, mb);
+    D2D(h->mk_w1, w->markov_w1, mb);
+    ALLOC(h->mk_w2, mb);
+    D2D(h->mk_w2, w->markov_w2, mb);
+    h->mk_ctl_bytes = markov_ctl_bytes(c.max_batch);
+    ALLOC(h->mk_ctl, h->mk_ctl_bytes);
+    int per_sm = 0;
+    if (markov_occupancy(c.dtype, c.max_batch, c.markov_rank, &per_sm) != cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      fail(h, DFLASH_EUNSUPPORTED, "the Markov-chain kernel cannot keep one CTA per SM for this batch and rank");
+      return bail(DFLASH_EUNSUPPORTED);
+    }
+  }
+
   // ---- RoPE table
   std::vector<double> inv_pi;
   rope_table(c, inv_pi, h->rope_mscale);
@@ -584,7 +612,7 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     // single-launch persistent forward for batch 1: needs the tensor-core attention, a bf16
     // lm_head, one resident CTA per SM, and at least one (tile, k-block) unit of every projection
     // per CTA (its split-K finisher counts every CTA between a tile's first and last owner)
-    if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && H <= persist_max_hidden() &&
+    if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && c.markov_rank == 0 && H <= persist_max_hidden() &&
         L <= kPersistMaxL && persist_every_cta_has_work(H, F, nh, nkv, V, h->num_sms)) {
       int per_sm = 0;
       if (persist_occupancy(&per_sm) == cudaSuccess && per_sm >= 1) h->persist_ok = true;
@@ -792,12 +820,36 @@ int propose_simple(dflash_handle* h, const int32_t* bonus_tokens, const int32_t*
   return DFLASH_OK;
 }
 
+// DSpark Markov head after the lm_head (dflash.rs draft step, semi-AR Markov chain): the
+// drafts (and logit rows 1..15 of every band, when written) are replaced by the chain's.
+int propose_markov(dflash_handle* h, const int32_t* bonus_tokens, int nb, int32_t* draft_tokens, void* logits,
+                   cudaStream_t st) {
+  const dflash_cfg& c = h->cfg;
+  MarkovParams m{};
+  m.z = h->logits32;
+  m.w1 = h->mk_w1;
+  m.w2 = h->mk_w2;
+  m.V = c.vocab;
+  m.R = c.markov_rank;
+  m.nb = nb;
+  m.bonus = bonus_tokens;
+  m.drafts = draft_tokens;
+  m.logits = logits;
+  m.status = h->d_status;
+  markov_bind_ctl(m, h->mk_ctl, nb);
+  CK(cudaMemsetAsync(h->mk_ctl, 0, h->mk_ctl_bytes, st), "Markov control reset");
+  KL(K_MARKOV, launch_markov(c.dtype, m, h->num_sms, st), "Markov chain");
+  return DFLASH_OK;
+}
+
 int propose_eager(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens, const int32_t* page_tables,
                   int nb, int max_ctx_len, int32_t* draft_tokens, void* logits, void* final_hidden, cudaStream_t st) {
-  if (h->tc)
-    return propose_tc(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits, final_hidden, st);
-  return propose_simple(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits, final_hidden,
-                        st);
+  const int rc = h->tc ? propose_tc(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits,
+                                    final_hidden, st)
+                       : propose_simple(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits,
+                                        final_hidden, st);
+  if (rc != DFLASH_OK || h->cfg.markov_rank == 0) return rc;
+  return propose_markov(h, bonus_tokens, nb, draft_tokens, logits, st);
 }
 
 // Replay the CUDA graph captured for these arguments (capturing it on first use on a private

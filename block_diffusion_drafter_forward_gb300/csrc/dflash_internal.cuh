@@ -57,12 +57,12 @@ template <> struct Elem<__nv_bfloat16> {
 // ---------------------------------------------------------------- profiling
 enum Kind {
   K_EMBED, K_NORM, K_QKV, K_QKV_POST, K_ATTN, K_OPROJ, K_GATEUP, K_SILU, K_DOWN, K_LMHEAD, K_ARGMAX,
-  K_COPY, K_W_FC, K_W_NORM, K_W_KV, K_W_POST, K_PERSIST, K_COUNT
+  K_COPY, K_W_FC, K_W_NORM, K_W_KV, K_W_POST, K_PERSIST, K_MARKOV, K_COUNT
 };
 static const char* const kKindNames[K_COUNT] = {
     "embed", "rmsnorm", "qkv_gemm", "qkv_post", "attention", "o_proj_gemm", "gate_up_gemm", "silu_mul",
     "down_gemm", "lm_head", "argmax", "copy", "writer_fc_gemm", "writer_norm", "writer_kv_gemm", "writer_post",
-    "persistent_forward"};
+    "persistent_forward", "markov_chain"};
 
 struct Prof {
   bool on = false;
@@ -160,6 +160,11 @@ struct dflash_handle {
   size_t p_ctl_words = 0;
   unsigned long long* p_trace = nullptr;  // phase timeline (DFLASH_PHASE_TRACE builds only)
   size_t p_trace_words = 0;
+  // DSpark Markov head (cfg.markov_rank > 0)
+  void* mk_w1 = nullptr;               // [V, rank] cfg.dtype (owned copy)
+  void* mk_w2 = nullptr;               // [V, rank]
+  void* mk_ctl = nullptr;              // per-step argmax keys and barriers, zeroed before each launch
+  size_t mk_ctl_bytes = 0;
 
   unsigned* d_status = nullptr;        // device status word
   dflash::Prof prof;

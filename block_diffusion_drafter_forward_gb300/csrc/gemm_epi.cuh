@@ -316,6 +316,7 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
       const int m = m0 + c0 + c;
       const float z = v[c] * sc * (p.ss_in ? rsc[c0 + c] : 1.f);
       if (p.logits && valid_row && m < p.M) p.logits[(int64_t)m * p.N + n] = __float2bfloat16_rn(z);
+      if (p.logits32 && valid_row && m < p.M) p.logits32[(int64_t)m * p.N + n] = z;
       es.xch[t][c] = valid_row ? z : -FLT_MAX;
     }
     epi_sync();

@@ -51,6 +51,7 @@ struct GemmParams {
   int F = 0;
   // EPI_LMHEAD
   __nv_bfloat16* logits = nullptr;
+  float* logits32 = nullptr;              // fp32 logits [M, N] as well (the Markov head reads them)
   const float* row_scale = nullptr;
   // per token row: max over vocabulary tiles of (orderable logit << 32 | ~index), combined
   // with 64-bit atomicMax (order-independent, so deterministic); zero between launches

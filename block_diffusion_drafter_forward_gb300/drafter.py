@@ -35,6 +35,7 @@ def make_cfg(cfg, num_pages: int, max_batch: int, max_pages_per_seq: int, max_wr
     c.max_batch = int(max_batch)
     c.max_pages_per_seq = int(max_pages_per_seq)
     c.max_write_rows = int(max_write_rows)
+    c.markov_rank = int(getattr(cfg, "markov_rank", 0))
     return c
 
 
@@ -76,6 +77,9 @@ def weight_shapes(cfg) -> Dict[str, Tuple[int, ...]]:
              "wo": (H, qd), "ln_post": (H,), "w_gate": (F, H), "w_up": (F, H), "w_down": (H, F)}
     for l in range(cfg.n_layers):
         out.update({f"L{l}.{t}": sh for t, sh in layer.items()})
+    R = int(getattr(cfg, "markov_rank", 0))
+    if R > 0:
+        out.update({"markov_w1": (V, R), "markov_w2": (V, R)})
     return out
 
 
@@ -102,6 +106,9 @@ class Drafter:
         w = L.dflash_weights()
         for t in ("fc", "hidden_norm", "norm", "embed", "lm_head"):
             setattr(w, t, tensors[t].data_ptr())
+        if int(getattr(cfg, "markov_rank", 0)) > 0:
+            w.markov_w1 = tensors["markov_w1"].data_ptr()
+            w.markov_w2 = tensors["markov_w2"].data_ptr()
         w.layers = layers
         self._w = w
         self.handle = L.dflash_create(self.ccfg, w, _stream(stream))

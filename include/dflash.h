@@ -94,6 +94,8 @@ typedef struct {
   int32_t max_batch;        /* largest nb passed to dflash_propose */
   int32_t max_pages_per_seq;/* row stride of page tables; capacity = 16 * this rows */
   int32_t max_write_rows;   /* rows per internal chunk of dflash_write_ctx_kv (>= 16) */
+  int32_t markov_rank;      /* DSpark Markov head rank; 0 = no head.  Otherwise a multiple of 32,
+                               <= 1024, with max_batch <= 64 and max_batch * rank <= 40960 */
 } dflash_cfg;
 
 /* One layer's weights, HF layout (Linear weights [out, in] row-major), all in cfg.dtype,
@@ -120,6 +122,10 @@ typedef struct {
   const void* lm_head;      /* [V, H] target lm_head (cfg.dtype): BORROWED when lm_head_dtype
                                == dtype; read once to quantise when it is FP8 */
   const dflash_layer_weights* layers; /* host array of n_layers entries */
+  /* DSpark Markov head (read when cfg.markov_rank > 0, copied; dflash.rs draft step, Markov
+   * chain block; dflash_head.rs DSpark fields), cfg.dtype, row-major: */
+  const void* markov_w1;    /* [V, rank] previous-token table */
+  const void* markov_w2;    /* [V, rank] Linear(rank, V) weight */
 } dflash_weights;
 
 /* Create a drafter: validates cfg, copies and repacks the layer weights into
@@ -161,6 +167,10 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
  *   logits       [nb*gamma, V] cfg.dtype (fp32 when dtype is F32, bf16 otherwise),
  *                all gamma rows of every band; NULL = not written.
  *   final_hidden [nb*gamma, H] cfg.dtype, final-normed hidden; NULL = not written.
+ * With a Markov head (cfg.markov_rank > 0) the drafts come from the DSpark semi-autoregressive
+ * chain instead (dflash.rs draft step): from chain_0 = bonus_tokens[s], for k = 0..gamma-2,
+ * logits row k+1 += markov_w2 . markov_w1[chain_k] and chain_{k+1} = its argmax; drafts are
+ * chain_1..chain_{gamma-1}, and logit rows 1..gamma-1 (when written) carry the added bias.
  * Inputs: bonus_tokens [nb] int32, ctx_lens [nb] int32, page_tables
  * [nb, max_pages_per_seq] int32 (row s = sequence s's pages; entries past
  * ceil((ctx_lens[s]+gamma)/16) are not read).  max_ctx_len is a HOST upper bound of

@@ -338,8 +338,9 @@ class Oracle:
 
     # ---- block path: dflash.rs forward_round + final norm
 
-    def block_tokens(self, bonus: int) -> np.ndarray:
-        g = self.cfg.gamma
+    def block_tokens(self, bonus: int, width: Optional[int] = None) -> np.ndarray:
+        """[bonus, mask x (b - 1)], b = width (default gamma)."""
+        g = self.cfg.gamma if width is None else int(width)
         tok = np.full(g, self.cfg.mask_token_id, dtype=np.int64)
         tok[0] = bonus
         return tok
@@ -350,17 +351,23 @@ class Oracle:
 
     def forward_block(self, k_ctx: Sequence[np.ndarray], v_ctx: Sequence[np.ndarray],
                       ctx_pos: np.ndarray, bonus: int, ctx_len: int,
-                      layer_hook=None, block_pos0: Optional[int] = None) -> np.ndarray:
-        """One gamma-block forward for one sequence over its cached context K/V
-        (per layer [ctx_len, nkv, hd]); returns the final normed hidden [gamma, H].
-        Block row r sits at position block_pos0 + r, block_pos0 = ctx_len by default
-        (the draft starts at the committed length)."""
+                      layer_hook=None, block_pos0: Optional[int] = None,
+                      width: Optional[int] = None) -> np.ndarray:
+        """One block forward for one sequence over its cached context K/V (per layer
+        [ctx_len, nkv, hd]); returns the final normed hidden [b, H], b = width (default gamma;
+        the Atlas head's active block width, dflash_head.rs).
+        Block row r takes RoPE position block_pos0 + r, block_pos0 = ctx_len by default (the
+        draft starts at the committed length; Atlas's q_rope_pos overrides it).  The sliding
+        window is measured on row indices of the sequence: context row i at i, block row r at
+        ctx_len + r (these equal the RoPE positions whenever the positions are 0, 1, 2, ...)."""
         c = self.cfg
-        g, nh, nkv, hd = c.gamma, c.n_q_heads, c.n_kv_heads, c.head_dim
+        g = c.gamma if width is None else int(width)
+        nh, nkv, hd = c.n_q_heads, c.n_kv_heads, c.head_dim
         p0 = ctx_len if block_pos0 is None else int(block_pos0)
         pos_b = np.arange(p0, p0 + g, dtype=np.int64)
-        key_pos = np.concatenate([np.asarray(ctx_pos, dtype=np.int64)[:ctx_len], pos_b])
-        x = self.embed_rows(self.block_tokens(bonus))
+        idx_b = np.arange(ctx_len, ctx_len + g, dtype=np.int64)
+        key_idx = np.arange(ctx_len + g, dtype=np.int64)
+        x = self.embed_rows(self.block_tokens(bonus, g))
         for l in range(c.n_layers):
             L = lambda t: self.W(f"L{l}.{t}")  # noqa: E731
             xn = rms_norm(x, L("ln_in"), c.rms_eps)
@@ -372,7 +379,7 @@ class Oracle:
             keys = np.concatenate([k_ctx[l][:ctx_len], kb], axis=0)
             vals = np.concatenate([v_ctx[l][:ctx_len], vb], axis=0)
             window = c.sliding_window if c.sliding(l) else 0
-            a = block_attention(q, keys, vals, pos_b, key_pos, window).reshape(g, nh * hd)
+            a = block_attention(q, keys, vals, idx_b, key_idx, window).reshape(g, nh * hd)
             x1 = x + a @ L("wo").T
             n = rms_norm(x1, L("ln_post"), c.rms_eps)
             act = silu(n @ L("w_gate").T) * (n @ L("w_up").T)
@@ -401,7 +408,7 @@ class Oracle:
             q = rope(rms_norm(q, L("q_norm"), c.rms_eps), pos_b, self.inv_freq, self.mscale)
             k = rope(rms_norm(k, L("k_norm"), c.rms_eps), pos_all, self.inv_freq, self.mscale)
             window = c.sliding_window if c.sliding(l) else 0
-            a = block_attention(q, k, v, pos_b, pos_all, window).reshape(g, nh * hd)
+            a = block_attention(q, k, v, np.arange(n, n + g), np.arange(n + g), window).reshape(g, nh * hd)
             x1 = x + a @ L("wo").T
             n1 = rms_norm(x1, L("ln_post"), c.rms_eps)
             x = x1 + (silu(n1 @ L("w_gate").T) * (n1 @ L("w_up").T)) @ L("w_down").T
@@ -443,9 +450,8 @@ class Oracle:
         return idx.astype(np.int64), margin
 
     def drafts(self, h: np.ndarray):
-        """Draft tokens = argmax over the vocabulary of rows 1..gamma-1 (row 0 is the
-        anchor echo and is dropped).  Returns (logits [gamma, V], tokens [gamma-1],
-        margins [gamma-1])."""
+        """Draft tokens = argmax over the vocabulary of rows 1..b-1 of a b-row block (row 0 is
+        the anchor echo and is dropped).  Returns (logits [b, V], tokens [b-1], margins [b-1])."""
         z = self.logits(h)
         tok, margin = self.argmax_rows(z[1:])
         return z, tok, margin
@@ -464,10 +470,11 @@ class Oracle:
 
     # ---- whole sequence: features -> cache -> block forward
 
-    def run_sequence(self, taps: np.ndarray, ctx_pos: np.ndarray, bonus: int):
+    def run_sequence(self, taps: np.ndarray, ctx_pos: np.ndarray, bonus: int,
+                     block_pos0: Optional[int] = None, width: Optional[int] = None):
         """Context of len(taps) rows, then one block: returns dict of K, V, h, z, tokens."""
         f = self.ctx_features(taps)
         ks, vs = self.ctx_kv(f, ctx_pos)
-        h = self.forward_block(ks, vs, ctx_pos, bonus, taps.shape[0])
+        h = self.forward_block(ks, vs, ctx_pos, bonus, taps.shape[0], block_pos0=block_pos0, width=width)
         z, tok, margin = self.drafts(h)
         return dict(f=f, k=ks, v=vs, h=h, logits=z, tokens=tok, margin=margin)

@@ -713,3 +713,45 @@ def test_markov_head_in_the_drafter():
     w1 = W.get("markov_w1").astype(np.float64)
     w2 = W.get("markov_w2").astype(np.float64)
     np.testing.assert_allclose(adj[0], ref["logits"][1] + w2 @ w1[77], rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- block width, RoPE start
+
+
+def test_block_width_is_a_narrower_block():
+    """A width-b block (the Atlas head's active block width) is exactly the forward of a drafter
+    whose block size is b: b rows [bonus, mask x (b-1)], attending to the context and to those b
+    rows only.  It is not the first b rows of the full block (whose extra mask rows are keys)."""
+    import dataclasses
+    cfg, wl, W = tiny()
+    o = O.Oracle(cfg, W, cache=True)
+    f = o.ctx_features(workload_taps(wl, 0, 0, 64))
+    pos = np.arange(64)
+    ks, vs = o.ctx_kv(f, pos)
+    full = o.forward_block(ks, vs, pos, 5, 64)
+    np.testing.assert_array_equal(o.forward_block(ks, vs, pos, 5, 64, width=16), full)
+    for b in (2, 7):
+        hb = o.forward_block(ks, vs, pos, 5, 64, width=b)
+        ob = O.Oracle(dataclasses.replace(cfg, gamma=b), W, cache=True)
+        np.testing.assert_allclose(hb, ob.forward_block(ks, vs, pos, 5, 64), rtol=1e-12, atol=1e-12)
+        assert hb.shape == (b, cfg.hidden) and np.abs(hb - full[:b]).max() > 1e-3
+        z, tok, _ = o.drafts(hb)
+        assert z.shape == (b, cfg.vocab) and tok.shape == (b - 1,)
+
+
+def test_window_is_measured_on_row_indices():
+    """The sliding window counts rows of the sequence (context row i at i, block row r at
+    ctx_len + r), not RoPE positions: with the block's RoPE start moved 5000 past the context, a
+    window covering every row changes nothing, while a window of 20 rows does mask keys."""
+    import dataclasses
+    cfg0, wl, W = tiny()
+    cfg_w = dataclasses.replace(cfg0, sliding_window=80, layer_sliding=(True,))
+    o_full, o_w = O.Oracle(cfg0, W, cache=True), O.Oracle(cfg_w, W, cache=True)
+    f = o_full.ctx_features(workload_taps(wl, 0, 0, 64))
+    pos = np.arange(64)
+    ks, vs = o_full.ctx_kv(f, pos)
+    a = o_full.forward_block(ks, vs, pos, 5, 64, block_pos0=5064)
+    b = o_w.forward_block(ks, vs, pos, 5, 64, block_pos0=5064)
+    np.testing.assert_array_equal(a, b)
+    o_20 = O.Oracle(dataclasses.replace(cfg0, sliding_window=20, layer_sliding=(True,)), W, cache=True)
+    assert np.abs(o_20.forward_block(ks, vs, pos, 5, 64, block_pos0=5064) - a).max() > 1e-3
