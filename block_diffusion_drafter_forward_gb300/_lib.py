@@ -26,6 +26,7 @@ DFLASH_DEV_BAD_PAGE = 0x1
 DFLASH_DEV_BAD_CTX = 0x2
 DFLASH_DEV_BAD_TOKEN = 0x4
 DFLASH_DEV_TIMEOUT = 0x8
+DFLASH_DEV_BAD_WIDTH = 0x10
 
 STATUS_NAMES = {0: "OK", -1: "EINVAL", -2: "ENOMEM", -3: "ECUDA", -4: "ECAPACITY", -5: "EUNSUPPORTED",
                 -6: "EDEVICE"}
@@ -69,7 +70,8 @@ class dflash_weights(ctypes.Structure):
 EXPORTS = ("dflash_create", "dflash_destroy", "dflash_write_ctx_kv", "dflash_propose", "dflash_kv_layout",
            "dflash_device_status", "dflash_last_error", "dflash_fp8_lm_head", "dflash_profile",
            "dflash_profile_kinds", "dflash_profile_read", "dflash_gemm_bf16",
-           "dflash_attention_check", "dflash_gemm_bf16_noalloc", "dflash_set_persistent", "dflash_persistent")
+           "dflash_attention_check", "dflash_gemm_bf16_noalloc", "dflash_set_persistent", "dflash_persistent",
+           "dflash_propose_ex")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -91,6 +93,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_write_ctx_kv.restype = c.c_int
     lib.dflash_propose.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
     lib.dflash_propose.restype = c.c_int
+    lib.dflash_propose_ex.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.dflash_propose_ex.restype = c.c_int
     lib.dflash_kv_layout.argtypes = [vp, c.POINTER(vp), c.POINTER(c.c_size_t), c.POINTER(c.c_int64)]
     lib.dflash_kv_layout.restype = c.c_int
     lib.dflash_device_status.argtypes = [vp, vp, c.POINTER(c.c_uint32)]
@@ -150,6 +154,17 @@ def dflash_propose(handle: int, bonus_tokens: int, ctx_lens: int, page_tables: i
                                ctypes.c_void_p(page_tables), nb, max_ctx_len, ctypes.c_void_p(draft_tokens),
                                ctypes.c_void_p(logits or None), ctypes.c_void_p(final_hidden or None),
                                ctypes.c_void_p(stream))
+    _check(rc, ctypes.c_void_p(handle))
+
+
+def dflash_propose_ex(handle: int, bonus_tokens: int, ctx_lens: int, page_tables: int, nb: int, max_ctx_len: int,
+                      q_rope_pos: int, widths: int, draft_tokens: int, logits: int = 0, final_hidden: int = 0,
+                      stream: int = 0) -> None:
+    rc = load().dflash_propose_ex(ctypes.c_void_p(handle), ctypes.c_void_p(bonus_tokens), ctypes.c_void_p(ctx_lens),
+                                  ctypes.c_void_p(page_tables), nb, max_ctx_len, ctypes.c_void_p(q_rope_pos or None),
+                                  ctypes.c_void_p(widths or None), ctypes.c_void_p(draft_tokens),
+                                  ctypes.c_void_p(logits or None), ctypes.c_void_p(final_hidden or None),
+                                  ctypes.c_void_p(stream))
     _check(rc, ctypes.c_void_p(handle))
 
 

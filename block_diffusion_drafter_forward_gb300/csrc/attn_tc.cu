@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
   const int c_begin = split * p.chunks_per_split;
   const int c_end = min(nch, c_begin + p.chunks_per_split);
   const int nkeys = ctx + kGamma;
+  const int nvis = ctx + block_width(p.widths, s);  // keys past the active block width are masked
   const int32_t* pt = p.page_tables + (int64_t)s * p.mpps;
   const int npages_seq = (nkeys + kPage - 1) / kPage;
 
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int key = kbase + q4 * 32 + j;
-        const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
+        const bool vis = key < nvis && (p.window <= 0 || pos_q - key < p.window);
         if (vis) mc = fmaxf(mc, v[j] * scale_log2);
       }
     }
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
           for (int u = 0; u < 2; ++u) {
             const int jj = j8 * 8 + 2 * e + u;
             const int key = kbase + q4 * 32 + jj;
-            const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
+            const bool vis = key < nvis && (p.window <= 0 || pos_q - key < p.window);
             pr[u] = vis ? exp2f(v[jj] * scale_log2 - m_new) : 0.f;
           }
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
@@ -357,6 +358,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnPar
   const int n = min(nch, c_begin + p.chunks_per_split) - c_begin;  // chunks of this CTA
   const int nsc = (n + kScChunks - 1) / kScChunks;                  // super-chunks
   const int nkeys = ctx + kGamma;
+  const int nvis = ctx + block_width(p.widths, s);  // keys past the active block width are masked
   const int32_t* pt = p.page_tables + (int64_t)s * p.mpps;
   const int npages_seq = (nkeys + kPage - 1) / kPage;
   const int safe_keys = ctx & ~(kPage - 1);
@@ -494,7 +496,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnPar
       tc_fence_after();
       // every key of the super-chunk visible to every row: no masking
       const int kb = k0 + (c_begin + i * kScChunks) * kKC;
-      const bool full = kb + nchk * kKC <= nkeys && (p.window <= 0 || ctx + kGamma - 1 - kb < p.window);
+      const bool full = kb + nchk * kKC <= nvis && (p.window <= 0 || ctx + kGamma - 1 - kb < p.window);
       float mc = -FLT_MAX;
 #pragma unroll 1
       for (int q4 = 0; q4 < 2 * nchk; ++q4) {
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnPar
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int key = kb + q4 * 32 + j;
-            if (key < nkeys && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[j]);
+            if (key < nvis && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[j]);
           }
         }
       }
@@ -552,7 +554,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnPar
 #pragma unroll
               for (int u = 0; u < 2; ++u) {
                 const int key = kb + (2 * h + q) * 32 + 2 * e + u;
-                const bool vis = key < nkeys && (p.window <= 0 || pos_q - key < p.window);
+                const bool vis = key < nvis && (p.window <= 0 || pos_q - key < p.window);
                 pr[u] = vis ? ex2_approx(fmaf(v[2 * e + u], scale_log2, -m_new)) : 0.f;
               }
               const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);

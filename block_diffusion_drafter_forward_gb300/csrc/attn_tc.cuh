@@ -15,6 +15,7 @@ struct AttnParams {
   PoolGeom g{};
   int layer = 0;
   const int32_t* ctx_lens = nullptr;     // [nb]
+  const int32_t* widths = nullptr;       // [nb] active block widths (null: gamma)
   const int32_t* page_tables = nullptr;  // [nb, mpps]
   int mpps = 0, nh = 0, nkv = 0, window = 0, max_ctx = 0;
   int chunks_per_split = 1;

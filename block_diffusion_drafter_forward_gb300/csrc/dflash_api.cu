@@ -230,6 +230,8 @@ int propose_persist(dflash_handle* h, const int32_t* bonus_tokens, const int32_t
   p.bonus = bonus_tokens;
   p.ctx_lens = ctx_lens;
   p.page_tables = page_tables;
+  p.rope_pos0 = h->cur_rope_pos;
+  p.widths = h->cur_widths;
   p.embed = static_cast<const __nv_bfloat16*>(h->embed);
   p.norm = static_cast<const __nv_bfloat16*>(h->norm);
   p.inv_pi = h->rope_inv_pi;
@@ -308,6 +310,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.nkv = c.n_kv_heads;
       p.ctx_lens = ctx_lens;
       p.page_tables = page_tables;
+      p.rope_pos0 = h->cur_rope_pos;
       p.mpps = c.max_pages_per_seq;
       p.g = h->geom;
       p.layer = l;
@@ -321,6 +324,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       a.g = h->geom;
       a.layer = l;
       a.ctx_lens = ctx_lens;
+      a.widths = h->cur_widths;
       a.page_tables = page_tables;
       a.mpps = c.max_pages_per_seq;
       a.nh = c.n_q_heads;
@@ -374,6 +378,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
     p.drafts = draft_tokens;
     p.row_scale = fp8 ? h->lm_scale : nullptr;
     p.logits32 = c.markov_rank > 0 ? h->logits32 : nullptr;  // the Markov head reads fp32 logits
+    p.widths = h->cur_widths;
     KL(K_LMHEAD, launch_gemm_tc(EPI_LMHEAD, fp8 ? (const void*)h->lm_fp8 : h->lm_head, c.vocab, H, h->xn, H, M, p, 1,
                                 st, false, fp8),
        "lm_head");
@@ -771,6 +776,14 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
 int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens,
                    const int32_t* page_tables, int32_t nb, int32_t max_ctx_len, int32_t* draft_tokens,
                    void* logits, void* final_hidden, dflash_stream stream) {
+  return dflash_propose_ex(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, nullptr, nullptr, draft_tokens,
+                           logits, final_hidden, stream);
+}
+
+int dflash_propose_ex(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens,
+                      const int32_t* page_tables, int32_t nb, int32_t max_ctx_len, const int32_t* q_rope_pos,
+                      const int32_t* widths, int32_t* draft_tokens, void* logits, void* final_hidden,
+                      dflash_stream stream) {
   if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
   h->err.clear();
   const dflash_cfg& c = h->cfg;
@@ -781,8 +794,13 @@ int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t*
     return fail(h, DFLASH_ECAPACITY, "max_ctx_len + gamma beyond the page-table capacity");
   if (!bonus_tokens || !ctx_lens || !page_tables || !draft_tokens) return fail(h, DFLASH_EINVAL, "null pointer");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return propose_graph(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits, final_hidden,
-                       st);
+  h->cur_rope_pos = q_rope_pos;
+  h->cur_widths = widths;
+  const int rc = propose_graph(h, bonus_tokens, ctx_lens, page_tables, nb, max_ctx_len, draft_tokens, logits,
+                               final_hidden, st);
+  h->cur_rope_pos = nullptr;
+  h->cur_widths = nullptr;
+  return rc;
 }
 
 }  // extern "C"
@@ -836,6 +854,7 @@ int propose_markov(dflash_handle* h, const int32_t* bonus_tokens, int nb, int32_
   m.drafts = draft_tokens;
   m.logits = logits;
   m.status = h->d_status;
+  m.widths = h->cur_widths;
   markov_bind_ctl(m, h->mk_ctl, nb);
   CK(cudaMemsetAsync(h->mk_ctl, 0, h->mk_ctl_bytes, st), "Markov control reset");
   KL(K_MARKOV, launch_markov(c.dtype, m, h->num_sms, st), "Markov chain");
@@ -856,7 +875,8 @@ int propose_eager(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* 
 // stream); the whole forward is then one graph launch on the caller's stream.
 int propose_graph(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens, const int32_t* page_tables,
                   int nb, int max_ctx_len, int32_t* draft_tokens, void* logits, void* final_hidden, cudaStream_t st) {
-  const void* args[6] = {bonus_tokens, ctx_lens, page_tables, draft_tokens, logits, final_hidden};
+  const void* args[8] = {bonus_tokens, ctx_lens, page_tables, draft_tokens, logits, final_hidden,
+                         h->cur_rope_pos, h->cur_widths};
   GraphEntry* e = nullptr;
   for (GraphEntry* g : h->graphs)
     if (g->nb == nb && g->max_ctx == max_ctx_len && g->prof == h->prof.on && g->persist == h->persist_on &&

@@ -75,7 +75,8 @@ struct Prof {
 // One captured propose (CUDA graph) and the arguments it was captured with.
 struct GraphEntry {
   int nb = 0, max_ctx = 0;
-  const void* args[6] = {};           // bonus, ctx_lens, page_tables, drafts, logits, hidden
+  const void* args[8] = {};           // bonus, ctx_lens, page_tables, drafts, logits, hidden,
+                                      // q_rope_pos, widths
   bool prof = false;                  // captured with per-kernel timing events
   bool persist = false;               // captured on the single-launch persistent forward
   cudaGraphExec_t exec = nullptr;
@@ -166,6 +167,11 @@ struct dflash_handle {
   void* mk_ctl = nullptr;              // per-step argmax keys and barriers, zeroed before each launch
   size_t mk_ctl_bytes = 0;
 
+  // per-call optional inputs of dflash_propose_ex (device arrays [nb] or null), read by the
+  // launchers of the call being issued or captured
+  const int32_t* cur_rope_pos = nullptr;
+  const int32_t* cur_widths = nullptr;
+
   unsigned* d_status = nullptr;        // device status word
   dflash::Prof prof;
   // CUDA graphs of dflash_propose, keyed by its arguments (small LRU)
@@ -177,6 +183,23 @@ struct dflash_handle {
 };
 
 namespace dflash {
+
+// Active block width of sequence s (dflash_propose_ex): widths[s] clamped to [2, gamma];
+// gamma when no widths are given.
+__device__ __forceinline__ int block_width(const int32_t* widths, int s) {
+  if (!widths) return kGamma;
+  const int w = __ldg(widths + s);
+  return w < 2 ? 2 : (w > kGamma ? kGamma : w);
+}
+__device__ __forceinline__ bool width_out_of_range(const int32_t* widths, int s) {
+  if (!widths) return false;
+  const int w = __ldg(widths + s);
+  return w < 2 || w > kGamma;
+}
+// RoPE position of block row 0 of sequence s: q_rope_pos[s], or the context length.
+__device__ __forceinline__ int rope_start(const int32_t* rope_pos, int s, int ctx) {
+  return rope_pos ? __ldg(rope_pos + s) : ctx;
+}
 
 // ---------------------------------------------------------------- launchers (kernels_simple.cu)
 // All launchers are stream-ordered and return cudaGetLastError() of the launch.

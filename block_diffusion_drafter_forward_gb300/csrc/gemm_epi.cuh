@@ -98,7 +98,8 @@ struct EpiPre {
   float lnw;     // EPI_RESID: next RMSNorm weight of the row
   float nw;      // EPI_QKV: q_norm / k_norm weight of the row
   float2 ip;     // EPI_QKV: RoPE inv_freq / pi of this thread's pair
-  int ctx;       // EPI_QKV: first position of the chunk's gamma block
+  int ctx;       // EPI_QKV: first row index of the chunk's gamma block (its K/V slots)
+  int rp0;       // EPI_QKV: RoPE position of the block's row 0
   int pg0, pg1;  // EPI_QKV: page ids of the block's rows (ctx / 16 and the next page)
 };
 
@@ -116,6 +117,7 @@ __device__ __forceinline__ void epilogue_pre(const GemmParams& p, EpiPre& q, int
     const int mb = m0 + c0;
     const int s = mb / kGamma;
     q.ctx = ctx_known >= 0 ? ctx_known : (mb < p.M ? __ldg(p.ctx_lens + s) : 0);
+    q.rp0 = mb < p.M ? rope_start(p.rope_pos0, s, q.ctx) : 0;
     q.nw = (is_q || is_k) ? __bfloat162float((is_q ? p.q_norm : p.k_norm)[t]) : 1.f;
     q.ip = p.inv_pi[t & 63];
     q.pg0 = q.pg1 = -1;
@@ -192,7 +194,7 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
       // angle (fp32 error ~c * 6e-8, far below the bf16 rounding of the result).
       const int j = t & 63;
       float cs, sn, c1, s1;
-      rope_cs(q.ip, ctx, &cs, &sn);
+      rope_cs(q.ip, q.rp0, &cs, &sn);
       rope_cs(q.ip, 1, &c1, &s1);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {

@@ -313,7 +313,9 @@ __global__ void __launch_bounds__(kThreads * WG, WG <= 2 ? 2 : 1)
             if (m < p.M) {
               const unsigned long long k = atomicExch(p.amax_best + m, 0ull);  // read and re-arm
               const int r = m % kGamma;
-              if (r > 0) p.drafts[(m / kGamma) * (kGamma - 1) + r - 1] = argmax_key_index(k);
+              if (r > 0)
+                p.drafts[(m / kGamma) * (kGamma - 1) + r - 1] =
+                    r < block_width(p.widths, m / kGamma) ? argmax_key_index(k) : -1;
             }
           }
           if (t == 0) p.amax_counter[tile_m] = 0;

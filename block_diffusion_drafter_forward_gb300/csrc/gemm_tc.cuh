@@ -35,6 +35,8 @@ struct GemmParams {
   int nh = 0, nkv = 0, mpps = 0, layer = 0;
   const int32_t* ctx_lens = nullptr;
   const int32_t* page_tables = nullptr;
+  const int32_t* rope_pos0 = nullptr;    // [nb] RoPE start of each block (null: ctx_lens)
+  const int32_t* widths = nullptr;       // [nb] active block widths (null: gamma); lm_head drafts
   PoolGeom g{};
   __nv_bfloat16* pool = nullptr;
   // EPI_CTXKV (k_norm: every layer's k_norm [L, 128]; page_tables: one sequence's table)

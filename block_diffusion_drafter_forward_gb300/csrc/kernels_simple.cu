@@ -60,12 +60,13 @@ __device__ __forceinline__ void flag(unsigned* status, unsigned bit) { atomicOr(
 // (dflash.rs draft step: block = [last, MASK x (b-1)]).
 template <typename T>
 __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict__ bonus, int mask, int V,
-                             int H, float* __restrict__ x, unsigned* status) {
+                             int H, float* __restrict__ x, unsigned* status, const int32_t* __restrict__ widths) {
   const int row = blockIdx.x;
   const int r = row % kGamma, s = row / kGamma;
   int tok = r == 0 ? bonus[s] : mask;
   const bool ok = tok >= 0 && tok < V;
   if (!ok && threadIdx.x == 0) flag(status, DFLASH_DEV_BAD_TOKEN);
+  if (r == 0 && threadIdx.x == 0 && width_out_of_range(widths, s)) flag(status, DFLASH_DEV_BAD_WIDTH);
   for (int i = threadIdx.x; i < H; i += blockDim.x)
     x[(int64_t)row * H + i] = ok ? Elem<T>::to_f(E[(int64_t)tok * H + i]) : 0.f;
 }
@@ -155,7 +156,8 @@ __global__ void qkv_post_kernel(const float* __restrict__ y, int ldy, const T* _
                                 const T* __restrict__ kn_w, const float2* __restrict__ inv_pi, float mscale,
                                 float eps, int nh, int nkv, int hd, const int32_t* __restrict__ ctx_lens,
                                 const int32_t* __restrict__ page_tables, int mpps, PoolGeom g, int layer,
-                                T* __restrict__ pool, T* __restrict__ qout, unsigned* status) {
+                                T* __restrict__ pool, T* __restrict__ qout, unsigned* status,
+                                const int32_t* __restrict__ rope_pos0) {
   extern __shared__ float sm[];
   const int row = blockIdx.x, hh = blockIdx.y, d = threadIdx.x;
   const int s = row / kGamma, r = row % kGamma;
@@ -164,7 +166,7 @@ __global__ void qkv_post_kernel(const float* __restrict__ y, int ldy, const T* _
     if (d == 0) flag(status, DFLASH_DEV_BAD_CTX);
     return;
   }
-  const int pos = ctx + r;
+  const int pos = rope_start(rope_pos0, s, ctx) + r;  // RoPE position; the K/V slot stays ctx + r
   float v = y[(int64_t)row * ldy + hh * hd + d];
   const bool is_q = hh < nh, is_k = !is_q && hh < nh + nkv;
   if (is_q || is_k) {
@@ -203,7 +205,7 @@ template <typename T>
 __global__ void attention_kernel(const T* __restrict__ q, const T* __restrict__ pool, PoolGeom g, int layer,
                                  const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ page_tables,
                                  int mpps, int max_ctx, int rows, int nh, int nkv, int hd, int window,
-                                 T* __restrict__ out, unsigned* status) {
+                                 T* __restrict__ out, unsigned* status, const int32_t* __restrict__ widths) {
   const int lane = threadIdx.x & 31;
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (wid >= rows * nh) return;
@@ -216,7 +218,7 @@ __global__ void attention_kernel(const T* __restrict__ q, const T* __restrict__ 
     if (lane == 0 && r == 0 && h == 0) flag(status, DFLASH_DEV_BAD_CTX);
     return;
   }
-  const int nkeys = ctx + kGamma, pq = ctx + r;
+  const int nkeys = ctx + block_width(widths, s), pq = ctx + r;  // keys past the block width are masked
   const int per = hd >> 5;  // dims per lane (2 or 4)
   float qv[4], o[4];
   for (int i = 0; i < per; ++i) {
@@ -262,7 +264,8 @@ __global__ void silu_mul_kernel(const float* __restrict__ y, int ldy, int F, int
 // drafts[s, r-1] = argmax_v z[s*gamma + r, v] for r = 1..gamma-1, ties to the lowest v
 // (dflash.rs draft step: argmax of lm_head over block rows 1..b-1).
 template <typename T>
-__global__ void argmax_kernel(const float* __restrict__ z, int V, int32_t* __restrict__ drafts, T* __restrict__ zout) {
+__global__ void argmax_kernel(const float* __restrict__ z, int V, int32_t* __restrict__ drafts, T* __restrict__ zout,
+                              const int32_t* __restrict__ widths) {
   const int row = blockIdx.x;
   const float* zr = z + (int64_t)row * V;
   float best = -FLT_MAX;
@@ -293,7 +296,7 @@ __global__ void argmax_kernel(const float* __restrict__ z, int V, int32_t* __res
       if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
     }
     const int r = row % kGamma;
-    if (lane == 0 && r > 0) drafts[(row / kGamma) * (kGamma - 1) + r - 1] = bi;
+    if (lane == 0 && r > 0) drafts[(row / kGamma) * (kGamma - 1) + r - 1] = r < block_width(widths, row / kGamma) ? bi : -1;
   }
 }
 
@@ -368,13 +371,15 @@ __global__ void quantize_fp8_kernel(const T* __restrict__ w, int cols, uint8_t* 
 // 1/RMS(x): W (x * ln) / RMS(x) = W RMSNorm(x).
 __global__ void embed_tc_kernel(const __nv_bfloat16* __restrict__ E, const int32_t* __restrict__ bonus, int mask,
                                 int V, int H, int Mp, const __nv_bfloat16* __restrict__ ln, float* __restrict__ x,
-                                __nv_bfloat16* __restrict__ xb, float* __restrict__ ss, unsigned* status) {
+                                __nv_bfloat16* __restrict__ xb, float* __restrict__ ss, unsigned* status,
+                                const int32_t* __restrict__ widths) {
   __shared__ float part[4];
   const int row = blockIdx.x, t = threadIdx.x;
   const int r = row % kGamma, s = row / kGamma;
   const int tok = r == 0 ? bonus[s] : mask;
   const bool ok = tok >= 0 && tok < V;
   if (!ok && t == 0) flag(status, DFLASH_DEV_BAD_TOKEN);
+  if (r == 0 && t == 0 && width_out_of_range(widths, s)) flag(status, DFLASH_DEV_BAD_WIDTH);
   for (int g = 0; g < H / 128; ++g) {
     const int i = g * 128 + t;
     const __nv_bfloat16 e = ok ? E[(int64_t)tok * H + i] : __float2bfloat16_rn(0.f);
@@ -433,7 +438,8 @@ cudaError_t launch_embed_tc(const dflash_handle* h, const int32_t* bonus, int nb
   embed_tc_kernel<<<nb * kGamma, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(h->embed), bonus, c.mask_token_id,
                                                c.vocab, c.hidden, h->rows_max,
                                                static_cast<const __nv_bfloat16*>(h->layer[0].ln_in), h->x,
-                                               static_cast<__nv_bfloat16*>(h->xb), h->ss_b, h->d_status);
+                                               static_cast<__nv_bfloat16*>(h->xb), h->ss_b, h->d_status,
+                                               h->cur_widths);
   return cudaGetLastError();
 }
 
@@ -462,7 +468,7 @@ cudaError_t launch_embed(const dflash_handle* h, const int32_t* bonus, int nb, f
   const dflash_cfg& c = h->cfg;
   DISPATCH_T(c.dtype, embed_kernel<T><<<nb * kGamma, 256, 0, st>>>(static_cast<const T*>(h->embed), bonus,
                                                                      c.mask_token_id, c.vocab, c.hidden, x,
-                                                                     h->d_status));
+                                                                     h->d_status, h->cur_widths));
   return cudaGetLastError();
 }
 
@@ -518,7 +524,8 @@ cudaError_t launch_qkv_post(const dflash_handle* h, int layer, const float* y, c
                           y, ldy, static_cast<const T*>(h->layer[layer].q_norm),
                           static_cast<const T*>(h->layer[layer].k_norm), h->rope_inv_pi, h->rope_mscale, c.rms_eps,
                           c.n_q_heads, c.n_kv_heads, c.head_dim, ctx_lens, page_tables, c.max_pages_per_seq,
-                          h->geom, layer, static_cast<T*>(h->pool), static_cast<T*>(q), h->d_status));
+                          h->geom, layer, static_cast<T*>(h->pool), static_cast<T*>(q), h->d_status,
+                          h->cur_rope_pos));
   return cudaGetLastError();
 }
 
@@ -531,7 +538,7 @@ cudaError_t launch_attention(const dflash_handle* h, int layer, const void* q, c
   DISPATCH_T(c.dtype, attention_kernel<T><<<(warps + 3) / 4, 128, 0, st>>>(
                           static_cast<const T*>(q), static_cast<const T*>(h->pool), h->geom, layer, ctx_lens,
                           page_tables, c.max_pages_per_seq, max_ctx_len, rows, c.n_q_heads, c.n_kv_heads,
-                          c.head_dim, window, static_cast<T*>(out), h->d_status));
+                          c.head_dim, window, static_cast<T*>(out), h->d_status, h->cur_widths));
   return cudaGetLastError();
 }
 
@@ -546,7 +553,7 @@ cudaError_t launch_silu_mul(const dflash_handle* h, const float* y, int rows, vo
 cudaError_t launch_argmax(const dflash_handle* h, const float* logits32, int nb, int32_t* drafts, void* logits_out,
                           cudaStream_t st) {
   DISPATCH_T(h->cfg.dtype, argmax_kernel<T><<<nb * kGamma, 1024, 0, st>>>(logits32, h->cfg.vocab, drafts,
-                                                                         static_cast<T*>(logits_out)));
+                                                                         static_cast<T*>(logits_out), h->cur_widths));
   return cudaGetLastError();
 }
 

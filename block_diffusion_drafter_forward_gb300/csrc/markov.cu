@@ -87,15 +87,19 @@ __global__ void __launch_bounds__(kMkThreads, 1) markov_kernel(const __grid_cons
   for (int k = 0; k < kGamma - 1; ++k) {
     if (t < p.nb) {
       int prev;
-      if (k == 0) {
-        prev = __ldg(p.bonus + t);
+      if (k + 1 >= block_width(p.widths, t)) {
+        prev = -2;                               // past the sequence's block width: idle
       } else {
-        const unsigned long long key = ld_acquire64(p.best + (size_t)(k - 1) * p.nb + t);
-        prev = key ? mk_index(key) : -1;
-      }
-      if (prev < 0 || prev >= p.V) {
-        if (c == 0) atomicOr(p.status, DFLASH_DEV_BAD_TOKEN);
-        prev = -1;                               // its bias is taken as zero
+        if (k == 0) {
+          prev = __ldg(p.bonus + t);
+        } else {
+          const unsigned long long key = ld_acquire64(p.best + (size_t)(k - 1) * p.nb + t);
+          prev = key ? mk_index(key) : -1;
+        }
+        if (prev < 0 || prev >= p.V) {
+          if (c == 0) atomicOr(p.status, DFLASH_DEV_BAD_TOKEN);
+          prev = -1;                             // its bias is taken as zero
+        }
       }
       sprev[t] = prev;
       sbest[t] = 0ull;
@@ -103,7 +107,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) markov_kernel(const __grid_cons
     __syncthreads();
     for (int i = t; i < p.nb * R; i += kMkThreads) {
       const int s = i / R, j = i - s * R;
-      sf[i] = sprev[s] >= 0 ? to_f(w1[(int64_t)sprev[s] * R + j]) : 0.f;
+      sf[i] = sprev[s] >= 0 ? to_f(w1[(int64_t)sprev[s] * R + j]) : 0.f;  // (a bad token: zero bias)
     }
     __syncthreads();
     for (int s0 = 0; s0 < p.nb; s0 += kSB) {
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) markov_kernel(const __grid_cons
           float a = acc[s];
           a += __shfl_xor_sync(0xffffffffu, a, 1);
           a += __shfl_xor_sync(0xffffffffu, a, 2);
-          if (s < ns && ok && q4 == 0) {
+          if (s < ns && ok && q4 == 0 && sprev[s0 + s] != -2) {
             const int64_t row = (int64_t)((s0 + s) * kGamma + k + 1) * p.V + v;
             const float z = __ldcg(p.z + row) + a;
             if (logits) store_logit(logits + row, z);
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) markov_kernel(const __grid_cons
     for (int i = t; i < p.nb * (kGamma - 1); i += kMkThreads) {
       const int s = i / (kGamma - 1), k = i - s * (kGamma - 1);
       const unsigned long long key = ld_acquire64(p.best + (size_t)k * p.nb + s);
-      p.drafts[i] = key ? mk_index(key) : 0;
+      p.drafts[i] = k + 1 < block_width(p.widths, s) ? (key ? mk_index(key) : 0) : -1;
     }
   }
 }

@@ -17,6 +17,7 @@ struct MarkovParams {
   const void* w2;               // [V, R] projection to the vocabulary (cfg.dtype)
   int V, R, nb;
   const int32_t* bonus;         // [nb] chain starts
+  const int32_t* widths;        // [nb] active block widths (null: gamma): b - 1 steps each
   int32_t* drafts;              // [nb, 15] out
   void* logits;                 // [nb * 16, V] cfg.dtype out or null: rows 1..15 adjusted
   unsigned long long* best;     // [15][nb] per-step argmax keys (control buffer, zeroed)

@@ -227,6 +227,7 @@ __device__ void embed_phase(const PersistParams& p, int c, int warp, int lane) {
     const int tok = r == 0 ? __ldg(p.bonus + s) : p.mask;
     const bool ok = tok >= 0 && tok < p.V;
     if (!ok && gi == 0 && lane == 0) atomicOr(p.status, DFLASH_DEV_BAD_TOKEN);
+    if (r == 0 && gi == 0 && lane == 0 && width_out_of_range(p.widths, s)) atomicOr(p.status, DFLASH_DEV_BAD_WIDTH);
     const int col = gi * 128 + lane * 4;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
@@ -397,7 +398,7 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
     return;
   }
   const int group = p.nh / p.nkv;
-  const int nkeys = a.ctx + kGamma;
+  const int nkeys = a.ctx + block_width(p.widths, a.s);  // keys past the active block width are masked
   uint8_t* sQ = sA + kAP;
   uint8_t* sKV = sQ + kAQ;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -830,6 +831,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         e.ss_n = p.H; e.ss_parts = p.H / 128;
         e.q = p.q; e.inv_pi = p.inv_pi; e.mscale = p.mscale; e.nh = p.nh; e.nkv = p.nkv;
         e.ctx_lens = p.ctx_lens; e.page_tables = p.page_tables; e.mpps = p.mpps; e.g = p.g;
+        e.rope_pos0 = p.rope_pos0; e.widths = p.widths;
         e.layer = gp.layer; e.pool = p.pool; e.x = p.x; e.xb = p.xb; e.H = p.H; e.act = p.act; e.F = p.F;
         e.logits = p.logits; e.amax_best = p.amax_best;
         const PersistLayer& Ly = p.layers[gp.layer];
@@ -972,7 +974,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
               __threadfence();
               if (t < p.M && (t % kGamma) > 0) {
                 const unsigned long long k = __ldcg(p.amax_best + t);
-                p.drafts[(t / kGamma) * (kGamma - 1) + (t % kGamma) - 1] = argmax_key_index(k);
+                p.drafts[(t / kGamma) * (kGamma - 1) + (t % kGamma) - 1] =
+                    (t % kGamma) < block_width(p.widths, t / kGamma) ? argmax_key_index(k) : -1;
               }
             }
           }

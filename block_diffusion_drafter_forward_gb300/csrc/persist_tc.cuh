@@ -29,6 +29,8 @@ struct PersistParams {
   const int32_t* bonus;
   const int32_t* ctx_lens;
   const int32_t* page_tables;
+  const int32_t* rope_pos0;   // [nb] RoPE start of each block, or null (ctx_lens)
+  const int32_t* widths;      // [nb] active block widths, or null (gamma)
   const __nv_bfloat16* embed;
   const __nv_bfloat16* norm;
   const float2* inv_pi;

@@ -140,7 +140,10 @@ class Drafter:
 
     def propose(self, bonus: torch.Tensor, ctx_lens: torch.Tensor, page_tables: torch.Tensor, max_ctx_len: int,
                 drafts: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
-                hidden: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                hidden: Optional[torch.Tensor] = None, stream=None, q_rope_pos: Optional[torch.Tensor] = None,
+                widths: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """One block forward over nb sequences (dflash_propose; dflash_propose_ex when a per-sequence
+        RoPE start `q_rope_pos` [nb] or block width `widths` [nb] int32 device tensor is given)."""
         nb = int(bonus.shape[0]) if bonus.dim() == 1 else -1
         g = self.cfg.gamma
         check_tensor(bonus, "bonus", torch.int32, (nb,))
@@ -153,9 +156,20 @@ class Drafter:
             check_tensor(logits, "logits", self.act_dtype, (nb * g, self.cfg.vocab))
         if hidden is not None:
             check_tensor(hidden, "hidden", self.act_dtype, (nb * g, self.cfg.hidden))
-        L.dflash_propose(self.handle, bonus.data_ptr(), ctx_lens.data_ptr(), page_tables.data_ptr(), nb,
-                         int(max_ctx_len), drafts.data_ptr(), logits.data_ptr() if logits is not None else 0,
-                         hidden.data_ptr() if hidden is not None else 0, _stream(stream))
+        if q_rope_pos is None and widths is None:
+            L.dflash_propose(self.handle, bonus.data_ptr(), ctx_lens.data_ptr(), page_tables.data_ptr(), nb,
+                             int(max_ctx_len), drafts.data_ptr(), logits.data_ptr() if logits is not None else 0,
+                             hidden.data_ptr() if hidden is not None else 0, _stream(stream))
+            return drafts
+        if q_rope_pos is not None:
+            check_tensor(q_rope_pos, "q_rope_pos", torch.int32, (nb,))
+        if widths is not None:
+            check_tensor(widths, "widths", torch.int32, (nb,))
+        L.dflash_propose_ex(self.handle, bonus.data_ptr(), ctx_lens.data_ptr(), page_tables.data_ptr(), nb,
+                            int(max_ctx_len), q_rope_pos.data_ptr() if q_rope_pos is not None else 0,
+                            widths.data_ptr() if widths is not None else 0, drafts.data_ptr(),
+                            logits.data_ptr() if logits is not None else 0,
+                            hidden.data_ptr() if hidden is not None else 0, _stream(stream))
         return drafts
 
     def set_persistent(self, enable: bool) -> None:

@@ -63,6 +63,7 @@ typedef enum {
 #define DFLASH_DEV_BAD_CTX 0x2u     /* ctx_len < 0 or > max_ctx_len, or ctx_len+gamma > capacity */
 #define DFLASH_DEV_BAD_TOKEN 0x4u   /* a bonus token outside [0, vocab) (row embedded as zeros) */
 #define DFLASH_DEV_TIMEOUT 0x8u     /* a kernel's bounded wait gave up (its outputs are invalid) */
+#define DFLASH_DEV_BAD_WIDTH 0x10u  /* dflash_propose_ex: a block width outside [2, gamma] (clamped) */
 
 /* Drafter configuration.  Names follow the drafter config.json of the pages
  * (hidden_size, num_attention_heads, num_key_value_heads, head_dim, intermediate_size,
@@ -186,6 +187,24 @@ int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t*
                    const int32_t* page_tables, int32_t nb, int32_t max_ctx_len,
                    int32_t* draft_tokens, void* logits, void* final_hidden,
                    dflash_stream stream);
+
+/* dflash_propose with two optional per-sequence inputs, both device arrays [nb] int32 read by
+ * the kernels at run time (so one captured graph serves every value; NULL = the default):
+ *   q_rope_pos  RoPE position of block row 0 of sequence s (block row r at q_rope_pos[s] + r);
+ *               default ctx_lens[s] (dflash_head.rs / from_weights.rs indirect arguments
+ *               [kv_len, q_offset, q_rope_pos]).  The K/V rows and the sliding window keep the
+ *               row indices ctx_lens[s] + r.  Positions must lie in [0, 2^24).
+ *   widths      active block width b of sequence s, 2 <= b <= gamma (dflash_head.rs block-width
+ *               resolver): the block is [bonus, mask x (b-1)], its b rows attend to the context
+ *               and to each other only, and drafts[s, 0..b-2] are the argmaxes of rows 1..b-1;
+ *               drafts[s, b-1..gamma-2] are set to -1 and logit / hidden rows b..gamma-1 of the
+ *               band hold no meaningful values.  Default gamma.  A width outside [2, gamma] is
+ *               clamped and sets DFLASH_DEV_BAD_WIDTH.
+ * Everything else as dflash_propose (the graph cache also keys on these two pointers). */
+int dflash_propose_ex(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens,
+                      const int32_t* page_tables, int32_t nb, int32_t max_ctx_len,
+                      const int32_t* q_rope_pos, const int32_t* widths, int32_t* draft_tokens,
+                      void* logits, void* final_hidden, dflash_stream stream);
 
 /* Layout of the library-owned K/V pool (for tests and inspection).  *pool = device base,
  * *bytes = size, strides (in ELEMENTS of cfg.dtype) for the tile index
