@@ -585,6 +585,40 @@ def main():
                            "hbm_frac": wbytes / (ms / 1e3) / (peaks()[0]["hbm_gbs"] * 1e9),
                            "tensor_frac": wflops / (ms / 1e3) / (peaks()[0]["bf16_tflops"] * 1e12)}
 
+    # batched writer: 32 sequences x 128 new rows in one call (rows of all sequences stacked),
+    # against the same rows written by 32 per-sequence calls; rows land on sequence 0's first
+    # 128 slots (same values as before), so the pool is unchanged
+    if c0 >= 128:
+        nseq, per = 32, 128
+        idx = (int(wl.tap_offsets[0]) + torch.arange(per, device="cuda")) % wl.taps_rows
+        taps1 = b.table[idx].contiguous()
+        taps_b = taps1.repeat(nseq, 1)
+        pos_b = to_torch(np.tile(wl.ctx_positions(0, 0, per), nseq), "i32")
+        rs_b = torch.zeros(nseq * per, dtype=torch.int32, device="cuda")
+        ri_b = to_torch(np.tile(np.arange(per, dtype=np.int32), nseq), "i32")
+        pt0 = b.page_tables[:1].contiguous()
+        pos1 = to_torch(wl.ctx_positions(0, 0, per), "i32")
+
+        def timed_calls(fn, reps):
+            for _ in range(2):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(b.stream)
+            for _ in range(reps):
+                fn()
+            e1.record(b.stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        ms_b = timed_calls(lambda: b.drafter.write_ctx_kv_batch(taps_b, pos_b, rs_b, ri_b, pt0), 5)
+        ms_s = timed_calls(lambda: [b.drafter.write_ctx_kv(taps1, pos1, b.page_tables[0], 0) for _ in range(nseq)], 3)
+        n = nseq * per
+        wflops = 2.0 * n * (cfg.hidden * cfg.tap_dim + cfg.n_layers * 2 * cfg.kv_dim * cfg.hidden)
+        writer["batched_32x128"] = {"rows_per_s": n / (ms_b / 1e3), "us_per_call": 1e3 * ms_b,
+                                    "tensor_frac": wflops / (ms_b / 1e3) / (peaks()[0]["bf16_tflops"] * 1e12),
+                                    "per_sequence_calls_us": 1e3 * ms_s, "speedup": ms_s / ms_b}
+
     roof, step_roof, fr, launches = b.roofline(prof, prof_steps, ms_per_step)
     launches_per_step = launches / prof_steps
     line = {

@@ -71,7 +71,7 @@ EXPORTS = ("dflash_create", "dflash_destroy", "dflash_write_ctx_kv", "dflash_pro
            "dflash_device_status", "dflash_last_error", "dflash_fp8_lm_head", "dflash_profile",
            "dflash_profile_kinds", "dflash_profile_read", "dflash_gemm_bf16",
            "dflash_attention_check", "dflash_gemm_bf16_noalloc", "dflash_set_persistent", "dflash_persistent",
-           "dflash_propose_ex")
+           "dflash_propose_ex", "dflash_write_ctx_kv_batch")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -91,6 +91,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_destroy.restype = c.c_int
     lib.dflash_write_ctx_kv.argtypes = [vp, vp, vp, vp, i32, i32, vp]
     lib.dflash_write_ctx_kv.restype = c.c_int
+    lib.dflash_write_ctx_kv_batch.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, vp]
+    lib.dflash_write_ctx_kv_batch.restype = c.c_int
     lib.dflash_propose.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
     lib.dflash_propose.restype = c.c_int
     lib.dflash_propose_ex.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
@@ -145,6 +147,14 @@ def dflash_write_ctx_kv(handle: int, taps: int, positions: int, page_table: int,
                         stream: int = 0) -> None:
     rc = load().dflash_write_ctx_kv(ctypes.c_void_p(handle), ctypes.c_void_p(taps), ctypes.c_void_p(positions),
                                     ctypes.c_void_p(page_table), first, n, ctypes.c_void_p(stream))
+    _check(rc, ctypes.c_void_p(handle))
+
+
+def dflash_write_ctx_kv_batch(handle: int, taps: int, positions: int, row_seq: int, row_index: int,
+                              page_tables: int, nseq: int, n: int, stream: int = 0) -> None:
+    rc = load().dflash_write_ctx_kv_batch(ctypes.c_void_p(handle), ctypes.c_void_p(taps), ctypes.c_void_p(positions),
+                                          ctypes.c_void_p(row_seq), ctypes.c_void_p(row_index),
+                                          ctypes.c_void_p(page_tables), nseq, n, ctypes.c_void_p(stream))
     _check(rc, ctypes.c_void_p(handle))
 
 

@@ -386,6 +386,74 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
   return DFLASH_OK;
 }
 
+// Context-K/V writer (dflash.rs ctx_features + ingest_ctx; from_weights.rs fused K/V weight +
+// reshape_and_cache) over n rows in chunks of max_write_rows: f = hidden_norm(fc . taps), then
+// every layer's K (k_norm, RoPE at positions[i], mscale) and V into the pool.  Row i goes to row
+// first + i of the one sequence whose table is page_tables (row_seq == nullptr), or to row
+// row_index[i] of sequence row_seq[i] (the batched writer: page_tables is [nseq, mpps]).
+int write_ctx_rows(dflash_handle* h, const void* taps, const int32_t* positions, const int32_t* page_tables,
+                   int nseq, const int32_t* row_seq, const int32_t* row_index, int first, int n, cudaStream_t st) {
+  const dflash_cfg& c = h->cfg;
+  const int64_t H = c.hidden, tapd = (int64_t)c.n_taps * c.target_hidden;
+  const int kvall = c.n_layers * 2 * c.n_kv_heads * c.head_dim;
+  for (int32_t done = 0; done < n; done += c.max_write_rows) {
+    const int m = std::min<int32_t>(c.max_write_rows, n - done);
+    const void* tp = static_cast<const char*>(taps) + (int64_t)done * tapd * h->esz;
+    const int32_t* rs = row_seq ? row_seq + done : nullptr;
+    const int32_t* ri = row_index ? row_index + done : nullptr;
+    if (h->tc) {
+      // tensor-core writer: fc GEMM -> hidden_norm (fp32) -> [hi | lo] bf16 -> one GEMM for every
+      // layer's K and V (each weight tile times both halves) with the k_norm / RoPE / scatter
+      // epilogue
+      auto splits = [&](int64_t N, int64_t K) {
+        const int tn = pick_tn(m);
+        return pick_splits((int)(((N + 127) / 128) * ((m + tn - 1) / tn)), (int)(K / 64), h->num_sms, tn);
+      };
+      GemmParams pf;
+      pf.ws = h->ws;
+      pf.counters = h->counters;
+      pf.status = h->d_status;
+      pf.out = h->wy;
+      pf.ldo = (int)H;
+      KL(K_W_FC, launch_gemm_tc(EPI_STORE, h->fc, (int)H, (int)tapd, tp, (int)tapd, m, pf, splits(H, tapd), st, false),
+         "writer fc");
+      KL(K_W_NORM, launch_rmsnorm_f32out(h, h->wy, h->hidden_norm, h->wf, m, (int)H, st), "writer hidden_norm");
+      KL(K_W_NORM, launch_split_hi_lo(h->wf, m, (int)H, h->wf2, st), "writer split");
+      GemmParams pk;
+      pk.ws = h->ws;
+      pk.counters = h->counters;
+      pk.status = h->d_status;
+      pk.eps = c.rms_eps;
+      pk.k_norm = static_cast<const __nv_bfloat16*>(h->kn_all);
+      pk.inv_pi = h->rope_inv_pi;
+      pk.mscale = h->rope_mscale;
+      pk.nkv = c.n_kv_heads;
+      pk.positions = positions + done;
+      pk.page_tables = page_tables;
+      pk.first = first + done;
+      pk.row_seq = rs;
+      pk.row_index = ri;
+      pk.nseq = nseq;
+      pk.mpps = c.max_pages_per_seq;
+      pk.g = h->geom;
+      pk.pool = static_cast<__nv_bfloat16*>(h->pool);
+      KL(K_W_KV, launch_gemm_tc(EPI_CTXKV, h->w_ctxkv, kvall, (int)H, h->wf2, (int)(2 * H), m, pk,
+                                splits(kvall, H), st, false),
+         "writer kv");
+      continue;
+    }
+    // f = hidden_norm(fc . taps)  (dflash.rs ctx_features)
+    KL(K_W_FC, launch_gemm(h, tp, (int)tapd, h->fc, m, (int)H, (int)tapd, h->wy, (int)H, false, st), "writer fc");
+    KL(K_W_NORM, launch_rmsnorm_f32out(h, h->wy, h->hidden_norm, h->wf, m, (int)H, st), "writer hidden_norm");
+    // every layer's K and V in one GEMM over the fused weight (fp32 features), then
+    // k_norm / RoPE / scatter
+    KL(K_W_KV, launch_gemm_xf32(h, h->wf, (int)H, h->w_ctxkv, m, kvall, (int)H, h->wy, kvall, st), "writer kv");
+    KL(K_W_POST, launch_ctxkv_post(h, h->wy, m, positions + done, page_tables, first + done, st, rs, ri, nseq),
+       "writer post");
+  }
+  return DFLASH_OK;
+}
+
 int propose_graph(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens, const int32_t* page_tables,
                   int nb, int max_ctx_len, int32_t* draft_tokens, void* logits, void* final_hidden, cudaStream_t st);
 
@@ -715,62 +783,20 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
     return fail(h, DFLASH_ECAPACITY, "first + n beyond the page-table capacity (16 * max_pages_per_seq)");
   if (n == 0) return DFLASH_OK;
   if (!taps || !positions || !page_table) return fail(h, DFLASH_EINVAL, "null pointer");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t H = c.hidden, tapd = (int64_t)c.n_taps * c.target_hidden;
-  const int kvall = c.n_layers * 2 * c.n_kv_heads * c.head_dim;
-  if (h->tc) {
-    // tensor-core writer: fc GEMM -> hidden_norm (fp32) -> [hi | lo] bf16 -> one GEMM for every
-    // layer's K and V (each weight tile times both halves) with the k_norm / RoPE / scatter
-    // epilogue
-    for (int32_t done = 0; done < n; done += c.max_write_rows) {
-      const int m = std::min<int32_t>(c.max_write_rows, n - done);
-      const void* tp = static_cast<const char*>(taps) + (int64_t)done * tapd * h->esz;
-      auto splits = [&](int64_t N, int64_t K) {
-        const int tn = pick_tn(m);
-        return pick_splits((int)(((N + 127) / 128) * ((m + tn - 1) / tn)), (int)(K / 64), h->num_sms, tn);
-      };
-      GemmParams pf;
-      pf.ws = h->ws;
-      pf.counters = h->counters;
-      pf.status = h->d_status;
-      pf.out = h->wy;
-      pf.ldo = (int)H;
-      KL(K_W_FC, launch_gemm_tc(EPI_STORE, h->fc, (int)H, (int)tapd, tp, (int)tapd, m, pf, splits(H, tapd), st, false),
-         "writer fc");
-      KL(K_W_NORM, launch_rmsnorm_f32out(h, h->wy, h->hidden_norm, h->wf, m, (int)H, st), "writer hidden_norm");
-      KL(K_W_NORM, launch_split_hi_lo(h->wf, m, (int)H, h->wf2, st), "writer split");
-      GemmParams pk;
-      pk.ws = h->ws;
-      pk.counters = h->counters;
-      pk.status = h->d_status;
-      pk.eps = c.rms_eps;
-      pk.k_norm = static_cast<const __nv_bfloat16*>(h->kn_all);
-      pk.inv_pi = h->rope_inv_pi;
-      pk.mscale = h->rope_mscale;
-      pk.nkv = c.n_kv_heads;
-      pk.positions = positions + done;
-      pk.page_tables = page_table;
-      pk.first = first + done;
-      pk.g = h->geom;
-      pk.pool = static_cast<__nv_bfloat16*>(h->pool);
-      KL(K_W_KV, launch_gemm_tc(EPI_CTXKV, h->w_ctxkv, kvall, (int)H, h->wf2, (int)(2 * H), m, pk,
-                                splits(kvall, H), st, false),
-         "writer kv");
-    }
-    return DFLASH_OK;
-  }
-  for (int32_t done = 0; done < n; done += c.max_write_rows) {
-    const int m = std::min<int32_t>(c.max_write_rows, n - done);
-    const void* tp = static_cast<const char*>(taps) + (int64_t)done * tapd * h->esz;
-    // f = hidden_norm(fc . taps)  (dflash.rs ctx_features)
-    KL(K_W_FC, launch_gemm(h, tp, (int)tapd, h->fc, m, (int)H, (int)tapd, h->wy, (int)H, false, st), "writer fc");
-    KL(K_W_NORM, launch_rmsnorm_f32out(h, h->wy, h->hidden_norm, h->wf, m, (int)H, st), "writer hidden_norm");
-    // every layer's K and V in one GEMM over the fused weight (fp32 features), then
-    // k_norm / RoPE / scatter
-    KL(K_W_KV, launch_gemm_xf32(h, h->wf, (int)H, h->w_ctxkv, m, kvall, (int)H, h->wy, kvall, st), "writer kv");
-    KL(K_W_POST, launch_ctxkv_post(h, h->wy, m, positions + done, page_table, first + done, st), "writer post");
-  }
-  return DFLASH_OK;
+  return write_ctx_rows(h, taps, positions, page_table, 1, nullptr, nullptr, first, n,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dflash_write_ctx_kv_batch(dflash_handle* h, const void* taps, const int32_t* positions, const int32_t* row_seq,
+                              const int32_t* row_index, const int32_t* page_tables, int32_t nseq, int32_t n,
+                              dflash_stream stream) {
+  if (!h) return fail(nullptr, DFLASH_EINVAL, "null handle");
+  h->err.clear();
+  if (n < 0 || nseq < 1) return fail(h, DFLASH_EINVAL, "n must be >= 0 and nseq >= 1");
+  if (n == 0) return DFLASH_OK;
+  if (!taps || !positions || !row_seq || !row_index || !page_tables) return fail(h, DFLASH_EINVAL, "null pointer");
+  return write_ctx_rows(h, taps, positions, page_tables, nseq, row_seq, row_index, 0, n,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dflash_propose(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx_lens,

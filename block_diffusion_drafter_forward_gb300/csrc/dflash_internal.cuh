@@ -225,8 +225,11 @@ cudaError_t launch_silu_mul(const dflash_handle* h, const float* y, int rows, vo
 cudaError_t launch_argmax(const dflash_handle* h, const float* logits32, int nb, int32_t* drafts,
                           void* logits_out, cudaStream_t st);
 cudaError_t launch_copy_hidden(const dflash_handle* h, const void* src, int rows, void* dst, cudaStream_t st);
+// Row i goes to row first + i of the one sequence of page_table, or (row_seq / row_index given,
+// the batched writer) to row row_index[i] of sequence row_seq[i] of page_table [nseq, mpps].
 cudaError_t launch_ctxkv_post(const dflash_handle* h, const float* ykv, int n, const int32_t* positions,
-                              const int32_t* page_table, int first, cudaStream_t st);
+                              const int32_t* page_table, int first, cudaStream_t st,
+                              const int32_t* row_seq = nullptr, const int32_t* row_index = nullptr, int nseq = 1);
 cudaError_t launch_embed_tc(const dflash_handle* h, const int32_t* bonus, int nb, cudaStream_t st);
 cudaError_t launch_split_hi_lo(const float* x, int rows, int n, void* out, cudaStream_t st);
 cudaError_t launch_fold_norm(const void* A, const void* B, int mode, int rows, int cols, const void* ln, void* out,

@@ -300,8 +300,13 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
     for (int c = 0; c < 16; ++c) {
       const int m = m0 + c0 + c;
       if (m >= p.M) continue;
-      const int li = p.first + m;
-      const int page = p.page_tables[li / kPage];
+      const int li = p.row_index ? __ldg(p.row_index + m) : p.first + m;
+      const int sq = p.row_seq ? __ldg(p.row_seq + m) : 0;
+      if (sq < 0 || sq >= p.nseq || li < 0 || li >= p.mpps * kPage) {  // batched rows: checked on the device
+        if (t == 0) set_status(p.status, DFLASH_DEV_BAD_CTX);
+        continue;
+      }
+      const int page = p.page_tables[(int64_t)sq * p.mpps + li / kPage];
       if (page < 0 || page >= p.g.num_pages) {
         if (t == 0) set_status(p.status, DFLASH_DEV_BAD_PAGE);
         continue;

@@ -39,9 +39,15 @@ struct GemmParams {
   const int32_t* widths = nullptr;       // [nb] active block widths (null: gamma); lm_head drafts
   PoolGeom g{};
   __nv_bfloat16* pool = nullptr;
-  // EPI_CTXKV (k_norm: every layer's k_norm [L, 128]; page_tables: one sequence's table)
+  // EPI_CTXKV (k_norm: every layer's k_norm [L, 128]).  Row m goes to row index first + m of the
+  // one sequence whose table is page_tables, or, with row_seq / row_index (the batched writer),
+  // to row index row_index[m] of sequence row_seq[m] (table row row_seq[m] of page_tables [nseq,
+  // mpps]).
   const int32_t* positions = nullptr;
   int first = 0;
+  const int32_t* row_seq = nullptr;
+  const int32_t* row_index = nullptr;
+  int nseq = 1;
   // EPI_RESID
   float* x = nullptr;
   __nv_bfloat16* xb = nullptr;

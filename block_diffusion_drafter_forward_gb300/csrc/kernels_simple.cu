@@ -308,7 +308,9 @@ template <typename T>
 __global__ void ctxkv_post_kernel(const float* __restrict__ ykv, int ldy, const T* __restrict__ kn_all,
                                   const float2* __restrict__ inv_pi, float mscale, float eps, int nkv, int hd,
                                   const int32_t* __restrict__ positions, const int32_t* __restrict__ page_table,
-                                  int first, PoolGeom g, T* __restrict__ pool, unsigned* status) {
+                                  int first, PoolGeom g, T* __restrict__ pool, unsigned* status,
+                                  const int32_t* __restrict__ row_seq, const int32_t* __restrict__ row_index,
+                                  int nseq, int mpps) {
   extern __shared__ float sm[];
   const int i = blockIdx.x, d = threadIdx.x;
   const int l = blockIdx.y / (2 * nkv), rem = blockIdx.y % (2 * nkv);
@@ -326,8 +328,14 @@ __global__ void ctxkv_post_kernel(const float* __restrict__ ykv, int ldy, const 
     const float a = sm[j], b = sm[j + half];
     v = (d < half ? a * c - b * sn : b * c + a * sn) * mscale;
   }
-  const int li = first + i;
-  const int page = page_table[li / kPage];
+  // row i -> row index first + i of the one sequence, or (batched) row_index[i] of row_seq[i]
+  const int li = row_index ? row_index[i] : first + i;
+  const int sq = row_seq ? row_seq[i] : 0;
+  if (sq < 0 || sq >= nseq || li < 0 || li >= mpps * kPage) {
+    if (d == 0) flag(status, DFLASH_DEV_BAD_CTX);
+    return;
+  }
+  const int page = page_table[(int64_t)sq * mpps + li / kPage];
   if (page < 0 || page >= g.num_pages) {
     if (d == 0) flag(status, DFLASH_DEV_BAD_PAGE);
     return;
@@ -562,7 +570,8 @@ cudaError_t launch_copy_hidden(const dflash_handle* h, const void* src, int rows
 }
 
 cudaError_t launch_ctxkv_post(const dflash_handle* h, const float* ykv, int n, const int32_t* positions,
-                              const int32_t* page_table, int first, cudaStream_t st) {
+                              const int32_t* page_table, int first, cudaStream_t st, const int32_t* row_seq,
+                              const int32_t* row_index, int nseq) {
   const dflash_cfg& c = h->cfg;
   if (n <= 0) return cudaSuccess;
   dim3 grid(n, c.n_layers * 2 * c.n_kv_heads);
@@ -570,7 +579,7 @@ cudaError_t launch_ctxkv_post(const dflash_handle* h, const float* ykv, int n, c
   DISPATCH_T(c.dtype, ctxkv_post_kernel<T><<<grid, c.head_dim, c.head_dim * sizeof(float), st>>>(
                           ykv, ldy, static_cast<const T*>(h->kn_all), h->rope_inv_pi, h->rope_mscale, c.rms_eps,
                           c.n_kv_heads, c.head_dim, positions, page_table, first, h->geom,
-                          static_cast<T*>(h->pool), h->d_status));
+                          static_cast<T*>(h->pool), h->d_status, row_seq, row_index, nseq, c.max_pages_per_seq));
   return cudaGetLastError();
 }
 

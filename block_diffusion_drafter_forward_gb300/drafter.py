@@ -138,6 +138,19 @@ class Drafter:
         L.dflash_write_ctx_kv(self.handle, taps.data_ptr(), positions.data_ptr(), page_table.data_ptr(), first, n,
                               _stream(stream))
 
+    def write_ctx_kv_batch(self, taps: torch.Tensor, positions: torch.Tensor, row_seq: torch.Tensor,
+                           row_index: torch.Tensor, page_tables: torch.Tensor, stream=None) -> None:
+        """Context rows of several sequences in one call: row i goes to row row_index[i] of
+        sequence row_seq[i] (a row of page_tables [nseq, max_pages_per_seq])."""
+        n = int(taps.shape[0]) if taps.dim() >= 1 else -1
+        check_tensor(taps, "taps", self.act_dtype, (n, self.cfg.n_taps * self.cfg.target_hidden))
+        for t, name in ((positions, "positions"), (row_seq, "row_seq"), (row_index, "row_index")):
+            check_tensor(t, name, torch.int32, (n,))
+        nseq = int(page_tables.shape[0]) if page_tables.dim() == 2 else -1
+        check_tensor(page_tables, "page_tables", torch.int32, (nseq, self.ccfg.max_pages_per_seq))
+        L.dflash_write_ctx_kv_batch(self.handle, taps.data_ptr(), positions.data_ptr(), row_seq.data_ptr(),
+                                    row_index.data_ptr(), page_tables.data_ptr(), nseq, n, _stream(stream))
+
     def propose(self, bonus: torch.Tensor, ctx_lens: torch.Tensor, page_tables: torch.Tensor, max_ctx_len: int,
                 drafts: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
                 hidden: Optional[torch.Tensor] = None, stream=None, q_rope_pos: Optional[torch.Tensor] = None,

@@ -158,6 +158,25 @@ int dflash_write_ctx_kv(dflash_handle* h, const void* taps, const int32_t* posit
                         const int32_t* page_table, int32_t first, int32_t n,
                         dflash_stream stream);
 
+/* Batched context-K/V writer: one call over the new rows of many sequences (dflash_head.rs
+ * batched precompute_ctx_kv over every sequence's uncommitted rows; dflash.rs prime ingest),
+ * the same arithmetic as dflash_write_ctx_kv row by row, with the fc and fused K/V weights
+ * streamed once per chunk of cfg.max_write_rows rows instead of once per sequence.
+ *   taps       [n, n_taps*target_hidden] cfg.dtype, rows of any sequences in any order.
+ *   positions  [n] int32 RoPE positions of the rows.
+ *   row_seq    [n] int32: sequence of row i (a row of page_tables), in [0, nseq).
+ *   row_index  [n] int32: logical row index of row i within its sequence, in
+ *              [0, 16 * max_pages_per_seq); row i goes to slot
+ *              page_tables[row_seq[i]][row_index[i] / 16] * 16 + row_index[i] % 16.
+ *   page_tables [nseq, max_pages_per_seq] int32.
+ * Two rows aimed at the same slot race (one of them wins).  A row whose row_seq or row_index
+ * is out of range is skipped and sets DFLASH_DEV_BAD_CTX; a bad page id DFLASH_DEV_BAD_PAGE.
+ * n == 0 is a no-op; nseq >= 1. */
+int dflash_write_ctx_kv_batch(dflash_handle* h, const void* taps, const int32_t* positions,
+                              const int32_t* row_seq, const int32_t* row_index,
+                              const int32_t* page_tables, int32_t nseq, int32_t n,
+                              dflash_stream stream);
+
 /* One gamma-block forward over nb sequences (dflash.rs forward_round + final norm +
  * lm_head + argmax; dflash_head.rs propose_batch band layout).  Sequence s drafts from
  * its block [bonus_tokens[s], mask x (gamma-1)] at positions ctx_lens[s] + r, attends
