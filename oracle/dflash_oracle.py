@@ -309,6 +309,25 @@ class Oracle:
             self._f64[name] = a
         return a
 
+    # the seven projections of a layer that the FP8 drafter lane stores in e4m3
+    FP8_LAYER = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+    def Wproj(self, l: int, t: str) -> np.ndarray:
+        """Projection weight of layer l as the block forward uses it: the stored weight, or, with
+        FP8 layer weights (from_weights.rs Phase G: q/k/v/o/gate/up/down quantised to e4m3 with a
+        per-output-row fp32 scale), its decoded codes times the row scales."""
+        name = f"L{l}.{t}"
+        if getattr(self.cfg, "layer_weight_dtype", "bf16") != "fp8" or t not in self.FP8_LAYER:
+            return self.W(name)
+        key = name + "#fp8"
+        if key in self._f64:
+            return self._f64[key]
+        codes, scale = fp8_quantize_rows(self.W(name).astype(np.float32))
+        a = e4m3_decode(codes) * scale.astype(np.float64)[:, None]
+        if self.cache:
+            self._f64[key] = a
+        return a
+
     # ---- context path: dflash.rs ctx_features + ingest_ctx
 
     def ctx_features(self, taps: np.ndarray) -> np.ndarray:
@@ -369,7 +388,7 @@ class Oracle:
         key_idx = np.arange(ctx_len + g, dtype=np.int64)
         x = self.embed_rows(self.block_tokens(bonus, g))
         for l in range(c.n_layers):
-            L = lambda t: self.W(f"L{l}.{t}")  # noqa: E731
+            L = lambda t: self.Wproj(l, t)  # noqa: E731
             xn = rms_norm(x, L("ln_in"), c.rms_eps)
             q = (xn @ L("wq").T).reshape(g, nh, hd)
             kb = (xn @ L("wk").T).reshape(g, nkv, hd)
@@ -399,12 +418,13 @@ class Oracle:
         pos_all = np.concatenate([np.asarray(ctx_pos, dtype=np.int64), pos_b])
         x = self.embed_rows(self.block_tokens(bonus))
         for l in range(c.n_layers):
-            L = lambda t: self.W(f"L{l}.{t}")  # noqa: E731
+            L = lambda t: self.Wproj(l, t)  # noqa: E731
             xn = rms_norm(x, L("ln_in"), c.rms_eps)
             q = (xn @ L("wq").T).reshape(g, nh, hd)
-            src = np.concatenate([f_ctx, xn], axis=0)
-            k = (src @ L("wk").T).reshape(n + g, nkv, hd)
-            v = (src @ L("wv").T).reshape(n + g, nkv, hd)
+            # context rows through the stored K/V weights (the fused context-K/V weight stays
+            # bf16 on the FP8 lane), block rows through the block's projections
+            k = np.concatenate([f_ctx @ self.W(f"L{l}.wk").T, xn @ L("wk").T], axis=0).reshape(n + g, nkv, hd)
+            v = np.concatenate([f_ctx @ self.W(f"L{l}.wv").T, xn @ L("wv").T], axis=0).reshape(n + g, nkv, hd)
             q = rope(rms_norm(q, L("q_norm"), c.rms_eps), pos_b, self.inv_freq, self.mscale)
             k = rope(rms_norm(k, L("k_norm"), c.rms_eps), pos_all, self.inv_freq, self.mscale)
             window = c.sliding_window if c.sliding(l) else 0

@@ -57,6 +57,7 @@ class DrafterConfig:
     markov_rank: int = 0          # DSpark Markov head rank (0: none)
     dtype: str = "bf16"          # 'f32' or 'bf16': weights, activations and KV cache
     lm_head_dtype: str = "bf16"  # same as dtype, or 'fp8' (e4m3 + per-row fp32 scale)
+    layer_weight_dtype: str = "bf16"  # 'bf16', or 'fp8': q/k/v/o/gate/up/down of every layer in e4m3
     page_size: int = 16
 
     @property
@@ -100,6 +101,13 @@ CONFIGS: Dict[str, DrafterConfig] = {
     "small_gqa4_bf16": DrafterConfig(
         name="small_gqa4_bf16", hidden=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, n_ff=2048,
         n_layers=2, vocab=8192, n_taps=2, target_hidden=1024),
+    # the FP8 drafter lane: every layer's seven projections and the lm_head in e4m3
+    "qwen3_8l_fp8w": DrafterConfig(name="qwen3_8l_fp8w", lm_head_dtype="fp8", layer_weight_dtype="fp8",
+                                   **_C2_ARCH),
+    "tiny_fp32_fp8w": DrafterConfig(
+        name="tiny_fp32_fp8w", hidden=256, n_q_heads=4, n_kv_heads=1, head_dim=64, n_ff=512,
+        n_layers=1, vocab=2048, n_taps=3, target_hidden=256, dtype="f32", lm_head_dtype="f32",
+        layer_weight_dtype="fp8"),
     # DSpark Markov head (rank 256, as in the pages' DSpark drafter) on the 8-layer drafter, and
     # a rank-32 head on the tiny fp32 drafter
     "qwen3_8l_markov": DrafterConfig(name="qwen3_8l_markov", markov_rank=256, **_C2_ARCH),
@@ -359,4 +367,7 @@ WORKLOADS = {
                                                    taps_rows=8192),
     "fp8head_nb64_ctx32768": lambda: make_workload(CONFIGS["qwen3_8l_fp8head"], 5, [32768] * 64,
                                                    taps_rows=8192),
+    # the FP8 drafter lane (layer weights and lm_head in e4m3) on the headline shape
+    "fp8w_nb1_ctx4096": lambda: make_workload(CONFIGS["qwen3_8l_fp8w"], 6, [4096]),
+    "fp8w_nb32_ragged": lambda: make_workload(CONFIGS["qwen3_8l_fp8w"], 7, _c3_ctx(3)),
 }

@@ -755,3 +755,59 @@ def test_window_is_measured_on_row_indices():
     np.testing.assert_array_equal(a, b)
     o_20 = O.Oracle(dataclasses.replace(cfg0, sliding_window=20, layer_sliding=(True,)), W, cache=True)
     assert np.abs(o_20.forward_block(ks, vs, pos, 5, 64, block_pos0=5064) - a).max() > 1e-3
+
+
+# ----------------------------------------------------------------------------- FP8 layer weights
+
+
+def test_fp8_layer_weights_rounding_bound_and_cached_equals_uncached():
+    """With FP8 layer weights every projection the block uses is within half an e4m3 step of the
+    stored weight (relative 2^-4 for normal codes, absolute 2^-10 * scale below them), the
+    context K/V keep the stored weights, and the cached and uncached forms still agree."""
+    cfg = CONFIGS["tiny_fp32_fp8w"]
+    W = make_weights(cfg, 1)
+    wl = make_workload(cfg, 1, [64])
+    o = O.Oracle(cfg, W, cache=True)
+    for t in O.Oracle.FP8_LAYER:
+        w = o.W(f"L0.{t}")
+        q = o.Wproj(0, t)
+        scale = np.abs(w).max(axis=1, keepdims=True).astype(np.float32) / np.float32(448.0)
+        err = np.abs(q - w)
+        bound = np.maximum(np.abs(w) * 2.0 ** -4, scale.astype(np.float64) * 2.0 ** -10)
+        assert np.all(err <= bound * (1 + 1e-6)), t
+        assert np.abs(q - w).max() > 0
+    taps = workload_taps(wl, 0, 0, 64)
+    pos = wl.ctx_positions(0, 0, 64)
+    f = o.ctx_features(taps)
+    ks, vs = o.ctx_kv(f, pos)
+    k_plain, _ = O.Oracle(CONFIGS["tiny_fp32"], W, cache=True).ctx_kv(f, pos)
+    np.testing.assert_array_equal(ks[0], k_plain[0])
+    np.testing.assert_allclose(o.forward_block(ks, vs, pos, 77, 64), o.forward_uncached(f, pos, 77),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_layer_weights_exact_on_the_e4m3_grid():
+    """Weights whose rows are e4m3 values times 2^-k with a +-448 entry quantise losslessly: the
+    FP8 forward then equals the full-precision forward; dividing by the scale instead of
+    multiplying would not."""
+    cfg8, cfg = CONFIGS["tiny_fp32_fp8w"], CONFIGS["tiny_fp32"]
+    W = make_weights(cfg, 1)
+    rng = np.random.default_rng(5)
+    grid = O.e4m3_decode(np.arange(256, dtype=np.uint8))
+    grid = grid[np.isfinite(grid)]
+    over = {}
+    for t in O.Oracle.FP8_LAYER:
+        shape = W.get(f"L0.{t}").shape
+        k = rng.integers(8, 14, size=(shape[0], 1))
+        vals = rng.choice(grid, size=shape)
+        vals[:, 0] = 448.0
+        over[f"L0.{t}"] = (vals * 2.0 ** -k).astype(np.float32)
+    src = DictWeights(W, over)
+    o8, o = O.Oracle(cfg8, src, cache=True), O.Oracle(cfg, src, cache=True)
+    for t in O.Oracle.FP8_LAYER:
+        np.testing.assert_array_equal(o8.Wproj(0, t), o.W(f"L0.{t}"))
+    wl = make_workload(cfg, 1, [32])
+    taps = workload_taps(wl, 0, 0, 32)
+    a = o8.run_sequence(taps, wl.ctx_positions(0, 0, 32), 9)
+    b = o.run_sequence(taps, wl.ctx_positions(0, 0, 32), 9)
+    np.testing.assert_array_equal(a["h"], b["h"])
