@@ -51,7 +51,7 @@ class dflash_cfg(ctypes.Structure):
         ("dtype", ctypes.c_int32), ("lm_head_dtype", ctypes.c_int32),
         ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("max_batch", ctypes.c_int32),
         ("max_pages_per_seq", ctypes.c_int32), ("max_write_rows", ctypes.c_int32),
-        ("markov_rank", ctypes.c_int32),
+        ("markov_rank", ctypes.c_int32), ("layer_weight_dtype", ctypes.c_int32),
     ]
 
 
@@ -71,7 +71,7 @@ EXPORTS = ("dflash_create", "dflash_destroy", "dflash_write_ctx_kv", "dflash_pro
            "dflash_device_status", "dflash_last_error", "dflash_fp8_lm_head", "dflash_profile",
            "dflash_profile_kinds", "dflash_profile_read", "dflash_gemm_bf16",
            "dflash_attention_check", "dflash_gemm_bf16_noalloc", "dflash_set_persistent", "dflash_persistent",
-           "dflash_propose_ex", "dflash_write_ctx_kv_batch")
+           "dflash_propose_ex", "dflash_write_ctx_kv_batch", "dflash_fp8_layer")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -103,6 +103,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_device_status.restype = c.c_int
     lib.dflash_fp8_lm_head.argtypes = [vp, c.POINTER(vp), c.POINTER(vp)]
     lib.dflash_fp8_lm_head.restype = c.c_int
+    lib.dflash_fp8_layer.argtypes = [vp, i32, i32, c.POINTER(vp), c.POINTER(vp)]
+    lib.dflash_fp8_layer.restype = c.c_int
     lib.dflash_profile.argtypes = [vp, c.c_int]
     lib.dflash_profile.restype = c.c_int
     lib.dflash_profile_kinds.argtypes = []
@@ -205,6 +207,15 @@ def dflash_fp8_lm_head(handle: int) -> Tuple[int, int]:
     """Device pointers of the e4m3 lm_head codes [V, H] and per-row scales [V]."""
     codes, scales = ctypes.c_void_p(), ctypes.c_void_p()
     _check(load().dflash_fp8_lm_head(ctypes.c_void_p(handle), ctypes.byref(codes), ctypes.byref(scales)),
+           ctypes.c_void_p(handle))
+    return codes.value, scales.value
+
+
+def dflash_fp8_layer(handle: int, layer: int, proj: int) -> Tuple[int, int]:
+    """Device pointers of one FP8 layer projection's e4m3 codes and per-row scales
+    (proj 0 qkv, 1 o_proj, 2 gate/up packed, 3 down)."""
+    codes, scales = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(load().dflash_fp8_layer(ctypes.c_void_p(handle), layer, proj, ctypes.byref(codes), ctypes.byref(scales)),
            ctypes.c_void_p(handle))
     return codes.value, scales.value
 

@@ -190,6 +190,10 @@ int check_cfg(const dflash_cfg& c) {
   for (int l = 0; l < c.n_layers; ++l)
     if (c.layer_sliding[l] && c.sliding_window <= 0) return bad("sliding layer with sliding_window <= 0");
   if ((int64_t)c.max_pages_per_seq * kPage > (1ll << 30)) return bad("max_pages_per_seq too large");
+  if (c.layer_weight_dtype != c.dtype && c.layer_weight_dtype != DFLASH_FP8E4M3_ROWSCALE)
+    return bad("layer_weight_dtype must equal dtype or be DFLASH_FP8E4M3_ROWSCALE");
+  if (c.layer_weight_dtype == DFLASH_FP8E4M3_ROWSCALE && c.dtype != DFLASH_BF16)
+    return fail(nullptr, DFLASH_EUNSUPPORTED, "FP8 layer weights need the bf16 drafter");
   if (c.markov_rank < 0) return bad("markov_rank must be >= 0");
   if (c.markov_rank > 0 &&
       (c.markov_rank % 32 || c.markov_rank > kMarkovMaxRank || c.max_batch > kMarkovMaxBatch ||
@@ -282,6 +286,7 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
   const int qkvd = qd + 2 * c.n_kv_heads * c.head_dim;
   const int Mp = h->rows_max;
   const int tn = pick_tn(M);
+  const bool fp8w = c.layer_weight_dtype == DFLASH_FP8E4M3_ROWSCALE;
   auto splits = [&](int N, int K) {
     const int tiles = ((N + 127) / 128) * ((M + tn - 1) / tn);
     return pick_splits(tiles, K / 64, h->num_sms, tn);
@@ -315,7 +320,10 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.g = h->geom;
       p.layer = l;
       p.pool = static_cast<__nv_bfloat16*>(h->pool);
-      KL(K_QKV, launch_gemm_tc(EPI_QKV, w.w_qkv, qkvd, H, h->xb, H, M, p, splits(qkvd, H), st, l > 0), "qkv");
+      p.row_scale = fp8w ? w.qkv_s : nullptr;
+      KL(K_QKV, launch_gemm_tc(EPI_QKV, fp8w ? (const void*)w.qkv8 : w.w_qkv, qkvd, H, h->xb, H, M, p,
+                               splits(qkvd, H), st, l > 0, fp8w),
+         "qkv");
     }
     if (h->tc_attn) {
       AttnParams a;
@@ -346,7 +354,10 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.ss_out = h->ss_a;
       p.ln_next = static_cast<const __nv_bfloat16*>(w.ln_post);
       p.H = H;
-      KL(K_OPROJ, launch_gemm_tc(EPI_RESID, w.w_o, H, qd, h->attn, qd, M, p, splits(H, qd), st, true), "o_proj");
+      p.row_scale = fp8w ? w.o_s : nullptr;
+      KL(K_OPROJ, launch_gemm_tc(EPI_RESID, fp8w ? (const void*)w.o8 : w.w_o, H, qd, h->attn, qd, M, p,
+                                 splits(H, qd), st, true, fp8w),
+         "o_proj");
     }
     {
       GemmParams p = base;
@@ -354,7 +365,9 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.ss_parts = H / 128;
       p.act = static_cast<__nv_bfloat16*>(h->act);
       p.F = F;
-      KL(K_GATEUP, launch_gemm_tc(EPI_GATEUP, w.w_gu, 2 * F, H, h->xb, H, M, p, splits(2 * F, H), st, true),
+      p.row_scale = fp8w ? w.gu_s : nullptr;
+      KL(K_GATEUP, launch_gemm_tc(EPI_GATEUP, fp8w ? (const void*)w.gu8 : w.w_gu, 2 * F, H, h->xb, H, M, p,
+                                  splits(2 * F, H), st, true, fp8w),
          "gate/up");
     }
     {
@@ -364,7 +377,10 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.ss_out = h->ss_b;
       p.ln_next = l + 1 < c.n_layers ? static_cast<const __nv_bfloat16*>(h->layer[l + 1].ln_in) : nullptr;
       p.H = H;
-      KL(K_DOWN, launch_gemm_tc(EPI_RESID, w.w_down, H, F, h->act, F, M, p, splits(H, F), st, true), "down");
+      p.row_scale = fp8w ? w.down_s : nullptr;
+      KL(K_DOWN, launch_gemm_tc(EPI_RESID, fp8w ? (const void*)w.down8 : w.w_down, H, F, h->act, F, M, p,
+                                splits(H, F), st, true, fp8w),
+         "down");
     }
   }
   KL(K_NORM, launch_rmsnorm_f32in(h, h->x, h->norm, h->xn, M, H, st), "final norm");
@@ -583,6 +599,32 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     D2D((char*)h->kn_all + l * hd * es, lw.k_norm, hd * es);
   }
 
+  // ---- FP8 drafter lane (from_weights.rs Phase G): every layer's packed q|k|v, o, gate/up and
+  // down weights quantised to e4m3 with a per-row fp32 scale (rows are output features, so the
+  // packing does not change any row's scale)
+  if (c.layer_weight_dtype == DFLASH_FP8E4M3_ROWSCALE) {
+    for (int l = 0; l < L; ++l) {
+      LayerW& d = h->layer[l];
+      const int64_t rows[4] = {qkvd, H, 2 * F, H}, cols[4] = {H, qd, H, F};
+      void* src[4] = {d.w_qkv, d.w_o, d.w_gu, d.w_down};
+      uint8_t** codes[4] = {&d.qkv8, &d.o8, &d.gu8, &d.down8};
+      float** scales[4] = {&d.qkv_s, &d.o_s, &d.gu_s, &d.down_s};
+      for (int k = 0; k < 4; ++k) {
+        uint8_t* cd = nullptr;
+        float* sc = nullptr;
+        ALLOC(cd, rows[k] * cols[k]);
+        ALLOC(sc, rows[k] * sizeof(float));
+        *codes[k] = cd;
+        *scales[k] = sc;
+        cudaError_t e = launch_quantize_fp8(src[k], (int)rows[k], (int)cols[k], c.dtype, cd, sc, st);
+        if (e != cudaSuccess) {
+          cuda_fail(h, e, "FP8 layer quantisation");
+          return bail(DFLASH_ECUDA);
+        }
+      }
+    }
+  }
+
   // ---- DSpark Markov head: both tables copied; per-step control words
   if (c.markov_rank > 0) {
     const size_t mb = (size_t)V * c.markov_rank * es;
@@ -685,7 +727,8 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     // single-launch persistent forward for batch 1: needs the tensor-core attention, a bf16
     // lm_head, one resident CTA per SM, and at least one (tile, k-block) unit of every projection
     // per CTA (its split-K finisher counts every CTA between a tile's first and last owner)
-    if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && c.markov_rank == 0 && H <= persist_max_hidden() &&
+    if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && c.layer_weight_dtype == c.dtype &&
+        c.markov_rank == 0 && H <= persist_max_hidden() &&
         L <= kPersistMaxL && persist_every_cta_has_work(H, F, nh, nkv, V, h->num_sms)) {
       int per_sm = 0;
       if (persist_occupancy(&per_sm) == cudaSuccess && per_sm >= 1) h->persist_ok = true;
@@ -1060,6 +1103,20 @@ int dflash_fp8_lm_head(const dflash_handle* h, const uint8_t** codes, const floa
   if (!h->lm_fp8) return DFLASH_EINVAL;
   *codes = h->lm_fp8;
   *scales = h->lm_scale;
+  return DFLASH_OK;
+}
+
+int dflash_fp8_layer(const dflash_handle* h, int32_t layer, int32_t proj, const uint8_t** codes,
+                     const float** scales) {
+  if (!h || !codes || !scales) return DFLASH_EINVAL;
+  if (h->cfg.layer_weight_dtype != DFLASH_FP8E4M3_ROWSCALE || layer < 0 || layer >= h->cfg.n_layers || proj < 0 ||
+      proj > 3)
+    return DFLASH_EINVAL;
+  const LayerW& d = h->layer[layer];
+  const uint8_t* cs[4] = {d.qkv8, d.o8, d.gu8, d.down8};
+  const float* ss[4] = {d.qkv_s, d.o_s, d.gu_s, d.down_s};
+  *codes = cs[proj];
+  *scales = ss[proj];
   return DFLASH_OK;
 }
 

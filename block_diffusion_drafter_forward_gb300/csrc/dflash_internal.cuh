@@ -96,6 +96,15 @@ struct LayerW {
   void* w_o = nullptr;     // [H, nh hd]
   void* w_gu = nullptr;    // [2F, H]: gate rows then up rows
   void* w_down = nullptr;  // [H, F]
+  // FP8 drafter lane: the same four packed projections as e4m3 codes + per-row fp32 scales
+  uint8_t* qkv8 = nullptr;
+  uint8_t* o8 = nullptr;
+  uint8_t* gu8 = nullptr;
+  uint8_t* down8 = nullptr;
+  float* qkv_s = nullptr;
+  float* o_s = nullptr;
+  float* gu_s = nullptr;
+  float* down_s = nullptr;
 };
 
 }  // namespace dflash

@@ -23,6 +23,8 @@
 //   EPI_LMHEAD: logits (optional, bf16), per-row fp32 scale for the FP8 head, each tile's
 //               per-token best (logit, index) folded in with a 64-bit atomicMax; the last
 //               tile turns them into drafts.
+//   With e4m3 layer weights (FP8A, from_weights.rs Phase G) the QKV / RESID / GATEUP tiles take
+//   D times the weight row's fp32 scale before their epilogue.
 //   EPI_CTXKV : context-K/V writer (dflash.rs ingest_ctx): tile = one head of one layer's
 //               K or V; K gets k_norm, RoPE at the row's position and mscale; both are
 //               scattered to the row's paged slot.  The fp32 operand comes as bf16 hi + lo
@@ -296,6 +298,12 @@ __global__ void __launch_bounds__(kThreads * WG, WG <= 2 ? 2 : 1)
         } else {
           tmem_ld16(lane_addr + c0, v);
         }
+        if constexpr (FP8A && EPI != EPI_LMHEAD) {
+          // e4m3 layer weight: this row's fp32 scale (the lm_head applies its own in the epilogue)
+          const float sc = __ldg(p.row_scale + n);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] *= sc;
+        }
         epilogue_chunk<EPI>(p, es, rsc, v, et, n, m0, c0, tile_n, pre);
       }
       if (p.nsplit > 1 && t == 0) p.counters[tile_lin] = 0;
@@ -377,6 +385,14 @@ cudaError_t launch_tn(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPa
   if constexpr (EPI == EPI_LMHEAD) {
     if (fp8a) return launch_t<EPI, TN, STAGES - 1, true, WG>(tw, tx, p, grid, st, pdl);
   }
+  if constexpr (EPI == EPI_QKV || EPI == EPI_RESID || EPI == EPI_GATEUP) {  // FP8 layer weights
+    if (fp8a) {
+      if constexpr (TN >= 64) {
+        if (p.nsplit > 1) return launch_t<EPI, TN, TN >= 128 ? 3 : 6, true, 4>(tw, tx, p, grid, st, pdl);
+      }
+      return launch_t<EPI, TN, STAGES - 1, true, WG>(tw, tx, p, grid, st, pdl);
+    }
+  }
   if constexpr (EPI == EPI_CTXKV) {  // two activation tiles per stage
     if constexpr (TN >= 128) {  // compute-heavy: two CTAs per SM rather than a deep ring
       if (p.nsplit > 1) return launch_t<EPI, TN, 4, false, 4>(tw, tx, p, grid, st, pdl);
@@ -452,7 +468,7 @@ cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, 
                            int nsplit, cudaStream_t st, bool pdl, bool w_fp8) {
   const int TN = pick_tn(M);
   CUtensorMap tw, tx;
-  if (w_fp8 && epi != EPI_LMHEAD) return cudaErrorInvalidValue;
+  if (w_fp8 && (epi == EPI_STORE || epi == EPI_CTXKV)) return cudaErrorInvalidValue;
   if (w_fp8 ? !make_tmap_u8(&tw, W, N, K) : !make_tmap_bf16(&tw, W, N, K, K, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tx, X, M, epi == EPI_CTXKV ? 2 * (int64_t)K : K, ldx, TN)) return cudaErrorInvalidValue;
   p.N = N;

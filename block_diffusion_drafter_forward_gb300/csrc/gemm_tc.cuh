@@ -73,7 +73,8 @@ int pick_tn(int M);
 int pick_splits(int tiles, int nkb, int num_sms, int tn);
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld_elems, int box_rows);
 // D = W [N, K] x X [M, K]^T with the epilogue `epi`; nsplit K-splits (1 for EPI_LMHEAD).
-// w_fp8: W holds e4m3 codes (EPI_LMHEAD only; p.row_scale carries the per-row scales).
+// w_fp8: W holds e4m3 codes and p.row_scale the per-row scales (EPI_LMHEAD, and the layer
+// projections EPI_QKV / EPI_RESID / EPI_GATEUP of the FP8 drafter lane).
 cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, int ldx, int M, GemmParams p,
                            int nsplit, cudaStream_t st, bool pdl, bool w_fp8 = false);
 

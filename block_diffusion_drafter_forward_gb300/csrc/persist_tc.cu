@@ -161,7 +161,8 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* ptr) {
 //   2 first weight copy of the phase issued        3 last MMA of the phase committed
 //   4 first accumulator (or attention Q) ready     5 split-K partials counted (finisher)
 //   6 split-K partials landed / last attention item done
-//   7 phase arrival
+//   7 phase arrival                                8 epilogue warps done (before the arrival)
+//   9 a contributor's partial counted in
 __device__ __forceinline__ void trace_stamp(const PersistParams& p, int ph, int slot) {
 #if DFLASH_PHASE_TRACE
   if (p.trace) {
@@ -187,17 +188,21 @@ __device__ bool grid_wait(const unsigned* ctr, unsigned target, volatile int* la
       return true;
     }
     if ((i & 127) == 127 && (*labort || *reinterpret_cast<volatile int*>(gabort))) return false;
-    __nanosleep(32);
   }
   *labort = 1;
   atomicExch(gabort, 1);
   return false;
 }
 
+// Release of everything the CTA wrote (its threads met at a barrier first) at GPU scope, then the
+// arrival: a cumulative acq_rel fence and a relaxed reduction (lighter than a full SC fence).
+__device__ __forceinline__ void release_add(unsigned* ctr) {
+  asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+
 __device__ __forceinline__ void grid_arrive(unsigned* ctr) {
   fence_proxy_async_global();
-  __threadfence();
-  atomicAdd(ctr, 1u);
+  release_add(ctr);
 }
 
 __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort, int* gabort) {
@@ -891,10 +896,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
 #pragma unroll
             for (int q = 0; q < 16; q += 4)
               __stcg(reinterpret_cast<float4*>(mine + q), make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]));
-            fence_proxy_async_global();
-            __threadfence();
+            fence_proxy_async_global();  // the finisher reads the partials with a bulk copy
             epi_sync();
-            if (t == 0) atomicAdd(&p.counters[sg.tile], 1u);
+            if (t == 0) release_add(&p.counters[sg.tile]);
+            if (t == 0) trace_stamp(p, ph, 9);
             continue;
           }
           if (sg.ncontrib > 1) {
@@ -908,7 +913,6 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
                   if (lane == 0) { *ab = 1; atomicExch(p.gabort, 1); }
                   break;
                 }
-                __nanosleep(20);
               }
               __syncwarp();
             }
@@ -982,6 +986,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         }
       }
       // phase done on this CTA
+      if (t == 0) trace_stamp(p, ph, 8);
       epi_sync();
       if (t == 0) grid_arrive(&p.bar[ph]);
       if (t == 0) trace_stamp(p, ph, 7);

@@ -36,6 +36,8 @@ def make_cfg(cfg, num_pages: int, max_batch: int, max_pages_per_seq: int, max_wr
     c.max_pages_per_seq = int(max_pages_per_seq)
     c.max_write_rows = int(max_write_rows)
     c.markov_rank = int(getattr(cfg, "markov_rank", 0))
+    c.layer_weight_dtype = _DT[getattr(cfg, "layer_weight_dtype", cfg.dtype)] \
+        if getattr(cfg, "layer_weight_dtype", cfg.dtype) == "fp8" else _DT[cfg.dtype]
     return c
 
 

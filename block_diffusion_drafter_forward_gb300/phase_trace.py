@@ -21,7 +21,7 @@ import numpy as np
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 TRACE_LIB = os.path.join(PKG, "libdflash_trace.so")
-SLOTS = ("barrier", "act", "w_first", "mma_last", "acc", "counted", "landed", "arrive")
+SLOTS = ("barrier", "act", "w_first", "mma_last", "acc", "counted", "landed", "arrive", "epi_done", "contrib")
 
 
 def phase_names(L: int):
@@ -48,7 +48,7 @@ def table(t: np.ndarray, L: int):
     prev = t0
     rows = []
     for ph in range(P):
-        arr = t[:, ph, 7]
+        arr = t[:, ph, SLOTS.index("arrive")]
         last = int(arr[arr > 0].max()) if (arr > 0).any() else prev
         cols = {}
         for k, name in enumerate(SLOTS):

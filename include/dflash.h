@@ -55,7 +55,8 @@ typedef enum {
 typedef enum {
   DFLASH_F32 = 0,              /* fp32 weights, activations and K/V cache (CUDA-core path) */
   DFLASH_BF16 = 1,             /* bf16 weights, activations and K/V cache (tensor-core path) */
-  DFLASH_FP8E4M3_ROWSCALE = 2  /* lm_head only: e4m3 codes + one fp32 scale per vocab row */
+  DFLASH_FP8E4M3_ROWSCALE = 2  /* lm_head_dtype / layer_weight_dtype: e4m3 codes + one fp32 scale
+                                  per output row */
 } dflash_dtype;
 
 /* Device status bits (dflash_device_status). */
@@ -97,6 +98,11 @@ typedef struct {
   int32_t max_write_rows;   /* rows per internal chunk of dflash_write_ctx_kv (>= 16) */
   int32_t markov_rank;      /* DSpark Markov head rank; 0 = no head.  Otherwise a multiple of 32,
                                <= 1024, with max_batch <= 64 and max_batch * rank <= 40960 */
+  int32_t layer_weight_dtype; /* == dtype, or DFLASH_FP8E4M3_ROWSCALE (bf16 drafters): the FP8
+                               drafter lane (from_weights.rs Phase G), q/k/v/o/gate/up/down of every
+                               layer quantised at create to e4m3 with a per-output-row fp32 scale
+                               (scale = fp32 rowmax|w| / 448) and used by dflash_propose; the
+                               context-K/V writer keeps the bf16 K/V weights */
 } dflash_cfg;
 
 /* One layer's weights, HF layout (Linear weights [out, in] row-major), all in cfg.dtype,
@@ -241,6 +247,15 @@ int dflash_kv_layout(const dflash_handle* h, void** pool, size_t* bytes, int64_t
  * *codes = [V, H] uint8 e4m3 codes, *scales = [V] fp32 per-row scales, device pointers
  * owned by the handle.  EINVAL when the lm_head is not FP8. */
 int dflash_fp8_lm_head(const dflash_handle* h, const uint8_t** codes, const float** scales);
+
+/* The e4m3 layer weights built by dflash_create when layer_weight_dtype is FP8 (for tests):
+ * proj 0 = fused q|k|v [(nh+2nkv)*hd, H] (q rows, then k, then v), 1 = o_proj [H, nh*hd],
+ * 2 = gate/up [2F, H] packed in blocks of 64 rows (block b: gate rows 64b..64b+63, then the
+ * matching up rows), 3 = down [H, F]; *codes row-major uint8, *scales fp32 per row, device
+ * pointers owned by the handle.  EINVAL when the layer weights are not FP8 or the indices are
+ * out of range. */
+int dflash_fp8_layer(const dflash_handle* h, int32_t layer, int32_t proj, const uint8_t** codes,
+                     const float** scales);
 
 /* Per-kernel timing for benchmarks.  dflash_profile(h, 1) clears the counters and from
  * then on brackets every kernel launch of the handle with CUDA events on the launch

@@ -17,7 +17,7 @@ STRUCTS = {
                    "mask_token_id", "n_taps", "target_hidden", "rms_eps", "rope_theta", "rope_yarn", "yarn_factor",
                    "yarn_orig_max_pos", "yarn_beta_fast", "yarn_beta_slow", "sliding_window", "layer_sliding", "dtype",
                    "lm_head_dtype", "page_size", "num_pages", "max_batch", "max_pages_per_seq", "max_write_rows",
-                   "markov_rank"),
+                   "markov_rank", "layer_weight_dtype"),
     "dflash_layer_weights": ("ln_in", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "ln_post", "w_gate", "w_up",
                              "w_down"),
     "dflash_weights": ("fc", "hidden_norm", "norm", "embed", "lm_head", "layers", "markov_w1", "markov_w2"),

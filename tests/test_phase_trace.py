@@ -6,7 +6,7 @@ from block_diffusion_drafter_forward_gb300 import phase_trace as pt
 
 
 def test_table_from_synthetic_stamps(tmp_path):
-    L, G, S = 1, 2, 8
+    L, G, S = 1, 2, 10
     P = 2 + 6 * L
     t = np.zeros((G, P, S), dtype=np.uint64)
     base = 1_000_000
