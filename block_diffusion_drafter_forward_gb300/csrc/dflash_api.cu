@@ -190,8 +190,8 @@ int check_cfg(const dflash_cfg& c) {
   for (int l = 0; l < c.n_layers; ++l)
     if (c.layer_sliding[l] && c.sliding_window <= 0) return bad("sliding layer with sliding_window <= 0");
   if ((int64_t)c.max_pages_per_seq * kPage > (1ll << 30)) return bad("max_pages_per_seq too large");
-  if (c.layer_weight_dtype != c.dtype && c.layer_weight_dtype != DFLASH_FP8E4M3_ROWSCALE)
-    return bad("layer_weight_dtype must equal dtype or be DFLASH_FP8E4M3_ROWSCALE");
+  if (c.layer_weight_dtype != c.dtype && c.layer_weight_dtype != 0 && c.layer_weight_dtype != DFLASH_FP8E4M3_ROWSCALE)
+    return bad("layer_weight_dtype must be 0 (same as dtype), dtype or DFLASH_FP8E4M3_ROWSCALE");
   if (c.layer_weight_dtype == DFLASH_FP8E4M3_ROWSCALE && c.dtype != DFLASH_BF16)
     return fail(nullptr, DFLASH_EUNSUPPORTED, "FP8 layer weights need the bf16 drafter");
   if (c.markov_rank < 0) return bad("markov_rank must be >= 0");
@@ -250,6 +250,7 @@ int propose_persist(dflash_handle* h, const int32_t* bonus_tokens, const int32_t
   p.maps = static_cast<const CUtensorMap*>(h->p_maps);
   p.x = h->x;
   p.xb = static_cast<__nv_bfloat16*>(h->xb);
+  p.xb2 = static_cast<__nv_bfloat16*>(h->xb2);
   p.ss_a = h->ss_a;
   p.ss_b = h->ss_b;
   p.q = static_cast<__nv_bfloat16*>(h->q);
@@ -258,6 +259,7 @@ int propose_persist(dflash_handle* h, const int32_t* bonus_tokens, const int32_t
   p.pool = static_cast<__nv_bfloat16*>(h->pool);
   p.g = h->geom;
   p.ws = h->ws;
+  p.ws_half = h->p_ws_half;
   p.o_part = h->attn_opart;
   p.ml_part = h->attn_ml;
   p.drafts = draft_tokens;
@@ -727,7 +729,7 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     // single-launch persistent forward for batch 1: needs the tensor-core attention, a bf16
     // lm_head, one resident CTA per SM, and at least one (tile, k-block) unit of every projection
     // per CTA (its split-K finisher counts every CTA between a tile's first and last owner)
-    if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && c.layer_weight_dtype == c.dtype &&
+    if (h->tc_attn && c.lm_head_dtype != DFLASH_FP8E4M3_ROWSCALE && c.layer_weight_dtype != DFLASH_FP8E4M3_ROWSCALE &&
         c.markov_rank == 0 && H <= persist_max_hidden() &&
         L <= kPersistMaxL && persist_every_cta_has_work(H, F, nh, nkv, V, h->num_sms)) {
       int per_sm = 0;
@@ -735,8 +737,11 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
       cudaGetLastError();
     }
     if (h->persist_ok) {
-      need = std::max(need, persist_ws_floats((int)H, (int)F, (int)nh, (int)nkv, (int)V, h->num_sms));
-      std::vector<CUtensorMap> maps(4 * L + 4);
+      // two halves of split-K partials, used by alternate phases of the single launch
+      h->p_ws_half = persist_ws_floats((int)H, (int)F, (int)nh, (int)nkv, (int)V, h->num_sms);
+      need = std::max(need, 2 * h->p_ws_half);
+      ALLOC(h->xb2, R * H * es);
+      std::vector<CUtensorMap> maps(4 * L + 5);
       bool ok = true;
       for (int l = 0; l < L && ok; ++l) {
         const LayerW& d = h->layer[l];
@@ -748,7 +753,8 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
       ok = ok && make_tmap_bf16(&maps[4 * L], h->lm_head, V, H, H, 128) &&
            make_tmap_bf16(&maps[4 * L + 1], h->xb, kGamma, H, H, kGamma) &&
            make_tmap_bf16(&maps[4 * L + 2], h->attn, kGamma, qd, qd, kGamma) &&
-           make_tmap_bf16(&maps[4 * L + 3], h->act, kGamma, F, F, kGamma);
+           make_tmap_bf16(&maps[4 * L + 3], h->act, kGamma, F, F, kGamma) &&
+           make_tmap_bf16(&maps[4 * L + 4], h->xb2, kGamma, H, H, kGamma);
       if (!ok) {
         fail(h, DFLASH_ECUDA, "tensor maps of the persistent forward");
         return bail(DFLASH_ECUDA);

@@ -166,6 +166,8 @@ struct dflash_handle {
   bool persist_ok = false;             // available for this configuration and device
   bool persist_on = false;             // used by dflash_propose (dflash_set_persistent)
   void* p_maps = nullptr;              // device CUtensorMap table
+  void* xb2 = nullptr;                 // [rows, H] bf16 gate/up operand of the single launch
+  size_t p_ws_half = 0;                // floats in each half of the single launch's partials
   unsigned* p_ctl = nullptr;           // control words, zeroed before each launch
   size_t p_ctl_words = 0;
   unsigned long long* p_trace = nullptr;  // phase timeline (DFLASH_PHASE_TRACE builds only)

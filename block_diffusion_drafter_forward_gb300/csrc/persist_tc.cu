@@ -5,9 +5,18 @@
 // as separate kernels every projection also pays grid completion, launch and activation-load
 // latency on the dependency chain.  Here the phases of the forward
 //     embed | per layer: QKV, attention, split combine, o_proj, gate/up, down | lm_head
-// run back to back inside one launch, separated by grid-wide arrival counters, and the
-// weight-tile producer runs ahead across those barriers: weights depend on nothing, so the
-// next projection's weights stream while the current phase finishes.  The final RMSNorm is
+// run back to back inside one launch and the weight-tile producer runs ahead of them: weights
+// depend on nothing, so the next projection's weights stream while the current phase finishes.
+// Between consecutive projections there is no grid-wide barrier: k-block kb of a projection's
+// operand comes from one tile of the projection before it (down -> QKV and lm_head, o_proj ->
+// gate/up: the 128-column tile kb / 2; gate/up -> down: tile kb) or from one attention unit
+// (combine -> o_proj), so the activation producer waits for that tile's ready flag only, and
+// the MMAs of a projection run while the previous projection's slowest split-K finishers are
+// still reducing.  Epilogues that need whole rows (1/RMS of their operand) wait for the count of
+// the previous projection's finished tiles instead.  Two buffers are doubled for this: the bf16
+// operand written by o_proj (read by gate/up) is not the one written by down (read by QKV and
+// lm_head), and alternate phases use alternate halves of the split-K partials and counters.
+// Embed -> QKV(0), QKV -> attention and attention -> combine keep grid-wide arrival counters.  The final RMSNorm is
 // folded into the last down projection's epilogue (operand bf16(x * norm), per-token 1/RMS
 // applied to the logits) the same way every other norm of the forward is.
 //
@@ -102,7 +111,7 @@ __device__ __forceinline__ GPh gemm_of(int ph, const PersistParams& p) {
   g.kind = k;
   if (k == 0) { g.epi = EPI_QKV; g.wmap = 4 * l; g.xmap = 0; g.N = qkvd; g.K = p.H; }
   else if (k == 3) { g.epi = EPI_RESID; g.wmap = 4 * l + 1; g.xmap = 1; g.N = p.H; g.K = qd; }
-  else if (k == 4) { g.epi = EPI_GATEUP; g.wmap = 4 * l + 2; g.xmap = 0; g.N = 2 * p.F; g.K = p.H; }
+  else if (k == 4) { g.epi = EPI_GATEUP; g.wmap = 4 * l + 2; g.xmap = 3; g.N = 2 * p.F; g.K = p.H; }
   else { g.epi = EPI_RESID; g.wmap = 4 * l + 3; g.xmap = 2; g.N = p.H; g.K = p.F; }
   return g;
 }
@@ -203,6 +212,44 @@ __device__ __forceinline__ void release_add(unsigned* ctr) {
 __device__ __forceinline__ void grid_arrive(unsigned* ctr) {
   fence_proxy_async_global();
   release_add(ctr);
+}
+
+// Same release, two counters (a projection tile finished: its flag and its phase's count).
+__device__ __forceinline__ void release_add2(unsigned* a, unsigned* b) {
+  asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.u32 [%0], 1;\n\t"
+               "red.relaxed.gpu.global.add.u32 [%1], 1;" ::"l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void release_addn(unsigned* a, unsigned n) {
+  asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(n) : "memory");
+}
+
+// Wait until *ctr >= target (acquire), bounded like grid_wait.
+__device__ bool count_wait(const unsigned* ctr, unsigned target, volatile int* labort, int* gabort) {
+  for (long long i = 0; i < kGridSpin; ++i) {
+    if (ld_acquire(ctr) >= target) {
+      fence_proxy_async_global();
+      return true;
+    }
+    if ((i & 127) == 127 && (*labort || *reinterpret_cast<volatile int*>(gabort))) return false;
+  }
+  *labort = 1;
+  atomicExch(gabort, 1);
+  return false;
+}
+
+// Fine-grained dependencies between consecutive projections: k-block kb of a projection's
+// operand is produced by one tile of the phase before it (128-column tiles give two k-blocks;
+// a gate/up tile gives the 64 act columns of one down k-block), and o_proj's by the attention
+// unit of the head it belongs to.  QKV of layer 0 follows the embedding with a grid barrier.
+__device__ __forceinline__ bool fine_deps(const GPh& g) { return !(g.kind == 0 && g.layer == 0); }
+__device__ __forceinline__ const unsigned* dep_flag(const PersistParams& p, const GPh& g, int ph, int kb,
+                                                    unsigned* target) {
+  if (g.kind == 3) {
+    *target = 32;
+    return p.head_done + g.layer * 64 + (kb / 2) / (p.nh / p.nkv);
+  }
+  *target = 1;
+  return p.ready + (size_t)(ph - 1) * p.ready_stride + (g.kind == 5 ? kb : kb / 2);
 }
 
 __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort, int* gabort) {
@@ -740,13 +787,24 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         SegIter it((gp.N + 127) / 128, gp.K / 64, G, c);
         Seg sg;
         bool waited = false;
+        const bool fine = fine_deps(gp);
+        const unsigned* last_dep = nullptr;
         while (it.next(sg) && !*ab) {
-          if (!waited) {
-            grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
-            trace_stamp(p, ph, 1);
-            waited = true;
-          }
+          if (!waited && !fine) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
           for (int kk = 0; kk < sg.nkb && !*ab; ++kk, ++j) {
+            if (fine) {
+              // this k-block's producer tile (or attention unit) has finished
+              unsigned target;
+              const unsigned* dep = dep_flag(p, gp, ph, sg.kb0 + kk, &target);
+              if (dep != last_dep) {
+                if (!count_wait(dep, target, ab, p.gabort)) break;
+                last_dep = dep;
+              }
+            }
+            if (!waited) {
+              trace_stamp(p, ph, 1);
+              waited = true;
+            }
             const int s = j % kS, u = j / kS;
             // use u of stage s starts once the MMA released use u - 1; the release of use u
             // needs this copy, so the stage cannot run a phase ahead of it
@@ -815,10 +873,16 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             if (kind == PH_ATTN) {
               // `pre` is only read by thread 0, which computed it
               attn_item(p, l, i / splits, i % splits, i == c ? pre : 0, sA, B, use, t);
+              fence_proxy_async_global();  // o_proj reads the attention output through TMA
               epi_sync();
+              // a unit with one split (or none: a bad context) is complete with its item
+              if (t == 0 && i % splits == 0 && attn_geom(p, l, i / splits, 0, B.ctx0).nsplit <= 1)
+                release_addn(p.head_done + l * 64 + i / splits, 32u);
             } else {
               combine_item(p, l, i / 32, i % 32, t, B.ctx0, sRed, B, red_use);
+              fence_proxy_async_global();
               epi_sync();  // the landing buffer is reused by the next item
+              if (t == 0 && attn_geom(p, l, i / 32, 0, B.ctx0).nsplit > 1) release_addn(p.head_done + l * 64 + i / 32, 1u);
             }
           }
           if (t == 0) trace_stamp(p, ph, 6);
@@ -849,12 +913,28 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         } else {
           const bool is_o = gp.kind == 3;
           e.ss_out = is_o ? p.ss_a : p.ss_b;
+          if (is_o) e.xb = p.xb2;
           // the last down projection prepares the lm_head operand bf16(x * norm)
           e.ln_next = is_o ? Ly.ln_post : (gp.layer + 1 < p.L ? p.layers[gp.layer + 1].ln_in : p.norm);
         }
+        // the phase the epilogue's inputs come from, and how long to wait for it: the previous
+        // projection's every tile where the epilogue needs whole rows (1/RMS of its operand; the
+        // residual of down comes from o_proj), every attention unit of the layer for o_proj
+        const int nt_h = p.H / 128;
+        auto epi_wait = [&]() {
+          if (t != 0) return;
+          if (!fine_deps(gp)) {
+            grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+          } else if (gp.kind == 3) {
+            for (int u = 0; u < p.nkv * (p.M / kGamma); ++u)
+              count_wait(p.head_done + gp.layer * 64 + u, 32u, ab, p.gabort);
+          } else {
+            count_wait(p.done + (gp.kind == 5 ? ph - 2 : ph - 1), (unsigned)nt_h, ab, p.gabort);
+          }
+        };
         if (gp.epi == EPI_LMHEAD && p.final_hidden && c < p.M) {
           // side job (nothing waits for it): the final hidden state of token c
-          if (t == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+          epi_wait();
           epi_sync();
           if (t == 0) rsc[0] = row_rscale(p, p.ss_b, c);
           epi_sync();
@@ -863,7 +943,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         }
         while (it.next(sg)) {
           if (first) {
-            if (t == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+            epi_wait();
             if (t == 0) trace_stamp(p, ph, 0);
             epi_sync();
             if (e.ss_in && t < TN) rsc[t] = t < p.M ? row_rscale(p, e.ss_in, t) : 1.f;
@@ -889,7 +969,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
           epi_sync();
           if (t == 0) mbar_arrive(&B.acc_empty[buf]);  // accumulator copied: MMA may reuse it
           ++segc;
-          float* tile_ws = p.ws + (int64_t)sg.tile * maxc * (kEThreads * TN);
+          // alternate phases use alternate halves of the partials and tile counters: the next
+          // phase's contributors may write while this phase's slowest finisher still reads
+          float* tile_ws = p.ws + (size_t)(ph & 1) * p.ws_half + (int64_t)sg.tile * maxc * (kEThreads * TN);
+          unsigned* cnt = p.counters + (ph & 1) * p.max_tiles;
           if (!finisher) {
             // fp32 partial of this CTA's k-range into slot `rank`, then count it in
             float* mine = tile_ws + ((int64_t)sg.rank * kEThreads + t) * TN;
@@ -898,7 +981,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
               __stcg(reinterpret_cast<float4*>(mine + q), make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]));
             fence_proxy_async_global();  // the finisher reads the partials with a bulk copy
             epi_sync();
-            if (t == 0) release_add(&p.counters[sg.tile]);
+            if (t == 0) release_add(&cnt[sg.tile]);
             if (t == 0) trace_stamp(p, ph, 9);
             continue;
           }
@@ -908,7 +991,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             if (warp == 0) {
               // the whole warp polls (one coalesced load), so no lane sleeps in an mbarrier
               // wait while lane 0 still has work to issue
-              for (long long sp = 0; ld_acquire(&p.counters[sg.tile]) < (unsigned)nother; ++sp) {
+              for (long long sp = 0; ld_acquire(&cnt[sg.tile]) < (unsigned)nother; ++sp) {
                 if (*ab || sp > kGridSpin) {
                   if (lane == 0) { *ab = 1; atomicExch(p.gabort, 1); }
                   break;
@@ -918,7 +1001,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             }
             if (t == 0) trace_stamp(p, ph, 5);
             if (t == 0) {
-              p.counters[sg.tile] = 0;  // re-armed for the next phase (ordered by its barrier)
+              cnt[sg.tile] = 0;  // re-armed for the phase after next (it depends on this one)
               if (nother <= kRedMax && !*ab) {
                 fence_proxy_async_global();
                 fence_proxy_async_smem();
@@ -967,6 +1050,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             case EPI_RESID: epilogue_chunk<EPI_RESID>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
             case EPI_GATEUP: epilogue_chunk<EPI_GATEUP>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
             default: epilogue_chunk<EPI_LMHEAD>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
+          }
+          if (gp.kind >= 3 && gp.kind <= 5) {
+            // tile finished: its outputs are the next projection's operand (read through TMA)
+            fence_proxy_async_global();
+            epi_sync();
+            if (t == 0) release_add2(p.ready + (size_t)ph * p.ready_stride + sg.tile, p.done + ph);
           }
           if (gp.epi == EPI_LMHEAD) {
             // the last vocabulary tile to finish turns the running argmaxes into drafts
@@ -1021,10 +1110,18 @@ static int max_tiles_of(int H, int F, int nh, int nkv, int V) {
   return std::max(std::max((nh + 2 * nkv) * 128, H), std::max(2 * F, V)) / 128 + 1;
 }
 
+// Tiles of any layer projection (the ones another projection's operand waits on, tile by tile).
+static int layer_tiles_of(int H, int F, int nh, int nkv) {
+  return std::max(std::max(nh + 2 * nkv, H / 128), (2 * F + 127) / 128);
+}
+
 // Control words: the packed argmax of every token (2 words each, first, so 8-byte aligned),
-// the phase counters, the abort flag, the lm_head tile counter, the split-K tile counters.
+// the phase counters, the abort flag, the lm_head tile counter, two halves of split-K tile
+// counters, the per-phase tile-ready flags and counts, the per-layer attention-unit counters.
 size_t persist_ctl_words(int L, int H, int F, int nh, int nkv, int V) {
-  return 2 * (size_t)kPersistMaxM + (size_t)(2 + 6 * L) + 2 + (size_t)max_tiles_of(H, F, nh, nkv, V);
+  const size_t P = 2 + 6 * (size_t)L;
+  return 2 * (size_t)kPersistMaxM + P + 2 + 2 * (size_t)max_tiles_of(H, F, nh, nkv, V) +
+         P * (size_t)layer_tiles_of(H, F, nh, nkv) + P + 64 * (size_t)L;
 }
 
 void persist_bind_ctl(PersistParams& p, unsigned* ctl) {
@@ -1035,6 +1132,11 @@ void persist_bind_ctl(PersistParams& p, unsigned* ctl) {
   p.gabort = reinterpret_cast<int*>(w + nbar);
   p.amax_counter = w + nbar + 1;
   p.counters = w + nbar + 2;
+  p.max_tiles = max_tiles_of(p.H, p.F, p.nh, p.nkv, p.V);
+  p.ready = p.counters + 2 * p.max_tiles;
+  p.ready_stride = layer_tiles_of(p.H, p.F, p.nh, p.nkv);
+  p.done = p.ready + (size_t)nbar * p.ready_stride;
+  p.head_done = p.done + nbar;
 }
 
 void persist_attn_split(int units, int max_ctx, int window, int G, int* cps, int* splits) {

@@ -36,9 +36,11 @@ struct PersistParams {
   const float2* inv_pi;
   PersistLayer layers[kPersistMaxL]; // per layer (in the kernel's parameter space)
   const CUtensorMap* maps;          // [4L + 1] weights (qkv, o, gate/up, down per layer; lm_head),
-                                    // then [3] activations (xb, attn, act), device, 64-B aligned
+                                    // then [4] activations (xb, attn, act, xb2), device, 64-B aligned
   float* x;
-  __nv_bfloat16* xb;
+  __nv_bfloat16* xb;    // bf16(x * ln_in) / bf16(x * norm): operand of QKV and the lm_head
+  __nv_bfloat16* xb2;   // bf16(x1 * ln_post): operand of gate/up (its own buffer, so down can
+                        // write xb while a slower CTA's gate/up still reads this one)
   float* ss_a;
   float* ss_b;
   __nv_bfloat16* q;
@@ -46,8 +48,10 @@ struct PersistParams {
   __nv_bfloat16* act;
   __nv_bfloat16* pool;
   PoolGeom g;
-  float* ws;
-  unsigned* counters;
+  float* ws;            // split-K partials, two halves of ws_half floats used by alternate phases
+  size_t ws_half;
+  unsigned* counters;   // split-K tile counters, two halves of max_tiles (alternate phases)
+  int max_tiles;
   unsigned long long* amax_best;    // [16] packed running argmax per token (control buffer)
   unsigned* amax_counter;
   float* o_part;
@@ -58,6 +62,10 @@ struct PersistParams {
   // One control buffer, zeroed before each launch (persist_ctl_words words):
   unsigned* bar;                    // [3 + 6L] phase arrival counters
   int* gabort;                      // grid-wide "a wait gave up" flag
+  unsigned* ready;                  // [phases][ready_stride] projection tile finished (0/1)
+  int ready_stride;
+  unsigned* done;                   // [phases] projection tiles finished
+  unsigned* head_done;              // [L][64] attention output rows of a unit written (32 = all)
   unsigned* status;
   // Phase timeline (builds with DFLASH_PHASE_TRACE=1 only; else unused and null):
   // [G][phases][kTraceSlots] %globaltimer stamps, see persist_tc.cu.
@@ -77,9 +85,11 @@ constexpr int kPersistMaxM = 16;
 int persist_smem_bytes();
 int persist_max_hidden();
 size_t persist_ws_floats(int H, int F, int nh, int nkv, int V, int num_sms);
-// Control words: phase counters, abort flag, lm_head tile counter, split-K tile counters.
+// Control words: phase counters, abort flag, lm_head tile counter, split-K tile counters (two
+// halves), per-phase tile-ready flags and counts, per-layer attention-unit counters.
 size_t persist_ctl_words(int L, int H, int F, int nh, int nkv, int V);
-// Point p.bar / p.gabort / p.amax_counter / p.counters into `ctl`.
+// Point p.bar / p.gabort / p.amax_counter / p.counters / p.ready / p.done / p.head_done into
+// `ctl` (p.L, p.H, p.F, p.nh, p.nkv, p.V set).
 void persist_bind_ctl(PersistParams& p, unsigned* ctl);
 // Attention work split for `units` (sequence, kv head) pairs over G CTAs.
 void persist_attn_split(int units, int max_ctx, int window, int G, int* cps, int* splits);

@@ -98,7 +98,7 @@ typedef struct {
   int32_t max_write_rows;   /* rows per internal chunk of dflash_write_ctx_kv (>= 16) */
   int32_t markov_rank;      /* DSpark Markov head rank; 0 = no head.  Otherwise a multiple of 32,
                                <= 1024, with max_batch <= 64 and max_batch * rank <= 40960 */
-  int32_t layer_weight_dtype; /* == dtype, or DFLASH_FP8E4M3_ROWSCALE (bf16 drafters): the FP8
+  int32_t layer_weight_dtype; /* 0 or dtype: as dtype; DFLASH_FP8E4M3_ROWSCALE (bf16 drafters): the FP8
                                drafter lane (from_weights.rs Phase G), q/k/v/o/gate/up/down of every
                                layer quantised at create to e4m3 with a per-output-row fp32 scale
                                (scale = fp32 rowmax|w| / 448) and used by dflash_propose; the

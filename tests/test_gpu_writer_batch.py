@@ -68,11 +68,15 @@ def test_batched_writer_against_oracle_and_per_sequence(cfg_name):
     if wl.cfg.dtype == "f32":
         assert torch.equal(pa, pb)
     else:
-        # same arithmetic; only the split-K summation order of the two GEMMs follows the row count
-        da = pa.float()
-        diff = (da - pb.float()).abs()
-        ulp = torch.maximum(da.abs(), pb.float().abs()) * 2.0 ** -7
-        assert bool((diff <= ulp + 1e-30).all())
+        # same arithmetic; only the split-K summation order of the two GEMMs follows the row count,
+        # so the fp32 values before the bf16 rounding differ in their last bits: one bf16 step of
+        # the value, or (for elements far below their head's scale, after k_norm) a few fp32 steps
+        # of the head's scale
+        da, db = pa.float(), pb.float()
+        diff = (da - db).abs()
+        bound = torch.maximum(da.abs(), db.abs()) * 2.0 ** -7 + 2.0 ** -18 * max(float(da.abs().max()), 1.0)
+        worst = float((diff - bound).max())
+        assert worst <= 0, (worst, float(diff.max()), int((diff > 0).sum()), diff.numel())
     tol = TOL[wl.cfg.dtype]
     o = Oracle(wl.cfg, a.W, cache=True)
     for s, first, n in SPANS:
