@@ -942,7 +942,11 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
           epi_sync();
         }
         while (it.next(sg)) {
-          if (first) {
+          // rank 0 holds the tile's first k-blocks and finishes the tile
+          const bool finisher = sg.rank == 0;
+          if (first && finisher) {
+            // only the finisher's epilogue reads what the previous phase wrote (whole rows for
+            // 1/RMS, the residual): a contributor stores its partial as soon as its MMAs are done
             epi_wait();
             if (t == 0) trace_stamp(p, ph, 0);
             epi_sync();
@@ -950,8 +954,6 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             epi_sync();
             first = false;
           }
-          // rank 0 holds the tile's first k-blocks and finishes the tile
-          const bool finisher = sg.rank == 0;
           const int n = sg.tile * 128 + t;
           EpiPre pre;
           if (finisher) {  // inputs of the epilogue, fetched while the MMAs run
@@ -1074,10 +1076,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
           }
         }
       }
-      // phase done on this CTA
+      // phase done on this CTA; only the embedding, QKV and attention phases are followed by a
+      // grid-wide wait (the others hand over tile by tile)
       if (t == 0) trace_stamp(p, ph, 8);
       epi_sync();
-      if (t == 0) grid_arrive(&p.bar[ph]);
+      const bool arrive = kind == PH_EMBED || kind == PH_ATTN || ((ph - 1) % 6 == 0 && ph != 1 + 6 * p.L);
+      if (t == 0 && arrive) grid_arrive(&p.bar[ph]);
       if (t == 0) trace_stamp(p, ph, 7);
     }
   }
