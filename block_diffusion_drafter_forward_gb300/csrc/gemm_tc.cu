@@ -479,9 +479,9 @@ cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, 
   dim3 grid((M + TN - 1) / TN, (N + 127) / 128, nsplit);
   switch (epi) {
     case EPI_STORE: return launch_epi<EPI_STORE>(TN, tw, tx, p, grid, st, pdl, false);
-    case EPI_QKV: return launch_epi<EPI_QKV>(TN, tw, tx, p, grid, st, pdl, false);
-    case EPI_RESID: return launch_epi<EPI_RESID>(TN, tw, tx, p, grid, st, pdl, false);
-    case EPI_GATEUP: return launch_epi<EPI_GATEUP>(TN, tw, tx, p, grid, st, pdl, false);
+    case EPI_QKV: return launch_epi<EPI_QKV>(TN, tw, tx, p, grid, st, pdl, w_fp8);
+    case EPI_RESID: return launch_epi<EPI_RESID>(TN, tw, tx, p, grid, st, pdl, w_fp8);
+    case EPI_GATEUP: return launch_epi<EPI_GATEUP>(TN, tw, tx, p, grid, st, pdl, w_fp8);
     case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(TN, tw, tx, p, grid, st, pdl, w_fp8);
     case EPI_CTXKV: return launch_epi<EPI_CTXKV>(TN, tw, tx, p, grid, st, pdl, false);
   }

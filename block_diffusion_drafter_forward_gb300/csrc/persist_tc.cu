@@ -242,14 +242,13 @@ __device__ bool count_wait(const unsigned* ctr, unsigned target, volatile int* l
 // a gate/up tile gives the 64 act columns of one down k-block), and o_proj's by the attention
 // unit of the head it belongs to.  QKV of layer 0 follows the embedding with a grid barrier.
 __device__ __forceinline__ bool fine_deps(const GPh& g) { return !(g.kind == 0 && g.layer == 0); }
-__device__ __forceinline__ const unsigned* dep_flag(const PersistParams& p, const GPh& g, int ph, int kb,
-                                                    unsigned* target) {
-  if (g.kind == 3) {
-    *target = 32;
-    return p.head_done + g.layer * 64 + (kb / 2) / (p.nh / p.nkv);
-  }
-  *target = 1;
-  return p.ready + (size_t)(ph - 1) * p.ready_stride + (g.kind == 5 ? kb : kb / 2);
+// index of the producer tile (attention unit for o_proj) of operand k-block kb
+__device__ __forceinline__ int dep_index(const PersistParams& p, const GPh& g, int kb) {
+  if (g.kind == 3) return (kb / 2) / (p.nh / p.nkv);
+  return g.kind == 5 ? kb : kb / 2;
+}
+__device__ __forceinline__ const unsigned* dep_ptr(const PersistParams& p, const GPh& g, int ph, int d) {
+  return g.kind == 3 ? p.head_done + g.layer * 64 + d : p.ready + (size_t)(ph - 1) * p.ready_stride + d;
 }
 
 __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort, int* gabort) {
@@ -641,9 +640,10 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
 }
 
 // Merge the split partials of rows 4 rb .. 4 rb + 3 of one unit (a warp per row, a lane per
-// 4 dims).  Every split's 4 rows of O (2 KB) and (m, l) (32 B) arrive by bulk copy into
-// shared memory in one round trip; the merge then takes the rows' global max first and sums
-// the splits in order.
+// 4 dims).  Every split's 4 rows of O (2 KB) and (m, l) (32 B) arrive in shared memory in one
+// round trip, as 16-byte asynchronous copies spread over the 128 threads (one thread issuing a
+// bulk copy per split serialises on the issue); the merge then takes the rows' global max first
+// and sums the splits in order.
 constexpr int kCmbBytes = kAQ + 2 * kAKVStage;  // landing buffer: the attention Q + K/V area
 
 __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb, int t, int ctx0, uint8_t* sBuf,
@@ -656,17 +656,16 @@ __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb
   const int ns = a.nsplit;
   float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   if (ns * (2048 + 32) <= kCmbBytes) {
-    volatile int* ab = &B.abort;
-    if (t == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&B.red_full, ns * (2048 + 32));
-      for (int q = 0; q < ns; ++q) {
-        bulk_load(sBuf + q * 2048, p.o_part + ((base + q) * 128 + r0) * 128, 2048, &B.red_full);
-        bulk_load(sBuf + ns * 2048 + q * 32, p.ml_part + ((base + q) * 128 + r0) * 2, 32, &B.red_full);
-      }
+    for (int i = t; i < ns * 128; i += kEThreads) {
+      const int q = i >> 7, off = i & 127;
+      cp_async16(sBuf + q * 2048 + off * 16, p.o_part + ((base + q) * 128 + r0) * 128 + off * 4);
     }
-    wait_ab(&B.red_full, red_use & 1, ab, p.gabort);
-    ++red_use;
+    for (int i = t; i < ns * 2; i += kEThreads) {
+      const int q = i >> 1, half = i & 1;
+      cp_async16(sBuf + ns * 2048 + q * 32 + half * 16, p.ml_part + ((base + q) * 128 + r0) * 2 + half * 4);
+    }
+    cp_async_wait_all();
+    epi_sync();
     const float* so = reinterpret_cast<const float*>(sBuf);
     const float2* sml = reinterpret_cast<const float2*>(sBuf + ns * 2048);
     for (int q = 0; q < ns; ++q) M = fmaxf(M, sml[q * 4 + warp].x);
@@ -776,42 +775,70 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
     }
     __syncwarp();
   } else if (warp == 6) {
-    if (lane == 0) {
-      // ---------------- activation producer: X tiles once the phase they come from is complete
-      const uint64_t pol = policy_evict_last();
-      int j = 0;
-      for (int ph = 0; ph < P && !*ab; ++ph) {
-        if (phase_kind(ph, p.L) != PH_GEMM) continue;
-        const GPh gp = gemm_of(ph, p);
-        const CUtensorMap* xm = p.maps + 4 * p.L + 1 + gp.xmap;
-        SegIter it((gp.N + 127) / 128, gp.K / 64, G, c);
-        Seg sg;
-        bool waited = false;
-        const bool fine = fine_deps(gp);
-        const unsigned* last_dep = nullptr;
-        while (it.next(sg) && !*ab) {
-          if (!waited && !fine) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
-          for (int kk = 0; kk < sg.nkb && !*ab; ++kk, ++j) {
-            if (fine) {
-              // this k-block's producer tile (or attention unit) has finished
-              unsigned target;
-              const unsigned* dep = dep_flag(p, gp, ph, sg.kb0 + kk, &target);
-              if (dep != last_dep) {
-                if (!count_wait(dep, target, ab, p.gabort)) break;
-                last_dep = dep;
+    // ---------------- activation producer: the whole warp.  For a segment of k-blocks its
+    // lanes poll the ready flags of the producer tiles together (one round trip per poll, lane i
+    // the i-th flag not yet seen set); lane 0 copies each k-block's X tile as soon as its own
+    // producer tile is done, so the MMAs start on the earliest tiles.
+    const uint64_t pol = policy_evict_last();
+    int j = 0;
+    bool stop = false;
+    for (int ph = 0; ph < P && !stop; ++ph) {
+      if (phase_kind(ph, p.L) != PH_GEMM) continue;
+      const GPh gp = gemm_of(ph, p);
+      const CUtensorMap* xm = p.maps + 4 * p.L + 1 + gp.xmap;
+      const unsigned target = gp.kind == 3 ? 32u : 1u;
+      SegIter it((gp.N + 127) / 128, gp.K / 64, G, c);
+      Seg sg;
+      bool waited = false;
+      const bool fine = fine_deps(gp);
+      while (!stop && it.next(sg)) {
+        if (!waited && !fine) {
+          if (lane == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
+          __syncwarp();
+        }
+        const int d1 = fine ? dep_index(p, gp, sg.kb0 + sg.nkb - 1) : 0;
+        int ready_lo = fine ? dep_index(p, gp, sg.kb0) : 0;  // producers below this one are done
+        for (int kk = 0; kk < sg.nkb; ++kk, ++j) {
+          if (fine) {
+            const int d = dep_index(p, gp, sg.kb0 + kk);
+            long long spin = 0;
+            while (d >= ready_lo) {
+              const bool mine = ready_lo + lane <= d1;
+              const unsigned v = mine ? ld_acquire(dep_ptr(p, gp, ph, ready_lo + lane)) : 0u;
+              const unsigned mask = __ballot_sync(0xffffffffu, mine && v >= target);
+              ready_lo += mask == 0xffffffffu ? 32 : __ffs(~mask) - 1;  // the leading run of done tiles
+              if (d < ready_lo) {
+                fence_proxy_async_global();
+                break;
+              }
+              int give_up = ++spin > kGridSpin;
+              if ((spin & 127) == 0 && lane == 0) give_up |= *ab || *reinterpret_cast<volatile int*>(p.gabort);
+              if (__shfl_sync(0xffffffffu, give_up, 0)) {
+                if (lane == 0) { *ab = 1; atomicExch(p.gabort, 1); }
+                stop = true;
+                break;
               }
             }
-            if (!waited) {
-              trace_stamp(p, ph, 1);
-              waited = true;
-            }
-            const int s = j % kS, u = j / kS;
+            if (stop) break;
+          }
+          if (!waited) {
+            if (lane == 0) trace_stamp(p, ph, 1);
+            waited = true;
+          }
+          const int s = j % kS, u = j / kS;
+          int ok = 1;
+          if (lane == 0) {
             // use u of stage s starts once the MMA released use u - 1; the release of use u
             // needs this copy, so the stage cannot run a phase ahead of it
-            if (u > 0 && !wait_ab(&B.empty[s], (u - 1) & 1, ab, p.gabort)) break;
-            tma_load_2d(stage(s) + kAB, xm, &B.full[s], (sg.kb0 + kk) * 64, 0, pol);
+            if (u > 0 && !wait_ab(&B.empty[s], (u - 1) & 1, ab, p.gabort)) ok = 0;
+            else tma_load_2d(stage(s) + kAB, xm, &B.full[s], (sg.kb0 + kk) * 64, 0, pol);
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            stop = true;
+            break;
           }
         }
+        if (__shfl_sync(0xffffffffu, lane == 0 ? (int)*ab : 0, 0)) stop = true;
       }
     }
     __syncwarp();
