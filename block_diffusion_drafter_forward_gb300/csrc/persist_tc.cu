@@ -948,8 +948,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         // projection's every tile where the epilogue needs whole rows (1/RMS of its operand; the
         // residual of down comes from o_proj), every attention unit of the layer for o_proj
         const int nt_h = p.H / 128;
-        auto epi_wait = [&]() {
-          if (t != 0) return;
+        auto epi_wait = [&]() {  // one thread
           if (!fine_deps(gp)) {
             grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
           } else if (gp.kind == 3) {
@@ -961,7 +960,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         };
         if (gp.epi == EPI_LMHEAD && p.final_hidden && c < p.M) {
           // side job (nothing waits for it): the final hidden state of token c
-          epi_wait();
+          if (t == 0) epi_wait();
           epi_sync();
           if (t == 0) rsc[0] = row_rscale(p, p.ss_b, c);
           epi_sync();
@@ -971,19 +970,14 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         while (it.next(sg)) {
           // rank 0 holds the tile's first k-blocks and finishes the tile
           const bool finisher = sg.rank == 0;
-          if (first && finisher) {
-            // only the finisher's epilogue reads what the previous phase wrote (whole rows for
-            // 1/RMS, the residual): a contributor stores its partial as soon as its MMAs are done
-            epi_wait();
-            if (t == 0) trace_stamp(p, ph, 0);
-            epi_sync();
-            if (e.ss_in && t < TN) rsc[t] = t < p.M ? row_rscale(p, e.ss_in, t) : 1.f;
-            epi_sync();
-            first = false;
-          }
+          // only a finisher's epilogue reads what the previous phase wrote (whole rows for 1/RMS,
+          // the residual): a contributor stores its partial as soon as its MMAs are done
+          const bool need_wait = first && finisher;
           const int n = sg.tile * 128 + t;
           EpiPre pre;
-          if (finisher) {  // inputs of the epilogue, fetched while the MMAs run
+          // inputs of the epilogue, fetched while the MMAs run (down's residual is o_proj's
+          // output: fetched after the wait for o_proj)
+          if (finisher && !(need_wait && gp.kind == 5)) {
             if (gp.epi == EPI_QKV) epilogue_pre<EPI_QKV>(e, pre, t, n, 0, 0, sg.tile, B.ctx0);
             else if (gp.epi == EPI_RESID) epilogue_pre<EPI_RESID>(e, pre, t, n, 0, 0, sg.tile);
           }
@@ -1008,68 +1002,76 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
 #pragma unroll
             for (int q = 0; q < 16; q += 4)
               __stcg(reinterpret_cast<float4*>(mine + q), make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]));
-            fence_proxy_async_global();  // the finisher reads the partials with a bulk copy
             epi_sync();
             if (t == 0) release_add(&cnt[sg.tile]);
             if (t == 0) trace_stamp(p, ph, 9);
             continue;
           }
-          if (sg.ncontrib > 1) {
-            // the other ncontrib - 1 partials: wait for their count, then add them in CTA order
-            const int nother = sg.ncontrib - 1;
-            if (warp == 0) {
-              // the whole warp polls (one coalesced load), so no lane sleeps in an mbarrier
-              // wait while lane 0 still has work to issue
-              for (long long sp = 0; ld_acquire(&cnt[sg.tile]) < (unsigned)nother; ++sp) {
-                if (*ab || sp > kGridSpin) {
-                  if (lane == 0) { *ab = 1; atomicExch(p.gabort, 1); }
-                  break;
-                }
+          // finisher: the other ncontrib - 1 partials (warp 0 waits for their count) and the previous
+          // phase (warp 1) are waited for at the same time; then every thread copies its rows of the
+          // partials in with 16-byte asynchronous copies (one round trip)
+          const int nother = sg.ncontrib - 1;
+          const bool bulk = nother > 0 && nother <= kRedMax;
+          if (nother > 0 && warp == 0) {
+            // the whole warp polls (one coalesced load)
+            for (long long sp = 0; ld_acquire(&cnt[sg.tile]) < (unsigned)nother; ++sp) {
+              if (*ab || sp > kGridSpin) {
+                if (lane == 0) { *ab = 1; atomicExch(p.gabort, 1); }
+                break;
               }
-              __syncwarp();
             }
-            if (t == 0) trace_stamp(p, ph, 5);
-            if (t == 0) {
+            __syncwarp();
+            if (lane == 0) {
+              trace_stamp(p, ph, 5);
               cnt[sg.tile] = 0;  // re-armed for the phase after next (it depends on this one)
-              if (nother <= kRedMax && !*ab) {
-                fence_proxy_async_global();
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&B.red_full, nother * kPartBytes);
-                bulk_load(sRed, tile_ws + kEThreads * TN, nother * kPartBytes, &B.red_full);
+            }
+          }
+          if (need_wait && t == 32) epi_wait();
+          epi_sync();
+          if (bulk && !*ab) {
+            for (int rk = 0; rk < nother; ++rk) {
+              const float* src = tile_ws + ((int64_t)(rk + 1) * kEThreads + t) * TN;
+              uint8_t* dst = sRed + (size_t)(rk * kEThreads + t) * TN * 4;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) cp_async16(dst + q * 16, src + q * 4);
+            }
+          }
+          if (need_wait) {
+            if (t == 0) trace_stamp(p, ph, 0);
+            if (e.ss_in && t < TN) rsc[t] = t < p.M ? row_rscale(p, e.ss_in, t) : 1.f;
+            if (gp.kind == 5) epilogue_pre<EPI_RESID>(e, pre, t, n, 0, 0, sg.tile);
+            epi_sync();
+            first = false;
+          }
+          if (bulk) {
+            cp_async_wait_all();  // this thread reads back only what it copied itself
+            if (t == 0) trace_stamp(p, ph, 6);
+            for (int rk = 0; rk < nother; ++rk) {
+              const float4* src = reinterpret_cast<const float4*>(sRed + (size_t)(rk * kEThreads + t) * TN * 4);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float4 f = src[q];
+                v[4 * q] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
               }
             }
-            if (nother <= kRedMax) {
-              wait_ab(&B.red_full, red_use & 1, ab, p.gabort);
-              if (t == 0) trace_stamp(p, ph, 6);
-              ++red_use;
-              for (int rk = 0; rk < nother; ++rk) {
-                const float4* src = reinterpret_cast<const float4*>(sRed + (size_t)(rk * kEThreads + t) * TN * 4);
+          } else if (nother > 0) {
+            __threadfence();  // warp 0 saw every partial counted (the barrier above orders the rest)
+            for (int rk0 = 1; rk0 < sg.ncontrib; rk0 += 4) {
+              float4 q4[4][4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int rk = rk0 + u < sg.ncontrib ? rk0 + u : rk0;
+                const float4* src = reinterpret_cast<const float4*>(tile_ws + ((int64_t)rk * kEThreads + t) * TN);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) q4[u][q] = __ldcg(src + q);
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (rk0 + u >= sg.ncontrib) break;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                  const float4 f = src[q];
-                  v[4 * q] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
-                }
-              }
-            } else {
-              epi_sync();  // thread 0 saw every partial counted
-              __threadfence();
-              for (int rk0 = 1; rk0 < sg.ncontrib; rk0 += 4) {
-                float4 q4[4][4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const int rk = rk0 + u < sg.ncontrib ? rk0 + u : rk0;
-                  const float4* src = reinterpret_cast<const float4*>(tile_ws + ((int64_t)rk * kEThreads + t) * TN);
-#pragma unroll
-                  for (int q = 0; q < 4; ++q) q4[u][q] = __ldcg(src + q);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  if (rk0 + u >= sg.ncontrib) break;
-#pragma unroll
-                  for (int q = 0; q < 4; ++q) {
-                    v[4 * q] += q4[u][q].x; v[4 * q + 1] += q4[u][q].y;
-                    v[4 * q + 2] += q4[u][q].z; v[4 * q + 3] += q4[u][q].w;
-                  }
+                  v[4 * q] += q4[u][q].x; v[4 * q + 1] += q4[u][q].y;
+                  v[4 * q + 2] += q4[u][q].z; v[4 * q + 3] += q4[u][q].w;
                 }
               }
             }
