@@ -1007,9 +1007,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             if (t == 0) trace_stamp(p, ph, 9);
             continue;
           }
-          // finisher: the other ncontrib - 1 partials (warp 0 waits for their count) and the previous
-          // phase (warp 1) are waited for at the same time; then every thread copies its rows of the
-          // partials in with 16-byte asynchronous copies (one round trip)
+          // finisher: the other ncontrib - 1 partials (warp 0 waits for their count and copies them in
+          // with one bulk copy) and the previous phase (warp 1) are waited for at the same time
           const int nother = sg.ncontrib - 1;
           const bool bulk = nother > 0 && nother <= kRedMax;
           if (nother > 0 && warp == 0) {
@@ -1024,18 +1023,18 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             if (lane == 0) {
               trace_stamp(p, ph, 5);
               cnt[sg.tile] = 0;  // re-armed for the phase after next (it depends on this one)
+              if (bulk && !*ab) {
+                // the contributors' generic stores, acquired above, then read through the async proxy
+                fence_proxy_async_global();
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&B.red_full, nother * kPartBytes);
+                bulk_load(sRed, tile_ws + kEThreads * TN, nother * kPartBytes, &B.red_full);
+              }
             }
+            __syncwarp();
           }
           if (need_wait && t == 32) epi_wait();
           epi_sync();
-          if (bulk && !*ab) {
-            for (int rk = 0; rk < nother; ++rk) {
-              const float* src = tile_ws + ((int64_t)(rk + 1) * kEThreads + t) * TN;
-              uint8_t* dst = sRed + (size_t)(rk * kEThreads + t) * TN * 4;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) cp_async16(dst + q * 16, src + q * 4);
-            }
-          }
           if (need_wait) {
             if (t == 0) trace_stamp(p, ph, 0);
             if (e.ss_in && t < TN) rsc[t] = t < p.M ? row_rscale(p, e.ss_in, t) : 1.f;
@@ -1044,8 +1043,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             first = false;
           }
           if (bulk) {
-            cp_async_wait_all();  // this thread reads back only what it copied itself
+            wait_ab(&B.red_full, red_use & 1, ab, p.gabort);
             if (t == 0) trace_stamp(p, ph, 6);
+            ++red_use;
             for (int rk = 0; rk < nother; ++rk) {
               const float4* src = reinterpret_cast<const float4*>(sRed + (size_t)(rk * kEThreads + t) * TN * 4);
 #pragma unroll
