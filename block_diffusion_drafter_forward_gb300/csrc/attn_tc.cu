@@ -300,22 +300,32 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Kernel for long key ranges (many chunks per CTA).  Keys go in super-chunks of two 64-key
-// chunks (128 keys): warp 4 streams their K/V pages into three 64 KB buffers (two
-// super-chunks of look-ahead: at full HBM load a page copy takes longer than one softmax
-// pass), warp 5 issues
-// the MMAs, warps 0-3 run the softmax.  While the softmax works on super-chunk i, the tensor
-// cores already compute S of super-chunk i + 1 into the second TMEM buffer.  Per super-chunk:
-// one max pass and one exp pass (ex2.approx) over the 128 scores of a row, P written back as
-// bf16 pairs over its own S columns and read from TMEM by the P V MMA, O accumulated in TMEM
-// and rescaled there only when a row's running max grows.  Loops stay rolled.  225 KB of
-// shared memory and 512 TMEM columns: one CTA per SM.
+// Kernel for long key ranges: stream-K over the key chunks of the whole batch.  The chunks of
+// every (sequence, kv head) unit, in unit order, form one index space of W chunks; CTA b of a
+// one-CTA-per-SM grid of G takes chunks [b W / G, (b + 1) W / G) whatever the context lengths,
+// so every SM streams the same number of K/V bytes and there is no tail wave.  The range falls
+// into segments (unit u, chunks [c_lo, c_hi) of it): a segment that covers its unit whole
+// writes the normalised output, the others write fp32 partials (O, m, l) into slot b + u, which
+// is unique (along the segments of the batch, b + u grows at every step), merged by
+// attn_combine_kernel.  W, the CTA's range and its first unit come from ctx_lens on the device,
+// so a captured graph replayed with new context lengths stays balanced.
+//
+// Inside a CTA the pipeline runs on from one segment into the next.  Keys go in super-chunks of
+// two 64-key chunks (128 keys): warp 4 streams their K/V pages into three 64 KB buffers (two
+// super-chunks of look-ahead: at full HBM load a page copy takes longer than one softmax pass),
+// warp 5 issues the MMAs, warps 0-3 run the softmax.  While the softmax works on super-chunk i,
+// the tensor cores already compute S of super-chunk i + 1 into the second TMEM buffer.  Per
+// super-chunk: one max pass and one exp pass (ex2.approx) over the 128 scores of a row, P
+// written back as bf16 pairs over its own S columns and read from TMEM by the P V MMA, O
+// accumulated in TMEM and rescaled there only when a row's running max grows.  The next
+// segment's queries are copied in (cp.async) once the last S of the current one is done.
+// Loops stay rolled.  225 KB of shared memory and 512 TMEM columns: one CTA per SM.
 constexpr int kScChunks = 2;                                 // chunks per super-chunk
 constexpr int kScBuf = kScChunks * kKVStage;                 // 64 KB of K/V per buffer
 constexpr int kScBufs = 3;                                   // K/V buffers (super-chunks in flight)
 constexpr int kScSmem = kQBytes + kScBufs * kScBuf + 512 + 1024;
 constexpr int kScThreads = 192;
-constexpr int kScWaves = 4;  // work items per SM the split size aims at
+constexpr int kScWaves = 4;  // partial slots per SM the compact kernel's split size allows
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -323,65 +333,189 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-__global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnParams p) {
+// Chunks unit u visits (0 for a context length out of range), its context and first key.
+__device__ __forceinline__ int sk_unit_chunks(const AttnParams& p, int u, int* ctx, int* k0) {
+  const int c = __ldg(p.ctx_lens + u / p.nkv);
+  *ctx = c;
+  *k0 = 0;
+  if (c < 0 || c > p.max_ctx || c + kGamma > p.mpps * kPage) return 0;
+  return chunk_range(p.window, c, k0);
+}
+
+// CTA b of G = min(grid, W) owns global chunks [lo, hi) = [floor(b W / G), floor((b + 1) W / G))
+// (never empty); global chunk x belongs to CTA ceil((x + 1) G / W) - 1.
+__host__ __device__ __forceinline__ int sk_owner(int64_t x, int64_t W, int G) {
+  return (int)(((x + 1) * G + W - 1) / W) - 1;
+}
+
+struct SkSeg {
+  int u, s, g, ctx, k0, nch;  // unit, its sequence, kv head, context, first key, chunks
+  int c_lo, c_hi;             // this CTA's chunks of the unit
+};
+
+// The segments of chunk range [lo, hi), walked unit by unit from unit u (first chunk pu).
+struct SkWalk {
+  int64_t lo, hi, pu;
+  int u, units;
+  __device__ bool next(const AttnParams& p, SkSeg& sg) {
+    while (pu < hi && u < units) {
+      int ctx, k0;
+      const int nch = sk_unit_chunks(p, u, &ctx, &k0);
+      const int64_t first = pu;
+      const int uu = u;
+      pu += nch;
+      ++u;
+      if (nch == 0 || pu <= lo) continue;
+      sg.u = uu;
+      sg.s = uu / p.nkv;
+      sg.g = uu % p.nkv;
+      sg.ctx = ctx;
+      sg.k0 = k0;
+      sg.nch = nch;
+      sg.c_lo = (int)(lo > first ? lo - first : 0);
+      sg.c_hi = (int)(hi - first < nch ? hi - first : nch);
+      return true;
+    }
+    return false;
+  }
+};
+
+// The super-chunks of a walk in order (the MMA issuer looks one ahead).
+struct SkIt {
+  SkWalk w;
+  SkSeg sg;
+  int j, nsc, seg;
+  bool valid;
+  __device__ void start(const AttnParams& p, const SkWalk& w0) {
+    w = w0;
+    seg = -1;
+    j = nsc = 0;
+    valid = false;
+    step(p);
+  }
+  __device__ void step(const AttnParams& p) {
+    if (valid && j + 1 < nsc) {
+      ++j;
+      return;
+    }
+    valid = w.next(p, sg);
+    if (valid) {
+      ++seg;
+      j = 0;
+      nsc = (sg.c_hi - sg.c_lo + kScChunks - 1) / kScChunks;
+    }
+  }
+  __device__ int nchk() const { return min(kScChunks, sg.c_hi - sg.c_lo - j * kScChunks); }
+};
+
+struct SkShared {
+  uint64_t kv_full[kScBufs], kv_empty[kScBufs], s_full[2], p_full[2], o_done, q_full;
+  uint32_t tmem_slot;
+  int flags[2];
+  long long red[8];
+  long long W, pu0;
+  int u0, found;
+};
+static_assert(sizeof(SkShared) <= 512, "stream-K control block overflows its slot");
+
+// This CTA's walk: W by a block reduction over the sequences, then the sequence holding chunk
+// lo by a block scan (its first unit starts the walk).  All kScThreads threads.
+__device__ SkWalk sk_plan(const AttnParams& p, SkShared& sh, int t) {
+  const int warp = t >> 5, lane = t & 31, nwarps = kScThreads / 32;
+  long long mine = 0;
+  for (int s = t; s < p.nb; s += kScThreads) {
+    int ctx, k0;
+    mine += sk_unit_chunks(p, s * p.nkv, &ctx, &k0);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) sh.red[warp] = mine;
+  if (t == 0) sh.found = 0;
+  __syncthreads();
+  long long tot = 0;
+  for (int w = 0; w < nwarps; ++w) tot += sh.red[w];
+  const long long W = tot * p.nkv;
+  // fewer chunks than CTAs: the first W CTAs take one each (every range is non-empty)
+  const int G = (int)min((long long)gridDim.x, W), b = blockIdx.x;
+  SkWalk wk;
+  wk.lo = b < G ? (int64_t)b * W / G : 0;
+  wk.hi = b < G ? (int64_t)(b + 1) * W / G : 0;
+  wk.units = p.nb * p.nkv;
+  wk.u = wk.units;
+  wk.pu = wk.hi;
+  __syncthreads();  // every thread has read red[]
+  if (wk.lo >= wk.hi) return wk;
+  long long carry = 0;
+  for (int s0 = 0; s0 < p.nb; s0 += kScThreads) {
+    const int s = s0 + t;
+    int ctx, k0;
+    const long long n = s < p.nb ? (long long)sk_unit_chunks(p, s * p.nkv, &ctx, &k0) * p.nkv : 0;
+    long long inc = n;  // inclusive scan: warp, then across warps
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    if (lane == 31) sh.red[warp] = inc;
+    __syncthreads();
+    long long before = carry;
+    for (int w = 0; w < warp; ++w) before += sh.red[w];
+    long long tile = 0;
+    for (int w = 0; w < nwarps; ++w) tile += sh.red[w];
+    const long long excl = before + inc - n;
+    if (n > 0 && excl <= wk.lo && wk.lo < excl + n) {
+      sh.u0 = s * p.nkv;
+      sh.pu0 = excl;
+      sh.found = 1;
+    }
+    carry += tile;
+    __syncthreads();
+    if (sh.found) break;
+  }
+  if (sh.found) {
+    wk.u = sh.u0;
+    wk.pu = sh.pu0;
+  }
+  return wk;
+}
+
+__global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sKV = sQ + kQBytes;  // buffer b at sKV + b * kScBuf: chunk i's K pages, then its V pages
-  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sKV + kScBufs * kScBuf);
-  uint64_t* kv_empty = kv_full + kScBufs;
-  uint64_t* s_full = kv_empty + kScBufs;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint64_t* q_full = o_done + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  SkShared& sh = *reinterpret_cast<SkShared*>(sKV + kScBufs * kScBuf);
+  volatile int* flags = sh.flags;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int unit = blockIdx.x, split = blockIdx.y;
-  const int s = unit / p.nkv, g = unit % p.nkv;
   const int group = p.nh / p.nkv;
-  const int ctx = p.ctx_lens[s];
-  if (ctx < 0 || ctx > p.max_ctx || ctx + kGamma > p.mpps * kPage) {
-    if (t == 0 && split == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
-    return;
+  // a context length out of range contributes no chunks; CTA 0 reports it
+  for (int s = t; blockIdx.x == 0 && s < p.nb; s += kScThreads) {
+    const int c = __ldg(p.ctx_lens + s);
+    if (c < 0 || c > p.max_ctx || c + kGamma > p.mpps * kPage) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
   }
-  int k0;
-  const int nch = chunk_range(p.window, ctx, &k0);
-  const int nsplit = (nch + p.chunks_per_split - 1) / p.chunks_per_split;
-  if (nsplit > (int)gridDim.y) {
-    if (t == 0 && split == 0) atomicOr(p.status, DFLASH_DEV_BAD_CTX);
-    return;
-  }
-  if (split >= nsplit) return;
-  const int c_begin = split * p.chunks_per_split;
-  const int n = min(nch, c_begin + p.chunks_per_split) - c_begin;  // chunks of this CTA
-  const int nsc = (n + kScChunks - 1) / kScChunks;                  // super-chunks
-  const int nkeys = ctx + kGamma;
-  const int nvis = ctx + block_width(p.widths, s);  // keys past the active block width are masked
-  const int32_t* pt = p.page_tables + (int64_t)s * p.mpps;
-  const int npages_seq = (nkeys + kPage - 1) / kPage;
-  const int safe_keys = ctx & ~(kPage - 1);
+  const SkWalk walk = sk_plan(p, sh, t);
+  if (walk.lo >= walk.hi || walk.u >= walk.units) return;  // nothing for this CTA
 
   if (t == 0) {
     for (int i = 0; i < kScBufs; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&sh.kv_full[i], 1);
+      mbar_init(&sh.kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.p_full[i], 128);
     }
-    mbar_init(o_done, 1);
-    mbar_init(q_full, 128);
+    mbar_init(&sh.o_done, 1);
+    mbar_init(&sh.q_full, 128);
     flags[0] = 0;
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 512);
+  if (warp == 0) tmem_alloc(&sh.tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = sh.tmem_slot;
   const uint32_t tS[2] = {tmem, tmem + 128}, tO = tmem + 256;
   constexpr uint32_t idesc_s = idesc_bf16(128, kKC);
   constexpr uint32_t idesc_o = idesc_bf16(128, 128);
@@ -391,53 +525,64 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnPar
     // ---------------- K/V page producer: lane l < 8 copies page l % 4 of chunk l / 4 of a
     // super-chunk (its K and V tiles, into the chunk's K and V regions); the page ids of the
     // next super-chunk are fetched while the warp waits for a free buffer
-    bool waited = false;
-    auto page_of = [&](int i) {
-      const int ci = lane >> 2, q = lane & 3;
-      const int c = c_begin + i * kScChunks + ci;
-      if (lane >= kScChunks * kPagesPerChunk || i >= nsc || c >= c_begin + n) return 0;
-      const int pg = (k0 + c * kKC) / kPage + q;
-      return __ldg(pt + (pg < npages_seq ? pg : 0));
-    };
-    int page = page_of(0);
-    for (int i = 0; i < nsc; ++i) {
-      const int b = i % kScBufs;
-      if (i >= kScBufs && !mbar_wait_ab(&kv_empty[b], ((i / kScBufs) - 1) & 1, flags)) {
-        flags[0] = 1;
-        break;
-      }
-      const int nchk = min(kScChunks, n - i * kScChunks);
-      if (!waited && k0 + (c_begin + i * kScChunks + nchk) * kKC > safe_keys) {  // holds block rows
-        pdl_wait();
-        waited = true;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[b], nchk * kKVStage);
-      __syncwarp();
-      if (lane < nchk * kPagesPerChunk) {
-        int pg = page;
-        if (pg < 0 || pg >= p.g.num_pages) {
-          atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
-          pg = 0;
+    bool waited = false, stop = false;
+    SkWalk w = walk;
+    SkSeg sg;
+    int i = 0;
+    while (!stop && w.next(p, sg)) {
+      const int32_t* pt = p.page_tables + (int64_t)sg.s * p.mpps;
+      const int npages_seq = (sg.ctx + kGamma + kPage - 1) / kPage;
+      const int safe_keys = sg.ctx & ~(kPage - 1);
+      const int n = sg.c_hi - sg.c_lo, nsc = (n + kScChunks - 1) / kScChunks;
+      auto page_of = [&](int jj) {
+        const int ci = lane >> 2, q = lane & 3;
+        const int c = sg.c_lo + jj * kScChunks + ci;
+        if (lane >= kScChunks * kPagesPerChunk || jj >= nsc || c >= sg.c_hi) return 0;
+        const int pg = (sg.k0 + c * kKC) / kPage + q;
+        return __ldg(pt + (pg < npages_seq ? pg : 0));
+      };
+      int page = page_of(0);
+      for (int jj = 0; jj < nsc; ++jj, ++i) {
+        const int b = i % kScBufs;
+        if (i >= kScBufs && !mbar_wait_ab(&sh.kv_empty[b], ((i / kScBufs) - 1) & 1, flags)) {
+          flags[0] = 1;
+          stop = true;
+          break;
         }
-        uint8_t* dK = sKV + b * kScBuf + (lane >> 2) * kKVStage + (lane & 3) * kTileBytes;
-        uint8_t* dV = dK + kPagesPerChunk * kTileBytes;
-        bulk_load(dK, p.pool + tile_base(p.g, p.layer, pg, 0, g), kTileBytes, &kv_full[b]);
-        bulk_load(dV, p.pool + tile_base(p.g, p.layer, pg, 1, g), kTileBytes, &kv_full[b]);
+        const int nchk = min(kScChunks, n - jj * kScChunks);
+        if (!waited && sg.k0 + (sg.c_lo + jj * kScChunks + nchk) * kKC > safe_keys) {  // holds block rows
+          pdl_wait();
+          waited = true;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&sh.kv_full[b], nchk * kKVStage);
+        __syncwarp();
+        if (lane < nchk * kPagesPerChunk) {
+          int pg = page;
+          if (pg < 0 || pg >= p.g.num_pages) {
+            atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
+            pg = 0;
+          }
+          uint8_t* dK = sKV + b * kScBuf + (lane >> 2) * kKVStage + (lane & 3) * kTileBytes;
+          uint8_t* dV = dK + kPagesPerChunk * kTileBytes;
+          bulk_load(dK, p.pool + tile_base(p.g, p.layer, pg, 0, sg.g), kTileBytes, &sh.kv_full[b]);
+          bulk_load(dV, p.pool + tile_base(p.g, p.layer, pg, 1, sg.g), kTileBytes, &sh.kv_full[b]);
+        }
+        page = page_of(jj + 1);
       }
-      page = page_of(i + 1);
     }
     if (!waited) pdl_wait();
     __syncwarp();
   } else if (warp == 5) {
-    // ---------------- MMA issuer (lane 0): S of super-chunk i + 1 goes out before P V of i
+    // ---------------- MMA issuer (lane 0): S of super-chunk i + 1 goes out before P V of i,
+    // across segment boundaries (the next segment's S waits for its queries)
     if (lane == 0) {
-      auto issue_s = [&](int i) {
+      auto issue_s = [&](const SkIt& it, int i) {
         const int b = i & 1, kb = i % kScBufs;
-        const int nchk = min(kScChunks, n - i * kScChunks);
-        if (!mbar_wait_ab(&kv_full[kb], (i / kScBufs) & 1, flags)) flags[0] = 1;
+        if (it.j == 0 && !mbar_wait_ab(&sh.q_full, it.seg & 1, flags)) flags[0] = 1;
+        if (!mbar_wait_ab(&sh.kv_full[kb], (i / kScBufs) & 1, flags)) flags[0] = 1;
         tc_fence_after();
         if (!flags[0]) {
-          for (int ci = 0; ci < nchk; ++ci) {
+          for (int ci = 0; ci < it.nchk(); ++ci) {
             const uint8_t* sK = sKV + kb * kScBuf + ci * kKVStage;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
@@ -445,164 +590,189 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnPar
                        idesc_s, k > 0 ? 1u : 0u);
           }
         }
-        mma_commit(&s_full[b]);
+        mma_commit(&sh.s_full[b]);
       };
-      if (!mbar_wait_ab(q_full, 0, flags)) flags[0] = 1;
-      tc_fence_after();
-      if (nsc > 0) issue_s(0);
-      for (int i = 0; i < nsc; ++i) {
+      SkIt cur, nx;
+      cur.start(p, walk);
+      nx = cur;
+      nx.step(p);
+      if (cur.valid) issue_s(cur, 0);
+      for (int i = 0; cur.valid; ++i) {
         const int b = i & 1, kb = i % kScBufs;
-        const int nchk = min(kScChunks, n - i * kScChunks);
-        if (i + 1 < nsc) issue_s(i + 1);
-        if (!mbar_wait_ab(&p_full[b], (i >> 1) & 1, flags)) flags[0] = 1;
+        if (nx.valid) issue_s(nx, i + 1);
+        if (!mbar_wait_ab(&sh.p_full[b], (i >> 1) & 1, flags)) flags[0] = 1;
         tc_fence_after();
         if (!flags[0]) {
+          const int nchk = cur.nchk();
           for (int kk = 0; kk < nchk * kPagesPerChunk; ++kk) {  // 16 keys = 8 TMEM columns of P each
             const uint8_t* sV = sKV + kb * kScBuf + (kk / kPagesPerChunk) * kKVStage + kPagesPerChunk * kTileBytes +
                                 (kk % kPagesPerChunk) * kTileBytes;
-            mma_bf16_tmem_a(tO, tS[b] + kk * 8, desc_noswz(sV, 128, 256), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_tmem_a(tO, tS[b] + kk * 8, desc_noswz(sV, 128, 256), idesc_o, (cur.j > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        mma_commit(&kv_empty[kb]);
-        mma_commit(o_done);
+        mma_commit(&sh.kv_empty[kb]);
+        mma_commit(&sh.o_done);
+        cur = nx;
+        if (nx.valid) nx.step(p);
       }
     }
     __syncwarp();
   } else {
     // ---------------- warps 0-3: queries, softmax, output
     pdl_wait();
-    {
-      const int hh = t >> 4, r = t & 15;
-      const uint4* src =
-          reinterpret_cast<const uint4*>(p.q + ((int64_t)(s * kGamma + r) * p.nh + g * group + hh) * 128);
-      uint4 qv[16];
-#pragma unroll
-      for (int d8 = 0; d8 < 16; ++d8) qv[d8] = src[d8];
-#pragma unroll
-      for (int d8 = 0; d8 < 16; ++d8) *reinterpret_cast<uint4*>(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16) = qv[d8];
-    }
-    fence_proxy_async_smem();
-    mbar_arrive(q_full);
-    const int r = t & 15;
-    const int pos_q = ctx + r;
+    const int r = t & 15, hh = t >> 4;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
-    float m_run = -FLT_MAX, l_run = 0.f;
-#pragma unroll 1
-    for (int i = 0; i < nsc; ++i) {
-      const int b = i & 1;
-      const int nchk = min(kScChunks, n - i * kScChunks);
-      if (!mbar_wait_ab(&s_full[b], (i >> 1) & 1, flags)) flags[0] = 1;
-      tc_fence_after();
-      // every key of the super-chunk visible to every row: no masking
-      const int kb = k0 + (c_begin + i * kScChunks) * kKC;
-      const bool full = kb + nchk * kKC <= nvis && (p.window <= 0 || ctx + kGamma - 1 - kb < p.window);
-      float mc = -FLT_MAX;
-#pragma unroll 1
-      for (int q4 = 0; q4 < 2 * nchk; ++q4) {
-        float v[32];
-        tmem_ld32(tS[b] + lane_off + q4 * 32, v);
-        if (full) {
+    // the queries of a unit into sQ (row t = head hh, token r), as 16-byte asynchronous copies
+    auto load_q = [&](const SkSeg& q) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(p.q + ((int64_t)(q.s * kGamma + r) * p.nh + q.g * group + hh) * 128);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mc = fmaxf(mc, v[j]);
-        } else {
+      for (int d8 = 0; d8 < 16; ++d8) cp_async16(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16, src + d8);
+    };
+    auto q_ready = [&]() {
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      mbar_arrive(&sh.q_full);
+    };
+    SkWalk w = walk;
+    SkSeg sg, nsg;
+    bool have = w.next(p, sg);
+    if (have) {
+      load_q(sg);
+      q_ready();
+    }
+    int i = 0;
+    while (have) {
+      const bool more = w.next(p, nsg);
+      const int n = sg.c_hi - sg.c_lo, nsc = (n + kScChunks - 1) / kScChunks;
+      const int nvis = sg.ctx + block_width(p.widths, sg.s);  // keys past the active block width are masked
+      const int pos_q = sg.ctx + r;
+      float m_run = -FLT_MAX, l_run = 0.f;
+#pragma unroll 1
+      for (int j = 0; j < nsc; ++j, ++i) {
+        const int b = i & 1;
+        const int nchk = min(kScChunks, n - j * kScChunks);
+        if (!mbar_wait_ab(&sh.s_full[b], (i >> 1) & 1, flags)) flags[0] = 1;
+        tc_fence_after();
+        const bool last = j == nsc - 1;
+        if (last && more) load_q(nsg);  // every S of this segment is done: sQ is free
+        // every key of the super-chunk visible to every row: no masking
+        const int kb = sg.k0 + (sg.c_lo + j * kScChunks) * kKC;
+        const bool full = kb + nchk * kKC <= nvis && (p.window <= 0 || sg.ctx + kGamma - 1 - kb < p.window);
+        float mc = -FLT_MAX;
+#pragma unroll 1
+        for (int q4 = 0; q4 < 2 * nchk; ++q4) {
+          float v[32];
+          tmem_ld32(tS[b] + lane_off + q4 * 32, v);
+          if (full) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int key = kb + q4 * 32 + j;
-            if (key < nvis && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[j]);
+            for (int e = 0; e < 32; ++e) mc = fmaxf(mc, v[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int key = kb + q4 * 32 + e;
+              if (key < nvis && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[e]);
+            }
           }
         }
+        // max(s) * c == max(s * c) for c > 0 (rounding is monotonic)
+        const float m_new = fmaxf(m_run, mc == -FLT_MAX ? -FLT_MAX : mc * scale_log2);
+        const float alpha = m_run == -FLT_MAX ? 1.f : ex2_approx(m_run - m_new);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O holds this segment's super-chunks before this one once the last P V is done
+          if (!mbar_wait_ab(&sh.o_done, (i - 1) & 1, flags)) flags[0] = 1;
+          tc_fence_after();
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {
+            float v[32];
+            tmem_ld32(tO + lane_off + q4 * 32, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] *= alpha;
+            tmem_st32(tO + lane_off + q4 * 32, v);
+          }
+        }
+        // P = 2^(s c - m) as bf16 pairs: keys 64 h .. 64 h + 63 into columns 32 h .. 32 h + 31
+        // (over scores already read)
+        float lsum = 0.f;
+#pragma unroll 1
+        for (int h = 0; h < nchk; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            float v[32];
+            tmem_ld32(tS[b] + lane_off + (2 * h + q) * 32, v);
+            if (full) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2_approx(fmaf(v[2 * e], scale_log2, -m_new)),
+                                                                ex2_approx(fmaf(v[2 * e + 1], scale_log2, -m_new)));
+                lsum += __low2float(h2) + __high2float(h2);
+                pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                float pr[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int key = kb + (2 * h + q) * 32 + 2 * e + u;
+                  const bool vis = key < nvis && (p.window <= 0 || pos_q - key < p.window);
+                  pr[u] = vis ? ex2_approx(fmaf(v[2 * e + u], scale_log2, -m_new)) : 0.f;
+                }
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
+                lsum += __low2float(h2) + __high2float(h2);
+                pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+            }
+          }
+          tmem_st32u(tS[b] + lane_off + h * 32, pk);
+        }
+        l_run = l_run * alpha + lsum;
+        m_run = m_new;
+        tc_fence_before();
+        mbar_arrive(&sh.p_full[b]);
+        if (last && more) q_ready();
       }
-      // max(s) * c == max(s * c) for c > 0 (rounding is monotonic)
-      const float m_new = fmaxf(m_run, mc == -FLT_MAX ? -FLT_MAX : mc * scale_log2);
-      const float alpha = m_run == -FLT_MAX ? 1.f : ex2_approx(m_run - m_new);
-      if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O holds super-chunks 0 .. i-1 once the P V of i-1 is done: scale it in TMEM
-        if (!mbar_wait_ab(o_done, (i - 1) & 1, flags)) flags[0] = 1;
-        tc_fence_after();
+      // the segment's O: normalised bf16 rows when it covers the unit, else an fp32 partial
+      if (!mbar_wait_ab(&sh.o_done, (i - 1) & 1, flags)) flags[0] = 1;
+      tc_fence_after();
+      const bool whole = sg.c_lo == 0 && sg.c_hi == sg.nch;
+      if (!flags[0]) {
+        __nv_bfloat16* dst = p.out + ((int64_t)(sg.s * kGamma + r) * p.nh + sg.g * group + hh) * 128;
+        const int64_t slot = (int64_t)blockIdx.x + sg.u;
+        float* op = p.o_part + (slot * 128 + t) * 128;
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           float v[32];
           tmem_ld32(tO + lane_off + q4 * 32, v);
+          if (whole) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= alpha;
-          tmem_st32(tO + lane_off + q4 * 32, v);
-        }
-      }
-      // P = 2^(s c - m) as bf16 pairs: keys 64 h .. 64 h + 63 into columns 32 h .. 32 h + 31
-      // (over scores already read)
-      float lsum = 0.f;
-#pragma unroll 1
-      for (int h = 0; h < nchk; ++h) {
-        uint32_t pk[32];
+            for (int d8 = 0; d8 < 4; ++d8) {
+              uint32_t pk[4];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float v[32];
-          tmem_ld32(tS[b] + lane_off + (2 * h + q) * 32, v);
-          if (full) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2_approx(fmaf(v[2 * e], scale_log2, -m_new)),
-                                                              ex2_approx(fmaf(v[2 * e + 1], scale_log2, -m_new)));
-              lsum += __low2float(h2) + __high2float(h2);
-              pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[d8 * 8 + 2 * e] * inv, v[d8 * 8 + 2 * e + 1] * inv);
+                pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              reinterpret_cast<uint4*>(dst)[q4 * 4 + d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float pr[2];
-#pragma unroll
-              for (int u = 0; u < 2; ++u) {
-                const int key = kb + (2 * h + q) * 32 + 2 * e + u;
-                const bool vis = key < nvis && (p.window <= 0 || pos_q - key < p.window);
-                pr[u] = vis ? ex2_approx(fmaf(v[2 * e + u], scale_log2, -m_new)) : 0.f;
-              }
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
-              lsum += __low2float(h2) + __high2float(h2);
-              pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
+            for (int e = 0; e < 32; e += 4)
+              __stcg(reinterpret_cast<float4*>(op + q4 * 32 + e), make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
           }
         }
-        tmem_st32u(tS[b] + lane_off + h * 32, pk);
+        if (!whole) __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
       }
-      l_run = l_run * alpha + lsum;
-      m_run = m_new;
-      tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      tc_fence_before();  // O read out before the next segment's first P V overwrites it
+      sg = nsg;
+      have = more;
     }
-    if (nsc > 0 && !mbar_wait_ab(o_done, (nsc - 1) & 1, flags)) flags[0] = 1;
-    tc_fence_after();
-    const int hh = t >> 4;
-    __nv_bfloat16* dst = p.out + ((int64_t)(s * kGamma + r) * p.nh + g * group + hh) * 128;
     if (flags[0]) {
       if (t == 0) atomicOr(p.status, DFLASH_DEV_TIMEOUT);
-      for (int i = 0; i < 2000; ++i) __nanosleep(1000);
-    } else {
-      const int64_t slot = (int64_t)unit * gridDim.y + split;
-      float* op = p.o_part + (slot * 128 + t) * 128;
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-#pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float v[32];
-        tmem_ld32(tO + lane_off + q4 * 32, v);
-        if (nsplit == 1) {
-#pragma unroll
-          for (int d8 = 0; d8 < 4; ++d8) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[d8 * 8 + 2 * e] * inv, v[d8 * 8 + 2 * e + 1] * inv);
-              pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            reinterpret_cast<uint4*>(dst)[q4 * 4 + d8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            __stcg(reinterpret_cast<float4*>(op + q4 * 32 + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
-        }
-      }
-      if (nsplit > 1) __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
+      for (int k = 0; k < 2000; ++k) __nanosleep(1000);  // copies still in flight land first
     }
   }
   tc_fence_before();
@@ -613,7 +783,10 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_tc_sc_kernel(const AttnPar
 // Merge the split partials of every (sequence, kv head) unit with more than one split, in
 // split order with a running maximum: o = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
 // Block (unit, rb) owns rows 4 rb .. 4 rb + 3; a warp per row, 4 dims per thread.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int splits_launched) {
+// sk_grid > 0: the partials of the stream-K kernel over sk_grid CTAs (the unit's splits are
+// the CTAs whose chunk ranges overlap it, slots b + unit); else those of the compact kernel
+// (splits_launched slots per unit).
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int splits_launched, int sk_grid) {
   pdl_trigger();  // the next projection may start streaming its weights
   pdl_wait();
   const int unit = blockIdx.x, t = threadIdx.x;
@@ -622,10 +795,42 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
   if (ctx < 0 || ctx > p.max_ctx || ctx + kGamma > p.mpps * kPage) return;
   int k0;
   const int nch = chunk_range(p.window, ctx, &k0);
-  const int nsplit = (nch + p.chunks_per_split - 1) / p.chunks_per_split;
-  if (nsplit <= 1 || nsplit > splits_launched) return;
+  int nsplit;
+  int64_t base;
+  if (sk_grid > 0) {
+    // the unit's first chunk in the batch's chunk space, and the space's size
+    __shared__ long long red[2][4];
+    long long before = 0, all = 0;
+    for (int s2 = t; s2 < p.nb; s2 += 128) {
+      const int c2 = __ldg(p.ctx_lens + s2);
+      int f2;
+      const long long n2 = (c2 < 0 || c2 > p.max_ctx || c2 + kGamma > p.mpps * kPage) ? 0 : chunk_range(p.window, c2, &f2);
+      all += n2;
+      if (s2 < s) before += n2;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      all += __shfl_xor_sync(0xffffffffu, all, o);
+    }
+    if ((t & 31) == 0) {
+      red[0][t >> 5] = before;
+      red[1][t >> 5] = all;
+    }
+    __syncthreads();
+    const long long first = (red[0][0] + red[0][1] + red[0][2] + red[0][3]) * p.nkv + (long long)g * nch;
+    const long long W = (red[1][0] + red[1][1] + red[1][2] + red[1][3]) * p.nkv;
+    const int G = (int)min((long long)sk_grid, W);  // CTAs with a non-empty range
+    const int b0 = sk_owner(first, W, G), b1 = sk_owner(first + nch - 1, W, G);
+    if (b0 == b1) return;  // one CTA covered the unit and wrote the output
+    nsplit = b1 - b0 + 1;
+    base = (int64_t)b0 + unit;
+  } else {
+    nsplit = (nch + p.chunks_per_split - 1) / p.chunks_per_split;
+    if (nsplit <= 1 || nsplit > splits_launched) return;
+    base = (int64_t)unit * splits_launched;
+  }
   const int row = blockIdx.y * 4 + (t >> 5), d0 = (t & 31) * 4;
-  const int64_t base = (int64_t)unit * splits_launched;
   float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   for (int q0 = 0; q0 < nsplit; q0 += 4) {
     float2 ml[4];
@@ -661,56 +866,58 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
 
 }  // namespace
 
-// Partial slots any launch needs: units * splits <= kScWaves * num_sms + units (splits =
-// ceil(nch / cps) with cps >= units * nch / (kScWaves * num_sms), and fewer for the compact
-// kernel).
+// Partial slots any launch needs: the compact kernel's units * splits <= kScWaves * num_sms +
+// units (splits = ceil(nch / cps) with cps >= units * nch / (kScWaves * num_sms)); the stream-K
+// kernel's slots b + unit < num_sms + units.
 int64_t attn_tc_partial_slots(int num_sms, int max_units) { return kScWaves * (int64_t)num_sms + max_units; }
 
 cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, cudaStream_t st) {
   static std::atomic<unsigned long long> attr{0}, attr2{0};
   if (cudaError_t e = smem_attr_once(attn_tc_kernel, kSmem, attr); e != cudaSuccess) return e;
-  if (cudaError_t e = smem_attr_once(attn_tc_sc_kernel, kScSmem, attr2); e != cudaSuccess) return e;
+  if (cudaError_t e = smem_attr_once(attn_sk_kernel, kScSmem, attr2); e != cudaSuccess) return e;
   const int units = nb * p.nkv;
+  p.nb = nb;
+  p.max_ctx = max_ctx_len;
   // the most chunks any sequence with ctx <= max_ctx_len visits
   int k0;
   int nch = chunk_range(0, max_ctx_len, &k0);
   if (p.window > 0) nch = std::min(nch, (p.window + kGamma + kPage + kKC - 1) / kKC);
   int cps = (units * nch + num_sms - 1) / num_sms;
   if (cps < 1) cps = 1;
-  p.max_ctx = max_ctx_len;
-  // many chunks per CTA: the super-chunk kernel (one CTA per SM); a few: the compact one (it
-  // fits beside a projection CTA on one SM, so it overlaps the QKV kernel under programmatic
-  // launch)
-  const bool sc = cps >= 4;
-  if (sc) {
-    // one CTA per SM and serial chunks inside a CTA: ~4 waves of short items let the block
-    // scheduler even out ragged context lengths
-    cps = std::max(4, (units * nch + kScWaves * num_sms - 1) / (kScWaves * num_sms));
-  }
-  const int splits_l = (nch + cps - 1) / cps;
-  p.chunks_per_split = cps;
-  cudaLaunchConfig_t ac = {};
-  ac.gridDim = dim3(units, splits_l);
-  ac.blockDim = dim3(sc ? kScThreads : 128);
-  ac.dynamicSmemBytes = sc ? kScSmem : kSmem;
-  ac.stream = st;
   cudaLaunchAttribute aa[1];
   aa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   aa[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t ac = {};
+  ac.stream = st;
   ac.attrs = aa;
   ac.numAttrs = 1;
-  cudaError_t e = sc ? cudaLaunchKernelEx(&ac, attn_tc_sc_kernel, p) : cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
-  if (e != cudaSuccess || splits_l == 1) return e;
+  // many chunks per SM: the stream-K kernel (one CTA per SM, an equal share of the batch's
+  // chunks each); a few: the compact kernel, split on the host from max_ctx_len (it fits beside
+  // a projection CTA on one SM, so it overlaps the QKV kernel under programmatic launch)
+  const bool sk = cps >= 4;
+  int splits_l = 1;
+  cudaError_t e;
+  if (sk) {
+    ac.gridDim = dim3(num_sms);
+    ac.blockDim = dim3(kScThreads);
+    ac.dynamicSmemBytes = kScSmem;
+    e = cudaLaunchKernelEx(&ac, attn_sk_kernel, p);
+  } else {
+    splits_l = (nch + cps - 1) / cps;
+    p.chunks_per_split = cps;
+    ac.gridDim = dim3(units, splits_l);
+    ac.blockDim = dim3(128);
+    ac.dynamicSmemBytes = kSmem;
+    e = cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
+  }
+  if (e != cudaSuccess || (!sk && splits_l == 1)) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units, 32);
   cfg.blockDim = dim3(128);
   cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
+  cfg.attrs = aa;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, splits_l);
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, splits_l, sk ? num_sms : 0);
 }
 
 }  // namespace dflash

@@ -18,9 +18,10 @@ struct AttnParams {
   const int32_t* widths = nullptr;       // [nb] active block widths (null: gamma)
   const int32_t* page_tables = nullptr;  // [nb, mpps]
   int mpps = 0, nh = 0, nkv = 0, window = 0, max_ctx = 0;
-  int chunks_per_split = 1;
-  float* o_part = nullptr;               // [units * splits, 128, 128] split partials
-  float* ml_part = nullptr;              // [units * splits, 128, 2] running max / sum
+  int nb = 0;                            // sequences (set by launch_attn_tc)
+  int chunks_per_split = 1;              // compact kernel: key chunks per split
+  float* o_part = nullptr;               // [slots, 128, 128] split partials
+  float* ml_part = nullptr;              // [slots, 128, 2] running max / sum
   unsigned* counters = nullptr;          // [units] (zero between launches)
   __nv_bfloat16* out = nullptr;          // [nb*16, nh*128]
   unsigned* status = nullptr;

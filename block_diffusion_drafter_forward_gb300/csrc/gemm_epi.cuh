@@ -75,8 +75,9 @@ struct EpiSmem {
 
 // Sum over the tile's 128 rows of w[row][c] for each of the chunk's 16 tokens, into es.tot.
 // Transposed through shared memory: thread (token c = t % 16, group g = t / 16) adds rows
-// 16g..16g+15 of token c, then one shuffle and a 4-warp combine.
-__device__ __forceinline__ void rowsum16(EpiSmem& es, const float (&w)[16], int t) {
+// 16g..16g+15 of token c, then one shuffle and a 4-warp combine.  eps >= 0: es.tot gets the
+// RMS scale 1 / sqrt(sum / 128 + eps) instead, computed once per token.
+__device__ __forceinline__ void rowsum16(EpiSmem& es, const float (&w)[16], int t, float eps = -1.f) {
 #pragma unroll
   for (int c = 0; c < 16; ++c) es.xch[t][c] = w[c];
   epi_sync();
@@ -87,7 +88,10 @@ __device__ __forceinline__ void rowsum16(EpiSmem& es, const float (&w)[16], int 
   a += __shfl_xor_sync(0xffffffffu, a, 16);
   if ((t & 31) < 16) es.red[t >> 5][c] = a;
   epi_sync();
-  if (t < 16) es.tot[t] = (es.red[0][t] + es.red[1][t]) + (es.red[2][t] + es.red[3][t]);
+  if (t < 16) {
+    const float sum = (es.red[0][t] + es.red[1][t]) + (es.red[2][t] + es.red[3][t]);
+    es.tot[t] = eps >= 0.f ? 1.f / sqrtf(sum * (1.f / 128.f) + eps) : sum;
+  }
   epi_sync();
 }
 
@@ -185,9 +189,9 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
       float sq[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) sq[c] = v[c] * v[c];
-      rowsum16(es, sq, t);
+      rowsum16(es, sq, t, p.eps);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * (1.f / sqrtf(es.tot[c] * (1.f / 128.f) + p.eps)) * q.nw;
+      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * es.tot[c] * q.nw;
       epi_sync();
       // RoPE: pair (j, j + 64), NeoX rotate-half.  The block's positions are consecutive, so
       // the angle at ctx + c comes from the one at ctx by c rotations through one position's
@@ -278,10 +282,10 @@ __device__ void epilogue_chunk(const GemmParams& p, EpiSmem& es, const float* rs
       float sq[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) sq[c] = v[c] * v[c];
-      rowsum16(es, sq, t);
+      rowsum16(es, sq, t, p.eps);
       const float w = __bfloat162float(p.k_norm[l * 128 + t]);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * (1.f / sqrtf(es.tot[c] * (1.f / 128.f) + p.eps)) * w;
+      for (int c = 0; c < 16; ++c) es.xch[t][c] = v[c] * es.tot[c] * w;
       epi_sync();
       const int j = t & 63;
       const float2 ipj = p.inv_pi[j];

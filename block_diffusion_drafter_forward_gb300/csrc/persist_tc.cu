@@ -172,6 +172,9 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* ptr) {
 //   6 split-K partials landed / last attention item done
 //   7 phase arrival                                8 epilogue warps done (before the arrival)
 //   9 a contributor's partial counted in
+//  10 finisher: partials added / attention: first S ready / combine: partials landed
+//  11 finisher: epilogue body done / attention: last P V done
+//  12 finisher: outputs fenced, before the release / attention: output stored
 __device__ __forceinline__ void trace_stamp(const PersistParams& p, int ph, int slot) {
 #if DFLASH_PHASE_TRACE
   if (p.trace) {
@@ -476,6 +479,9 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
   }
   fence_proxy_async_smem();
   epi_sync();
+  const int tph = 2 + 6 * layer;  // this attention phase (trace stamps)
+  const bool stamp = t == 0 && unit * a.splits + split == (int)blockIdx.x;  // the CTA's first item
+  if (stamp) trace_stamp(p, tph, 4);
 
   const int pos_q = a.ctx + (t & 15);
   const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
@@ -508,6 +514,7 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
     wait_ab(&B.s_done, use.s & 1, ab, p.gabort);
     use.s++;
     tc_fence_after();
+    if (stamp && sc == a.c_begin) trace_stamp(p, tph, 10);
 
     // every key of the super-chunk visible to every row: no masking
     const int kb = a.k0 + sc * kAKC, nk = nchk * kAKC;
@@ -608,6 +615,7 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
       __syncwarp();
     }
   }
+  if (stamp) trace_stamp(p, tph, 11);
   // O out of TMEM: normalised bf16 rows, or the split's fp32 partial (O, m, l)
   const int hh = t >> 4;
   __nv_bfloat16* dst = p.attn + ((int64_t)(a.s * kGamma + (t & 15)) * p.nh + a.g * group + hh) * 128;
@@ -636,6 +644,7 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
     }
   }
   if (a.nsplit > 1) __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
+  if (stamp) trace_stamp(p, tph, 12);
   tc_fence_before();  // TMEM reads done before the next item's MMAs overwrite S and O
 }
 
@@ -997,11 +1006,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
           float* tile_ws = p.ws + (size_t)(ph & 1) * p.ws_half + (int64_t)sg.tile * maxc * (kEThreads * TN);
           unsigned* cnt = p.counters + (ph & 1) * p.max_tiles;
           if (!finisher) {
-            // fp32 partial of this CTA's k-range into slot `rank`, then count it in
-            float* mine = tile_ws + ((int64_t)sg.rank * kEThreads + t) * TN;
+            // fp32 partial of this CTA's k-range into slot `rank` (float4 q of thread t at
+            // q * 128 + t: the finisher's shared-memory reads are conflict-free), then count it in
+            float4* mine = reinterpret_cast<float4*>(tile_ws + (int64_t)sg.rank * kEThreads * TN) + t;
 #pragma unroll
-            for (int q = 0; q < 16; q += 4)
-              __stcg(reinterpret_cast<float4*>(mine + q), make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]));
+            for (int q = 0; q < 4; ++q)
+              __stcg(mine + q * kEThreads, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
             epi_sync();
             if (t == 0) release_add(&cnt[sg.tile]);
             if (t == 0) trace_stamp(p, ph, 9);
@@ -1047,10 +1057,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
             if (t == 0) trace_stamp(p, ph, 6);
             ++red_use;
             for (int rk = 0; rk < nother; ++rk) {
-              const float4* src = reinterpret_cast<const float4*>(sRed + (size_t)(rk * kEThreads + t) * TN * 4);
+              const float4* src = reinterpret_cast<const float4*>(sRed + (size_t)rk * kPartBytes) + t;
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const float4 f = src[q];
+                const float4 f = src[q * kEThreads];
                 v[4 * q] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
               }
             }
@@ -1061,9 +1071,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 const int rk = rk0 + u < sg.ncontrib ? rk0 + u : rk0;
-                const float4* src = reinterpret_cast<const float4*>(tile_ws + ((int64_t)rk * kEThreads + t) * TN);
+                const float4* src = reinterpret_cast<const float4*>(tile_ws + (int64_t)rk * kEThreads * TN) + t;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) q4[u][q] = __ldcg(src + q);
+                for (int q = 0; q < 4; ++q) q4[u][q] = __ldcg(src + q * kEThreads);
               }
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
@@ -1076,16 +1086,19 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
               }
             }
           }
+          if (t == 0) trace_stamp(p, ph, 10);
           switch (gp.epi) {
             case EPI_QKV: epilogue_chunk<EPI_QKV>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
             case EPI_RESID: epilogue_chunk<EPI_RESID>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
             case EPI_GATEUP: epilogue_chunk<EPI_GATEUP>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
             default: epilogue_chunk<EPI_LMHEAD>(e, es, rsc, v, t, n, 0, 0, sg.tile, pre); break;
           }
+          if (t == 0) trace_stamp(p, ph, 11);
           if (gp.kind >= 3 && gp.kind <= 5) {
             // tile finished: its outputs are the next projection's operand (read through TMA)
             fence_proxy_async_global();
             epi_sync();
+            if (t == 0) trace_stamp(p, ph, 12);
             if (t == 0) release_add2(p.ready + (size_t)ph * p.ready_stride + sg.tile, p.done + ph);
           }
           if (gp.epi == EPI_LMHEAD) {

@@ -75,7 +75,7 @@ struct PersistParams {
 #ifndef DFLASH_PHASE_TRACE
 #define DFLASH_PHASE_TRACE 0
 #endif
-constexpr int kTraceSlots = 10;
+constexpr int kTraceSlots = 13;
 
 // Tokens (M = 16 * nb) the persistent kernel handles: one sequence (bf16 lm_head only); larger
 // batches and the FP8 lm_head use the per-projection kernels.

@@ -21,7 +21,8 @@ import numpy as np
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 TRACE_LIB = os.path.join(PKG, "libdflash_trace.so")
-SLOTS = ("barrier", "act", "w_first", "mma_last", "acc", "counted", "landed", "arrive", "epi_done", "contrib")
+SLOTS = ("barrier", "act", "w_first", "mma_last", "acc", "counted", "landed", "arrive", "epi_done", "contrib",
+         "reduced", "epi_body", "fenced")
 
 
 def phase_names(L: int):
@@ -51,7 +52,7 @@ def table(t: np.ndarray, L: int):
         arr = t[:, ph, SLOTS.index("arrive")]
         last = int(arr[arr > 0].max()) if (arr > 0).any() else prev
         cols = {}
-        for k, name in enumerate(SLOTS):
+        for k, name in enumerate(SLOTS[:S]):  # older traces hold fewer slots
             v = t[:, ph, k]
             v = v[v > 0]
             if v.size:
