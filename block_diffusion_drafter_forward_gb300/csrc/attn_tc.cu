@@ -311,20 +311,24 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
 // so a captured graph replayed with new context lengths stays balanced.
 //
 // Inside a CTA the pipeline runs on from one segment into the next.  Keys go in super-chunks of
-// two 64-key chunks (128 keys): warp 4 streams their K/V pages into three 64 KB buffers (two
+// two 64-key chunks (128 keys): warp 8 streams their K/V pages into three 64 KB buffers (two
 // super-chunks of look-ahead: at full HBM load a page copy takes longer than one softmax pass),
-// warp 5 issues the MMAs, warps 0-3 run the softmax.  While the softmax works on super-chunk i,
-// the tensor cores already compute S of super-chunk i + 1 into the second TMEM buffer.  Per
-// super-chunk: one max pass and one exp pass (ex2.approx) over the 128 scores of a row, P
-// written back as bf16 pairs over its own S columns and read from TMEM by the P V MMA, O
-// accumulated in TMEM and rescaled there only when a row's running max grows.  The next
-// segment's queries are copied in (cp.async) once the last S of the current one is done.
-// Loops stay rolled.  225 KB of shared memory and 512 TMEM columns: one CTA per SM.
+// warp 9 issues the MMAs, warps 0-7 run the softmax: warps w and w + 4 share the TMEM lanes of
+// rows 32 (w % 4) .. + 31 and take one 64-key chunk each (their partial row maxima and sums
+// meet in shared memory), so two warps per scheduler hide each other's latencies.  While the
+// softmax works on super-chunk i, the tensor cores already compute S of super-chunk i + 1 into
+// the second TMEM buffer.  Per super-chunk: one max pass and one exp pass (ex2.approx) over the
+// scores of a row, P written back as bf16 pairs over its own S columns and read from TMEM by
+// the P V MMA, O accumulated in TMEM and rescaled there only when a row's running max grows.
+// The next segment's queries are copied in (cp.async) once the last S of the current one is
+// done.  Loops stay rolled.  226 KB of shared memory and 512 TMEM columns: one CTA per SM.
 constexpr int kScChunks = 2;                                 // chunks per super-chunk
 constexpr int kScBuf = kScChunks * kKVStage;                 // 64 KB of K/V per buffer
 constexpr int kScBufs = 3;                                   // K/V buffers (super-chunks in flight)
-constexpr int kScSmem = kQBytes + kScBufs * kScBuf + 512 + 1024;
-constexpr int kScThreads = 192;
+constexpr int kScCtl = 2560;                                 // barriers, plan, row exchange
+constexpr int kScSmem = kQBytes + kScBufs * kScBuf + kScCtl + 128;
+constexpr int kScThreads = 320;                              // 8 softmax warps, producer, MMA
+constexpr int kScSoft = 256;
 constexpr int kScWaves = 4;  // partial slots per SM the compact kernel's split size allows
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -412,11 +416,12 @@ struct SkShared {
   uint64_t kv_full[kScBufs], kv_empty[kScBufs], s_full[2], p_full[2], o_done, q_full;
   uint32_t tmem_slot;
   int flags[2];
-  long long red[8];
+  long long red[16];
   long long W, pu0;
   int u0, found;
+  float xm[2][2][128];  // [super-chunk parity][half][row]: partial row maxima (and sums at a segment's end)
 };
-static_assert(sizeof(SkShared) <= 512, "stream-K control block overflows its slot");
+static_assert(sizeof(SkShared) <= kScCtl, "stream-K control block overflows its slot");
 
 // This CTA's walk: W by a block reduction over the sequences, then the sequence holding chunk
 // lo by a block scan (its first unit starts the walk).  All kScThreads threads.
@@ -481,7 +486,8 @@ __device__ SkWalk sk_plan(const AttnParams& p, SkShared& sh, int t) {
 
 __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // no-swizzle operand tiles and bulk copies need 16-byte alignment
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* sQ = smem;
   uint8_t* sKV = sQ + kQBytes;  // buffer b at sKV + b * kScBuf: chunk i's K pages, then its V pages
   SkShared& sh = *reinterpret_cast<SkShared*>(sKV + kScBufs * kScBuf);
@@ -504,10 +510,10 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
-      mbar_init(&sh.p_full[i], 128);
+      mbar_init(&sh.p_full[i], kScSoft);
     }
     mbar_init(&sh.o_done, 1);
-    mbar_init(&sh.q_full, 128);
+    mbar_init(&sh.q_full, kScSoft);
     flags[0] = 0;
     fence_barrier_init();
   }
@@ -521,7 +527,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
   constexpr uint32_t idesc_o = idesc_bf16(128, 128);
   pdl_trigger();
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- K/V page producer: lane l < 8 copies page l % 4 of chunk l / 4 of a
     // super-chunk (its K and V tiles, into the chunk's K and V regions); the page ids of the
     // next super-chunk are fetched while the warp waits for a free buffer
@@ -572,7 +578,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
     }
     if (!waited) pdl_wait();
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer (lane 0): S of super-chunk i + 1 goes out before P V of i,
     // across segment boundaries (the next segment's S waits for its queries)
     if (lane == 0) {
@@ -679,10 +685,14 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
         // max(s) * c == max(s * c) for c > 0 (rounding is monotonic)
         const float m_new = fmaxf(m_run, mc == -FLT_MAX ? -FLT_MAX : mc * scale_log2);
         const float alpha = m_run == -FLT_MAX ? 1.f : ex2_approx(m_run - m_new);
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // O holds this segment's super-chunks before this one once the last P V is done
+        if (j > 0) {
+          // every P V completion is waited for once, in order: a parity wait is only exact
+          // while the barrier is at most one phase behind (the segment's last wait relies on it)
           if (!mbar_wait_ab(&sh.o_done, (i - 1) & 1, flags)) flags[0] = 1;
           tc_fence_after();
+        }
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O holds this segment's super-chunks before this one (their P V are done)
 #pragma unroll 1
           for (int q4 = 0; q4 < 4; ++q4) {
             float v[32];
