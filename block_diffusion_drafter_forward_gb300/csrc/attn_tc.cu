@@ -611,9 +611,10 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
         if (!flags[0]) {
           const int nchk = cur.nchk();
           for (int kk = 0; kk < nchk * kPagesPerChunk; ++kk) {  // 16 keys = 8 TMEM columns of P each
-            const uint8_t* sV = sKV + kb * kScBuf + (kk / kPagesPerChunk) * kKVStage + kPagesPerChunk * kTileBytes +
-                                (kk % kPagesPerChunk) * kTileBytes;
-            mma_bf16_tmem_a(tO, tS[b] + kk * 8, desc_noswz(sV, 128, 256), idesc_o, (cur.j > 0 || kk > 0) ? 1u : 0u);
+            const int ci = kk / kPagesPerChunk, pg = kk % kPagesPerChunk;
+            const uint8_t* sV = sKV + kb * kScBuf + ci * kKVStage + kPagesPerChunk * kTileBytes + pg * kTileBytes;
+            mma_bf16_tmem_a(tO, tS[b] + ci * kKC + pg * 8, desc_noswz(sV, 128, 256), idesc_o,
+                            (cur.j > 0 || kk > 0) ? 1u : 0u);
           }
         }
         mma_commit(&sh.kv_empty[kb]);
@@ -624,17 +625,23 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
     }
     __syncwarp();
   } else {
-    // ---------------- warps 0-3: queries, softmax, output
+    // ---------------- warps 0-7: queries, softmax, output.  Thread t holds row t % 128 (head
+    // row / 16, token row % 16); half hf = warp / 4 takes chunk hf of each super-chunk and the
+    // O columns 64 hf .. 64 hf + 63.
     pdl_wait();
-    const int r = t & 15, hh = t >> 4;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int row = t & 127, hf = warp >> 2, r = row & 15, hh = row >> 4;
+    const int pair_bar = 1 + (warp & 3);  // named barrier of warps w % 4 and w % 4 + 4
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
-    // the queries of a unit into sQ (row t = head hh, token r), as 16-byte asynchronous copies
+    // this half of a unit's query row into sQ (row-major core matrices), 16-byte async copies
     auto load_q = [&](const SkSeg& q) {
       const uint4* src =
           reinterpret_cast<const uint4*>(p.q + ((int64_t)(q.s * kGamma + r) * p.nh + q.g * group + hh) * 128);
 #pragma unroll
-      for (int d8 = 0; d8 < 16; ++d8) cp_async16(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16, src + d8);
+      for (int d = 0; d < 8; ++d) {
+        const int d8 = hf * 8 + d;
+        cp_async16(sQ + ((row >> 3) * 16 + d8) * 128 + (row & 7) * 16, src + d8);
+      }
     };
     auto q_ready = [&]() {
       cp_async_wait_all();
@@ -654,11 +661,12 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
       const int n = sg.c_hi - sg.c_lo, nsc = (n + kScChunks - 1) / kScChunks;
       const int nvis = sg.ctx + block_width(p.widths, sg.s);  // keys past the active block width are masked
       const int pos_q = sg.ctx + r;
-      float m_run = -FLT_MAX, l_run = 0.f;
+      float m_run = -FLT_MAX, l_half = 0.f;
 #pragma unroll 1
       for (int j = 0; j < nsc; ++j, ++i) {
         const int b = i & 1;
         const int nchk = min(kScChunks, n - j * kScChunks);
+        const bool mine = hf < nchk;  // this half's chunk exists
         if (!mbar_wait_ab(&sh.s_full[b], (i >> 1) & 1, flags)) flags[0] = 1;
         tc_fence_after();
         const bool last = j == nsc - 1;
@@ -666,22 +674,30 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
         // every key of the super-chunk visible to every row: no masking
         const int kb = sg.k0 + (sg.c_lo + j * kScChunks) * kKC;
         const bool full = kb + nchk * kKC <= nvis && (p.window <= 0 || sg.ctx + kGamma - 1 - kb < p.window);
+        const int kh = kb + hf * kKC;  // first key of this half's chunk
         float mc = -FLT_MAX;
+        if (mine) {
 #pragma unroll 1
-        for (int q4 = 0; q4 < 2 * nchk; ++q4) {
-          float v[32];
-          tmem_ld32(tS[b] + lane_off + q4 * 32, v);
-          if (full) {
+          for (int q4 = 0; q4 < 2; ++q4) {
+            float v[32];
+            tmem_ld32(tS[b] + lane_off + (2 * hf + q4) * 32, v);
+            if (full) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mc = fmaxf(mc, v[e]);
-          } else {
+              for (int e = 0; e < 32; ++e) mc = fmaxf(mc, v[e]);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int key = kb + q4 * 32 + e;
-              if (key < nvis && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[e]);
+              for (int e = 0; e < 32; ++e) {
+                const int key = kh + q4 * 32 + e;
+                if (key < nvis && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[e]);
+              }
             }
           }
         }
+        // the row's maximum over both chunks (buffer by super-chunk parity: the next write to
+        // this one comes after the next exchange, which the partner reaches after its read)
+        sh.xm[b][hf][row] = mc;
+        named_barrier(pair_bar, 64);
+        mc = fmaxf(mc, sh.xm[b][hf ^ 1][row]);
         // max(s) * c == max(s * c) for c > 0 (rounding is monotonic)
         const float m_new = fmaxf(m_run, mc == -FLT_MAX ? -FLT_MAX : mc * scale_log2);
         const float alpha = m_run == -FLT_MAX ? 1.f : ex2_approx(m_run - m_new);
@@ -692,26 +708,25 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
           tc_fence_after();
         }
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // O holds this segment's super-chunks before this one (their P V are done)
+          // this half's O columns hold the segment's super-chunks before this one: scale them
 #pragma unroll 1
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q4 = 0; q4 < 2; ++q4) {
             float v[32];
-            tmem_ld32(tO + lane_off + q4 * 32, v);
+            tmem_ld32(tO + lane_off + (2 * hf + q4) * 32, v);
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] *= alpha;
-            tmem_st32(tO + lane_off + q4 * 32, v);
+            tmem_st32(tO + lane_off + (2 * hf + q4) * 32, v);
           }
         }
-        // P = 2^(s c - m) as bf16 pairs: keys 64 h .. 64 h + 63 into columns 32 h .. 32 h + 31
-        // (over scores already read)
+        // P = 2^(s c - m) as bf16 pairs: the 64 keys of chunk hf into the first 32 of its own 64
+        // S columns (the scores this thread has read; the other half's columns stay untouched)
         float lsum = 0.f;
-#pragma unroll 1
-        for (int h = 0; h < nchk; ++h) {
+        if (mine) {
           uint32_t pk[32];
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             float v[32];
-            tmem_ld32(tS[b] + lane_off + (2 * h + q) * 32, v);
+            tmem_ld32(tS[b] + lane_off + (2 * hf + q) * 32, v);
             if (full) {
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
@@ -726,7 +741,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
                 float pr[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                  const int key = kb + (2 * h + q) * 32 + 2 * e + u;
+                  const int key = kh + q * 32 + 2 * e + u;
                   const bool vis = key < nvis && (p.window <= 0 || pos_q - key < p.window);
                   pr[u] = vis ? ex2_approx(fmaf(v[2 * e + u], scale_log2, -m_new)) : 0.f;
                 }
@@ -736,27 +751,33 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
               }
             }
           }
-          tmem_st32u(tS[b] + lane_off + h * 32, pk);
+          tmem_st32u(tS[b] + lane_off + hf * kKC, pk);
         }
-        l_run = l_run * alpha + lsum;
+        l_half = l_half * alpha + lsum;
         m_run = m_new;
         tc_fence_before();
         mbar_arrive(&sh.p_full[b]);
         if (last && more) q_ready();
       }
+      // the row's sum over both halves (slot parity of super-chunk i + 1, written after the next
+      // exchange; the barrier first keeps the partner's last maximum read ahead of this write)
+      named_barrier(pair_bar, 64);
+      sh.xm[(i + 1) & 1][hf][row] = l_half;
+      named_barrier(pair_bar, 64);
+      const float l_run = l_half + sh.xm[(i + 1) & 1][hf ^ 1][row];
       // the segment's O: normalised bf16 rows when it covers the unit, else an fp32 partial
       if (!mbar_wait_ab(&sh.o_done, (i - 1) & 1, flags)) flags[0] = 1;
       tc_fence_after();
       const bool whole = sg.c_lo == 0 && sg.c_hi == sg.nch;
       if (!flags[0]) {
-        __nv_bfloat16* dst = p.out + ((int64_t)(sg.s * kGamma + r) * p.nh + sg.g * group + hh) * 128;
+        __nv_bfloat16* dst = p.out + ((int64_t)(sg.s * kGamma + r) * p.nh + sg.g * group + hh) * 128 + hf * 64;
         const int64_t slot = (int64_t)blockIdx.x + sg.u;
-        float* op = p.o_part + (slot * 128 + t) * 128;
+        float* op = p.o_part + (slot * 128 + row) * 128 + hf * 64;
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < 2; ++q4) {
           float v[32];
-          tmem_ld32(tO + lane_off + q4 * 32, v);
+          tmem_ld32(tO + lane_off + (2 * hf + q4) * 32, v);
           if (whole) {
 #pragma unroll
             for (int d8 = 0; d8 < 4; ++d8) {
@@ -774,7 +795,8 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
               __stcg(reinterpret_cast<float4*>(op + q4 * 32 + e), make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
           }
         }
-        if (!whole) __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
+        if (!whole && hf == 0)
+          __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + row) * 2), make_float2(m_run, l_run));
       }
       tc_fence_before();  // O read out before the next segment's first P V overwrites it
       sg = nsg;
