@@ -288,10 +288,9 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
   } else {
     // partial (O unnormalised, m, l) of this split; attn_combine_kernel merges the splits
     const int64_t slot = (int64_t)unit * gridDim.y + split;
-    float* op = p.o_part + (slot * 128 + t) * 128;
+    float4* op = o_part_row(p.o_part, slot, t);
 #pragma unroll
-    for (int i = 0; i < 128; i += 4)
-      __stcg(reinterpret_cast<float4*>(op + i), make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
+    for (int i = 0; i < 128; i += 4) __stcg(op + (i >> 2) * 128, make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
     __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
   }
   tc_fence_before();
@@ -579,13 +578,13 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
     if (!waited) pdl_wait();
     __syncwarp();
   } else if (warp == 9) {
-    // ---------------- MMA issuer (lane 0): S of super-chunk i + 1 goes out before P V of i,
-    // across segment boundaries (the next segment's S waits for its queries)
+    // ---------------- MMA issuer (lane 0): S of super-chunk i + 1 and P V of i are independent;
+    // each goes out as soon as its inputs are there (S: the K/V copy, and the segment's
+    // queries for a segment's first super-chunk; P V: the softmax's P), so a late copy never
+    // holds back the P V that frees a K/V buffer
     if (lane == 0) {
       auto issue_s = [&](const SkIt& it, int i) {
         const int b = i & 1, kb = i % kScBufs;
-        if (it.j == 0 && !mbar_wait_ab(&sh.q_full, it.seg & 1, flags)) flags[0] = 1;
-        if (!mbar_wait_ab(&sh.kv_full[kb], (i / kScBufs) & 1, flags)) flags[0] = 1;
         tc_fence_after();
         if (!flags[0]) {
           for (int ci = 0; ci < it.nchk(); ++ci) {
@@ -598,27 +597,45 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
         }
         mma_commit(&sh.s_full[b]);
       };
+      auto s_ready = [&](const SkIt& it, int i) {
+        return (it.j != 0 || mbar_test_wait(&sh.q_full, it.seg & 1)) &&
+               mbar_test_wait(&sh.kv_full[i % kScBufs], (i / kScBufs) & 1);
+      };
       SkIt cur, nx;
       cur.start(p, walk);
       nx = cur;
       nx.step(p);
-      if (cur.valid) issue_s(cur, 0);
+      if (cur.valid) {
+        if (!mbar_wait_ab(&sh.q_full, 0, flags)) flags[0] = 1;
+        if (!mbar_wait_ab(&sh.kv_full[0], 0, flags)) flags[0] = 1;
+        issue_s(cur, 0);
+      }
       for (int i = 0; cur.valid; ++i) {
         const int b = i & 1, kb = i % kScBufs;
-        if (nx.valid) issue_s(nx, i + 1);
-        if (!mbar_wait_ab(&sh.p_full[b], (i >> 1) & 1, flags)) flags[0] = 1;
-        tc_fence_after();
-        if (!flags[0]) {
-          const int nchk = cur.nchk();
-          for (int kk = 0; kk < nchk * kPagesPerChunk; ++kk) {  // 16 keys = 8 TMEM columns of P each
-            const int ci = kk / kPagesPerChunk, pg = kk % kPagesPerChunk;
-            const uint8_t* sV = sKV + kb * kScBuf + ci * kKVStage + kPagesPerChunk * kTileBytes + pg * kTileBytes;
-            mma_bf16_tmem_a(tO, tS[b] + ci * kKC + pg * 8, desc_noswz(sV, 128, 256), idesc_o,
-                            (cur.j > 0 || kk > 0) ? 1u : 0u);
+        bool s_out = !nx.valid, pv_out = false;
+        for (long long spin = 0; !(s_out && pv_out); ++spin) {
+          if (spin > kSpinLimit) flags[0] = 1;
+          const bool give_up = flags[0];  // after a timeout: commits only, no MMAs
+          if (!s_out && (give_up || s_ready(nx, i + 1))) {
+            issue_s(nx, i + 1);
+            s_out = true;
+          }
+          if (!pv_out && (give_up || mbar_test_wait(&sh.p_full[b], (i >> 1) & 1))) {
+            tc_fence_after();
+            if (!give_up) {
+              const int nchk = cur.nchk();
+              for (int kk = 0; kk < nchk * kPagesPerChunk; ++kk) {  // 16 keys = 8 TMEM columns of P each
+                const int ci = kk / kPagesPerChunk, pg = kk % kPagesPerChunk;
+                const uint8_t* sV = sKV + kb * kScBuf + ci * kKVStage + kPagesPerChunk * kTileBytes + pg * kTileBytes;
+                mma_bf16_tmem_a(tO, tS[b] + ci * kKC + pg * 8, desc_noswz(sV, 128, 256), idesc_o,
+                                (cur.j > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(&sh.kv_empty[kb]);
+            mma_commit(&sh.o_done);
+            pv_out = true;
           }
         }
-        mma_commit(&sh.kv_empty[kb]);
-        mma_commit(&sh.o_done);
         cur = nx;
         if (nx.valid) nx.step(p);
       }
@@ -772,7 +789,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
       if (!flags[0]) {
         __nv_bfloat16* dst = p.out + ((int64_t)(sg.s * kGamma + r) * p.nh + sg.g * group + hh) * 128 + hf * 64;
         const int64_t slot = (int64_t)blockIdx.x + sg.u;
-        float* op = p.o_part + (slot * 128 + row) * 128 + hf * 64;
+        float4* op = o_part_row(p.o_part, slot, row) + hf * 16 * 128;  // dims 64 hf ..
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
         for (int q4 = 0; q4 < 2; ++q4) {
@@ -792,7 +809,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
           } else {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              __stcg(reinterpret_cast<float4*>(op + q4 * 32 + e), make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
+              __stcg(op + (q4 * 8 + (e >> 2)) * 128, make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
           }
         }
         if (!whole && hf == 0)
@@ -814,7 +831,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
 
 // Merge the split partials of every (sequence, kv head) unit with more than one split, in
 // split order with a running maximum: o = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
-// Block (unit, rb) owns rows 4 rb .. 4 rb + 3; a warp per row, 4 dims per thread.
+// Block (unit, rb) owns rows 4 rb .. 4 rb + 3, 4 dims per thread.
 // sk_grid > 0: the partials of the stream-K kernel over sk_grid CTAs (the unit's splits are
 // the CTAs whose chunk ranges overlap it, slots b + unit); else those of the compact kernel
 // (splits_launched slots per unit).
@@ -862,7 +879,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
     if (nsplit <= 1 || nsplit > splits_launched) return;
     base = (int64_t)unit * splits_launched;
   }
-  const int row = blockIdx.y * 4 + (t >> 5), d0 = (t & 31) * 4;
+  // thread t: row 4 rb + t % 4, dims 4 (t / 4) ..: a warp reads 64 contiguous bytes per dim block
+  const int row = blockIdx.y * 4 + (t & 3), db = t >> 2, d0 = db * 4;
   float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   for (int q0 = 0; q0 < nsplit; q0 += 4) {
     float2 ml[4];
@@ -872,8 +890,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
       const int64_t sl = base + q0 + u;
       const bool v = q0 + u < nsplit;
       ml[u] = v ? __ldcg(reinterpret_cast<const float2*>(p.ml_part + (sl * 128 + row) * 2)) : make_float2(-FLT_MAX, 0.f);
-      ov[u] = v ? __ldcg(reinterpret_cast<const float4*>(p.o_part + (sl * 128 + row) * 128 + d0))
-                : make_float4(0.f, 0.f, 0.f, 0.f);
+      ov[u] = v ? __ldcg(o_part_row(p.o_part, sl, row) + db * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {

@@ -212,6 +212,15 @@ __device__ __forceinline__ int rope_start(const int32_t* rope_pos, int s, int ct
   return rope_pos ? __ldg(rope_pos + s) : ctx;
 }
 
+// Split-attention partial O (fp32, unnormalised) of slot `slot`, 128 rows x 128 dims stored
+// dim-block major: float4 db (dims 4 db .. 4 db + 3) of row r at float4 index
+// (slot * 32 + db) * 128 + r, so 32 consecutive rows of one dim block are 512 contiguous
+// bytes (coalesced stores by the row-per-thread attention kernels).  Returns row r's float4
+// of dim block 0; dim block db is 128 float4 further per block.
+__host__ __device__ __forceinline__ float4* o_part_row(float* o_part, int64_t slot, int r) {
+  return reinterpret_cast<float4*>(o_part) + slot * 32 * 128 + r;
+}
+
 // ---------------------------------------------------------------- launchers (kernels_simple.cu)
 // All launchers are stream-ordered and return cudaGetLastError() of the launch.
 cudaError_t launch_embed(const dflash_handle* h, const int32_t* bonus, int nb, float* x, cudaStream_t st);

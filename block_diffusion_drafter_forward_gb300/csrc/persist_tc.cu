@@ -620,7 +620,7 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
   const int hh = t >> 4;
   __nv_bfloat16* dst = p.attn + ((int64_t)(a.s * kGamma + (t & 15)) * p.nh + a.g * group + hh) * 128;
   const int64_t slot = (int64_t)unit * a.splits + split;
-  float* op = p.o_part + (slot * 128 + t) * 128;
+  float4* op = o_part_row(p.o_part, slot, t);
   const float inv = a.nsplit == 1 ? (l_run > 0.f ? 1.f / l_run : 0.f) : 1.f;
 #pragma unroll 1
   for (int q4 = 0; q4 < 4; ++q4) {
@@ -640,7 +640,7 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
     } else {
 #pragma unroll
       for (int i = 0; i < 32; i += 4)
-        __stcg(reinterpret_cast<float4*>(op + q4 * 32 + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+        __stcg(op + (q4 * 8 + (i >> 2)) * 128, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
     }
   }
   if (a.nsplit > 1) __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
@@ -666,8 +666,10 @@ __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb
   float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   if (ns * (2048 + 32) <= kCmbBytes) {
     for (int i = t; i < ns * 128; i += kEThreads) {
-      const int q = i >> 7, off = i & 127;
-      cp_async16(sBuf + q * 2048 + off * 16, p.o_part + ((base + q) * 128 + r0) * 128 + off * 4);
+      // 16 bytes of split q: dim block db, row r0 + rr (consecutive i: consecutive rows of one
+      // dim block, 64 contiguous bytes), landing row-major as [q][rr][db]
+      const int q = i >> 7, db = (i & 127) >> 2, rr = i & 3;
+      cp_async16(sBuf + q * 2048 + (rr * 32 + db) * 16, o_part_row(p.o_part, base + q, r0 + rr) + db * 128);
     }
     for (int i = t; i < ns * 2; i += kEThreads) {
       const int q = i >> 1, half = i & 1;
@@ -693,7 +695,7 @@ __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb
       for (int u = 0; u < 8; ++u) {
         const int q = q0 + u < ns ? q0 + u : q0;
         ml[u] = __ldcg(reinterpret_cast<const float2*>(p.ml_part + ((base + q) * 128 + row) * 2));
-        ov[u] = __ldcg(reinterpret_cast<const float4*>(p.o_part + ((base + q) * 128 + row) * 128 + d0));
+        ov[u] = __ldcg(o_part_row(p.o_part, base + q, row) + lane * 128);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
