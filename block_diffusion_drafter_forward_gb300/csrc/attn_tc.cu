@@ -412,7 +412,7 @@ struct SkIt {
 };
 
 struct SkShared {
-  uint64_t kv_full[kScBufs], kv_empty[kScBufs], s_full[2], p_full[2], o_done, q_full;
+  uint64_t kv_full[kScBufs], kv_empty[kScBufs], s_full[2], p_full[2], o_done[2], q_full;
   uint32_t tmem_slot;
   int flags[2];
   long long red[16];
@@ -511,7 +511,8 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_full[i], kScSoft);
     }
-    mbar_init(&sh.o_done, 1);
+    mbar_init(&sh.o_done[0], 1);
+    mbar_init(&sh.o_done[1], 1);
     mbar_init(&sh.q_full, kScSoft);
     flags[0] = 0;
     fence_barrier_init();
@@ -632,7 +633,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
               }
             }
             mma_commit(&sh.kv_empty[kb]);
-            mma_commit(&sh.o_done);
+            mma_commit(&sh.o_done[b]);
             pv_out = true;
           }
         }
@@ -718,14 +719,12 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
         // max(s) * c == max(s * c) for c > 0 (rounding is monotonic)
         const float m_new = fmaxf(m_run, mc == -FLT_MAX ? -FLT_MAX : mc * scale_log2);
         const float alpha = m_run == -FLT_MAX ? 1.f : ex2_approx(m_run - m_new);
-        if (j > 0) {
-          // every P V completion is waited for once, in order: a parity wait is only exact
-          // while the barrier is at most one phase behind (the segment's last wait relies on it)
-          if (!mbar_wait_ab(&sh.o_done, (i - 1) & 1, flags)) flags[0] = 1;
-          tc_fence_after();
-        }
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // this half's O columns hold the segment's super-chunks before this one: scale them
+          // this half's O columns hold the segment's super-chunks before this one once P V of
+          // i - 1 is done.  P V of i alternate between two barriers: S(i) went out after P V of
+          // i - 2, so the barrier of i - 1 is at most one phase behind and the parity wait exact
+          if (!mbar_wait_ab(&sh.o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, flags)) flags[0] = 1;
+          tc_fence_after();
 #pragma unroll 1
           for (int q4 = 0; q4 < 2; ++q4) {
             float v[32];
@@ -782,8 +781,9 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
       sh.xm[(i + 1) & 1][hf][row] = l_half;
       named_barrier(pair_bar, 64);
       const float l_run = l_half + sh.xm[(i + 1) & 1][hf ^ 1][row];
-      // the segment's O: normalised bf16 rows when it covers the unit, else an fp32 partial
-      if (!mbar_wait_ab(&sh.o_done, (i - 1) & 1, flags)) flags[0] = 1;
+      // the segment's O (its last P V done, hence every earlier one): normalised bf16 rows when
+      // it covers the unit, else an fp32 partial
+      if (!mbar_wait_ab(&sh.o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, flags)) flags[0] = 1;
       tc_fence_after();
       const bool whole = sg.c_lo == 0 && sg.c_hi == sg.nch;
       if (!flags[0]) {
