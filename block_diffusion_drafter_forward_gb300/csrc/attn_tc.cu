@@ -153,15 +153,9 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
   }
 
   // Q tile: row i = hh * 16 + r  <-  q[s*16 + r, (g*group + hh) * 128 + :], 8x8-block layout
-  {
-    const int hh = t >> 4, r = t & 15;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)(s * kGamma + r) * p.nh + g * group + hh) * 128);
 #pragma unroll
-    for (int d8 = 0; d8 < 16; ++d8) {
-      const uint4 v = src[d8];
-      *reinterpret_cast<uint4*>(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16) = v;
-    }
-  }
+  for (int k = 0; k < 16; ++k) stage_q_piece(sQ, p.q, s, g, p.nh, k * 128 + t);
+  cp_async_wait_all();
   fence_proxy_async_smem();
   __syncthreads();
 
@@ -651,15 +645,10 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
     const int pair_bar = 1 + (warp & 3);  // named barrier of warps w % 4 and w % 4 + 4
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
-    // this half of a unit's query row into sQ (row-major core matrices), 16-byte async copies
+    // a unit's queries into sQ: 2048 pieces of 16 bytes over the 256 softmax threads
     auto load_q = [&](const SkSeg& q) {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(p.q + ((int64_t)(q.s * kGamma + r) * p.nh + q.g * group + hh) * 128);
 #pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        const int d8 = hf * 8 + d;
-        cp_async16(sQ + ((row >> 3) * 16 + d8) * 128 + (row & 7) * 16, src + d8);
-      }
+      for (int k = 0; k < 8; ++k) stage_q_piece(sQ, p.q, q.s, q.g, p.nh, k * kScSoft + t);
     };
     auto q_ready = [&]() {
       cp_async_wait_all();

@@ -212,6 +212,19 @@ __device__ __forceinline__ int rope_start(const int32_t* rope_pos, int s, int ct
   return rope_pos ? __ldg(rope_pos + s) : ctx;
 }
 
+// One 16-byte piece x (0 <= x < 2048) of the queries of unit (sequence s, kv head g) into sQ,
+// the no-swizzle K-major operand of S = Q K^T (row = head hh * 16 + token r in 8-row x 16-byte
+// core matrices), as a cp.async copy.  x = 128 r + 16 hh + d8: the 8 query heads of one token
+// are 2 KB contiguous in q, so 32 consecutive x read 512 contiguous bytes.  The caller waits
+// (cp.async.wait_group), then fences the copies for the async proxy before the MMA reads sQ.
+__device__ __forceinline__ void stage_q_piece(uint8_t* sQ, const __nv_bfloat16* q, int s, int g, int nh, int x) {
+  const int r = x >> 7, hh = (x >> 4) & 7, d8 = x & 15;
+  const int row = hh * 16 + r;
+  const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sQ + ((row >> 3) * 16 + d8) * 128 + (row & 7) * 16));
+  const __nv_bfloat16* src = q + ((int64_t)(s * kGamma + r) * nh + g * 8 + hh) * 128 + d8 * 8;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // Split-attention partial O (fp32, unnormalised) of slot `slot`, 128 rows x 128 dims stored
 // dim-block major: float4 db (dims 4 db .. 4 db + 3) of row r at float4 index
 // (slot * 32 + db) * 128 + r, so 32 consecutive rows of one dim block are 512 contiguous

@@ -467,16 +467,10 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
     }
     __syncwarp();
   }
-  {
-    const int hh = t >> 4, r = t & 15;
-    const uint4* src =
-        reinterpret_cast<const uint4*>(p.q + ((int64_t)(a.s * kGamma + r) * p.nh + a.g * group + hh) * 128);
-    uint4 qv[16];
+  // the unit's queries: 16-byte copies, 32 consecutive ones reading 512 contiguous bytes
 #pragma unroll
-    for (int d8 = 0; d8 < 16; ++d8) qv[d8] = __ldcg(src + d8);
-#pragma unroll
-    for (int d8 = 0; d8 < 16; ++d8) *reinterpret_cast<uint4*>(sQ + ((t >> 3) * 16 + d8) * 128 + (t & 7) * 16) = qv[d8];
-  }
+  for (int k = 0; k < 16; ++k) stage_q_piece(sQ, p.q, a.s, a.g, p.nh, k * kEThreads + t);
+  cp_async_wait_all();
   fence_proxy_async_smem();
   epi_sync();
   const int tph = 2 + 6 * layer;  // this attention phase (trace stamps)
