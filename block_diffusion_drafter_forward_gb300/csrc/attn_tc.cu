@@ -682,32 +682,33 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
         const int kb = sg.k0 + (sg.c_lo + j * kScChunks) * kKC;
         const bool full = kb + nchk * kKC <= nvis && (p.window <= 0 || sg.ctx + kGamma - 1 - kb < p.window);
         const int kh = kb + hf * kKC;  // first key of this half's chunk
+        // this half's 64 scores, read from TMEM once (the max and the exp pass both use them)
+        float sv[64];
         float mc = -FLT_MAX;
         if (mine) {
-#pragma unroll 1
-          for (int q4 = 0; q4 < 2; ++q4) {
-            float v[32];
-            tmem_ld32(tS[b] + lane_off + (2 * hf + q4) * 32, v);
-            if (full) {
+          tmem_ld64(tS[b] + lane_off + hf * kKC, sv);
+          if (!full) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) mc = fmaxf(mc, v[e]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int key = kh + q4 * 32 + e;
-                if (key < nvis && (p.window <= 0 || pos_q - key < p.window)) mc = fmaxf(mc, v[e]);
-              }
+            for (int e = 0; e < 64; ++e) {
+              const int key = kh + e;
+              if (!(key < nvis && (p.window <= 0 || pos_q - key < p.window))) sv[e] = -FLT_MAX;
             }
           }
+#pragma unroll
+          for (int e = 0; e < 64; ++e) mc = fmaxf(mc, sv[e]);
         }
         // the row's maximum over both chunks (buffer by super-chunk parity: the next write to
         // this one comes after the next exchange, which the partner reaches after its read)
         sh.xm[b][hf][row] = mc;
         named_barrier(pair_bar, 64);
         mc = fmaxf(mc, sh.xm[b][hf ^ 1][row]);
-        // max(s) * c == max(s * c) for c > 0 (rounding is monotonic)
-        const float m_new = fmaxf(m_run, mc == -FLT_MAX ? -FLT_MAX : mc * scale_log2);
-        const float alpha = m_run == -FLT_MAX ? 1.f : ex2_approx(m_run - m_new);
+        // The reference maximum m_run moves only when the chunk's maximum exceeds it by more than
+        // 8 (log2 units): otherwise P = 2^(s c - m_run) <= 2^8 stays exact in fp32 and bf16, and O
+        // and l need no rescale (the final O / l is the same).  max(s) * c == max(s * c) for c > 0.
+        const float mcs = mc == -FLT_MAX ? -FLT_MAX : mc * scale_log2;
+        const bool grow = mcs > m_run + 8.f;
+        const float m_new = grow ? mcs : m_run;
+        const float alpha = (grow && m_run != -FLT_MAX) ? ex2_approx(m_run - m_new) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // this half's O columns hold the segment's super-chunks before this one once P V of
           // i - 1 is done.  P V of i alternate between two barriers: S(i) went out after P V of
@@ -724,37 +725,19 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
           }
         }
         // P = 2^(s c - m) as bf16 pairs: the 64 keys of chunk hf into the first 32 of its own 64
-        // S columns (the scores this thread has read; the other half's columns stay untouched)
+        // S columns (scores already in registers; the other half's columns stay untouched);
+        // masked keys hold -FLT_MAX, whose exp2 is 0 (also while a row has seen no visible key:
+        // m_new is -FLT_MAX then and the offset is taken as 0)
         float lsum = 0.f;
         if (mine) {
+          const float mneg = m_new == -FLT_MAX ? 0.f : -m_new;
           uint32_t pk[32];
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            float v[32];
-            tmem_ld32(tS[b] + lane_off + (2 * hf + q) * 32, v);
-            if (full) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2_approx(fmaf(v[2 * e], scale_log2, -m_new)),
-                                                                ex2_approx(fmaf(v[2 * e + 1], scale_log2, -m_new)));
-                lsum += __low2float(h2) + __high2float(h2);
-                pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                float pr[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  const int key = kh + q * 32 + 2 * e + u;
-                  const bool vis = key < nvis && (p.window <= 0 || pos_q - key < p.window);
-                  pr[u] = vis ? ex2_approx(fmaf(v[2 * e + u], scale_log2, -m_new)) : 0.f;
-                }
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[0], pr[1]);
-                lsum += __low2float(h2) + __high2float(h2);
-                pk[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&h2);
-              }
-            }
+          for (int e = 0; e < 32; ++e) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2_approx(fmaf(sv[2 * e], scale_log2, mneg)),
+                                                            ex2_approx(fmaf(sv[2 * e + 1], scale_log2, mneg)));
+            lsum += __low2float(h2) + __high2float(h2);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
           }
           tmem_st32u(tS[b] + lane_off + hf * kKC, pk);
         }
