@@ -282,9 +282,9 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
   } else {
     // partial (O unnormalised, m, l) of this split; attn_combine_kernel merges the splits
     const int64_t slot = (int64_t)unit * gridDim.y + split;
-    float4* op = o_part_row(p.o_part, slot, t);
 #pragma unroll
-    for (int i = 0; i < 128; i += 4) __stcg(op + (i >> 2) * 128, make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
+    for (int i = 0; i < 128; i += 4)
+      __stcg(o_part_at(p.o_part, slot, t, i >> 2), make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]));
     __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
   }
   tc_fence_before();
@@ -318,9 +318,11 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
 constexpr int kScChunks = 2;                                 // chunks per super-chunk
 constexpr int kScBuf = kScChunks * kKVStage;                 // 64 KB of K/V per buffer
 constexpr int kScBufs = 3;                                   // K/V buffers (super-chunks in flight)
+constexpr int kScKV = kScBuf / 2;                            // the K (or V) half of a buffer: 32 KB
+constexpr int kChunkKV = kPagesPerChunk * kTileBytes;        // one chunk's K (or V) pages: 16 KB
 constexpr int kScCtl = 2560;                                 // barriers, plan, row exchange
 constexpr int kScSmem = kQBytes + kScBufs * kScBuf + kScCtl + 128;
-constexpr int kScThreads = 320;                              // 8 softmax warps, producer, MMA
+constexpr int kScThreads = 352;                              // 8 softmax warps, K producer, MMA, V producer
 constexpr int kScSoft = 256;
 constexpr int kScWaves = 4;  // partial slots per SM the compact kernel's split size allows
 
@@ -406,7 +408,8 @@ struct SkIt {
 };
 
 struct SkShared {
-  uint64_t kv_full[kScBufs], kv_empty[kScBufs], s_full[2], p_full[2], o_done[2], q_full;
+  uint64_t k_full[kScBufs], k_empty[kScBufs], v_full[kScBufs], v_empty[kScBufs];
+  uint64_t s_full[2], p_full[2], o_done[2], q_full;
   uint32_t tmem_slot;
   int flags[2];
   long long red[16];
@@ -482,7 +485,9 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
   // no-swizzle operand tiles and bulk copies need 16-byte alignment
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + kQBytes;  // buffer b at sKV + b * kScBuf: chunk i's K pages, then its V pages
+  // K slot b at sKV + b * kScKV, V slot b at sKV + (kScBufs + b) * kScKV; in a slot, chunk ci's
+  // 4 pages at ci * kChunkKV
+  uint8_t* sKV = sQ + kQBytes;
   SkShared& sh = *reinterpret_cast<SkShared*>(sKV + kScBufs * kScBuf);
   volatile int* flags = sh.flags;
 
@@ -498,8 +503,10 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
 
   if (t == 0) {
     for (int i = 0; i < kScBufs; ++i) {
-      mbar_init(&sh.kv_full[i], 1);
-      mbar_init(&sh.kv_empty[i], 1);
+      mbar_init(&sh.k_full[i], 1);
+      mbar_init(&sh.k_empty[i], 1);
+      mbar_init(&sh.v_full[i], 1);
+      mbar_init(&sh.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
@@ -521,10 +528,15 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
   constexpr uint32_t idesc_o = idesc_bf16(128, 128);
   pdl_trigger();
 
-  if (warp == 8) {
-    // ---------------- K/V page producer: lane l < 8 copies page l % 4 of chunk l / 4 of a
-    // super-chunk (its K and V tiles, into the chunk's K and V regions); the page ids of the
-    // next super-chunk are fetched while the warp waits for a free buffer
+  if (warp == 8 || warp == 10) {
+    // ---------------- page producers: warp 8 the K pages, warp 10 the V pages, each into its own
+    // ring of three slots.  A K slot is free once the S MMA that read it is done, a V slot once
+    // its P V is done, so the K copies run a softmax pass further ahead than the V copies.  Lane
+    // l < 8 copies page l % 4 of chunk l / 4 of a super-chunk; the page ids of the next
+    // super-chunk are fetched while the warp waits for a free slot.
+    const int kv = warp == 10;
+    uint64_t* full = kv ? sh.v_full : sh.k_full;
+    uint64_t* empty = kv ? sh.v_empty : sh.k_empty;
     bool waited = false, stop = false;
     SkWalk w = walk;
     SkSeg sg;
@@ -544,7 +556,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
       int page = page_of(0);
       for (int jj = 0; jj < nsc; ++jj, ++i) {
         const int b = i % kScBufs;
-        if (i >= kScBufs && !mbar_wait_ab(&sh.kv_empty[b], ((i / kScBufs) - 1) & 1, flags)) {
+        if (i >= kScBufs && !mbar_wait_ab(&empty[b], ((i / kScBufs) - 1) & 1, flags)) {
           flags[0] = 1;
           stop = true;
           break;
@@ -554,7 +566,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
           pdl_wait();
           waited = true;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&sh.kv_full[b], nchk * kKVStage);
+        if (lane == 0) mbar_arrive_expect_tx(&full[b], nchk * kChunkKV);
         __syncwarp();
         if (lane < nchk * kPagesPerChunk) {
           int pg = page;
@@ -562,10 +574,8 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
             atomicOr(p.status, DFLASH_DEV_BAD_PAGE);
             pg = 0;
           }
-          uint8_t* dK = sKV + b * kScBuf + (lane >> 2) * kKVStage + (lane & 3) * kTileBytes;
-          uint8_t* dV = dK + kPagesPerChunk * kTileBytes;
-          bulk_load(dK, p.pool + tile_base(p.g, p.layer, pg, 0, sg.g), kTileBytes, &sh.kv_full[b]);
-          bulk_load(dV, p.pool + tile_base(p.g, p.layer, pg, 1, sg.g), kTileBytes, &sh.kv_full[b]);
+          uint8_t* d = sKV + (kv * kScBufs + b) * kScKV + (lane >> 2) * kChunkKV + (lane & 3) * kTileBytes;
+          bulk_load(d, p.pool + tile_base(p.g, p.layer, pg, kv, sg.g), kTileBytes, &full[b]);
         }
         page = page_of(jj + 1);
       }
@@ -574,16 +584,16 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
     __syncwarp();
   } else if (warp == 9) {
     // ---------------- MMA issuer (lane 0): S of super-chunk i + 1 and P V of i are independent;
-    // each goes out as soon as its inputs are there (S: the K/V copy, and the segment's
-    // queries for a segment's first super-chunk; P V: the softmax's P), so a late copy never
-    // holds back the P V that frees a K/V buffer
+    // each goes out as soon as its inputs are there (S: the K copy, and the segment's queries
+    // for a segment's first super-chunk; P V: the softmax's P and the V copy), so a late copy
+    // never holds back the MMA that frees a slot
     if (lane == 0) {
       auto issue_s = [&](const SkIt& it, int i) {
         const int b = i & 1, kb = i % kScBufs;
         tc_fence_after();
         if (!flags[0]) {
           for (int ci = 0; ci < it.nchk(); ++ci) {
-            const uint8_t* sK = sKV + kb * kScBuf + ci * kKVStage;
+            const uint8_t* sK = sKV + kb * kScKV + ci * kChunkKV;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               mma_bf16(tS[b] + ci * kKC, desc_noswz(sQ + k * 256, 128, 2048), desc_noswz(sK + k * 256, 128, 2048),
@@ -591,10 +601,11 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
           }
         }
         mma_commit(&sh.s_full[b]);
+        mma_commit(&sh.k_empty[kb]);  // the K slot is free once these MMAs are done
       };
       auto s_ready = [&](const SkIt& it, int i) {
         return (it.j != 0 || mbar_test_wait(&sh.q_full, it.seg & 1)) &&
-               mbar_test_wait(&sh.kv_full[i % kScBufs], (i / kScBufs) & 1);
+               mbar_test_wait(&sh.k_full[i % kScBufs], (i / kScBufs) & 1);
       };
       SkIt cur, nx;
       cur.start(p, walk);
@@ -602,7 +613,7 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
       nx.step(p);
       if (cur.valid) {
         if (!mbar_wait_ab(&sh.q_full, 0, flags)) flags[0] = 1;
-        if (!mbar_wait_ab(&sh.kv_full[0], 0, flags)) flags[0] = 1;
+        if (!mbar_wait_ab(&sh.k_full[0], 0, flags)) flags[0] = 1;
         issue_s(cur, 0);
       }
       for (int i = 0; cur.valid; ++i) {
@@ -615,18 +626,19 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
             issue_s(nx, i + 1);
             s_out = true;
           }
-          if (!pv_out && (give_up || mbar_test_wait(&sh.p_full[b], (i >> 1) & 1))) {
+          if (!pv_out && (give_up || (mbar_test_wait(&sh.p_full[b], (i >> 1) & 1) &&
+                                      mbar_test_wait(&sh.v_full[kb], (i / kScBufs) & 1)))) {
             tc_fence_after();
             if (!give_up) {
               const int nchk = cur.nchk();
               for (int kk = 0; kk < nchk * kPagesPerChunk; ++kk) {  // 16 keys = 8 TMEM columns of P each
                 const int ci = kk / kPagesPerChunk, pg = kk % kPagesPerChunk;
-                const uint8_t* sV = sKV + kb * kScBuf + ci * kKVStage + kPagesPerChunk * kTileBytes + pg * kTileBytes;
+                const uint8_t* sV = sKV + (kScBufs + kb) * kScKV + ci * kChunkKV + pg * kTileBytes;
                 mma_bf16_tmem_a(tO, tS[b] + ci * kKC + pg * 8, desc_noswz(sV, 128, 256), idesc_o,
                                 (cur.j > 0 || kk > 0) ? 1u : 0u);
               }
             }
-            mma_commit(&sh.kv_empty[kb]);
+            mma_commit(&sh.v_empty[kb]);
             mma_commit(&sh.o_done[b]);
             pv_out = true;
           }
@@ -761,7 +773,6 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
       if (!flags[0]) {
         __nv_bfloat16* dst = p.out + ((int64_t)(sg.s * kGamma + r) * p.nh + sg.g * group + hh) * 128 + hf * 64;
         const int64_t slot = (int64_t)blockIdx.x + sg.u;
-        float4* op = o_part_row(p.o_part, slot, row) + hf * 16 * 128;  // dims 64 hf ..
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
         for (int q4 = 0; q4 < 2; ++q4) {
@@ -781,7 +792,8 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
           } else {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              __stcg(op + (q4 * 8 + (e >> 2)) * 128, make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
+              __stcg(o_part_at(p.o_part, slot, row, hf * 16 + q4 * 8 + (e >> 2)),
+                     make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
           }
         }
         if (!whole && hf == 0)
@@ -851,7 +863,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
     if (nsplit <= 1 || nsplit > splits_launched) return;
     base = (int64_t)unit * splits_launched;
   }
-  // thread t: row 4 rb + t % 4, dims 4 (t / 4) ..: a warp reads 64 contiguous bytes per dim block
+  // thread t: row 4 rb + t % 4, dims 4 (t / 4) ..: the block reads 2 KB contiguous per split
   const int row = blockIdx.y * 4 + (t & 3), db = t >> 2, d0 = db * 4;
   float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   for (int q0 = 0; q0 < nsplit; q0 += 4) {
@@ -862,7 +874,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
       const int64_t sl = base + q0 + u;
       const bool v = q0 + u < nsplit;
       ml[u] = v ? __ldcg(reinterpret_cast<const float2*>(p.ml_part + (sl * 128 + row) * 2)) : make_float2(-FLT_MAX, 0.f);
-      ov[u] = v ? __ldcg(o_part_row(p.o_part, sl, row) + db * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+      ov[u] = v ? __ldcg(o_part_at(p.o_part, sl, row, db)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {

@@ -225,13 +225,12 @@ __device__ __forceinline__ void stage_q_piece(uint8_t* sQ, const __nv_bfloat16* 
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// Split-attention partial O (fp32, unnormalised) of slot `slot`, 128 rows x 128 dims stored
-// dim-block major: float4 db (dims 4 db .. 4 db + 3) of row r at float4 index
-// (slot * 32 + db) * 128 + r, so 32 consecutive rows of one dim block are 512 contiguous
-// bytes (coalesced stores by the row-per-thread attention kernels).  Returns row r's float4
-// of dim block 0; dim block db is 128 float4 further per block.
-__host__ __device__ __forceinline__ float4* o_part_row(float* o_part, int64_t slot, int r) {
-  return reinterpret_cast<float4*>(o_part) + slot * 32 * 128 + r;
+// Split-attention partial O (fp32, unnormalised) of slot `slot`: 128 rows x 128 dims as float4
+// dim blocks (dims 4 db .. 4 db + 3), stored [slot][row / 4][db][row % 4]: the 4 rows a combine
+// block merges are 2 KB contiguous per slot, and a row-per-thread writer's warp stores 64
+// contiguous bytes per group of 4 rows.  Returns the float4 of (row r, dim block db).
+__host__ __device__ __forceinline__ float4* o_part_at(float* o_part, int64_t slot, int r, int db) {
+  return reinterpret_cast<float4*>(o_part) + ((slot * 32 + (r >> 2)) * 32 + db) * 4 + (r & 3);
 }
 
 // ---------------------------------------------------------------- launchers (kernels_simple.cu)

@@ -614,7 +614,6 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
   const int hh = t >> 4;
   __nv_bfloat16* dst = p.attn + ((int64_t)(a.s * kGamma + (t & 15)) * p.nh + a.g * group + hh) * 128;
   const int64_t slot = (int64_t)unit * a.splits + split;
-  float4* op = o_part_row(p.o_part, slot, t);
   const float inv = a.nsplit == 1 ? (l_run > 0.f ? 1.f / l_run : 0.f) : 1.f;
 #pragma unroll 1
   for (int q4 = 0; q4 < 4; ++q4) {
@@ -634,7 +633,7 @@ __device__ void attn_item(const PersistParams& p, int layer, int unit, int split
     } else {
 #pragma unroll
       for (int i = 0; i < 32; i += 4)
-        __stcg(op + (q4 * 8 + (i >> 2)) * 128, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+        __stcg(o_part_at(p.o_part, slot, t, q4 * 8 + (i >> 2)), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
     }
   }
   if (a.nsplit > 1) __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + t) * 2), make_float2(m_run, l_run));
@@ -660,10 +659,10 @@ __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb
   float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   if (ns * (2048 + 32) <= kCmbBytes) {
     for (int i = t; i < ns * 128; i += kEThreads) {
-      // 16 bytes of split q: dim block db, row r0 + rr (consecutive i: consecutive rows of one
-      // dim block, 64 contiguous bytes), landing row-major as [q][rr][db]
+      // 16 bytes of split q: dim block db, row r0 + rr (the 4 rows are 2 KB contiguous per
+      // split), landing row-major as [q][rr][db]
       const int q = i >> 7, db = (i & 127) >> 2, rr = i & 3;
-      cp_async16(sBuf + q * 2048 + (rr * 32 + db) * 16, o_part_row(p.o_part, base + q, r0 + rr) + db * 128);
+      cp_async16(sBuf + q * 2048 + (rr * 32 + db) * 16, o_part_at(p.o_part, base + q, r0 + rr, db));
     }
     for (int i = t; i < ns * 2; i += kEThreads) {
       const int q = i >> 1, half = i & 1;
@@ -689,7 +688,7 @@ __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb
       for (int u = 0; u < 8; ++u) {
         const int q = q0 + u < ns ? q0 + u : q0;
         ml[u] = __ldcg(reinterpret_cast<const float2*>(p.ml_part + ((base + q) * 128 + row) * 2));
-        ov[u] = __ldcg(o_part_row(p.o_part, base + q, row) + lane * 128);
+        ov[u] = __ldcg(o_part_at(p.o_part, base + q, row, lane));
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -885,6 +884,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
     // ---------------- warps 0-3: epilogues and the non-GEMM phases
     AttnUse use = {{0, 0}, 0, 0};
     int segc = 0, red_use = 0;
+    int kv_pre = -1;  // thread 0: stages of the next attention item already being copied (-1: none)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     for (int ph = 0; ph < P; ++ph) {
       const int kind = phase_kind(ph, p.L);
@@ -897,7 +897,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         const int items = kind == PH_ATTN ? units * splits : units * 32;
         if (c < items) {
           int pre = 0;
-          if (kind == PH_ATTN && t == 0) pre = attn_prefetch(p, l, c / splits, c % splits, sA + kAP + kAQ, B);
+          if (kind == PH_ATTN && t == 0)
+            pre = kv_pre >= 0 ? kv_pre : attn_prefetch(p, l, c / splits, c % splits, sA + kAP + kAQ, B);
+          kv_pre = -1;
           if (t == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
           if (t == 0) trace_stamp(p, ph, 0);
           epi_sync();
@@ -927,6 +929,16 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         SegIter it(tiles, nkb, G, c);
         Seg sg;
         bool first = true;
+        if (gp.kind == 0 && t == 0) {
+          // a CTA that finishes no QKV tile never uses the partial landing buffer (the attention
+          // Q + K/V area) in this phase: its first attention item's context pages start copying now
+          bool fin = false;
+          SegIter probe(tiles, nkb, G, c);
+          for (Seg q; probe.next(q);) fin |= q.rank == 0;
+          const int units = (p.M / kGamma) * p.nkv;
+          const int splits = p.attn_splits[p.layers[gp.layer].window > 0];
+          if (!fin && c < units * splits) kv_pre = attn_prefetch(p, gp.layer, c / splits, c % splits, sA + kAP + kAQ, B);
+        }
         GemmParams e;
         e.N = gp.N; e.K = gp.K; e.M = p.M; e.Mp = p.M; e.eps = p.eps; e.status = p.status;
         e.ss_n = p.H; e.ss_parts = p.H / 128;
