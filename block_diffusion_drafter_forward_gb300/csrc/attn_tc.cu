@@ -341,6 +341,12 @@ __device__ __forceinline__ int sk_unit_chunks(const AttnParams& p, int u, int* c
   return chunk_range(p.window, c, k0);
 }
 
+// In the index space a unit with chunks occupies kSkUnitCost slots of no work before them: the
+// cost of a segment (its queries, the pipeline restart, its output) in chunks, so a CTA whose
+// range opens several segments gets fewer chunks.
+constexpr int kSkUnitCost = 4;
+__host__ __device__ __forceinline__ long long sk_slots(int nch) { return nch > 0 ? nch + kSkUnitCost : 0; }
+
 // CTA b of G = min(grid, W) owns global chunks [lo, hi) = [floor(b W / G), floor((b + 1) W / G))
 // (never empty); global chunk x belongs to CTA ceil((x + 1) G / W) - 1.
 __host__ __device__ __forceinline__ int sk_owner(int64_t x, int64_t W, int G) {
@@ -352,7 +358,7 @@ struct SkSeg {
   int c_lo, c_hi;             // this CTA's chunks of the unit
 };
 
-// The segments of chunk range [lo, hi), walked unit by unit from unit u (first chunk pu).
+// The segments of index range [lo, hi), walked unit by unit from unit u (first slot pu).
 struct SkWalk {
   int64_t lo, hi, pu;
   int u, units;
@@ -360,11 +366,11 @@ struct SkWalk {
     while (pu < hi && u < units) {
       int ctx, k0;
       const int nch = sk_unit_chunks(p, u, &ctx, &k0);
-      const int64_t first = pu;
+      const int64_t first = pu + kSkUnitCost;  // the unit's first chunk
       const int uu = u;
-      pu += nch;
+      pu += sk_slots(nch);
       ++u;
-      if (nch == 0 || pu <= lo) continue;
+      if (nch == 0 || hi <= first || lo >= first + nch) continue;  // no chunk of this unit in range
       sg.u = uu;
       sg.s = uu / p.nkv;
       sg.g = uu % p.nkv;
@@ -426,7 +432,7 @@ __device__ SkWalk sk_plan(const AttnParams& p, SkShared& sh, int t) {
   long long mine = 0;
   for (int s = t; s < p.nb; s += kScThreads) {
     int ctx, k0;
-    mine += sk_unit_chunks(p, s * p.nkv, &ctx, &k0);
+    mine += sk_slots(sk_unit_chunks(p, s * p.nkv, &ctx, &k0));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
@@ -450,7 +456,7 @@ __device__ SkWalk sk_plan(const AttnParams& p, SkShared& sh, int t) {
   for (int s0 = 0; s0 < p.nb; s0 += kScThreads) {
     const int s = s0 + t;
     int ctx, k0;
-    const long long n = s < p.nb ? (long long)sk_unit_chunks(p, s * p.nkv, &ctx, &k0) * p.nkv : 0;
+    const long long n = s < p.nb ? sk_slots(sk_unit_chunks(p, s * p.nkv, &ctx, &k0)) * p.nkv : 0;
     long long inc = n;  // inclusive scan: warp, then across warps
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -837,7 +843,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
     for (int s2 = t; s2 < p.nb; s2 += 128) {
       const int c2 = __ldg(p.ctx_lens + s2);
       int f2;
-      const long long n2 = (c2 < 0 || c2 > p.max_ctx || c2 + kGamma > p.mpps * kPage) ? 0 : chunk_range(p.window, c2, &f2);
+      const long long n2 =
+          (c2 < 0 || c2 > p.max_ctx || c2 + kGamma > p.mpps * kPage) ? 0 : sk_slots(chunk_range(p.window, c2, &f2));
       all += n2;
       if (s2 < s) before += n2;
     }
@@ -851,7 +858,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
       red[1][t >> 5] = all;
     }
     __syncthreads();
-    const long long first = (red[0][0] + red[0][1] + red[0][2] + red[0][3]) * p.nkv + (long long)g * nch;
+    const long long first =
+        (red[0][0] + red[0][1] + red[0][2] + red[0][3]) * p.nkv + (long long)g * sk_slots(nch) + kSkUnitCost;
     const long long W = (red[1][0] + red[1][1] + red[1][2] + red[1][3]) * p.nkv;
     const int G = (int)min((long long)sk_grid, W);  // CTAs with a non-empty range
     const int b0 = sk_owner(first, W, G), b1 = sk_owner(first + nch - 1, W, G);

@@ -652,17 +652,16 @@ __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb
                              Bars& B, int& red_use) {
   const AItem a = attn_geom(p, layer, unit, 0, ctx0);
   if (!a.run || a.nsplit <= 1) return;
-  const int warp = t >> 5, lane = t & 31;
-  const int r0 = rb * 4, row = r0 + warp, d0 = lane * 4;
+  // thread t: row r0 + t % 4, dims 4 (t / 4) .. (the order of the 4 rows' 2 KB in o_part)
+  const int r0 = rb * 4, rr = t & 3, row = r0 + rr, db = t >> 2, d0 = db * 4;
   const int64_t base = (int64_t)unit * a.splits;
   const int ns = a.nsplit;
   float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   if (ns * (2048 + 32) <= kCmbBytes) {
     for (int i = t; i < ns * 128; i += kEThreads) {
-      // 16 bytes of split q: dim block db, row r0 + rr (the 4 rows are 2 KB contiguous per
-      // split), landing row-major as [q][rr][db]
-      const int q = i >> 7, db = (i & 127) >> 2, rr = i & 3;
-      cp_async16(sBuf + q * 2048 + (rr * 32 + db) * 16, o_part_at(p.o_part, base + q, r0 + rr, db));
+      // the 4 rows of split q: 2 KB contiguous, copied as they lie
+      const int q = i >> 7, off = i & 127;
+      cp_async16(sBuf + q * 2048 + off * 16, o_part_at(p.o_part, base + q, r0, 0) + off);
     }
     for (int i = t; i < ns * 2; i += kEThreads) {
       const int q = i >> 1, half = i & 1;
@@ -670,13 +669,14 @@ __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb
     }
     cp_async_wait_all();
     epi_sync();
-    const float* so = reinterpret_cast<const float*>(sBuf);
+    const float4* so = reinterpret_cast<const float4*>(sBuf);
     const float2* sml = reinterpret_cast<const float2*>(sBuf + ns * 2048);
-    for (int q = 0; q < ns; ++q) M = fmaxf(M, sml[q * 4 + warp].x);
+    for (int q = 0; q < ns; ++q) M = fmaxf(M, sml[q * 4 + rr].x);
+#pragma unroll 4
     for (int q = 0; q < ns; ++q) {
-      const float2 ml = sml[q * 4 + warp];
+      const float2 ml = sml[q * 4 + rr];
       const float w = ml.x == -FLT_MAX ? 0.f : exp2f(ml.x - M);
-      const float4 ov = *reinterpret_cast<const float4*>(so + (q * 4 + warp) * 128 + d0);
+      const float4 ov = so[q * 128 + t];
       a0 += ov.x * w; a1 += ov.y * w; a2 += ov.z * w; a3 += ov.w * w;
       L += ml.y * w;
     }
@@ -688,7 +688,7 @@ __device__ void combine_item(const PersistParams& p, int layer, int unit, int rb
       for (int u = 0; u < 8; ++u) {
         const int q = q0 + u < ns ? q0 + u : q0;
         ml[u] = __ldcg(reinterpret_cast<const float2*>(p.ml_part + ((base + q) * 128 + row) * 2));
-        ov[u] = __ldcg(o_part_at(p.o_part, base + q, row, lane));
+        ov[u] = __ldcg(o_part_at(p.o_part, base + q, row, db));
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -884,7 +884,6 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
     // ---------------- warps 0-3: epilogues and the non-GEMM phases
     AttnUse use = {{0, 0}, 0, 0};
     int segc = 0, red_use = 0;
-    int kv_pre = -1;  // thread 0: stages of the next attention item already being copied (-1: none)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     for (int ph = 0; ph < P; ++ph) {
       const int kind = phase_kind(ph, p.L);
@@ -897,9 +896,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         const int items = kind == PH_ATTN ? units * splits : units * 32;
         if (c < items) {
           int pre = 0;
-          if (kind == PH_ATTN && t == 0)
-            pre = kv_pre >= 0 ? kv_pre : attn_prefetch(p, l, c / splits, c % splits, sA + kAP + kAQ, B);
-          kv_pre = -1;
+          if (kind == PH_ATTN && t == 0) pre = attn_prefetch(p, l, c / splits, c % splits, sA + kAP + kAQ, B);
           if (t == 0) grid_wait(&p.bar[ph - 1], (unsigned)G, ab, p.gabort);
           if (t == 0) trace_stamp(p, ph, 0);
           epi_sync();
@@ -929,16 +926,6 @@ __global__ void __launch_bounds__(kBlockThreads, 1) persist_kernel(const __grid_
         SegIter it(tiles, nkb, G, c);
         Seg sg;
         bool first = true;
-        if (gp.kind == 0 && t == 0) {
-          // a CTA that finishes no QKV tile never uses the partial landing buffer (the attention
-          // Q + K/V area) in this phase: its first attention item's context pages start copying now
-          bool fin = false;
-          SegIter probe(tiles, nkb, G, c);
-          for (Seg q; probe.next(q);) fin |= q.rank == 0;
-          const int units = (p.M / kGamma) * p.nkv;
-          const int splits = p.attn_splits[p.layers[gp.layer].window > 0];
-          if (!fin && c < units * splits) kv_pre = attn_prefetch(p, gp.layer, c / splits, c % splits, sA + kAP + kAQ, B);
-        }
         GemmParams e;
         e.N = gp.N; e.K = gp.K; e.M = p.M; e.Mp = p.M; e.eps = p.eps; e.status = p.status;
         e.ss_n = p.H; e.ss_parts = p.H / 128;
