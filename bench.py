@@ -88,6 +88,7 @@ def work_model(cfg, wl, logits: bool):
 KERNEL_SOURCES = {
     "persistent_forward": ("persist_tc.cu", "persist_tc.cuh", "gemm_epi.cuh", "gemm_tc.cuh", "tc_common.cuh",
                            "dflash_internal.cuh"),
+    "attention": ("attn_tc.cu", "attn_tc.cuh", "tc_common.cuh", "dflash_internal.cuh"),
 }
 
 
