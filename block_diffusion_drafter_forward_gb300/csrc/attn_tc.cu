@@ -299,8 +299,8 @@ __global__ void __launch_bounds__(128, 1) attn_tc_kernel(const AttnParams p) {
 // so every SM streams the same number of K/V bytes and there is no tail wave.  The range falls
 // into segments (unit u, chunks [c_lo, c_hi) of it): a segment that covers its unit whole
 // writes the normalised output, the others write fp32 partials (O, m, l) into slot b + u, which
-// is unique (along the segments of the batch, b + u grows at every step); the last of a unit's
-// segments to finish (a per-unit counter) merges its partials, so no combine launch follows.  W, the CTA's range and its first unit come from ctx_lens on the device,
+// is unique (along the segments of the batch, b + u grows at every step), merged by
+// attn_combine_kernel.  W, the CTA's range and its first unit come from ctx_lens on the device,
 // so a captured graph replayed with new context lengths stays balanced.
 //
 // Inside a CTA the pipeline runs on from one segment into the next.  Keys go in super-chunks of
@@ -356,15 +356,12 @@ __host__ __device__ __forceinline__ int sk_owner(int64_t x, int64_t W, int G) {
 struct SkSeg {
   int u, s, g, ctx, k0, nch;  // unit, its sequence, kv head, context, first key, chunks
   int c_lo, c_hi;             // this CTA's chunks of the unit
-  int64_t first;              // index of the unit's first chunk
 };
 
 // The segments of index range [lo, hi), walked unit by unit from unit u (first slot pu).
 struct SkWalk {
   int64_t lo, hi, pu;
   int u, units;
-  long long W;  // index space size
-  int G;        // CTAs with a non-empty range
   __device__ bool next(const AttnParams& p, SkSeg& sg) {
     while (pu < hi && u < units) {
       int ctx, k0;
@@ -380,7 +377,6 @@ struct SkWalk {
       sg.ctx = ctx;
       sg.k0 = k0;
       sg.nch = nch;
-      sg.first = first;
       sg.c_lo = (int)(lo > first ? lo - first : 0);
       sg.c_hi = (int)(hi - first < nch ? hi - first : nch);
       return true;
@@ -424,7 +420,7 @@ struct SkShared {
   int flags[2];
   long long red[16];
   long long W, pu0;
-  int u0, found, merge_b0;
+  int u0, found;
   float xm[2][2][128];  // [super-chunk parity][half][row]: partial row maxima (and sums at a segment's end)
 };
 static_assert(sizeof(SkShared) <= kScCtl, "stream-K control block overflows its slot");
@@ -452,8 +448,6 @@ __device__ SkWalk sk_plan(const AttnParams& p, SkShared& sh, int t) {
   wk.lo = b < G ? (int64_t)b * W / G : 0;
   wk.hi = b < G ? (int64_t)(b + 1) * W / G : 0;
   wk.units = p.nb * p.nkv;
-  wk.W = W;
-  wk.G = G;
   wk.u = wk.units;
   wk.pu = wk.hi;
   __syncthreads();  // every thread has read red[]
@@ -812,47 +806,6 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
           __stcg(reinterpret_cast<float2*>(p.ml_part + (slot * 128 + row) * 2), make_float2(m_run, l_run));
       }
       tc_fence_before();  // O read out before the next segment's first P V overwrites it
-      if (!whole) {  // uniform over the softmax threads (the barriers below need all of them)
-        // the last of the unit's segments to finish (its CTAs b0..b1, counted per unit) merges
-        // the partials, in split order: o = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q
-        const int b0 = sk_owner(sg.first, walk.W, walk.G), b1 = sk_owner(sg.first + sg.nch - 1, walk.W, walk.G);
-        __threadfence();
-        named_barrier(5, kScSoft);
-        if (t == 0) sh.merge_b0 = atomicAdd(p.counters + sg.u, 1u) == (unsigned)(b1 - b0) ? b0 : -1;
-        named_barrier(5, kScSoft);
-        if (sh.merge_b0 >= 0) {
-          __threadfence();
-          const int ns = b1 - b0 + 1;
-          __nv_bfloat16* out = p.out + ((int64_t)sg.s * kGamma * p.nh + sg.g * group) * 128;
-          // x = (row group, dim block, row % 4): the partials' own order, so loads are contiguous
-#pragma unroll 1
-          for (int x = t; x < 128 * 32; x += kScSoft) {
-            const int db = (x >> 2) & 31, mrow = (x >> 7) * 4 + (x & 3);
-            float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 1
-            for (int q = 0; q < ns; ++q) {
-              const int64_t sl = (int64_t)b0 + q + sg.u;
-              const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ml_part + (sl * 128 + mrow) * 2));
-              const float4 ov = __ldcg(o_part_at(p.o_part, sl, mrow, db));
-              if (ml.x > M) {
-                const float sc = M == -FLT_MAX ? 0.f : exp2f(M - ml.x);
-                a0 *= sc; a1 *= sc; a2 *= sc; a3 *= sc; L *= sc;
-                M = ml.x;
-              }
-              const float w = ml.x == -FLT_MAX ? 0.f : exp2f(ml.x - M);
-              a0 += ov.x * w; a1 += ov.y * w; a2 += ov.z * w; a3 += ov.w * w;
-              L += ml.y * w;
-            }
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            const __nv_bfloat162 h0 = __floats2bfloat162_rn(a0 * inv, a1 * inv);
-            const __nv_bfloat162 h1 = __floats2bfloat162_rn(a2 * inv, a3 * inv);
-            // row mrow = head (mrow / 16) x token (mrow % 16)
-            *reinterpret_cast<uint2*>(out + ((int64_t)(mrow & 15) * p.nh + (mrow >> 4)) * 128 + db * 4) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-          }
-          if (t == 0) p.counters[sg.u] = 0;  // re-armed for the next launch
-        }
-      }
       sg = nsg;
       have = more;
     }
@@ -866,11 +819,13 @@ __global__ void __launch_bounds__(kScThreads, 1) attn_sk_kernel(const AttnParams
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// Merge the split partials of the compact kernel's (sequence, kv head) units with more than one
-// split (splits_launched slots per unit), in split order with a running maximum:
-// o = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.  Block (unit, rb) owns rows 4 rb .. 4 rb + 3,
-// 4 dims per thread.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int splits_launched) {
+// Merge the split partials of every (sequence, kv head) unit with more than one split, in
+// split order with a running maximum: o = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
+// Block (unit, rb) owns rows 4 rb .. 4 rb + 3, 4 dims per thread.
+// sk_grid > 0: the partials of the stream-K kernel over sk_grid CTAs (the unit's splits are
+// the CTAs whose chunk ranges overlap it, slots b + unit); else those of the compact kernel
+// (splits_launched slots per unit).
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, int splits_launched, int sk_grid) {
   pdl_trigger();  // the next projection may start streaming its weights
   pdl_wait();
   const int unit = blockIdx.x, t = threadIdx.x;
@@ -879,9 +834,43 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p, i
   if (ctx < 0 || ctx > p.max_ctx || ctx + kGamma > p.mpps * kPage) return;
   int k0;
   const int nch = chunk_range(p.window, ctx, &k0);
-  const int nsplit = (nch + p.chunks_per_split - 1) / p.chunks_per_split;
-  if (nsplit <= 1 || nsplit > splits_launched) return;
-  const int64_t base = (int64_t)unit * splits_launched;
+  int nsplit;
+  int64_t base;
+  if (sk_grid > 0) {
+    // the unit's first chunk in the batch's chunk space, and the space's size
+    __shared__ long long red[2][4];
+    long long before = 0, all = 0;
+    for (int s2 = t; s2 < p.nb; s2 += 128) {
+      const int c2 = __ldg(p.ctx_lens + s2);
+      int f2;
+      const long long n2 =
+          (c2 < 0 || c2 > p.max_ctx || c2 + kGamma > p.mpps * kPage) ? 0 : sk_slots(chunk_range(p.window, c2, &f2));
+      all += n2;
+      if (s2 < s) before += n2;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      all += __shfl_xor_sync(0xffffffffu, all, o);
+    }
+    if ((t & 31) == 0) {
+      red[0][t >> 5] = before;
+      red[1][t >> 5] = all;
+    }
+    __syncthreads();
+    const long long first =
+        (red[0][0] + red[0][1] + red[0][2] + red[0][3]) * p.nkv + (long long)g * sk_slots(nch) + kSkUnitCost;
+    const long long W = (red[1][0] + red[1][1] + red[1][2] + red[1][3]) * p.nkv;
+    const int G = (int)min((long long)sk_grid, W);  // CTAs with a non-empty range
+    const int b0 = sk_owner(first, W, G), b1 = sk_owner(first + nch - 1, W, G);
+    if (b0 == b1) return;  // one CTA covered the unit and wrote the output
+    nsplit = b1 - b0 + 1;
+    base = (int64_t)b0 + unit;
+  } else {
+    nsplit = (nch + p.chunks_per_split - 1) / p.chunks_per_split;
+    if (nsplit <= 1 || nsplit > splits_launched) return;
+    base = (int64_t)unit * splits_launched;
+  }
   // thread t: row 4 rb + t % 4, dims 4 (t / 4) ..: the block reads 2 KB contiguous per split
   const int row = blockIdx.y * 4 + (t & 3), db = t >> 2, d0 = db * 4;
   float M = -FLT_MAX, L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -962,15 +951,14 @@ cudaError_t launch_attn_tc(AttnParams p, int nb, int max_ctx_len, int num_sms, c
     ac.dynamicSmemBytes = kSmem;
     e = cudaLaunchKernelEx(&ac, attn_tc_kernel, p);
   }
-  // the stream-K kernel merges its split units itself (the last segment of a unit to finish)
-  if (e != cudaSuccess || sk || splits_l == 1) return e;
+  if (e != cudaSuccess || (!sk && splits_l == 1)) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units, 32);
   cfg.blockDim = dim3(128);
   cfg.stream = st;
   cfg.attrs = aa;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, splits_l);
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p, splits_l, sk ? num_sms : 0);
 }
 
 }  // namespace dflash
