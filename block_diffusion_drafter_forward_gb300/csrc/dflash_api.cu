@@ -291,10 +291,9 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
   const bool fp8w = c.layer_weight_dtype == DFLASH_FP8E4M3_ROWSCALE;
   auto splits = [&](int N, int K) {
     const int tiles = ((N + 127) / 128) * ((M + tn - 1) / tn);
-    return pick_splits(tiles, K / 64, h->num_sms, tn, true);
+    return pick_splits(tiles, K / 64, h->num_sms, tn);
   };
   GemmParams base;
-  base.wide_pairs = 1;  // the projections' split wide tiles run two CTAs per SM
   base.ws = h->ws;
   base.counters = h->counters;
   base.status = h->d_status;
@@ -708,20 +707,19 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
     // split-K workspace: the largest need over every projection and batch size, and over
     // the writer's two GEMMs for every chunk size
     size_t need = 16;
-    auto account = [&](int64_t N, int64_t K, int64_t m, bool wide_pairs) {
+    auto account = [&](int64_t N, int64_t K, int64_t m) {
       const int tn = pick_tn((int)m);
       const int64_t tiles = ((N + 127) / 128) * ((m + tn - 1) / tn);
-      const int ns = pick_splits((int)tiles, (int)(K / 64), h->num_sms, tn, wide_pairs);
+      const int ns = pick_splits((int)tiles, (int)(K / 64), h->num_sms, tn);
       if (ns > 1) need = std::max(need, (size_t)(tiles * ns * 128 * tn));
       return tiles <= kCounters - 64;
     };
     bool fits = true;
     for (int64_t m = kGamma; m <= R; m += kGamma)
-      fits = account(qkvd, H, m, true) && account(H, qd, m, true) && account(2 * F, H, m, true) &&
-             account(H, F, m, true) && fits;
+      fits = account(qkvd, H, m) && account(H, qd, m) && account(2 * F, H, m) && account(H, F, m) && fits;
     for (int64_t m = 1; m <= Rw; m = m < 256 ? m + 1 : m + 256)
-      fits = account(H, tapd, m, false) && account(L * 2 * kvd, H, m, false) && fits;
-    fits = account(H, tapd, Rw, false) && account(L * 2 * kvd, H, Rw, false) && fits;
+      fits = account(H, tapd, m) && account(L * 2 * kvd, H, m) && fits;
+    fits = account(H, tapd, Rw) && account(L * 2 * kvd, H, Rw) && fits;
     if (!fits || tapd % 64) {
       fail(h, DFLASH_EUNSUPPORTED, "GEMM tiling out of range (too many tiles or n_taps*target_hidden % 64 != 0)");
       return bail(DFLASH_EUNSUPPORTED);

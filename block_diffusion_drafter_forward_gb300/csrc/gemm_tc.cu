@@ -388,7 +388,7 @@ cudaError_t launch_tn(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPa
   if constexpr (EPI == EPI_QKV || EPI == EPI_RESID || EPI == EPI_GATEUP) {  // FP8 layer weights
     if (fp8a) {
       if constexpr (TN >= 64) {
-        if (p.nsplit > 1 && !p.wide_pairs) return launch_t<EPI, TN, TN >= 128 ? 3 : 6, true, 4>(tw, tx, p, grid, st, pdl);
+        if (p.nsplit > 1) return launch_t<EPI, TN, TN >= 128 ? 3 : 6, true, 4>(tw, tx, p, grid, st, pdl);
       }
       return launch_t<EPI, TN, STAGES - 1, true, WG>(tw, tx, p, grid, st, pdl);
     }
@@ -401,8 +401,8 @@ cudaError_t launch_tn(const CUtensorMap& tw, const CUtensorMap& tx, const GemmPa
     if constexpr (TN == 64) return launch_t<EPI, TN, 3, false, 2>(tw, tx, p, grid, st, pdl);
     return launch_t<EPI, TN, 5, false, 1>(tw, tx, p, grid, st, pdl);
   }
-  if constexpr (TN >= 64) {  // split tiles: one CTA per SM, 4 warpgroups, a deep ring (or two per SM)
-    if (p.nsplit > 1 && !p.wide_pairs) return launch_t<EPI, TN, TN >= 128 ? 4 : 8, false, 4>(tw, tx, p, grid, st, pdl);
+  if constexpr (TN >= 64) {  // split tiles: one CTA per SM, 4 warpgroups, a deep ring
+    if (p.nsplit > 1) return launch_t<EPI, TN, TN >= 128 ? 4 : 8, false, 4>(tw, tx, p, grid, st, pdl);
   }
   return launch_t<EPI, TN, STAGES, false, WG>(tw, tx, p, grid, st, pdl);
 }
@@ -442,11 +442,10 @@ int pick_tn(int M) {
   return 128;  // larger batches: several 128-token tiles, consecutive in the grid (weight tile reuse in L2)
 }
 
-int pick_splits(int tiles, int nkb, int num_sms, int tn, bool wide_pairs) {
-  // about one CTA per SM slot; wide tiles that split run one CTA per SM (4 epilogue
-  // warpgroups), or two per SM with wide_pairs, and round down rather than start a second,
-  // mostly empty wave
-  int s = tn >= 64 ? (wide_pairs ? 2 * num_sms : num_sms) / tiles : (num_sms + tiles - 1) / tiles;
+int pick_splits(int tiles, int nkb, int num_sms, int tn) {
+  // about one CTA per SM; wide tiles that split run one CTA per SM (4 epilogue warpgroups),
+  // so they round down rather than start a second, mostly empty wave
+  int s = tn >= 64 ? num_sms / tiles : (num_sms + tiles - 1) / tiles;
   if (s > nkb) s = nkb;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : s;

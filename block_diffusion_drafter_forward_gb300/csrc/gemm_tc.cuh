@@ -16,7 +16,6 @@ constexpr int kMaxSplits = 16;
 // Everything an epilogue may need; fields an epilogue does not use stay zero.
 struct GemmParams {
   int N = 0, K = 0, M = 0, nkb = 0, nsplit = 1;
-  int wide_pairs = 0;               // split wide tiles run two CTAs per SM (see pick_splits)
   float* ws = nullptr;              // split-K partials
   unsigned* counters = nullptr;     // split-K tile counters (zero between launches)
   unsigned* status = nullptr;       // device status word
@@ -71,9 +70,7 @@ struct GemmParams {
 
 int pick_tn(int M);
 // Split-K ways for `tiles` output tiles of `nkb` k-blocks with tn-token tiles.
-// wide_pairs: split wide tiles (64+ tokens) run two CTAs per SM (GemmParams.wide_pairs = 1 at
-// launch), so the split count aims at two CTAs per SM
-int pick_splits(int tiles, int nkb, int num_sms, int tn, bool wide_pairs = false);
+int pick_splits(int tiles, int nkb, int num_sms, int tn);
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld_elems, int box_rows);
 // D = W [N, K] x X [M, K]^T with the epilogue `epi`; nsplit K-splits (1 for EPI_LMHEAD).
 // w_fp8: W holds e4m3 codes and p.row_scale the per-row scales (EPI_LMHEAD, and the layer
