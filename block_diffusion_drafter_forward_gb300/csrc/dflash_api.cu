@@ -13,7 +13,6 @@
 #include "dflash_internal.cuh"
 #include "attn_tc.cuh"
 #include "gemm_tc.cuh"
-#include "gemm_sk.cuh"
 #include "markov.cuh"
 #include "persist_tc.cuh"
 
@@ -301,13 +300,6 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
   base.Mp = Mp;
   base.eps = c.rms_eps;
   base.ss_n = H;
-  // a layer projection: stream-K over two CTAs per SM where the shape allows, else split-K
-  auto proj = [&](int epi, const void* W, int N, int K, const void* X, int ldx, const GemmParams& p, bool pdl,
-                  const void* W8) {
-    if (gemm_sk_eligible(epi, M, N, K, fp8w, h->num_sms))
-      return launch_gemm_sk(epi, W, N, K, X, ldx, M, p, h->num_sms, st, pdl);
-    return launch_gemm_tc(epi, fp8w ? W8 : W, N, K, X, ldx, M, p, splits(N, K), st, pdl, fp8w);
-  };
 
   KL(K_EMBED, launch_embed_tc(h, bonus_tokens, nb, st), "embed");
   for (int l = 0; l < c.n_layers; ++l) {
@@ -331,7 +323,9 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.layer = l;
       p.pool = static_cast<__nv_bfloat16*>(h->pool);
       p.row_scale = fp8w ? w.qkv_s : nullptr;
-      KL(K_QKV, proj(EPI_QKV, w.w_qkv, qkvd, H, h->xb, H, p, l > 0, w.qkv8), "qkv");
+      KL(K_QKV, launch_gemm_tc(EPI_QKV, fp8w ? (const void*)w.qkv8 : w.w_qkv, qkvd, H, h->xb, H, M, p,
+                               splits(qkvd, H), st, l > 0, fp8w),
+         "qkv");
     }
     if (h->tc_attn) {
       AttnParams a;
@@ -363,7 +357,9 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.ln_next = static_cast<const __nv_bfloat16*>(w.ln_post);
       p.H = H;
       p.row_scale = fp8w ? w.o_s : nullptr;
-      KL(K_OPROJ, proj(EPI_RESID, w.w_o, H, qd, h->attn, qd, p, true, w.o8), "o_proj");
+      KL(K_OPROJ, launch_gemm_tc(EPI_RESID, fp8w ? (const void*)w.o8 : w.w_o, H, qd, h->attn, qd, M, p,
+                                 splits(H, qd), st, true, fp8w),
+         "o_proj");
     }
     {
       GemmParams p = base;
@@ -372,7 +368,9 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.act = static_cast<__nv_bfloat16*>(h->act);
       p.F = F;
       p.row_scale = fp8w ? w.gu_s : nullptr;
-      KL(K_GATEUP, proj(EPI_GATEUP, w.w_gu, 2 * F, H, h->xb, H, p, true, w.gu8), "gate/up");
+      KL(K_GATEUP, launch_gemm_tc(EPI_GATEUP, fp8w ? (const void*)w.gu8 : w.w_gu, 2 * F, H, h->xb, H, M, p,
+                                  splits(2 * F, H), st, true, fp8w),
+         "gate/up");
     }
     {
       GemmParams p = base;
@@ -382,7 +380,9 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       p.ln_next = l + 1 < c.n_layers ? static_cast<const __nv_bfloat16*>(h->layer[l + 1].ln_in) : nullptr;
       p.H = H;
       p.row_scale = fp8w ? w.down_s : nullptr;
-      KL(K_DOWN, proj(EPI_RESID, w.w_down, H, F, h->act, F, p, true, w.down8), "down");
+      KL(K_DOWN, launch_gemm_tc(EPI_RESID, fp8w ? (const void*)w.down8 : w.w_down, H, F, h->act, F, M, p,
+                                splits(H, F), st, true, fp8w),
+         "down");
     }
   }
   KL(K_NORM, launch_rmsnorm_f32in(h, h->x, h->norm, h->xn, M, H, st), "final norm");
@@ -714,22 +714,9 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
       if (ns > 1) need = std::max(need, (size_t)(tiles * ns * 128 * tn));
       return tiles <= kCounters - 64;
     };
-    // the projections' stream-K shapes (bf16 layer weights): partial slots per tile
-    auto account_sk = [&](int epi, int64_t N, int64_t K, int64_t m) {
-      if (!gemm_sk_eligible(epi, (int)m, (int)N, (int)K, c.layer_weight_dtype == DFLASH_FP8E4M3_ROWSCALE, h->num_sms))
-        return;
-      const int64_t tiles = ((N + 127) / 128) * ((m + 127) / 128);
-      const int G = (int)std::min<int64_t>(gemm_sk_grid(h->num_sms), tiles * (K / 64));
-      need = std::max(need, (size_t)(tiles * gemm_sk_max_contrib((int)tiles, (int)(K / 64), G) * 128 * 128));
-    };
     bool fits = true;
-    for (int64_t m = kGamma; m <= R; m += kGamma) {
+    for (int64_t m = kGamma; m <= R; m += kGamma)
       fits = account(qkvd, H, m) && account(H, qd, m) && account(2 * F, H, m) && account(H, F, m) && fits;
-      account_sk(EPI_QKV, qkvd, H, m);
-      account_sk(EPI_RESID, H, qd, m);
-      account_sk(EPI_GATEUP, 2 * F, H, m);
-      account_sk(EPI_RESID, H, F, m);
-    }
     for (int64_t m = 1; m <= Rw; m = m < 256 ? m + 1 : m + 256)
       fits = account(H, tapd, m) && account(L * 2 * kvd, H, m) && fits;
     fits = account(H, tapd, Rw) && account(L * 2 * kvd, H, Rw) && fits;

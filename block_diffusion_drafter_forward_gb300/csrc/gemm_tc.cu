@@ -34,14 +34,11 @@
 #include <cuda_fp8.h>
 #include <float.h>
 
-#include <algorithm>
-#include <atomic>
 #include <mutex>
 
 #include "dflash_internal.cuh"
 #include "gemm_epi.cuh"
 #include "gemm_tc.cuh"
-#include "gemm_sk.cuh"
 #include "launch_util.cuh"
 #include "tc_common.cuh"
 
@@ -339,261 +336,6 @@ __global__ void __launch_bounds__(kThreads * WG, WG <= 2 ? 2 : 1)
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// ---------------------------------------------------------------------------------------
-// Stream-K projection GEMM for wide token tiles (TN = 128, bf16 weights): the
-// tiles x k-blocks of the projection are cut into G equal ranges, two CTAs per SM, so every SM
-// streams the same operand bytes whatever the tile count (160 QKV tiles on 152 SMs would
-// otherwise leave 8 SMs with two tiles).  A CTA's range falls into segments (tile, k-blocks);
-// the weight/activation ring runs on across them, the MMA issuer alternates two TMEM
-// accumulators, and one epilogue warpgroup finishes each segment: a segment covering its whole
-// tile runs the fused epilogue, the others store fp32 partials into slot (tile, rank) and the
-// last of the tile's segments to arrive (tile counter) adds them in rank order (deterministic)
-// and runs the epilogue.  Warps: 0 producer, 1 MMA, 2 TMEM owner, 3 idle, 4-7 epilogue.
-constexpr int kSkTN = 128;
-constexpr int kSkStages = 3;
-constexpr int kSkStage = 128 * 64 * 2 + kSkTN * 64 * 2;  // 32 KB: weight tile + token tile
-constexpr int kSkThreads = 256;
-
-struct SkGSeg {
-  int tile, kb0, nkb, rank, ncontrib;
-};
-
-// Segments of CTA c's range of the tiles x nkb units split over G CTAs (CTA c owns units
-// [c T / G, (c + 1) T / G)); rank 0 holds the tile's first k-blocks.
-struct SkGIter {
-  int64_t k, hi, total;
-  int nkb, G, c;
-  __device__ SkGIter(int tiles, int nkb_, int G_, int c_) : nkb(nkb_), G(G_), c(c_) {
-    total = (int64_t)tiles * nkb_;
-    k = (int64_t)c_ * total / G_;
-    hi = (int64_t)(c_ + 1) * total / G_;
-  }
-  __device__ static int owner(int64_t x, int64_t total, int G) { return (int)(((x + 1) * G + total - 1) / total) - 1; }
-  __device__ bool next(SkGSeg& s) {
-    if (k >= hi) return false;
-    const int tile = (int)(k / nkb);
-    const int64_t tb = (int64_t)tile * nkb, te = tb + nkb;
-    const int64_t end = hi < te ? hi : te;
-    const int first = owner(tb, total, G), last = owner(te - 1, total, G);
-    s.tile = tile;
-    s.kb0 = (int)(k - tb);
-    s.nkb = (int)(end - k);
-    s.rank = c - first;
-    s.ncontrib = last - first + 1;
-    k = end;
-    return true;
-  }
-};
-
-template <int EPI>
-__global__ void __launch_bounds__(kSkThreads, 2)
-    gemm_sk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const GemmParams p, int tiles_m, int tiles, int maxc) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  EpiSmem& es = *reinterpret_cast<EpiSmem*>(smem + kSkStages * kSkStage);
-  float* rsc = reinterpret_cast<float*>(smem + kSkStages * kSkStage + sizeof(EpiSmem));
-  uint64_t* full = reinterpret_cast<uint64_t*>(rsc + kSkTN);
-  uint64_t* empty = full + kSkStages;
-  uint64_t* acc_full = empty + kSkStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] a wait gave up, [1] last arrival
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int G = gridDim.x, c = blockIdx.x;
-
-  if (t == 0) {
-    for (int s = 0; s < kSkStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 1);
-    }
-    flags[0] = 0;
-    flags[1] = 0;
-    fence_barrier_init();
-    prefetch_tensormap(&tmW);
-    prefetch_tensormap(&tmX);
-  }
-  if (warp == 2) tmem_alloc(tmem_slot, 2 * kSkTN);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  pdl_trigger();
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer: the weight tiles of the first stages go out before the
-      // programmatic-launch wait (weights depend on nothing), every activation tile after it
-      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-      SkGIter it(tiles, p.nkb, G, c);
-      SkGSeg sg;
-      int j = 0;
-      bool waited = false;
-      int pre_tm[kSkStages], pre_kb[kSkStages], npre = 0;
-      while (!flags[0] && it.next(sg)) {
-        const int tile_m = sg.tile % tiles_m, tile_n = sg.tile / tiles_m;
-        for (int kk = 0; kk < sg.nkb; ++kk, ++j) {
-          const int s = j % kSkStages, u = j / kSkStages;
-          if (u > 0 && !mbar_wait_ab(&empty[s], (u - 1) & 1, flags)) {
-            flags[0] = 1;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[s], kSkStage);
-          tma_load_2d(smem + s * kSkStage, &tmW, &full[s], (sg.kb0 + kk) * 64, tile_n * 128, pol_w);
-          if (!waited) {
-            if (j < kSkStages) {  // its activation tile after the wait
-              pre_tm[npre] = tile_m;
-              pre_kb[npre] = sg.kb0 + kk;
-              ++npre;
-              if (npre < kSkStages) continue;
-            }
-            pdl_wait();  // everything the previous kernel wrote is visible from here on
-            waited = true;
-            for (int i = 0; i < npre; ++i)
-              tma_load_2d(smem + i * kSkStage + 128 * 64 * 2, &tmX, &full[i], pre_kb[i] * 64, pre_tm[i] * kSkTN, pol_x);
-            if (j < kSkStages) continue;
-          }
-          tma_load_2d(smem + s * kSkStage + 128 * 64 * 2, &tmX, &full[s], (sg.kb0 + kk) * 64, tile_m * kSkTN, pol_x);
-        }
-      }
-      if (!waited) {
-        pdl_wait();
-        for (int i = 0; i < npre; ++i)
-          tma_load_2d(smem + i * kSkStage + 128 * 64 * 2, &tmX, &full[i], pre_kb[i] * 64, pre_tm[i] * kSkTN, pol_x);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer: one accumulator per segment, two in TMEM alternating
-      constexpr uint32_t idesc = idesc_bf16(128, kSkTN);
-      SkGIter it(tiles, p.nkb, G, c);
-      SkGSeg sg;
-      int j = 0, q = 0;
-      while (it.next(sg)) {
-        const int buf = q & 1;
-        if (q >= 2 && !mbar_wait_ab(&acc_empty[buf], ((q >> 1) - 1) & 1, flags)) flags[0] = 1;
-        tc_fence_after();
-        const uint32_t d = tmem + buf * kSkTN;
-        for (int kk = 0; kk < sg.nkb; ++kk, ++j) {
-          const int s = j % kSkStages, u = j / kSkStages;
-          if (!mbar_wait_ab(&full[s], u & 1, flags)) flags[0] = 1;
-          tc_fence_after();
-          if (!flags[0]) {
-            const uint64_t ad = desc_sw128(smem + s * kSkStage);
-            const uint64_t bd = desc_sw128(smem + s * kSkStage + 128 * 64 * 2);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || k > 0) ? 1u : 0u);
-          }
-          mma_commit(&empty[s]);
-        }
-        mma_commit(&acc_full[buf]);
-        ++q;
-      }
-    }
-    __syncwarp();
-  } else if (warp >= 4) {
-    // ---------------- epilogue warpgroup (warps 4-7): thread et holds weight row et of the tile
-    pdl_wait();
-    const int et = t - 128;
-    SkGIter it(tiles, p.nkb, G, c);
-    SkGSeg sg;
-    int q = 0;
-    while (it.next(sg)) {
-      const int buf = q & 1;
-      const int tile_m = sg.tile % tiles_m, tile_n = sg.tile / tiles_m;
-      const int m0 = tile_m * kSkTN, n = tile_n * 128 + et;
-      if (p.ss_in) {  // this token tile's input row scales 1/RMS(x_m)
-        const int m = m0 + et;
-        float r = 1.f;
-        if (m < p.M) {
-          float ssum = 0.f;
-          for (int q0 = 0; q0 < p.ss_parts; ++q0) ssum += __ldcg(p.ss_in + (int64_t)q0 * p.Mp + m);
-          r = 1.f / sqrtf(ssum / (float)p.ss_n + p.eps);
-        }
-        rsc[et] = r;
-      }
-      if (!mbar_wait_ab(&acc_full[buf], (q >> 1) & 1, flags)) flags[0] = 1;
-      tc_fence_after();
-      epi_sync();  // row scales written, every thread past the accumulator wait
-      const uint32_t lane_addr = tmem + buf * kSkTN + ((uint32_t)((warp & 3) * 32) << 16);
-      if (flags[0]) {
-        tc_fence_before();
-        epi_sync();
-        if (et == 0) mbar_arrive(&acc_empty[buf]);
-      } else if (sg.ncontrib == 1) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < kSkTN; c0 += 16) {
-          EpiPre pre;
-          epilogue_pre<EPI>(p, pre, et, n, m0, c0, tile_n);
-          float v[16];
-          tmem_ld16(lane_addr + c0, v);
-          epilogue_chunk<EPI>(p, es, rsc, v, et, n, m0, c0, tile_n, pre);
-        }
-        tc_fence_before();
-        epi_sync();
-        if (et == 0) mbar_arrive(&acc_empty[buf]);
-      } else {
-        // fp32 partial into slot (tile, rank); the accumulator is free once it is read
-        float* mine = p.ws + (((int64_t)sg.tile * maxc + sg.rank) * kThreads + et) * kSkTN;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kSkTN; c0 += 16) {
-          float v[16];
-          tmem_ld16(lane_addr + c0, v);
-#pragma unroll
-          for (int cc = 0; cc < 16; cc += 4)
-            __stcg(reinterpret_cast<float4*>(mine + c0 + cc), make_float4(v[cc], v[cc + 1], v[cc + 2], v[cc + 3]));
-        }
-        tc_fence_before();
-        __threadfence();
-        epi_sync();
-        if (et == 0) {
-          mbar_arrive(&acc_empty[buf]);
-          flags[1] = atomicAdd(&p.counters[sg.tile], 1u) == (unsigned)(sg.ncontrib - 1);
-        }
-        epi_sync();
-        if (flags[1]) {
-          // the last of the tile's segments: every partial in rank order, then the epilogue
-          __threadfence();
-          const float* base = p.ws + ((int64_t)sg.tile * maxc * kThreads + et) * kSkTN;
-#pragma unroll 1
-          for (int c0 = 0; c0 < kSkTN; c0 += 16) {
-            EpiPre pre;
-            epilogue_pre<EPI>(p, pre, et, n, m0, c0, tile_n);
-            float v[16];
-#pragma unroll
-            for (int cc = 0; cc < 16; ++cc) v[cc] = 0.f;
-#pragma unroll 1
-            for (int r = 0; r < sg.ncontrib; ++r) {
-              const float4* src = reinterpret_cast<const float4*>(base + (int64_t)r * kThreads * kSkTN + c0);
-#pragma unroll
-              for (int cc = 0; cc < 4; ++cc) {
-                const float4 f = __ldcg(src + cc);
-                v[4 * cc] += f.x; v[4 * cc + 1] += f.y; v[4 * cc + 2] += f.z; v[4 * cc + 3] += f.w;
-              }
-            }
-            epilogue_chunk<EPI>(p, es, rsc, v, et, n, m0, c0, tile_n, pre);
-          }
-          if (et == 0) p.counters[sg.tile] = 0;  // re-armed for the next launch
-        }
-        epi_sync();  // flags[1] read by every thread before the next segment's arrival writes it
-      }
-      ++q;
-    }
-    if (flags[0] && et == 0) set_status(p.status, DFLASH_DEV_TIMEOUT);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (flags[0]) {
-    for (int i = 0; i < 2000; ++i) __nanosleep(1000);  // copies still in flight land first
-  }
-  if (warp == 2) tmem_dealloc(tmem, 2 * kSkTN);
-}
-
 // ------------------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -720,60 +462,6 @@ bool make_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
-}
-
-int gemm_sk_grid(int num_sms) { return 2 * num_sms; }
-
-int gemm_sk_max_contrib(int tiles, int nkb, int G) {
-  const int64_t total = (int64_t)tiles * nkb;
-  const int64_t per = total / G;
-  return (int)(per > 0 ? (nkb + per - 1) / per + 1 : G);
-}
-
-bool gemm_sk_eligible(int epi, int M, int N, int K, bool w_fp8, int num_sms) {
-  if (w_fp8 || (epi != EPI_QKV && epi != EPI_RESID && epi != EPI_GATEUP) || pick_tn(M) != kSkTN) return false;
-  const int64_t tiles = (int64_t)((N + 127) / 128) * ((M + kSkTN - 1) / kSkTN);
-  return tiles * (K / 64) >= 4 * (int64_t)gemm_sk_grid(num_sms);  // at least 4 k-blocks per CTA
-}
-
-cudaError_t launch_gemm_sk(int epi, const void* W, int N, int K, const void* X, int ldx, int M, GemmParams p,
-                           int num_sms, cudaStream_t st, bool pdl) {
-  CUtensorMap tw, tx;
-  if (!make_tmap_bf16(&tw, W, N, K, K, 128) || !make_tmap_bf16(&tx, X, M, K, ldx, kSkTN)) return cudaErrorInvalidValue;
-  p.N = N;
-  p.K = K;
-  p.M = M;
-  p.nkb = K / 64;
-  const int tiles_m = (M + kSkTN - 1) / kSkTN, tiles = ((N + 127) / 128) * tiles_m;
-  const int G = (int)std::min<int64_t>(gemm_sk_grid(num_sms), (int64_t)tiles * p.nkb);
-  const int maxc = gemm_sk_max_contrib(tiles, p.nkb, G);
-  constexpr int smem = kSkStages * kSkStage + (int)sizeof(EpiSmem) + kSkTN * 4 + 256 + 1024;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(G);
-  cfg.blockDim = dim3(kSkThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  static std::atomic<unsigned long long> a_qkv{0}, a_res{0}, a_gu{0};
-  switch (epi) {
-    case EPI_QKV: {
-      if (cudaError_t e = smem_attr_once(gemm_sk_kernel<EPI_QKV>, smem, a_qkv); e != cudaSuccess) return e;
-      return cudaLaunchKernelEx(&cfg, gemm_sk_kernel<EPI_QKV>, tw, tx, p, tiles_m, tiles, maxc);
-    }
-    case EPI_RESID: {
-      if (cudaError_t e = smem_attr_once(gemm_sk_kernel<EPI_RESID>, smem, a_res); e != cudaSuccess) return e;
-      return cudaLaunchKernelEx(&cfg, gemm_sk_kernel<EPI_RESID>, tw, tx, p, tiles_m, tiles, maxc);
-    }
-    case EPI_GATEUP: {
-      if (cudaError_t e = smem_attr_once(gemm_sk_kernel<EPI_GATEUP>, smem, a_gu); e != cudaSuccess) return e;
-      return cudaLaunchKernelEx(&cfg, gemm_sk_kernel<EPI_GATEUP>, tw, tx, p, tiles_m, tiles, maxc);
-    }
-  }
-  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_tc(int epi, const void* W, int N, int K, const void* X, int ldx, int M, GemmParams p,
