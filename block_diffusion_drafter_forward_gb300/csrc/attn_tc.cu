@@ -344,7 +344,7 @@ __device__ __forceinline__ int sk_unit_chunks(const AttnParams& p, int u, int* c
 // In the index space a unit with chunks occupies kSkUnitCost slots of no work before them: the
 // cost of a segment (its queries, the pipeline restart, its output) in chunks, so a CTA whose
 // range opens several segments gets fewer chunks.
-constexpr int kSkUnitCost = 4;
+constexpr int kSkUnitCost = 8;
 __host__ __device__ __forceinline__ long long sk_slots(int nch) { return nch > 0 ? nch + kSkUnitCost : 0; }
 
 // CTA b of G = min(grid, W) owns global chunks [lo, hi) = [floor(b W / G), floor((b + 1) W / G))
