@@ -22,7 +22,6 @@ struct AttnParams {
   int chunks_per_split = 1;              // compact kernel: key chunks per split
   float* o_part = nullptr;               // [slots, 128, 128] split partials
   float* ml_part = nullptr;              // [slots, 128, 2] running max / sum
-  unsigned* counters = nullptr;          // [units] (zero between launches)
   __nv_bfloat16* out = nullptr;          // [nb*16, nh*128]
   unsigned* status = nullptr;
 };

@@ -342,7 +342,6 @@ int propose_tc(dflash_handle* h, const int32_t* bonus_tokens, const int32_t* ctx
       a.window = c.layer_sliding[l] ? c.sliding_window : 0;
       a.o_part = h->attn_opart;
       a.ml_part = h->attn_ml;
-      a.counters = h->attn_counters;
       a.out = static_cast<__nv_bfloat16*>(h->attn);
       a.status = h->d_status;
       KL(K_ATTN, launch_attn_tc(a, nb, max_ctx_len, h->num_sms, st), "attention");
@@ -781,11 +780,6 @@ int dflash_create(const dflash_cfg* cfg, const dflash_weights* w, dflash_stream 
       const int64_t slots = attn_tc_partial_slots(h->num_sms, (int)units);
       ALLOC(h->attn_opart, slots * 128 * 128 * 4);
       ALLOC(h->attn_ml, slots * 128 * 2 * 4);
-      ALLOC(h->attn_counters, units * sizeof(unsigned));
-      if (cudaMemsetAsync(h->attn_counters, 0, units * sizeof(unsigned), st) != cudaSuccess) {
-        fail(h, DFLASH_ECUDA, "counter memset");
-        return bail(DFLASH_ECUDA);
-      }
     }
   }
   if (cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
@@ -1097,7 +1091,6 @@ int dflash_attention_check(dflash_handle* h, int32_t layer, const int32_t* ctx_l
   a.window = c.layer_sliding[layer] ? c.sliding_window : 0;
   a.o_part = h->attn_opart;
   a.ml_part = h->attn_ml;
-  a.counters = h->attn_counters;
   a.out = static_cast<__nv_bfloat16*>(out_tensor_core);
   a.status = h->d_status;
   CK(launch_attn_tc(a, nb, max_ctx_len, h->num_sms, st), "attention tc");
@@ -1137,9 +1130,6 @@ int dflash_device_status(dflash_handle* h, dflash_stream stream, uint32_t* flags
     // a kernel that gave up a wait may have left split-K and argmax tile counters part-counted:
     // re-arm them so the next call starts from zero
     CK(cudaMemsetAsync(h->counters, 0, kCounters * sizeof(unsigned), st), "counter reset");
-    if (h->attn_counters)
-      CK(cudaMemsetAsync(h->attn_counters, 0, (size_t)h->cfg.max_batch * h->cfg.n_kv_heads * sizeof(unsigned), st),
-         "counter reset");
     CK(cudaStreamSynchronize(st), "counter reset sync");
   }
 #if DFLASH_PHASE_TRACE

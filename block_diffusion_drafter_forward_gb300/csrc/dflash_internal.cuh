@@ -159,7 +159,6 @@ struct dflash_handle {
   unsigned long long* amax_best = nullptr;  // [rows] packed running argmax (zero between launches)
   float* attn_opart = nullptr;         // attention split partials (O)
   float* attn_ml = nullptr;            // attention split partials (max, sum)
-  unsigned* attn_counters = nullptr;   // per (sequence, kv head) unit
   bool tc = false;                     // bf16 tensor-core path in use
   bool tc_attn = false;                // tensor-core attention (8 query heads per kv head)
   // single-launch persistent forward (batch 1, bf16 lm_head)
