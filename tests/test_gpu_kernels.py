@@ -63,3 +63,25 @@ def test_tensor_core_attention_matches_cuda_core(cfgname, ctx):
         assert rig.drafter.device_status() == 0
         err = ((a.float() - b.float()).abs().max() / a.float().abs().max()).item()
         assert err < 1e-2, (layer, err)
+
+
+@pytest.mark.parametrize("ctx", [[5, 17, 3, 40], [0, 2, 900, 1]])
+def test_stream_k_attention_under_a_loose_max_context(ctx):
+    """max_ctx_len far above every context (20000): the host picks the stream-K kernel from it,
+    while the batch holds fewer key chunks than the kernel has CTAs (most CTAs get no chunk, a
+    unit's chunks sit in one CTA or span a few).  Same comparison as above."""
+    from helpers import Rig
+    cfg = CONFIGS["qwen3_8l_bf16"]
+    wl = make_workload(cfg, 63, ctx, extra_pages_per_seq=1260)
+    rig = Rig(wl)
+    rig.propose()
+    M = wl.nb * 16
+    layer = cfg.n_layers - 1
+    a = torch.zeros((M, cfg.q_dim), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros_like(a)
+    dflash_attention_check(rig.drafter.handle, layer, rig.ctx_lens.data_ptr(), rig.page_tables.data_ptr(),
+                           wl.nb, 20000, a.data_ptr(), b.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rig.drafter.device_status() == 0
+    err = ((a.float() - b.float()).abs().max() / a.float().abs().max()).item()
+    assert err < 1e-2, err
