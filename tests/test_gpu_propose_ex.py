@@ -72,6 +72,13 @@ def test_propose_ex_per_projection_ragged():
     check_ex(rig, [40 + 3, 9000, 1000], [16, 5, 2])
 
 
+def test_propose_ex_stream_k_attention():
+    """Long contexts: the per-projection path's stream-K attention with per-sequence widths and
+    RoPE starts."""
+    rig = Rig(make_workload(CONFIGS["qwen3_8l_bf16"], 87, [3000, 2500, 4000, 3500]))
+    check_ex(rig, [3000 + 5, 2500, 100, 3500], [16, 7, 2, 12])
+
+
 def test_propose_ex_fp32_path():
     rig = Rig(make_workload(CONFIGS["tiny_fp32"], 83, [64, 17]))
     check_ex(rig, [64 + 200, 17], [4, 13])
