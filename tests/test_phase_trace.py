@@ -30,3 +30,26 @@ def test_table_from_synthetic_stamps(tmp_path):
         assert abs(cols["barrier"][0] - 2.55) < 1e-9 and abs(cols["barrier"][1] - 2.6) < 1e-9
         assert cols["arrive"][1] == dur and "mma_last" not in cols
     assert abs(total - (7.5 + 10.0 * (P - 1))) < 1e-9
+
+
+def test_table_reads_every_slot_the_trace_holds(tmp_path):
+    """A trace with every slot reports the epilogue stamps too; an older, shorter trace
+    reports the slots it holds and no others."""
+    L, G = 1, 3
+    P = 2 + 6 * L
+    for S in (len(pt.SLOTS), 10):
+        t = np.zeros((G, P, S), dtype=np.uint64)
+        for ph in range(P):
+            for c in range(G):
+                for k in range(S):
+                    t[c, ph, k] = 1_000_000 + ph * 10_000 + 100 * k + c
+        path = tmp_path / f"trace{S}.bin"
+        with open(path, "wb") as fh:
+            fh.write(np.array([G, P, S], dtype=np.int32).tobytes())
+            fh.write(t.tobytes())
+        rows, _ = pt.table(pt.read_trace(str(path)), L)
+        names = set(rows[3][2])
+        assert names == set(pt.SLOTS[:S]), (S, names)
+        # stamps 100 ns apart per slot: the slot's median sits 100 k ns after slot 0's
+        r = rows[3][2]
+        assert abs((r[pt.SLOTS[S - 1]][0] - r["barrier"][0]) - 0.1 * (S - 1)) < 1e-9
